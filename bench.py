@@ -1,0 +1,457 @@
+#!/usr/bin/env python3
+"""Benchmark of the data-parallel ZeRO-2 gradient step on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME] [--impl dpg|reference]
+
+One step = one pass of the whole hot path over one batch of synthetic input:
+(for accumulation workloads, the no_sync accumulation of every microbatch but
+the last, then) the fused reduce-scatter -> 1/G normalisation -> Adam ->
+bf16 all-gather over every bucket, with the per-bucket squared norms.  The R
+data-parallel replicas are R gradient buffers in this GPU's HBM.  The default
+workload is the 1B Llama-shaped parameter list with R = 8 and 25 MiB buckets
+(50.6 GB of HBM traffic per step, far larger than L2, so no flush is needed).
+
+Under torchrun every rank runs its own independent step on its own GPU (no
+collective on the data path; the replicas are simulated inside each GPU);
+value = parameters updated by all ranks per second (weak scaling).
+
+Prints one JSON line (rank 0).  --impl reference times the CPU oracle (one
+host core) on a bounded sample of the same workload instead.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from workloads import (CONFIGS, KIND_GRAD, KIND_MASTER, flat_grads_bf16, master_f32,  # noqa: E402
+                       segments, stream_seed, token_counts)
+
+KERNEL_SRC = os.path.join(ROOT, "zero_optimizer_step_gb300", "csrc", "dpg_kernels.cu")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
+PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
+FALLBACK_HBM_GBS = 6800.0
+CPU_SAMPLE_ELEMS = 16 << 20          # oracle sample per CPU step
+
+
+def parse():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--config", default="llama1b", choices=sorted(set(CONFIGS) - {"tiny"}))
+    ap.add_argument("--cap-mib", type=float, default=None, help="override the bucket cap")
+    ap.add_argument("--impl", default="dpg", choices=["dpg", "reference"])
+    ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    a = ap.parse_args()
+    if a.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    return a
+
+
+def dist_info():
+    return (int(os.environ.get("RANK", 0)), int(os.environ.get("LOCAL_RANK", 0)),
+            int(os.environ.get("WORLD_SIZE", 1)))
+
+
+def cap_of(cfg, a) -> int:
+    return int(a.cap_mib * (1 << 20)) if a.cap_mib else cfg.cap_bytes
+
+
+def workload_desc(cfg, cap, plan_nb, total) -> dict:
+    return {"workload": f"{cfg.name}: {len(cfg.shapes)} tensors, psi={cfg.psi}, R={cfg.R} simulated "
+                        f"replicas, {cap / (1 << 20):g} MiB buckets, K={cfg.K} microbatch(es), ZeRO-2 "
+                        f"fused reduce-scatter+Adam+all-gather",
+            "psi": cfg.psi, "R": cfg.R, "K": cfg.K, "cap_bytes": cap, "n_buckets": plan_nb,
+            "total_padded": total, "grad_dtype": "bf16", "state_dtype": "f32",
+            "param_views": 1, "l2": "inputs larger than L2 (no flush)"}
+
+
+def algorithmic_bytes_per_param(cfg) -> dict:
+    R, K = cfg.R, cfg.K
+    fused = (6 * R + 26) if K > 1 else (2 * R + 26)
+    step = fused + ((6 * R + (K - 2) * 10 * R) if K > 1 else 0)
+    return {"fused": fused, "step": step}
+
+
+# --------------------------------------------------------------------------
+# clocks
+# --------------------------------------------------------------------------
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"dpg_clocks_{os.getpid()}.csv")
+
+    def start(self):
+        try:
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                 "-i", str(self.idx), "-lms", "50"], stdout=self.fh, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except OSError:
+            self.proc = None
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.1)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.fh.close()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, val in zip(names, f[5:9]):
+                if val.lower() == "active":
+                    reasons.add(n)
+        os.unlink(self.path)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# --------------------------------------------------------------------------
+# CPU oracle baseline (rank 0, N = 1 only)
+# --------------------------------------------------------------------------
+def oracle_sample_step(cfg, h_grads, h_last, tokens, w, m, v, t):
+    """One oracle step over a contiguous sample (elementwise: reduce, scale,
+    Adam, bf16 cast)."""
+    import oracle
+    g = oracle.reduce(h_grads, oracle.grad_scale(tokens), last=h_last)
+    oracle.adam(g, w, m, v, t=t)
+    oracle.f32_to_bf16(w)
+
+
+def cpu_sample_inputs(cfg, n, device):
+    """Host copies of a contiguous n-element sample of the workload's inputs
+    (drawn like the full workload; accumulation workloads get fp32 buffers
+    holding K-1 microbatches plus a last bf16 microbatch)."""
+    import torch
+    seg = [(0, n)]
+    R, K = cfg.R, cfg.K
+    bf = lambda r, k: flat_grads_bf16(seg, n, cfg.grad_std, stream_seed(cfg.seed, KIND_GRAD, r, k),
+                                      device=device).cpu().view(torch.int16).numpy().view(np.uint16)
+    if K > 1:
+        import oracle
+        grads, last = [], []
+        for r in range(R):
+            acc = np.empty(n, np.float32)
+            for k in range(K - 1):
+                oracle.accumulate(bf(r, k), acc, first=(k == 0))
+            grads.append(acc)
+            last.append(bf(r, K - 1))
+    else:
+        grads, last = [bf(r, 0) for r in range(R)], None
+    w = master_f32(n, stream_seed(cfg.seed, KIND_MASTER), device=device).cpu().numpy()
+    return grads, last, w, np.zeros(n, np.float32), np.zeros(n, np.float32)
+
+
+def cpu_baseline(cfg, device, target_s=12.0) -> dict:
+    """Time the oracle, as it stands, on one host core over a bounded sample."""
+    import oracle
+    oracle.build()
+    try:
+        os.sched_setaffinity(0, {sorted(os.sched_getaffinity(0))[0]})
+    except (AttributeError, OSError):
+        pass
+    n = CPU_SAMPLE_ELEMS
+    grads, last, w, m, v = cpu_sample_inputs(cfg, n, device)
+    tokens = token_counts(cfg)
+    t0 = time.perf_counter()
+    reps = 0
+    while True:
+        reps += 1
+        oracle_sample_step(cfg, grads, last, tokens, w, m, v, reps)
+        if time.perf_counter() - t0 >= target_s:
+            break
+    dt = time.perf_counter() - t0
+    cores = 1
+    return {"value": reps * n / dt, "unit": "params/s", "cores": cores, "kind": "oracle",
+            "sample": f"{reps} oracle steps over the first {n} elements of the workload "
+                      f"(elementwise reduce+scale+Adam+bf16 cast; fixed-order fp32), one pinned core"}
+
+
+# --------------------------------------------------------------------------
+# GPU run
+# --------------------------------------------------------------------------
+def load_peak():
+    try:
+        pk = json.load(open(PEAKS_FILE))
+        return float(pk["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def traffic_per_launch(cfg, cap, total_padded):
+    """DRAM bytes per fused launch from the committed ncu summary, if it was
+    taken on the current kernel source; scaled by elements if the capture ran
+    a smaller case of the same kernel.  None otherwise."""
+    try:
+        t = json.load(open(TRAFFIC_FILE))["k_rs_adam"]
+    except (OSError, KeyError, ValueError):
+        return None
+    src = hashlib.sha256(open(KERNEL_SRC, "rb").read()).hexdigest()
+    if t.get("source_sha256") != src or t.get("R") != cfg.R or t.get("K", 1) != cfg.K:
+        return None
+    return float(t["dram_bytes_per_launch"]) * total_padded / float(t["elements"])
+
+
+def run_dpg(a):
+    import torch
+    import torch.distributed as dist
+    rank, local, world = dist_info()
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    from zero_optimizer_step_gb300 import build as _build
+    if rank == 0 or world == 1:
+        _build.build()
+    if world > 1:
+        dist.barrier()
+    import zero_optimizer_step_gb300 as dpg
+
+    cfg = CONFIGS[a.config]
+    cap = cap_of(cfg, a)
+    R, K = cfg.R, cfg.K
+    plan = dpg.dpg_plan_buckets(cfg.numels, cap, R)
+    dpg.dpg_plan_upload(plan)
+    N = plan.total_padded
+    segs = segments(plan.param_offset, cfg.numels)
+    dev = torch.device("cuda", local)
+    tokens = token_counts(cfg)
+    g = [flat_grads_bf16(segs, N, cfg.grad_std, stream_seed(cfg.seed, KIND_GRAD, r, 0), device=dev)
+         for r in range(R)]
+    acc = [torch.empty(N, device=dev) for _ in range(R)] if K > 1 else None
+    w = master_f32(N, stream_seed(cfg.seed, KIND_MASTER), device=dev)
+    m = torch.zeros(N, device=dev)
+    v = torch.zeros(N, device=dev)
+    param = torch.empty(N, dtype=torch.bfloat16, device=dev)
+    sq = torch.empty(plan.n_buckets, device=dev)
+    nf = torch.empty(plan.n_buckets, dtype=torch.int64, device=dev)
+    stream = torch.cuda.current_stream()
+    state = {"t": 0}
+
+    def step(ev_pair=None):
+        state["t"] += 1
+        hp = dpg.HParams(step=state["t"])
+        if K > 1:
+            for k in range(K - 1):
+                for r in range(R):
+                    dpg.dpg_accumulate(plan, g[r], acc[r], first=(k == 0), stream=stream)
+        if ev_pair is not None:
+            dpg.dpg_time_next_fused_launch(*ev_pair)
+        if K > 1:
+            dpg.dpg_step(plan, acc, tokens, hp, w, m, v, [param], last_micro=g,
+                         bucket_sqnorm=sq, bucket_nonfinite=nf, stream=stream)
+        else:
+            dpg.dpg_step(plan, g, tokens, hp, w, m, v, [param], bucket_sqnorm=sq,
+                         bucket_nonfinite=nf, stream=stream)
+
+    for _ in range(a.warmup):
+        step()
+    torch.cuda.synchronize()
+
+    # events that bracket the fused kernel inside each timed step
+    ev_k = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+            for _ in range(a.steps)]
+    for e0, e1 in ev_k:
+        e0.record(stream)
+        e1.record(stream)
+    ev_start, ev_stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(local)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    launches0 = dpg.dpg_launch_count()
+    ev_start.record(stream)
+    for i in range(a.steps):
+        step(ev_k[i])
+    ev_stop.record(stream)
+    torch.cuda.synchronize()
+    launches = dpg.dpg_launch_count() - launches0
+    if world > 1:
+        dist.barrier()
+    clk = clocks.stop()
+    ms = ev_start.elapsed_time(ev_stop) / a.steps
+    k_ms = statistics.mean(e0.elapsed_time(e1) for e0, e1 in ev_k)
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+
+    # end to end: host (pinned) gradients copied in, norms copied out, every step
+    e2e = None
+    if not a.no_e2e:
+        e2e = run_e2e(a, dpg, plan, g, acc, w, m, v, param, sq, nf, tokens, cfg, dev, stream,
+                      state, world)
+
+    bpp = algorithmic_bytes_per_param(cfg)
+    peak, peak_kind = load_peak()
+    achieved = bpp["fused"] * cfg.psi / (k_ms * 1e-3) / 1e9
+    traffic = traffic_per_launch(cfg, cap, N)
+    value = cfg.psi * world / (ms * 1e-3)
+    line = {
+        "metric": "params/s of the fused bucket reduce-scatter + Adam + all-gather step "
+                  "(achieved HBM GB/s vs GB300 peak in roofline)",
+        "value": value, "unit": "params/s", "n_gpus": world, "steps": a.steps,
+        "warmup": a.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": workload_desc(cfg, cap, plan.n_buckets, N),
+        "hbm_gbs_step": bpp["step"] * cfg.psi / (ms * 1e-3) / 1e9,
+        "roofline": {"bound": "hbm", "kernel": f"k_rs_adam<R={R}>", "achieved": achieved,
+                     "peak": peak, "peak_kind": f"{peak_kind} (copy bandwidth)", "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": traffic,
+                     "algorithmic_bytes_per_launch": bpp["fused"] * cfg.psi,
+                     "kernel_ms": k_ms},
+        "gpu_launches": int(launches),
+        "clocks": clk,
+        "e2e": e2e,
+    }
+    if rank == 0 and world == 1 and not a.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(cfg, dev)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+def run_e2e(a, dpg, plan, g, acc, w, m, v, param, sq, nf, tokens, cfg, dev, stream, state, world):
+    import torch
+    R, K = cfg.R, cfg.K
+    N = plan.total_padded
+    # one pinned host buffer per (replica, microbatch) input of a step
+    h_in = [[torch.empty(N, dtype=torch.bfloat16, pin_memory=True) for _ in range(K)]
+            for _ in range(R)]
+    for r in range(R):
+        for k in range(K):
+            h_in[r][k].copy_(g[r])
+    h_sq = torch.empty(plan.n_buckets, pin_memory=True)
+    h_nf = torch.empty(plan.n_buckets, dtype=torch.int64, pin_memory=True)
+
+    def e2e_step():
+        state["t"] += 1
+        hp = dpg.HParams(step=state["t"])
+        for k in range(K):
+            for r in range(R):
+                g[r].copy_(h_in[r][k], non_blocking=True)
+            if k < K - 1:
+                for r in range(R):
+                    dpg.dpg_accumulate(plan, g[r], acc[r], first=(k == 0), stream=stream)
+        if K > 1:
+            dpg.dpg_step(plan, acc, tokens, hp, w, m, v, [param], last_micro=g, bucket_sqnorm=sq,
+                         bucket_nonfinite=nf, stream=stream)
+        else:
+            dpg.dpg_step(plan, g, tokens, hp, w, m, v, [param], bucket_sqnorm=sq,
+                         bucket_nonfinite=nf, stream=stream)
+        h_sq.copy_(sq, non_blocking=True)
+        h_nf.copy_(nf, non_blocking=True)
+
+    steps = max(3, min(a.steps, 10))
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    e0.record(stream)
+    for _ in range(steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    return {"value": cfg.psi * world / (ms * 1e-3), "unit": "params/s", "steps": steps,
+            "h2d_bytes_per_step": R * K * N * 2, "d2h_bytes_per_step": plan.n_buckets * 12,
+            "ms_per_step": ms}
+
+
+# --------------------------------------------------------------------------
+# reference arm: the CPU oracle on the host cores
+# --------------------------------------------------------------------------
+def run_reference(a):
+    rank, _, world = dist_info()
+    if rank != 0:
+        return
+    cfg = CONFIGS[a.config]
+    cap = cap_of(cfg, a)
+    import oracle
+    oracle.build()
+    try:
+        os.sched_setaffinity(0, {sorted(os.sched_getaffinity(0))[0]})
+    except (AttributeError, OSError):
+        pass
+    n = CPU_SAMPLE_ELEMS
+    grads, last, w, m, v = cpu_sample_inputs(cfg, n, "cpu")
+    tokens = token_counts(cfg)
+    t = 0
+    for _ in range(a.warmup):
+        t += 1
+        oracle_sample_step(cfg, grads, last, tokens, w, m, v, t)
+    t0 = time.perf_counter()
+    for _ in range(a.steps):
+        t += 1
+        oracle_sample_step(cfg, grads, last, tokens, w, m, v, t)
+    dt = (time.perf_counter() - t0) / a.steps
+    value = n / dt
+    plan = oracle.plan_buckets(cfg.numels, cap, cfg.R)
+    sample = (f"each step: oracle reduce+scale+Adam+bf16 cast over the first {n} elements of the "
+              f"workload, one pinned host core")
+    line = {"metric": "params/s of the fused bucket reduce-scatter + Adam + all-gather step "
+                      "(achieved HBM GB/s vs GB300 peak in roofline)",
+            "value": value, "unit": "params/s", "n_gpus": world, "steps": a.steps,
+            "warmup": a.warmup, "ms_per_step": dt * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": workload_desc(cfg, cap, plan.n_buckets, plan.total_padded),
+            "impl": "reference",
+            "cpu_baseline": {"value": value, "unit": "params/s", "cores": 1, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": "params/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    a = parse()
+    if a.impl == "reference":
+        run_reference(a)
+    else:
+        run_dpg(a)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,219 @@
+/*
+ * dpg.h -- C ABI of the GB300 (sm_103a) data-parallel ZeRO-2 gradient step.
+ *
+ * The step, as the pages describe it for DDP and ZeRO-1/2:
+ *   gradients are collected into byte-capped flat buckets in backward-ready
+ *   (reverse) order; each bucket is reduce-scattered so that rank r owns the
+ *   r-th 1/R shard of the summed gradient; the owner normalises it by the
+ *   global valid-token count and applies mixed-precision Adam to its shard of
+ *   fp32 master weight and moments; the updated bf16 parameters are
+ *   all-gathered back to every replica.
+ * Sources (page title, section):
+ *   "Parallelisms" -- Data parallel; Gradient bucketing; ZeRO-1; ZeRO-2;
+ *       FSDP (Flat parameter; YaFSDP writes gradients into comm buffers).
+ *   "Distributed Training and Parallelism" -- Data parallelism and the global
+ *       gradient (R/global_count normalisation, no_sync accumulation).
+ *   "Parallelism Starts With the Bottleneck" -- Allreduce equals
+ *       reducescatter plus allgather; ZeRO removes the copies.
+ *   Adam itself: Kingma & Ba (2015), Algorithm 1 (the pages name it only).
+ *
+ * On one GPU the R data-parallel replicas are R gradient buffers resident in
+ * the same HBM; the reduce-scatter is an on-device rank-ordered reduction into
+ * R shards and the all-gather is a bf16 cast written to the replica views.
+ *
+ * Conventions for every function below
+ *   - Returns DPG_OK (0) or a negative DPG_ERR_* code; dpg_last_error() then
+ *     holds a message for the calling thread.  No exception crosses the ABI;
+ *     nothing calls exit() or traps on the device.
+ *   - The CALLER owns every device buffer passed in.  The library owns only
+ *     the plan object (host tables, their device copy and the scratch used for
+ *     the per-bucket norm partials), freed by dpg_plan_destroy().
+ *   - "flat" buffers hold plan->total_padded elements laid out bucket after
+ *     bucket (see dpg_plan_buckets).  bf16 buffers must be 16-byte aligned,
+ *     fp32 buffers 32-byte aligned (DPG_ERR_MISALIGNED otherwise).
+ *   - Device work is asynchronous on `stream` (a cudaStream_t; NULL = the
+ *     legacy default stream).  Host arrays passed in (pointer tables, token
+ *     counts, hparams) are read before the call returns.
+ *   - A plan uploads its tables to the current device on its first device
+ *     call (a synchronous copy), or explicitly with dpg_plan_upload(); call
+ *     that before capturing a stream into a CUDA graph.  A plan serves one
+ *     device.  Calls that use the norm scratch of the same plan must not
+ *     overlap on the GPU (issue them on one stream).
+ */
+#ifndef DPG_H
+#define DPG_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* status codes */
+#define DPG_OK 0
+#define DPG_ERR_INVALID_ARG (-1)    /* bad pointer/size/count/dtype/range      */
+#define DPG_ERR_ZERO_TOKENS (-2)    /* global valid-token count G == 0          */
+#define DPG_ERR_MISALIGNED (-3)     /* a buffer breaks the alignment rule       */
+#define DPG_ERR_CUDA (-4)           /* a CUDA runtime call or launch failed     */
+#define DPG_ERR_DEVICE_TIMEOUT (-5) /* a bounded device-side wait gave up       */
+#define DPG_ERR_OOM (-6)            /* host or device allocation of the plan    */
+
+/* gradient buffer element types */
+#define DPG_BF16 0
+#define DPG_F32 1
+
+#define DPG_MAX_REPLICAS 64 /* R */
+#define DPG_MAX_VIEWS 64    /* bf16 parameter views written by one call */
+
+typedef struct dpg_plan dpg_plan_t;
+
+/* Adam hyper-parameters.  step = t of this update, after increment (the first
+ * update uses 1).  The library rounds each constant once to fp32:
+ * beta1, beta2, 1-beta1, 1-beta2, 1-beta1^t, 1-beta2^t, lr, eps, lr*wd are
+ * computed in double and converted.  weight_decay != 0 applies decoupled
+ * (AdamW) decay w <- w - (lr*wd)*w before the Adam update. */
+typedef struct {
+    double lr, beta1, beta2, eps, weight_decay;
+    int64_t step;
+} dpg_hparams;
+
+/* Message describing the last failure on the calling thread ("" if none). */
+const char* dpg_last_error(void);
+/* Static name of a status code. */
+const char* dpg_status_string(int status);
+/* ABI version of this header (bumped on any signature change). */
+int dpg_abi_version(void);
+#define DPG_ABI_VERSION 1
+
+/* ---------------------------------------------------------------------------
+ * Bucket plan (host)                ["Parallelisms" -- Data parallel; Gradient
+ *                                    bucketing; ZeRO-2; FSDP / Flat parameter]
+ * numels[n_params]: element counts in module REGISTRATION order (>= 0).
+ * Parameters are placed in REVERSE order (later layers are ready first in
+ * backward).  Each slice starts on a multiple of 8 elements.  A parameter with
+ * elements that would take a bucket already holding elements past cap_bytes
+ * (2 bytes per bf16 gradient element, alignment included) first closes it; a
+ * parameter larger than the cap sits alone; parameters are never split;
+ * zero-size parameters never close a bucket.  A closed bucket is zero-padded
+ * to a multiple of 8*R elements; shard r of bucket b is
+ * [r*padded_b/R, (r+1)*padded_b/R) inside it.  Buckets follow one another in
+ * the flat buffer in closing order (bucket 0 holds the last parameters).
+ * 1 <= R <= DPG_MAX_REPLICAS, cap_bytes > 0, n_params >= 0.  Host only: needs
+ * no GPU.  *out receives a new plan (free with dpg_plan_destroy).
+ * ------------------------------------------------------------------------- */
+int dpg_plan_buckets(const int64_t* numels, int32_t n_params, int64_t cap_bytes,
+                     int32_t R, dpg_plan_t** out);
+void dpg_plan_destroy(dpg_plan_t* plan);
+/* Sizes of a plan; any output pointer may be NULL. */
+int dpg_plan_info(const dpg_plan_t* plan, int32_t* n_params, int32_t* n_buckets,
+                  int64_t* total_padded, int32_t* R);
+/* Bucket b: element offset in the flat buffer, padded size, shard size. */
+int dpg_plan_bucket(const dpg_plan_t* plan, int32_t b, int64_t* offset,
+                    int64_t* padded_numel, int64_t* shard_numel);
+/* Parameter p (registration index): bucket and element offset in the flat
+ * buffer of its slice, and its element count. */
+int dpg_plan_param(const dpg_plan_t* plan, int32_t p, int32_t* bucket,
+                   int64_t* offset, int64_t* numel);
+/* Bulk copy of the maps into caller host arrays (n_params / n_buckets
+ * entries; any pointer may be NULL). */
+int dpg_plan_export(const dpg_plan_t* plan, int32_t* param_bucket, int64_t* param_offset,
+                    int64_t* bucket_offset, int64_t* bucket_padded);
+/* Upload the plan's tables to the current device (synchronous; idempotent). */
+int dpg_plan_upload(dpg_plan_t* plan);
+
+/* ---------------------------------------------------------------------------
+ * Pack / unpack (one replica)       ["Parallelisms" -- FSDP / Flat parameter]
+ * param_grads: HOST array of n_params DEVICE pointers to bf16 gradients
+ * (2-byte aligned; NULL allowed only for zero-size parameters).
+ * dpg_pack:   flat[offset_p + i] = grad_p[i]; every padding slot set to 0.
+ * dpg_unpack: grad_p[i] = flat[offset_p + i]; padding is not read.
+ * In steady state gradients are views into the flat buffer and no pack runs.
+ * ------------------------------------------------------------------------- */
+int dpg_pack(const dpg_plan_t* plan, const void* const* param_grads, void* flat_bf16,
+             void* stream);
+int dpg_unpack(const dpg_plan_t* plan, const void* flat_bf16, void* const* param_grads,
+               void* stream);
+
+/* ---------------------------------------------------------------------------
+ * no_sync gradient accumulation (one replica)   ["Distributed Training and
+ *                    Parallelism" -- Data parallelism and the global gradient]
+ * acc_f32[i] = f32(g[i]) if first != 0, else acc_f32[i] + f32(g[i]) (binary32,
+ * round to nearest), for all total_padded elements.  The final microbatch is
+ * not accumulated here: pass it as last_micro_bf16 to the reduction below.
+ * ------------------------------------------------------------------------- */
+int dpg_accumulate(const dpg_plan_t* plan, const void* flat_bf16, float* acc_f32,
+                   int32_t first, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * Fused reduce-scatter + normalisation + Adam + all-gather, buckets [b0, b1)
+ *      ["Parallelisms" -- ZeRO-1, ZeRO-2; "Parallelism Starts With the
+ *       Bottleneck" -- Allreduce equals reducescatter plus allgather;
+ *       "Distributed Training and Parallelism" -- Data parallelism and the
+ *       global gradient; Kingma & Ba Alg. 1]
+ * For every element i of every shard of buckets b0..b1-1, in one pass:
+ *   x_r = f32(grads[r][i])                         (grads_dtype == DPG_BF16)
+ *       | grads[r][i]                              (DPG_F32: fp32 accumulation)
+ *   x_r = x_r + f32(last_micro_bf16[r][i])         (if last_micro_bf16 != NULL)
+ *   s   = x_0 + x_1 + ... + x_{R-1}                (binary32, rank order)
+ *   g   = s * fp32(1/G),  G = sum(valid_tokens[0..n_counts))   (int64)
+ *   Adam on master/exp_avg/exp_avg_sq (see dpg_hparams), binary32, no FMA
+ *   param_views[k][i] = bf16_rne(master[i])        (k < n_views)
+ * grads: HOST array of R device pointers to flat buffers (R = plan's R).
+ * last_micro_bf16: NULL or HOST array of R device pointers (flat bf16).
+ * valid_tokens: HOST array (e.g. R*K counts); each >= 0; G == 0 -> error.
+ * master, exp_avg, exp_avg_sq: flat fp32, updated in place.
+ * param_views: HOST array of n_views device pointers to flat bf16 buffers
+ *   (0 <= n_views <= DPG_MAX_VIEWS; views alias one buffer in the usual case).
+ * bucket_sqnorm (nullable, device, n_buckets floats): entry b receives the
+ *   sum over bucket b of g*g (fp32 partials summed in double; deterministic).
+ * bucket_nonfinite (nullable, device, n_buckets int64): count of elements of
+ *   bucket b whose g is NaN or infinite (they are propagated, not skipped).
+ * reduced_grad (nullable, device, flat fp32): receives g (debug/parity).
+ * 0 <= b0 <= b1 <= n_buckets; b0 == b1 does nothing and returns DPG_OK.
+ * The gradient buffers' padding slots must hold zeros (dpg_pack writes them).
+ * ------------------------------------------------------------------------- */
+int dpg_reduce_scatter_adam(const dpg_plan_t* plan, const void* const* grads,
+                            int32_t grads_dtype, const void* const* last_micro_bf16,
+                            const int64_t* valid_tokens, int32_t n_counts,
+                            const dpg_hparams* hp, float* master, float* exp_avg,
+                            float* exp_avg_sq, void* const* param_views, int32_t n_views,
+                            float* bucket_sqnorm, int64_t* bucket_nonfinite,
+                            float* reduced_grad, int32_t b0, int32_t b1, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * All-gather / cast on its own, buckets [b0, b1)
+ *      ["Parallelisms" -- ZeRO-1: workers all-gather the updated shards]
+ * param_views[k][i] = bf16_rne(master[i]) for every element of the buckets.
+ * ------------------------------------------------------------------------- */
+int dpg_allgather_params(const dpg_plan_t* plan, const float* master,
+                         void* const* param_views, int32_t n_views, int32_t b0, int32_t b1,
+                         void* stream);
+
+/* ---------------------------------------------------------------------------
+ * One whole optimizer step over every bucket (one fused launch plus, when a
+ * norm output is requested, one small finalize launch).  Same arguments and
+ * semantics as dpg_reduce_scatter_adam with b0 = 0, b1 = n_buckets and no
+ * reduced-gradient output.
+ * ------------------------------------------------------------------------- */
+int dpg_step(const dpg_plan_t* plan, const void* const* grads, int32_t grads_dtype,
+             const void* const* last_micro_bf16, const int64_t* valid_tokens,
+             int32_t n_counts, const dpg_hparams* hp, float* master, float* exp_avg,
+             float* exp_avg_sq, void* const* param_views, int32_t n_views,
+             float* bucket_sqnorm, int64_t* bucket_nonfinite, void* stream);
+
+/* Diagnostics -------------------------------------------------------------- */
+/* Number of kernels this library has launched since it was loaded. */
+int64_t dpg_launch_count(void);
+/* The next fused reduce-scatter-Adam launch issued by the calling thread
+ * records start_event immediately before itself and stop_event immediately
+ * after itself, on its own stream (cudaEvent_t handles created by the caller);
+ * the request is then cleared.  NULL, NULL clears a pending request.  Lets a
+ * caller time the fused kernel alone inside a whole step. */
+int dpg_time_next_fused_launch(void* start_event, void* stop_event);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DPG_H */

@@ -189,6 +189,14 @@ def flat_grads_bf16(segs, total: int, std: float, seed: int, device="cpu", chunk
     return out
 
 
+def flat_values_f32(segs, total: int, std: float, seed: int, device="cpu"):
+    """float32 tensor [total]: N(0, std) in every segment, zero in padding."""
+    out = normal_f32(total, std, seed, device)
+    for a, b in padding_ranges(segs, total):
+        out[a:b].zero_()
+    return out
+
+
 def master_f32(total: int, seed: int, std: float = 0.02, device="cpu"):
     return normal_f32(total, std, seed, device)
 

@@ -1,0 +1,368 @@
+"""GB300 data-parallel ZeRO-2 gradient step -- Python binding of libdpg.so.
+
+Thin ctypes marshalling over the C ABI in include/dpg.h: every function has
+the C name, takes torch tensors (or raw integer device pointers) and the
+current CUDA stream, and calls the library; all arithmetic of the step runs
+in the library's sm_103a kernels.  PyTorch only supplies device memory and
+streams.  If libdpg.so has not been built, importing works but every call
+raises ``DpgLibraryMissing``: there is no CPU fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+from typing import Optional, Sequence, Union
+
+import numpy as np
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libdpg.so")
+
+DPG_OK = 0
+DPG_ERR_INVALID_ARG = -1
+DPG_ERR_ZERO_TOKENS = -2
+DPG_ERR_MISALIGNED = -3
+DPG_ERR_CUDA = -4
+DPG_ERR_DEVICE_TIMEOUT = -5
+DPG_ERR_OOM = -6
+DPG_BF16 = 0
+DPG_F32 = 1
+DPG_MAX_REPLICAS = 64
+DPG_MAX_VIEWS = 64
+
+# symbols declared in include/dpg.h
+EXPORTED = (
+    "dpg_last_error", "dpg_status_string", "dpg_abi_version", "dpg_plan_buckets",
+    "dpg_plan_destroy", "dpg_plan_info", "dpg_plan_bucket", "dpg_plan_param",
+    "dpg_plan_export", "dpg_plan_upload", "dpg_pack", "dpg_unpack", "dpg_accumulate",
+    "dpg_reduce_scatter_adam", "dpg_allgather_params", "dpg_step", "dpg_launch_count",
+    "dpg_time_next_fused_launch",
+)
+
+
+class DpgLibraryMissing(ImportError):
+    pass
+
+
+class DpgError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{_status_name(status)} ({status}): {message}")
+        self.status = status
+
+
+class dpg_hparams(ctypes.Structure):
+    _fields_ = [("lr", ctypes.c_double), ("beta1", ctypes.c_double), ("beta2", ctypes.c_double),
+                ("eps", ctypes.c_double), ("weight_decay", ctypes.c_double),
+                ("step", ctypes.c_int64)]
+
+
+@dataclass
+class HParams:
+    """Adam hyper-parameters; ``step`` is t of this update (first update: 1)."""
+    lr: float = 1e-3
+    beta1: float = 0.9
+    beta2: float = 0.999
+    eps: float = 1e-8
+    weight_decay: float = 0.0
+    step: int = 1
+
+    def c(self) -> dpg_hparams:
+        return dpg_hparams(self.lr, self.beta1, self.beta2, self.eps, self.weight_decay,
+                           int(self.step))
+
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """Load libdpg.so (built in-tree by zero_optimizer_step_gb300.build)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise DpgLibraryMissing(
+                f"{LIB_PATH} is missing: build it with `python -m zero_optimizer_step_gb300.build`")
+        L = ctypes.CDLL(LIB_PATH)
+        P, i32, i64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64
+        c_int = ctypes.c_int
+        L.dpg_last_error.restype = ctypes.c_char_p
+        L.dpg_status_string.restype = ctypes.c_char_p
+        L.dpg_status_string.argtypes = [c_int]
+        L.dpg_abi_version.restype = c_int
+        L.dpg_plan_buckets.argtypes = [P, i32, i64, i32, ctypes.POINTER(P)]
+        L.dpg_plan_destroy.argtypes = [P]
+        L.dpg_plan_destroy.restype = None
+        L.dpg_plan_info.argtypes = [P, P, P, P, P]
+        L.dpg_plan_bucket.argtypes = [P, i32, P, P, P]
+        L.dpg_plan_param.argtypes = [P, i32, P, P, P]
+        L.dpg_plan_export.argtypes = [P, P, P, P, P]
+        L.dpg_plan_upload.argtypes = [P]
+        L.dpg_pack.argtypes = [P, P, P, P]
+        L.dpg_unpack.argtypes = [P, P, P, P]
+        L.dpg_accumulate.argtypes = [P, P, P, i32, P]
+        L.dpg_reduce_scatter_adam.argtypes = [P, P, i32, P, P, i32, P, P, P, P, P, i32, P, P, P,
+                                              i32, i32, P]
+        L.dpg_allgather_params.argtypes = [P, P, P, i32, i32, i32, P]
+        L.dpg_step.argtypes = [P, P, i32, P, P, i32, P, P, P, P, P, i32, P, P, P]
+        L.dpg_launch_count.restype = i64
+        L.dpg_time_next_fused_launch.argtypes = [P, P]
+        L.dpg_time_next_fused_launch.restype = c_int
+        for name in ("dpg_plan_buckets", "dpg_plan_info", "dpg_plan_bucket", "dpg_plan_param",
+                     "dpg_plan_export", "dpg_plan_upload", "dpg_pack", "dpg_unpack",
+                     "dpg_accumulate", "dpg_reduce_scatter_adam", "dpg_allgather_params",
+                     "dpg_step"):
+            getattr(L, name).restype = c_int
+        _lib = L
+    return _lib
+
+
+def _status_name(status: int) -> str:
+    try:
+        return lib().dpg_status_string(status).decode()
+    except Exception:
+        return "DPG_ERR"
+
+
+def _check(status: int):
+    if status != DPG_OK:
+        raise DpgError(status, lib().dpg_last_error().decode())
+
+
+# --------------------------------------------------------------------------
+# argument marshalling
+# --------------------------------------------------------------------------
+Ptr = Union[int, "torch.Tensor", None]  # noqa: F821
+
+
+def _ptr(x: Ptr) -> Optional[int]:
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    return x.data_ptr()
+
+
+def _ptrs(xs: Sequence[Ptr]):
+    arr = (ctypes.c_void_p * max(1, len(xs)))()
+    for k, x in enumerate(xs):
+        arr[k] = _ptr(x)
+    return arr
+
+
+def _stream(stream) -> Optional[int]:
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _tokens(valid_tokens):
+    t = np.ascontiguousarray(np.asarray(valid_tokens, dtype=np.int64).reshape(-1))
+    return t, t.size
+
+
+def _need(t, dtype_name: str, numel: int, what: str):
+    """Tensors must be CUDA, contiguous, of the right dtype and large enough."""
+    if t is None or isinstance(t, int):
+        return
+    import torch
+    want = {"bf16": torch.bfloat16, "f32": torch.float32}[dtype_name]
+    if t.dtype != want:
+        raise TypeError(f"{what}: expected {want}, got {t.dtype}")
+    if not t.is_cuda:
+        raise TypeError(f"{what}: expected a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{what}: tensor must be contiguous")
+    if t.numel() < numel:
+        raise ValueError(f"{what}: needs >= {numel} elements, has {t.numel()}")
+
+
+# --------------------------------------------------------------------------
+# plan
+# --------------------------------------------------------------------------
+class Plan:
+    """Owning handle of a dpg_plan_t plus numpy copies of its maps."""
+
+    def __init__(self, handle: int):
+        self._h = ctypes.c_void_p(handle)
+        L = lib()
+        n_params, n_buckets, R = ctypes.c_int32(), ctypes.c_int32(), ctypes.c_int32()
+        total = ctypes.c_int64()
+        _check(L.dpg_plan_info(self._h, ctypes.byref(n_params), ctypes.byref(n_buckets),
+                               ctypes.byref(total), ctypes.byref(R)))
+        self.n_params, self.n_buckets = n_params.value, n_buckets.value
+        self.total_padded, self.R = total.value, R.value
+        self.param_bucket = np.zeros(max(1, self.n_params), np.int32)
+        self.param_offset = np.zeros(max(1, self.n_params), np.int64)
+        self.bucket_offset = np.zeros(max(1, self.n_buckets), np.int64)
+        self.bucket_padded = np.zeros(max(1, self.n_buckets), np.int64)
+        _check(L.dpg_plan_export(self._h, self.param_bucket.ctypes.data,
+                                 self.param_offset.ctypes.data, self.bucket_offset.ctypes.data,
+                                 self.bucket_padded.ctypes.data))
+        self.param_bucket = self.param_bucket[: self.n_params]
+        self.param_offset = self.param_offset[: self.n_params]
+        self.bucket_offset = self.bucket_offset[: self.n_buckets]
+        self.bucket_padded = self.bucket_padded[: self.n_buckets]
+
+    @property
+    def handle(self) -> ctypes.c_void_p:
+        if self._h is None:
+            raise ValueError("plan has been destroyed")
+        return self._h
+
+    @property
+    def shard_numel(self) -> np.ndarray:
+        return self.bucket_padded // self.R
+
+    def destroy(self):
+        if getattr(self, "_h", None) is not None and _lib is not None:
+            _lib.dpg_plan_destroy(self._h)
+        self._h = None
+
+    def __del__(self):
+        try:
+            self.destroy()
+        except Exception:
+            pass
+
+
+def dpg_plan_buckets(numels: Sequence[int], cap_bytes: int, R: int) -> Plan:
+    n = np.ascontiguousarray(np.asarray(numels, dtype=np.int64).reshape(-1))
+    out = ctypes.c_void_p()
+    _check(lib().dpg_plan_buckets(n.ctypes.data if n.size else None, n.size, int(cap_bytes),
+                                  int(R), ctypes.byref(out)))
+    return Plan(out.value)
+
+
+def dpg_plan_upload(plan: Plan):
+    _check(lib().dpg_plan_upload(plan.handle))
+
+
+def dpg_plan_bucket(plan: Plan, b: int):
+    o, pd, sh = ctypes.c_int64(), ctypes.c_int64(), ctypes.c_int64()
+    _check(lib().dpg_plan_bucket(plan.handle, b, ctypes.byref(o), ctypes.byref(pd), ctypes.byref(sh)))
+    return o.value, pd.value, sh.value
+
+
+def dpg_plan_param(plan: Plan, p: int):
+    b, o, n = ctypes.c_int32(), ctypes.c_int64(), ctypes.c_int64()
+    _check(lib().dpg_plan_param(plan.handle, p, ctypes.byref(b), ctypes.byref(o), ctypes.byref(n)))
+    return b.value, o.value, n.value
+
+
+# --------------------------------------------------------------------------
+# device calls
+# --------------------------------------------------------------------------
+def dpg_pack(plan: Plan, param_grads: Sequence[Ptr], flat_bf16: Ptr, stream=None):
+    if len(param_grads) != plan.n_params:
+        raise ValueError(f"need {plan.n_params} gradients, got {len(param_grads)}")
+    _need(flat_bf16, "bf16", plan.total_padded, "flat_bf16")
+    for k, g in enumerate(param_grads):
+        _need(g, "bf16", 0, f"param_grads[{k}]")
+    _check(lib().dpg_pack(plan.handle, _ptrs(param_grads), _ptr(flat_bf16), _stream(stream)))
+
+
+def dpg_unpack(plan: Plan, flat_bf16: Ptr, param_grads: Sequence[Ptr], stream=None):
+    if len(param_grads) != plan.n_params:
+        raise ValueError(f"need {plan.n_params} gradients, got {len(param_grads)}")
+    _need(flat_bf16, "bf16", plan.total_padded, "flat_bf16")
+    for k, g in enumerate(param_grads):
+        _need(g, "bf16", 0, f"param_grads[{k}]")
+    _check(lib().dpg_unpack(plan.handle, _ptr(flat_bf16), _ptrs(param_grads), _stream(stream)))
+
+
+def dpg_accumulate(plan: Plan, flat_bf16: Ptr, acc_f32: Ptr, first: bool, stream=None):
+    _need(flat_bf16, "bf16", plan.total_padded, "flat_bf16")
+    _need(acc_f32, "f32", plan.total_padded, "acc_f32")
+    _check(lib().dpg_accumulate(plan.handle, _ptr(flat_bf16), _ptr(acc_f32), 1 if first else 0,
+                                _stream(stream)))
+
+
+def _grad_dtype(grads) -> int:
+    import torch
+    g0 = grads[0]
+    if isinstance(g0, int):
+        raise TypeError("pass grads_dtype explicitly with raw pointers")
+    return DPG_BF16 if g0.dtype == torch.bfloat16 else DPG_F32
+
+
+def dpg_reduce_scatter_adam(plan: Plan, grads: Sequence[Ptr], valid_tokens, hp: HParams,
+                            master: Ptr, exp_avg: Ptr, exp_avg_sq: Ptr,
+                            param_views: Sequence[Ptr] = (), *, last_micro: Sequence[Ptr] = None,
+                            bucket_sqnorm: Ptr = None, bucket_nonfinite: Ptr = None,
+                            reduced_grad: Ptr = None, b0: int = 0, b1: Optional[int] = None,
+                            grads_dtype: Optional[int] = None, stream=None):
+    if len(grads) != plan.R:
+        raise ValueError(f"need R={plan.R} gradient buffers, got {len(grads)}")
+    gd = _grad_dtype(grads) if grads_dtype is None else grads_dtype
+    N = plan.total_padded
+    for k, g in enumerate(grads):
+        _need(g, "bf16" if gd == DPG_BF16 else "f32", N, f"grads[{k}]")
+    for k, g in enumerate(last_micro or ()):
+        _need(g, "bf16", N, f"last_micro[{k}]")
+    for name, t in (("master", master), ("exp_avg", exp_avg), ("exp_avg_sq", exp_avg_sq),
+                    ("reduced_grad", reduced_grad)):
+        _need(t, "f32", N, name)
+    for k, t in enumerate(param_views):
+        _need(t, "bf16", N, f"param_views[{k}]")
+    _need(bucket_sqnorm, "f32", plan.n_buckets, "bucket_sqnorm")
+    tok, n_tok = _tokens(valid_tokens)
+    hpc = hp.c()
+    _check(lib().dpg_reduce_scatter_adam(
+        plan.handle, _ptrs(grads), gd, None if last_micro is None else _ptrs(last_micro),
+        tok.ctypes.data, n_tok, ctypes.byref(hpc), _ptr(master), _ptr(exp_avg), _ptr(exp_avg_sq),
+        _ptrs(param_views), len(param_views), _ptr(bucket_sqnorm), _ptr(bucket_nonfinite),
+        _ptr(reduced_grad), b0, plan.n_buckets if b1 is None else b1, _stream(stream)))
+
+
+def dpg_step(plan: Plan, grads: Sequence[Ptr], valid_tokens, hp: HParams, master: Ptr,
+             exp_avg: Ptr, exp_avg_sq: Ptr, param_views: Sequence[Ptr] = (), *,
+             last_micro: Sequence[Ptr] = None, bucket_sqnorm: Ptr = None,
+             bucket_nonfinite: Ptr = None, grads_dtype: Optional[int] = None, stream=None):
+    if len(grads) != plan.R:
+        raise ValueError(f"need R={plan.R} gradient buffers, got {len(grads)}")
+    gd = _grad_dtype(grads) if grads_dtype is None else grads_dtype
+    N = plan.total_padded
+    for k, g in enumerate(grads):
+        _need(g, "bf16" if gd == DPG_BF16 else "f32", N, f"grads[{k}]")
+    for k, g in enumerate(last_micro or ()):
+        _need(g, "bf16", N, f"last_micro[{k}]")
+    for name, t in (("master", master), ("exp_avg", exp_avg), ("exp_avg_sq", exp_avg_sq)):
+        _need(t, "f32", N, name)
+    for k, t in enumerate(param_views):
+        _need(t, "bf16", N, f"param_views[{k}]")
+    _need(bucket_sqnorm, "f32", plan.n_buckets, "bucket_sqnorm")
+    tok, n_tok = _tokens(valid_tokens)
+    hpc = hp.c()
+    _check(lib().dpg_step(
+        plan.handle, _ptrs(grads), gd, None if last_micro is None else _ptrs(last_micro),
+        tok.ctypes.data, n_tok, ctypes.byref(hpc), _ptr(master), _ptr(exp_avg), _ptr(exp_avg_sq),
+        _ptrs(param_views), len(param_views), _ptr(bucket_sqnorm), _ptr(bucket_nonfinite),
+        _stream(stream)))
+
+
+def dpg_allgather_params(plan: Plan, master: Ptr, param_views: Sequence[Ptr], *, b0: int = 0,
+                         b1: Optional[int] = None, stream=None):
+    _need(master, "f32", plan.total_padded, "master")
+    for k, t in enumerate(param_views):
+        _need(t, "bf16", plan.total_padded, f"param_views[{k}]")
+    _check(lib().dpg_allgather_params(plan.handle, _ptr(master), _ptrs(param_views),
+                                      len(param_views), b0,
+                                      plan.n_buckets if b1 is None else b1, _stream(stream)))
+
+
+def dpg_launch_count() -> int:
+    return int(lib().dpg_launch_count())
+
+
+def dpg_time_next_fused_launch(start_event, stop_event):
+    """Events are torch.cuda.Event objects already recorded once (so that
+    their CUDA handles exist), or raw cudaEvent_t integers, or None."""
+    h = lambda e: None if e is None else (e if isinstance(e, int) else e.cuda_event)
+    _check(lib().dpg_time_next_fused_launch(h(start_event), h(stop_event)))
+
+
+def dpg_abi_version() -> int:
+    return int(lib().dpg_abi_version())

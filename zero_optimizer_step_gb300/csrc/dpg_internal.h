@@ -1,0 +1,70 @@
+// dpg_internal.h -- private declarations shared by the planner (host C++) and
+// the CUDA translation unit of libdpg.  Not part of the public ABI.
+#pragma once
+
+#include <cstdint>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "dpg.h"
+
+namespace dpg {
+
+// Geometry of the fused pass.  One thread owns one 8-element vector (16 bytes
+// of bf16 gradient per replica, 32 bytes of each fp32 state array); a CTA of
+// kThreads threads covers one tile of kTile elements.  Tiles never straddle a
+// bucket (the last tile of a bucket may be partial), so every tile's norm
+// partials belong to exactly one bucket.
+constexpr int kVec = 8;
+constexpr int kThreads = 256;
+constexpr int kWarps = kThreads / 32;
+constexpr int64_t kTile = int64_t(kThreads) * kVec;
+
+// Pack/unpack work is cut into items of at most kPackChunk elements; one CTA
+// copies one item.  kPackPtrs parameter pointers travel in one launch's
+// argument block.
+constexpr int64_t kPackChunk = 8192;
+constexpr int kPackPtrs = 1024;
+
+struct PackItem {
+    int32_t param;     // registration index of the parameter
+    int32_t reserved;
+    int64_t src_off;   // element offset inside the parameter
+    int64_t flat_off;  // element offset in the flat buffer
+    int64_t count;     // elements copied
+    int64_t tail;      // zero elements written right after the copy (pack only)
+};
+
+struct Plan {
+    int32_t n_params = 0, n_buckets = 0, R = 1;
+    int64_t cap_bytes = 0, total_padded = 0, n_tiles = 0;
+    std::vector<int64_t> numels, param_offset;
+    std::vector<int32_t> param_bucket;
+    std::vector<int64_t> bucket_offset;  // n_buckets + 1 entries, last = total_padded
+    std::vector<int64_t> tile_begin;     // n_buckets + 1 entries, last = n_tiles
+    std::vector<PackItem> items;         // flat (= descending registration) order
+
+    // device copy, made on first device use
+    std::mutex mu;
+    int device = -1;
+    int64_t* d_bucket_offset = nullptr;
+    int64_t* d_tile_begin = nullptr;
+    PackItem* d_items = nullptr;
+    float* d_part_sq = nullptr;     // kWarps * n_tiles
+    int32_t* d_part_nf = nullptr;   // kWarps * n_tiles
+};
+
+// thread-local error message
+int fail(int status, const char* fmt, ...);
+void clear_error();
+
+// device side (dpg_kernels.cu)
+int upload(Plan& p);
+void release_device(Plan& p);
+
+}  // namespace dpg
+
+struct dpg_plan {
+    dpg::Plan p;
+};

@@ -1,0 +1,780 @@
+// dpg_kernels.cu -- sm_103a kernels and the device half of the libdpg C ABI.
+//
+// Everything on this path is a stream of HBM traffic with a few dozen ALU
+// operations per element, so the kernels are built for bandwidth:
+//   * one thread owns one 8-element vector: 128-bit loads of every bf16
+//     replica gradient, 256-bit loads/stores of the fp32 master/m/v state;
+//   * persistent grids (SM count x resident CTAs) striding over bucket-aligned
+//     tiles, so the whole GPU streams through the flat buffers in one wave;
+//   * the reduce-scatter, the normalisation, Adam and the bf16 all-gather are
+//     ONE pass: every byte of the step is read or written exactly once;
+//   * per-bucket squared-norm partials are warp-shuffle reductions written per
+//     (tile, warp) and summed in a fixed order by a small second kernel, so
+//     the norms are deterministic run to run.
+// Arithmetic of the update uses the IEEE round-to-nearest intrinsics
+// (__fadd_rn, __fmul_rn, __fdiv_rn, __fsqrt_rn, __fsub_rn), which the compiler
+// never contracts into FMAs, in the order of Kingma & Ba's Algorithm 1.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+#include <map>
+#include <mutex>
+#include <utility>
+
+#include "dpg_internal.h"
+
+namespace dpg {
+
+static std::atomic<int64_t> g_launches{0};
+static thread_local cudaEvent_t t_fused_start = nullptr, t_fused_stop = nullptr;
+
+#define DPG_CUDA_TRY(call)                                                              \
+    do {                                                                                \
+        cudaError_t e_ = (call);                                                        \
+        if (e_ != cudaSuccess)                                                          \
+            return fail(DPG_ERR_CUDA, "%s: %s (%s)", __func__, cudaGetErrorString(e_),  \
+                        #call);                                                         \
+    } while (0)
+
+// ---------------------------------------------------------------------------
+// memory access: streaming vector loads and stores (inline PTX)
+// ---------------------------------------------------------------------------
+struct F8 {
+    float v[8];
+};
+
+// read-only gradient stream: bypass L1, first to leave L2
+__device__ __forceinline__ uint4 ld_grad_u4(const void* p) {
+    uint4 r;
+    asm("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+        : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+        : "l"(p));
+    return r;
+}
+
+__device__ __forceinline__ F8 ld_grad_f8(const float* p) {
+    F8 r;
+    asm("ld.global.nc.L1::no_allocate.L2::evict_first.v8.f32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+        : "=f"(r.v[0]), "=f"(r.v[1]), "=f"(r.v[2]), "=f"(r.v[3]), "=f"(r.v[4]), "=f"(r.v[5]),
+          "=f"(r.v[6]), "=f"(r.v[7])
+        : "l"(p));
+    return r;
+}
+
+// read-modify-write state (master / m / v / accumulation buffer)
+__device__ __forceinline__ F8 ld_state_f8(const float* p) {
+    F8 r;
+    asm("ld.global.L1::no_allocate.L2::evict_first.v8.f32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+        : "=f"(r.v[0]), "=f"(r.v[1]), "=f"(r.v[2]), "=f"(r.v[3]), "=f"(r.v[4]), "=f"(r.v[5]),
+          "=f"(r.v[6]), "=f"(r.v[7])
+        : "l"(p));
+    return r;
+}
+
+__device__ __forceinline__ void st_f8(float* p, const F8& x) {
+    asm volatile("st.global.L1::no_allocate.v8.f32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(p),
+                 "f"(x.v[0]), "f"(x.v[1]), "f"(x.v[2]), "f"(x.v[3]), "f"(x.v[4]), "f"(x.v[5]),
+                 "f"(x.v[6]), "f"(x.v[7]));
+}
+
+__device__ __forceinline__ void st_u4(void* p, uint4 x) {
+    asm volatile("st.global.L1::no_allocate.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(x.x),
+                 "r"(x.y), "r"(x.z), "r"(x.w));
+}
+
+// bf16 pair (low half = lower address) -> two exact fp32 values
+__device__ __forceinline__ void widen2(uint32_t u, float& lo, float& hi) {
+    lo = __uint_as_float(u << 16);
+    hi = __uint_as_float(u & 0xFFFF0000u);
+}
+
+__device__ __forceinline__ void widen8(uint4 x, float* f) {
+    widen2(x.x, f[0], f[1]);
+    widen2(x.y, f[2], f[3]);
+    widen2(x.z, f[4], f[5]);
+    widen2(x.w, f[6], f[7]);
+}
+
+// eight fp32 -> eight bf16 (round to nearest even), packed for a 128-bit store
+__device__ __forceinline__ uint4 narrow8(const float* f) {
+    uint4 r;
+    __nv_bfloat162 h;
+    h = __floats2bfloat162_rn(f[0], f[1]);
+    r.x = *reinterpret_cast<uint32_t*>(&h);
+    h = __floats2bfloat162_rn(f[2], f[3]);
+    r.y = *reinterpret_cast<uint32_t*>(&h);
+    h = __floats2bfloat162_rn(f[4], f[5]);
+    r.z = *reinterpret_cast<uint32_t*>(&h);
+    h = __floats2bfloat162_rn(f[6], f[7]);
+    r.w = *reinterpret_cast<uint32_t*>(&h);
+    return r;
+}
+
+// ---------------------------------------------------------------------------
+// fused reduce-scatter -> scale -> Adam -> all-gather
+// ---------------------------------------------------------------------------
+enum : int { kInBf16 = 0, kInF32 = 1, kInF32PlusBf16 = 2 };
+
+struct RsAdamArgs {
+    const void* grads[DPG_MAX_REPLICAS];
+    const void* last[DPG_MAX_REPLICAS];
+    void* views[DPG_MAX_VIEWS];
+    float* master;
+    float* m;
+    float* v;
+    float* reduced;      // nullable
+    float* part_sq;      // nullable (no norm requested)
+    int32_t* part_nf;
+    const int64_t* bucket_offset;
+    const int64_t* tile_begin;
+    int64_t t0, t1;      // tile range of buckets [b0, b1)
+    int32_t b0, b1;
+    int32_t R, n_views;
+    float scale;         // fp32(1/G)
+    float beta1, beta2, omb1, omb2, bias1, bias2, lr, eps, lr_wd;
+    int32_t decay;
+};
+
+// Bucket holding tile t, searching forward from bucket b (tile_begin[b] <= t
+// and t < tile_begin[b_end] hold on entry).  Empty buckets are skipped.
+__device__ __forceinline__ int bucket_of_tile(const int64_t* tile_begin, int b, int b_end,
+                                              int64_t t) {
+    if (t < __ldg(tile_begin + b + 1)) return b;
+    int lo = b + 1, hi = b_end;
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (__ldg(tile_begin + mid) <= t) lo = mid;
+        else hi = mid;
+    }
+    return lo;
+}
+
+// x_r widened (and, for the accumulation path, plus the last microbatch),
+// summed in rank order 0..R-1 in binary32.
+template <int RT, int MODE>
+__device__ __forceinline__ void reduce_vector(const RsAdamArgs& a, int64_t i, float* s) {
+    const int R = RT > 0 ? RT : a.R;
+    if constexpr (MODE == kInBf16) {
+        if constexpr (RT > 0) {
+            uint4 x[RT];
+#pragma unroll
+            for (int r = 0; r < RT; ++r)
+                x[r] = ld_grad_u4(static_cast<const uint16_t*>(a.grads[r]) + i);
+            widen8(x[0], s);
+#pragma unroll
+            for (int r = 1; r < RT; ++r) {
+                float t[8];
+                widen8(x[r], t);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) s[j] = __fadd_rn(s[j], t[j]);
+            }
+        } else {
+            widen8(ld_grad_u4(static_cast<const uint16_t*>(a.grads[0]) + i), s);
+#pragma unroll 4
+            for (int r = 1; r < R; ++r) {
+                float t[8];
+                widen8(ld_grad_u4(static_cast<const uint16_t*>(a.grads[r]) + i), t);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) s[j] = __fadd_rn(s[j], t[j]);
+            }
+        }
+    } else {
+        // fp32 accumulation buffers (optionally + the final bf16 microbatch)
+#pragma unroll(RT > 0 ? RT : 2)
+        for (int r = 0; r < R; ++r) {
+            F8 x = ld_grad_f8(static_cast<const float*>(a.grads[r]) + i);
+            if constexpr (MODE == kInF32PlusBf16) {
+                float t[8];
+                widen8(ld_grad_u4(static_cast<const uint16_t*>(a.last[r]) + i), t);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) x.v[j] = __fadd_rn(x.v[j], t[j]);
+            }
+            if (r == 0) {
+#pragma unroll
+                for (int j = 0; j < 8; ++j) s[j] = x.v[j];
+            } else {
+#pragma unroll
+                for (int j = 0; j < 8; ++j) s[j] = __fadd_rn(s[j], x.v[j]);
+            }
+        }
+    }
+}
+
+template <int RT, int MODE>
+__global__ void __launch_bounds__(kThreads, 2) k_rs_adam(const __grid_constant__ RsAdamArgs a) {
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    int b = a.b0;
+    for (int64_t t = a.t0 + blockIdx.x; t < a.t1; t += gridDim.x) {
+        b = bucket_of_tile(a.tile_begin, b, a.b1, t);
+        const int64_t bucket_end = __ldg(a.bucket_offset + b + 1);
+        const int64_t i = __ldg(a.bucket_offset + b) + (t - __ldg(a.tile_begin + b)) * kTile +
+                          int64_t(threadIdx.x) * kVec;
+        float sq = 0.0f;
+        int nf = 0;
+        if (i < bucket_end) {
+            float s[8];
+            reduce_vector<RT, MODE>(a, i, s);
+            F8 w = ld_state_f8(a.master + i);
+            F8 m = ld_state_f8(a.m + i);
+            F8 v = ld_state_f8(a.v + i);
+            float g[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                g[j] = __fmul_rn(s[j], a.scale);
+                float wj = w.v[j];
+                if (a.decay) wj = __fsub_rn(wj, __fmul_rn(a.lr_wd, wj));
+                const float mj = __fadd_rn(__fmul_rn(a.beta1, m.v[j]), __fmul_rn(a.omb1, g[j]));
+                const float vj =
+                    __fadd_rn(__fmul_rn(a.beta2, v.v[j]), __fmul_rn(a.omb2, __fmul_rn(g[j], g[j])));
+                const float m_hat = __fdiv_rn(mj, a.bias1);
+                const float v_hat = __fdiv_rn(vj, a.bias2);
+                const float u = __fdiv_rn(m_hat, __fadd_rn(__fsqrt_rn(v_hat), a.eps));
+                w.v[j] = __fsub_rn(wj, __fmul_rn(a.lr, u));
+                m.v[j] = mj;
+                v.v[j] = vj;
+                sq = fmaf(g[j], g[j], sq);
+                nf += (__float_as_uint(g[j]) & 0x7F800000u) == 0x7F800000u;
+            }
+            st_f8(a.master + i, w);
+            st_f8(a.m + i, m);
+            st_f8(a.v + i, v);
+            const uint4 p = narrow8(w.v);
+            for (int k = 0; k < a.n_views; ++k) st_u4(static_cast<uint16_t*>(a.views[k]) + i, p);
+            if (a.reduced) {
+                F8 gg;
+#pragma unroll
+                for (int j = 0; j < 8; ++j) gg.v[j] = g[j];
+                st_f8(a.reduced + i, gg);
+            }
+        }
+        if (a.part_sq) {
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+                sq += __shfl_xor_sync(0xFFFFFFFFu, sq, o);
+                nf += __shfl_xor_sync(0xFFFFFFFFu, nf, o);
+            }
+            if (lane == 0) {
+                a.part_sq[t * kWarps + warp] = sq;
+                a.part_nf[t * kWarps + warp] = nf;
+            }
+        }
+    }
+}
+
+// One CTA per bucket: sum the bucket's (tile, warp) partials in a fixed order
+// (double), so the result does not depend on scheduling.
+__global__ void __launch_bounds__(256) k_norm_finalize(const float* __restrict__ part_sq,
+                                                       const int32_t* __restrict__ part_nf,
+                                                       const int64_t* __restrict__ tile_begin,
+                                                       int32_t b0, float* sqnorm,
+                                                       int64_t* nonfinite) {
+    __shared__ double s_sq[256];
+    __shared__ long long s_nf[256];
+    const int b = b0 + blockIdx.x;
+    const int64_t lo = tile_begin[b] * kWarps, hi = tile_begin[b + 1] * kWarps;
+    double acc = 0.0;
+    long long cnt = 0;
+    for (int64_t k = lo + threadIdx.x; k < hi; k += blockDim.x) {
+        acc += double(part_sq[k]);
+        cnt += part_nf[k];
+    }
+    s_sq[threadIdx.x] = acc;
+    s_nf[threadIdx.x] = cnt;
+    __syncthreads();
+    for (int w = 128; w > 0; w >>= 1) {
+        if (threadIdx.x < w) {
+            s_sq[threadIdx.x] += s_sq[threadIdx.x + w];
+            s_nf[threadIdx.x] += s_nf[threadIdx.x + w];
+        }
+        __syncthreads();
+    }
+    if (threadIdx.x == 0) {
+        if (sqnorm) sqnorm[b] = float(s_sq[0]);
+        if (nonfinite) nonfinite[b] = s_nf[0];
+    }
+}
+
+// ---------------------------------------------------------------------------
+// no_sync accumulation and the stand-alone all-gather
+// ---------------------------------------------------------------------------
+template <bool FIRST>
+__global__ void __launch_bounds__(256) k_accumulate(const uint16_t* __restrict__ g,
+                                                    float* __restrict__ acc, int64_t n_vec) {
+    for (int64_t k = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; k < n_vec;
+         k += int64_t(gridDim.x) * blockDim.x) {
+        const int64_t i = k * kVec;
+        float x[8];
+        widen8(ld_grad_u4(g + i), x);
+        F8 r;
+        if (FIRST) {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) r.v[j] = x[j];
+        } else {
+            const F8 a = ld_state_f8(acc + i);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) r.v[j] = __fadd_rn(a.v[j], x[j]);
+        }
+        st_f8(acc + i, r);
+    }
+}
+
+struct ViewArgs {
+    void* views[DPG_MAX_VIEWS];
+    int32_t n_views;
+};
+
+__global__ void __launch_bounds__(256) k_allgather(const float* __restrict__ master,
+                                                   const __grid_constant__ ViewArgs va,
+                                                   int64_t lo_vec, int64_t hi_vec) {
+    for (int64_t k = lo_vec + int64_t(blockIdx.x) * blockDim.x + threadIdx.x; k < hi_vec;
+         k += int64_t(gridDim.x) * blockDim.x) {
+        const int64_t i = k * kVec;
+        const F8 w = ld_grad_f8(master + i);
+        const uint4 p = narrow8(w.v);
+        for (int v = 0; v < va.n_views; ++v) st_u4(static_cast<uint16_t*>(va.views[v]) + i, p);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// pack / unpack: one CTA per item (<= kPackChunk elements of one parameter)
+// ---------------------------------------------------------------------------
+struct PackArgs {
+    const void* ptrs[kPackPtrs];  // parameter gradients p_base .. p_base + kPackPtrs - 1
+    int32_t p_base;
+    int32_t unpack;
+    const PackItem* items;
+    int64_t item0;
+    uint16_t* flat;
+};
+
+__device__ __forceinline__ void copy_elems(uint16_t* dst, const uint16_t* src, int64_t n) {
+    const bool vec = ((reinterpret_cast<uintptr_t>(dst) | reinterpret_cast<uintptr_t>(src)) & 15) == 0;
+    int64_t done = 0;
+    if (vec) {
+        const int64_t nv = n / kVec;
+        const uint4* s4 = reinterpret_cast<const uint4*>(src);
+        uint4* d4 = reinterpret_cast<uint4*>(dst);
+        for (int64_t k = threadIdx.x; k < nv; k += blockDim.x) d4[k] = s4[k];
+        done = nv * kVec;
+    }
+    for (int64_t k = done + threadIdx.x; k < n; k += blockDim.x) dst[k] = src[k];
+}
+
+__global__ void __launch_bounds__(256) k_pack(const __grid_constant__ PackArgs a) {
+    const PackItem it = a.items[a.item0 + blockIdx.x];
+    uint16_t* param = static_cast<uint16_t*>(const_cast<void*>(a.ptrs[it.param - a.p_base]));
+    uint16_t* flat = a.flat + it.flat_off;
+    if (!a.unpack) {
+        if (it.count > 0) copy_elems(flat, param + it.src_off, it.count);
+        for (int64_t k = threadIdx.x; k < it.tail; k += blockDim.x) flat[it.count + k] = 0;
+    } else if (it.count > 0) {
+        copy_elems(param + it.src_off, flat, it.count);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// host helpers
+// ---------------------------------------------------------------------------
+static int sm_count(int dev, int* out) {
+    static std::mutex mu;
+    static std::map<int, int> cache;
+    std::lock_guard<std::mutex> g(mu);
+    auto it = cache.find(dev);
+    if (it == cache.end()) {
+        int n = 0;
+        DPG_CUDA_TRY(cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev));
+        it = cache.emplace(dev, n).first;
+    }
+    *out = it->second;
+    return DPG_OK;
+}
+
+// persistent-grid size: SM count x resident CTAs of `fn` (cached per device)
+static int grid_for(const void* fn, int threads, int dev, int64_t work_ctas, int* grid) {
+    static std::mutex mu;
+    static std::map<std::pair<const void*, int>, int> cache;
+    int sms = 0;
+    int st = sm_count(dev, &sms);
+    if (st != DPG_OK) return st;
+    int per_sm = 0;
+    {
+        std::lock_guard<std::mutex> g(mu);
+        auto key = std::make_pair(fn, dev);
+        auto it = cache.find(key);
+        if (it == cache.end()) {
+            DPG_CUDA_TRY(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, threads, 0));
+            if (per_sm < 1) per_sm = 1;
+            it = cache.emplace(key, per_sm).first;
+        }
+        per_sm = it->second;
+    }
+    const int64_t full = int64_t(sms) * per_sm;
+    *grid = int(work_ctas < full ? (work_ctas > 0 ? work_ctas : 1) : full);
+    return DPG_OK;
+}
+
+static bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+static int after_launch(const char* what) {
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return fail(DPG_ERR_CUDA, "%s: launch failed: %s", what, cudaGetErrorString(e));
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+    return DPG_OK;
+}
+
+int upload(Plan& p) {
+    std::lock_guard<std::mutex> g(p.mu);
+    int dev = 0;
+    DPG_CUDA_TRY(cudaGetDevice(&dev));
+    if (p.device >= 0) {
+        if (p.device != dev)
+            return fail(DPG_ERR_INVALID_ARG,
+                        "plan tables live on device %d but device %d is current", p.device, dev);
+        return DPG_OK;
+    }
+    const size_t nb1 = size_t(p.n_buckets) + 1;
+    const size_t n_items = p.items.size() ? p.items.size() : 1;
+    const size_t n_part = size_t(p.n_tiles) * kWarps ? size_t(p.n_tiles) * kWarps : 1;
+    void *bo = nullptr, *tb = nullptr, *it = nullptr, *ps = nullptr, *pn = nullptr;
+    cudaError_t e = cudaSuccess;
+    if (e == cudaSuccess) e = cudaMalloc(&bo, nb1 * sizeof(int64_t));
+    if (e == cudaSuccess) e = cudaMalloc(&tb, nb1 * sizeof(int64_t));
+    if (e == cudaSuccess) e = cudaMalloc(&it, n_items * sizeof(PackItem));
+    if (e == cudaSuccess) e = cudaMalloc(&ps, n_part * sizeof(float));
+    if (e == cudaSuccess) e = cudaMalloc(&pn, n_part * sizeof(int32_t));
+    if (e == cudaSuccess) e = cudaMemcpy(bo, p.bucket_offset.data(), nb1 * sizeof(int64_t), cudaMemcpyHostToDevice);
+    if (e == cudaSuccess) e = cudaMemcpy(tb, p.tile_begin.data(), nb1 * sizeof(int64_t), cudaMemcpyHostToDevice);
+    if (e == cudaSuccess && !p.items.empty())
+        e = cudaMemcpy(it, p.items.data(), p.items.size() * sizeof(PackItem), cudaMemcpyHostToDevice);
+    if (e != cudaSuccess) {
+        cudaFree(bo); cudaFree(tb); cudaFree(it); cudaFree(ps); cudaFree(pn);
+        cudaGetLastError();
+        return fail(e == cudaErrorMemoryAllocation ? DPG_ERR_OOM : DPG_ERR_CUDA,
+                    "plan upload: %s", cudaGetErrorString(e));
+    }
+    p.d_bucket_offset = static_cast<int64_t*>(bo);
+    p.d_tile_begin = static_cast<int64_t*>(tb);
+    p.d_items = static_cast<PackItem*>(it);
+    p.d_part_sq = static_cast<float*>(ps);
+    p.d_part_nf = static_cast<int32_t*>(pn);
+    p.device = dev;
+    return DPG_OK;
+}
+
+void release_device(Plan& p) {
+    std::lock_guard<std::mutex> g(p.mu);
+    if (p.device < 0) return;
+    int cur = -1;
+    const bool have_cur = cudaGetDevice(&cur) == cudaSuccess;
+    if (cudaSetDevice(p.device) == cudaSuccess) {
+        cudaFree(p.d_bucket_offset);
+        cudaFree(p.d_tile_begin);
+        cudaFree(p.d_items);
+        cudaFree(p.d_part_sq);
+        cudaFree(p.d_part_nf);
+    }
+    if (have_cur) cudaSetDevice(cur);
+    cudaGetLastError();
+    p.device = -1;
+}
+
+// fp32 Adam constants, each computed in double and rounded once
+static int adam_constants(const dpg_hparams* hp, RsAdamArgs& a) {
+    if (!hp) return fail(DPG_ERR_INVALID_ARG, "hparams is NULL");
+    if (hp->step < 1) return fail(DPG_ERR_INVALID_ARG, "hparams.step must be >= 1 (got %lld)", (long long)hp->step);
+    if (!(hp->beta1 >= 0.0 && hp->beta1 < 1.0) || !(hp->beta2 >= 0.0 && hp->beta2 < 1.0))
+        return fail(DPG_ERR_INVALID_ARG, "betas must lie in [0, 1)");
+    const double t = double(hp->step);
+    a.beta1 = float(hp->beta1);
+    a.beta2 = float(hp->beta2);
+    a.omb1 = float(1.0 - hp->beta1);
+    a.omb2 = float(1.0 - hp->beta2);
+    a.bias1 = float(1.0 - std::pow(hp->beta1, t));
+    a.bias2 = float(1.0 - std::pow(hp->beta2, t));
+    a.lr = float(hp->lr);
+    a.eps = float(hp->eps);
+    a.lr_wd = float(hp->lr * hp->weight_decay);
+    a.decay = hp->weight_decay != 0.0;
+    return DPG_OK;
+}
+
+// fp32(1/G) with G the int64 sum of the valid-token counts
+static int token_scale(const int64_t* tokens, int32_t n, float* scale) {
+    if (!tokens || n < 1) return fail(DPG_ERR_INVALID_ARG, "valid_tokens must hold >= 1 count");
+    int64_t G = 0;
+    for (int32_t k = 0; k < n; ++k) {
+        if (tokens[k] < 0) return fail(DPG_ERR_INVALID_ARG, "valid_tokens[%d] < 0", k);
+        if (__builtin_add_overflow(G, tokens[k], &G))
+            return fail(DPG_ERR_INVALID_ARG, "valid-token sum overflows int64");
+    }
+    if (G == 0) return fail(DPG_ERR_ZERO_TOKENS, "global valid-token count is 0");
+    *scale = float(1.0 / double(G));
+    return DPG_OK;
+}
+
+using RsKernel = void (*)(RsAdamArgs);
+
+template <int MODE>
+static RsKernel pick_rs_kernel(int R) {
+    switch (R) {
+        case 1: return k_rs_adam<1, MODE>;
+        case 2: return k_rs_adam<2, MODE>;
+        case 4: return k_rs_adam<4, MODE>;
+        case 8: return k_rs_adam<8, MODE>;
+        default: return k_rs_adam<0, MODE>;
+    }
+}
+
+static int rs_adam(const dpg_plan_t* plan, const void* const* grads, int32_t grads_dtype,
+                   const void* const* last, const int64_t* tokens, int32_t n_counts,
+                   const dpg_hparams* hp, float* master, float* m, float* v,
+                   void* const* views, int32_t n_views, float* sqnorm, int64_t* nonfinite,
+                   float* reduced, int32_t b0, int32_t b1, void* stream, const char* who) {
+    if (!plan) return fail(DPG_ERR_INVALID_ARG, "%s: plan is NULL", who);
+    Plan& p = const_cast<dpg_plan_t*>(plan)->p;
+    if (b0 < 0 || b1 < b0 || b1 > p.n_buckets)
+        return fail(DPG_ERR_INVALID_ARG, "%s: bucket range [%d, %d) outside [0, %d]", who, b0, b1,
+                    p.n_buckets);
+    if (grads_dtype != DPG_BF16 && grads_dtype != DPG_F32)
+        return fail(DPG_ERR_INVALID_ARG, "%s: grads_dtype %d unknown", who, grads_dtype);
+    if (last && grads_dtype != DPG_F32)
+        return fail(DPG_ERR_INVALID_ARG, "%s: last_micro_bf16 needs fp32 accumulation grads", who);
+    if (n_views < 0 || n_views > DPG_MAX_VIEWS)
+        return fail(DPG_ERR_INVALID_ARG, "%s: n_views %d outside [0, %d]", who, n_views, DPG_MAX_VIEWS);
+    RsAdamArgs a{};
+    int st = adam_constants(hp, a);
+    if (st != DPG_OK) return st;
+    st = token_scale(tokens, n_counts, &a.scale);
+    if (st != DPG_OK) return st;
+    if (b0 == b1) return DPG_OK;  // nothing to update; buffers are not touched
+    if (!grads) return fail(DPG_ERR_INVALID_ARG, "%s: grads is NULL", who);
+    if (!master || !m || !v) return fail(DPG_ERR_INVALID_ARG, "%s: master/m/v must not be NULL", who);
+    if (n_views > 0 && !views) return fail(DPG_ERR_INVALID_ARG, "%s: param_views is NULL", who);
+    const uintptr_t galign = grads_dtype == DPG_BF16 ? 16 : 32;
+    for (int r = 0; r < p.R; ++r) {
+        if (!grads[r]) return fail(DPG_ERR_INVALID_ARG, "%s: grads[%d] is NULL", who, r);
+        if (!aligned(grads[r], galign)) return fail(DPG_ERR_MISALIGNED, "%s: grads[%d] misaligned", who, r);
+        a.grads[r] = grads[r];
+        if (last) {
+            if (!last[r]) return fail(DPG_ERR_INVALID_ARG, "%s: last_micro_bf16[%d] is NULL", who, r);
+            if (!aligned(last[r], 16)) return fail(DPG_ERR_MISALIGNED, "%s: last_micro_bf16[%d] misaligned", who, r);
+            a.last[r] = last[r];
+        }
+    }
+    for (int k = 0; k < n_views; ++k) {
+        if (!views[k]) return fail(DPG_ERR_INVALID_ARG, "%s: param_views[%d] is NULL", who, k);
+        if (!aligned(views[k], 16)) return fail(DPG_ERR_MISALIGNED, "%s: param_views[%d] misaligned", who, k);
+        a.views[k] = views[k];
+    }
+    if (!aligned(master, 32) || !aligned(m, 32) || !aligned(v, 32) || !aligned(reduced, 32))
+        return fail(DPG_ERR_MISALIGNED, "%s: fp32 buffers must be 32-byte aligned", who);
+    st = upload(p);
+    if (st != DPG_OK) return st;
+
+    a.master = master;
+    a.m = m;
+    a.v = v;
+    a.reduced = reduced;
+    const bool want_norm = sqnorm || nonfinite;
+    a.part_sq = want_norm ? p.d_part_sq : nullptr;
+    a.part_nf = want_norm ? p.d_part_nf : nullptr;
+    a.bucket_offset = p.d_bucket_offset;
+    a.tile_begin = p.d_tile_begin;
+    a.t0 = p.tile_begin[b0];
+    a.t1 = p.tile_begin[b1];
+    a.b0 = b0;
+    a.b1 = b1;
+    a.R = p.R;
+    a.n_views = n_views;
+    const int mode = grads_dtype == DPG_BF16 ? kInBf16 : (last ? kInF32PlusBf16 : kInF32);
+    RsKernel fn = mode == kInBf16 ? pick_rs_kernel<kInBf16>(p.R)
+                : mode == kInF32 ? pick_rs_kernel<kInF32>(p.R)
+                                 : pick_rs_kernel<kInF32PlusBf16>(p.R);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (a.t1 > a.t0) {
+        int grid = 0;
+        st = grid_for(reinterpret_cast<const void*>(fn), kThreads, p.device, a.t1 - a.t0, &grid);
+        if (st != DPG_OK) return st;
+        cudaEvent_t ev0 = t_fused_start, ev1 = t_fused_stop;
+        t_fused_start = t_fused_stop = nullptr;
+        if (ev0) DPG_CUDA_TRY(cudaEventRecord(ev0, s));
+        fn<<<grid, kThreads, 0, s>>>(a);
+        st = after_launch(who);
+        if (st != DPG_OK) return st;
+        if (ev1) DPG_CUDA_TRY(cudaEventRecord(ev1, s));
+    }
+    if (want_norm) {
+        k_norm_finalize<<<b1 - b0, 256, 0, s>>>(p.d_part_sq, p.d_part_nf, p.d_tile_begin, b0,
+                                                 sqnorm, nonfinite);
+        st = after_launch(who);
+        if (st != DPG_OK) return st;
+    }
+    return DPG_OK;
+}
+
+}  // namespace dpg
+
+using dpg::fail;
+
+extern "C" {
+
+int64_t dpg_launch_count(void) { return dpg::g_launches.load(); }
+
+int dpg_time_next_fused_launch(void* start_event, void* stop_event) {
+    dpg::clear_error();
+    if ((start_event == nullptr) != (stop_event == nullptr))
+        return fail(DPG_ERR_INVALID_ARG, "dpg_time_next_fused_launch: give both events or neither");
+    dpg::t_fused_start = static_cast<cudaEvent_t>(start_event);
+    dpg::t_fused_stop = static_cast<cudaEvent_t>(stop_event);
+    return DPG_OK;
+}
+
+int dpg_plan_upload(dpg_plan_t* plan) {
+    dpg::clear_error();
+    if (!plan) return fail(DPG_ERR_INVALID_ARG, "dpg_plan_upload: plan is NULL");
+    return dpg::upload(plan->p);
+}
+
+int dpg_reduce_scatter_adam(const dpg_plan_t* plan, const void* const* grads, int32_t grads_dtype,
+                            const void* const* last_micro_bf16, const int64_t* valid_tokens,
+                            int32_t n_counts, const dpg_hparams* hp, float* master,
+                            float* exp_avg, float* exp_avg_sq, void* const* param_views,
+                            int32_t n_views, float* bucket_sqnorm, int64_t* bucket_nonfinite,
+                            float* reduced_grad, int32_t b0, int32_t b1, void* stream) {
+    dpg::clear_error();
+    return dpg::rs_adam(plan, grads, grads_dtype, last_micro_bf16, valid_tokens, n_counts, hp,
+                        master, exp_avg, exp_avg_sq, param_views, n_views, bucket_sqnorm,
+                        bucket_nonfinite, reduced_grad, b0, b1, stream, "dpg_reduce_scatter_adam");
+}
+
+int dpg_step(const dpg_plan_t* plan, const void* const* grads, int32_t grads_dtype,
+             const void* const* last_micro_bf16, const int64_t* valid_tokens, int32_t n_counts,
+             const dpg_hparams* hp, float* master, float* exp_avg, float* exp_avg_sq,
+             void* const* param_views, int32_t n_views, float* bucket_sqnorm,
+             int64_t* bucket_nonfinite, void* stream) {
+    dpg::clear_error();
+    if (!plan) return fail(DPG_ERR_INVALID_ARG, "dpg_step: plan is NULL");
+    return dpg::rs_adam(plan, grads, grads_dtype, last_micro_bf16, valid_tokens, n_counts, hp,
+                        master, exp_avg, exp_avg_sq, param_views, n_views, bucket_sqnorm,
+                        bucket_nonfinite, nullptr, 0, plan->p.n_buckets, stream, "dpg_step");
+}
+
+int dpg_accumulate(const dpg_plan_t* plan, const void* flat_bf16, float* acc_f32, int32_t first,
+                   void* stream) {
+    dpg::clear_error();
+    if (!plan) return fail(DPG_ERR_INVALID_ARG, "dpg_accumulate: plan is NULL");
+    if (plan->p.total_padded == 0) return DPG_OK;
+    if (!flat_bf16 || !acc_f32) return fail(DPG_ERR_INVALID_ARG, "dpg_accumulate: NULL buffer");
+    if (!dpg::aligned(flat_bf16, 16) || !dpg::aligned(acc_f32, 32))
+        return fail(DPG_ERR_MISALIGNED, "dpg_accumulate: misaligned buffer");
+    dpg::Plan& p = const_cast<dpg_plan_t*>(plan)->p;
+    const int64_t n_vec = p.total_padded / dpg::kVec;
+    if (n_vec == 0) return DPG_OK;
+    int dev = 0;
+    DPG_CUDA_TRY(cudaGetDevice(&dev));
+    const void* fn = first ? reinterpret_cast<const void*>(dpg::k_accumulate<true>)
+                           : reinterpret_cast<const void*>(dpg::k_accumulate<false>);
+    int grid = 0;
+    int st = dpg::grid_for(fn, 256, dev, (n_vec + 255) / 256, &grid);
+    if (st != DPG_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const uint16_t* g = static_cast<const uint16_t*>(flat_bf16);
+    if (first) dpg::k_accumulate<true><<<grid, 256, 0, s>>>(g, acc_f32, n_vec);
+    else dpg::k_accumulate<false><<<grid, 256, 0, s>>>(g, acc_f32, n_vec);
+    return dpg::after_launch("dpg_accumulate");
+}
+
+int dpg_allgather_params(const dpg_plan_t* plan, const float* master, void* const* views,
+                         int32_t n_views, int32_t b0, int32_t b1, void* stream) {
+    dpg::clear_error();
+    if (!plan) return fail(DPG_ERR_INVALID_ARG, "dpg_allgather_params: plan is NULL");
+    const dpg::Plan& p = plan->p;
+    if (b0 < 0 || b1 < b0 || b1 > p.n_buckets)
+        return fail(DPG_ERR_INVALID_ARG, "dpg_allgather_params: bucket range [%d, %d) outside [0, %d]",
+                    b0, b1, p.n_buckets);
+    if (n_views < 0 || n_views > DPG_MAX_VIEWS)
+        return fail(DPG_ERR_INVALID_ARG, "dpg_allgather_params: n_views %d outside [0, %d]", n_views,
+                    DPG_MAX_VIEWS);
+    if (b0 == b1 || n_views == 0 || p.bucket_offset[b1] == p.bucket_offset[b0]) return DPG_OK;
+    if (!master) return fail(DPG_ERR_INVALID_ARG, "dpg_allgather_params: master is NULL");
+    if (!dpg::aligned(master, 32)) return fail(DPG_ERR_MISALIGNED, "dpg_allgather_params: master misaligned");
+    if (n_views > 0 && !views) return fail(DPG_ERR_INVALID_ARG, "dpg_allgather_params: views is NULL");
+    dpg::ViewArgs va{};
+    va.n_views = n_views;
+    for (int k = 0; k < n_views; ++k) {
+        if (!views[k]) return fail(DPG_ERR_INVALID_ARG, "dpg_allgather_params: views[%d] is NULL", k);
+        if (!dpg::aligned(views[k], 16))
+            return fail(DPG_ERR_MISALIGNED, "dpg_allgather_params: views[%d] misaligned", k);
+        va.views[k] = views[k];
+    }
+    const int64_t lo = p.bucket_offset[b0] / dpg::kVec, hi = p.bucket_offset[b1] / dpg::kVec;
+    if (hi <= lo || n_views == 0) return DPG_OK;
+    int dev = 0;
+    DPG_CUDA_TRY(cudaGetDevice(&dev));
+    int grid = 0;
+    int st = dpg::grid_for(reinterpret_cast<const void*>(dpg::k_allgather), 256, dev,
+                           (hi - lo + 255) / 256, &grid);
+    if (st != DPG_OK) return st;
+    dpg::k_allgather<<<grid, 256, 0, static_cast<cudaStream_t>(stream)>>>(master, va, lo, hi);
+    return dpg::after_launch("dpg_allgather_params");
+}
+
+static int pack_common(const dpg_plan_t* plan, const void* const* ptrs, void* flat, int unpack,
+                       void* stream, const char* who) {
+    if (!plan) return fail(DPG_ERR_INVALID_ARG, "%s: plan is NULL", who);
+    dpg::Plan& p = const_cast<dpg_plan_t*>(plan)->p;
+    if (!flat && p.total_padded > 0) return fail(DPG_ERR_INVALID_ARG, "%s: flat buffer is NULL", who);
+    if (!dpg::aligned(flat, 16)) return fail(DPG_ERR_MISALIGNED, "%s: flat buffer misaligned", who);
+    if (p.n_params > 0 && !ptrs) return fail(DPG_ERR_INVALID_ARG, "%s: gradient table is NULL", who);
+    for (int32_t q = 0; q < p.n_params; ++q) {
+        if (p.numels[q] > 0 && !ptrs[q]) return fail(DPG_ERR_INVALID_ARG, "%s: gradient %d is NULL", who, q);
+        if (!dpg::aligned(ptrs[q], 2)) return fail(DPG_ERR_MISALIGNED, "%s: gradient %d misaligned", who, q);
+    }
+    if (p.items.empty()) return DPG_OK;
+    int st = dpg::upload(p);
+    if (st != DPG_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    // items are in descending parameter order; launch one window of
+    // kPackPtrs parameters at a time
+    size_t i0 = 0;
+    while (i0 < p.items.size()) {
+        const int32_t top = p.items[i0].param;
+        const int32_t base = top - dpg::kPackPtrs + 1 > 0 ? top - dpg::kPackPtrs + 1 : 0;
+        size_t i1 = i0;
+        while (i1 < p.items.size() && p.items[i1].param >= base) ++i1;
+        dpg::PackArgs a{};
+        for (int32_t q = base; q <= top; ++q) a.ptrs[q - base] = ptrs[q];
+        a.p_base = base;
+        a.unpack = unpack;
+        a.items = p.d_items;
+        a.item0 = int64_t(i0);
+        a.flat = static_cast<uint16_t*>(flat);
+        int64_t n = int64_t(i1 - i0);
+        for (int64_t off = 0; off < n; off += 65535 * 1024LL) {
+            const int64_t chunk = n - off < 65535 * 1024LL ? n - off : 65535 * 1024LL;
+            a.item0 = int64_t(i0) + off;
+            dpg::k_pack<<<dim3(unsigned(chunk)), 256, 0, s>>>(a);
+            st = dpg::after_launch(who);
+            if (st != DPG_OK) return st;
+        }
+        i0 = i1;
+    }
+    return DPG_OK;
+}
+
+int dpg_pack(const dpg_plan_t* plan, const void* const* param_grads, void* flat_bf16, void* stream) {
+    dpg::clear_error();
+    return pack_common(plan, param_grads, flat_bf16, 0, stream, "dpg_pack");
+}
+
+int dpg_unpack(const dpg_plan_t* plan, const void* flat_bf16, void* const* param_grads, void* stream) {
+    dpg::clear_error();
+    return pack_common(plan, const_cast<const void* const*>(param_grads), const_cast<void*>(flat_bf16),
+                       1, stream, "dpg_unpack");
+}
+
+}  // extern "C"
