@@ -265,27 +265,40 @@ __global__ void __launch_bounds__(kThreads, 2) k_rs_adam(const __grid_constant__
     }
 }
 
-// One CTA per bucket: sum the bucket's (tile, warp) partials in a fixed order
-// (double), so the result does not depend on scheduling.
-__global__ void __launch_bounds__(256) k_norm_finalize(const float* __restrict__ part_sq,
-                                                       const int32_t* __restrict__ part_nf,
-                                                       const int64_t* __restrict__ tile_begin,
-                                                       int32_t b0, float* sqnorm,
-                                                       int64_t* nonfinite) {
-    __shared__ double s_sq[256];
-    __shared__ long long s_nf[256];
+// One CTA per bucket: sum the bucket's (tile, warp) partials in a fixed order,
+// so the result does not depend on scheduling.  A bucket's partials start at a
+// multiple of kWarps entries (32 bytes), so they are read as 16-byte vectors;
+// each thread keeps four independent fp32 sums (a handful of terms each) and
+// the block combines them in double.
+constexpr int kFinalizeThreads = 512;
+
+__global__ void __launch_bounds__(kFinalizeThreads)
+k_norm_finalize(const float* __restrict__ part_sq, const int32_t* __restrict__ part_nf,
+                const int64_t* __restrict__ tile_begin, int32_t b0, float* sqnorm,
+                int64_t* nonfinite) {
+    __shared__ double s_sq[kFinalizeThreads];
+    __shared__ long long s_nf[kFinalizeThreads];
     const int b = b0 + blockIdx.x;
-    const int64_t lo = tile_begin[b] * kWarps, hi = tile_begin[b + 1] * kWarps;
-    double acc = 0.0;
+    const int64_t lo = tile_begin[b] * kWarps;
+    const int64_t n4 = (tile_begin[b + 1] * kWarps - lo) / 4;
+    const float4* sq4 = reinterpret_cast<const float4*>(part_sq + lo);
+    const int4* nf4 = reinterpret_cast<const int4*>(part_nf + lo);
+    float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
     long long cnt = 0;
-    for (int64_t k = lo + threadIdx.x; k < hi; k += blockDim.x) {
-        acc += double(part_sq[k]);
-        cnt += part_nf[k];
+#pragma unroll 4
+    for (int64_t k = threadIdx.x; k < n4; k += kFinalizeThreads) {
+        const float4 x = __ldg(sq4 + k);
+        const int4 c = __ldg(nf4 + k);
+        a0 += x.x;
+        a1 += x.y;
+        a2 += x.z;
+        a3 += x.w;
+        cnt += (long long)c.x + c.y + c.z + c.w;
     }
-    s_sq[threadIdx.x] = acc;
+    s_sq[threadIdx.x] = (double(a0) + double(a1)) + (double(a2) + double(a3));
     s_nf[threadIdx.x] = cnt;
     __syncthreads();
-    for (int w = 128; w > 0; w >>= 1) {
+    for (int w = kFinalizeThreads / 2; w > 0; w >>= 1) {
         if (threadIdx.x < w) {
             s_sq[threadIdx.x] += s_sq[threadIdx.x + w];
             s_nf[threadIdx.x] += s_nf[threadIdx.x + w];
@@ -551,11 +564,16 @@ static int rs_adam(const dpg_plan_t* plan, const void* const* grads, int32_t gra
     st = token_scale(tokens, n_counts, &a.scale);
     if (st != DPG_OK) return st;
     if (b0 == b1) return DPG_OK;  // nothing to update; buffers are not touched
-    if (!grads) return fail(DPG_ERR_INVALID_ARG, "%s: grads is NULL", who);
-    if (!master || !m || !v) return fail(DPG_ERR_INVALID_ARG, "%s: master/m/v must not be NULL", who);
+    const bool want_norm = sqnorm || nonfinite;
+    const bool has_elems = p.bucket_offset[b1] > p.bucket_offset[b0];
+    if (!has_elems && !want_norm) return DPG_OK;
+    if (!has_elems) n_views = 0;  // only the (zero) norms of empty buckets are written
+    if (has_elems && !grads) return fail(DPG_ERR_INVALID_ARG, "%s: grads is NULL", who);
+    if (has_elems && (!master || !m || !v))
+        return fail(DPG_ERR_INVALID_ARG, "%s: master/m/v must not be NULL", who);
     if (n_views > 0 && !views) return fail(DPG_ERR_INVALID_ARG, "%s: param_views is NULL", who);
     const uintptr_t galign = grads_dtype == DPG_BF16 ? 16 : 32;
-    for (int r = 0; r < p.R; ++r) {
+    for (int r = 0; has_elems && r < p.R; ++r) {
         if (!grads[r]) return fail(DPG_ERR_INVALID_ARG, "%s: grads[%d] is NULL", who, r);
         if (!aligned(grads[r], galign)) return fail(DPG_ERR_MISALIGNED, "%s: grads[%d] misaligned", who, r);
         a.grads[r] = grads[r];
@@ -579,7 +597,6 @@ static int rs_adam(const dpg_plan_t* plan, const void* const* grads, int32_t gra
     a.m = m;
     a.v = v;
     a.reduced = reduced;
-    const bool want_norm = sqnorm || nonfinite;
     a.part_sq = want_norm ? p.d_part_sq : nullptr;
     a.part_nf = want_norm ? p.d_part_nf : nullptr;
     a.bucket_offset = p.d_bucket_offset;
@@ -608,8 +625,8 @@ static int rs_adam(const dpg_plan_t* plan, const void* const* grads, int32_t gra
         if (ev1) DPG_CUDA_TRY(cudaEventRecord(ev1, s));
     }
     if (want_norm) {
-        k_norm_finalize<<<b1 - b0, 256, 0, s>>>(p.d_part_sq, p.d_part_nf, p.d_tile_begin, b0,
-                                                 sqnorm, nonfinite);
+        k_norm_finalize<<<b1 - b0, kFinalizeThreads, 0, s>>>(p.d_part_sq, p.d_part_nf,
+                                                              p.d_tile_begin, b0, sqnorm, nonfinite);
         st = after_launch(who);
         if (st != DPG_OK) return st;
     }
