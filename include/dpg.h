@@ -202,6 +202,39 @@ int dpg_step(const dpg_plan_t* plan, const void* const* grads, int32_t grads_dty
              float* exp_avg_sq, void* const* param_views, int32_t n_views,
              float* bucket_sqnorm, int64_t* bucket_nonfinite, void* stream);
 
+/* ---------------------------------------------------------------------------
+ * dpg_step without any device allocation.  The pages have no counterpart to
+ * this entry point: it exists for callers that must not have the library
+ * allocate device memory -- for example code whose device memory is owned
+ * by another allocator (a framework's caching pool or a fixed memory
+ * budget), or that cannot accept the implicit synchronisation of
+ * cudaMalloc/cudaFree in the middle of a training step.
+ *
+ * Same arguments, semantics and results as dpg_step.  Instead of the plan's
+ * device copy and norm scratch (which dpg_step allocates on first use), it
+ * uses one static device array of DPG_NOALLOC_SCRATCH_BYTES compiled into the
+ * library, which every GPU that loads the library holds until the process
+ * exits.  That array holds the bucket tables (16 bytes per bucket, copied in
+ * from the plan's host tables on `stream` at every call) and the per-(tile,
+ * warp) norm partials (64 bytes per 2048-element tile), each section rounded
+ * up to 256 bytes.  A plan that does not fit is rejected with
+ * DPG_ERR_INVALID_ARG before any device work.  Nothing in the array needs to
+ * start at zero: each call rewrites the tables and every partial it reads.
+ * The call never calls cudaMalloc, cudaFree or any allocating routine.
+ *
+ * The first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress, once per device, with that device current); make
+ * that first call before any stream capture.  Every call shares the one
+ * array, so calls whose device work overlaps (for example on two streams)
+ * race and must not be issued.
+ * ------------------------------------------------------------------------- */
+#define DPG_NOALLOC_SCRATCH_BYTES (8u << 20)
+int dpg_step_noalloc(const dpg_plan_t* plan, const void* const* grads, int32_t grads_dtype,
+                     const void* const* last_micro_bf16, const int64_t* valid_tokens,
+                     int32_t n_counts, const dpg_hparams* hp, float* master, float* exp_avg,
+                     float* exp_avg_sq, void* const* param_views, int32_t n_views,
+                     float* bucket_sqnorm, int64_t* bucket_nonfinite, void* stream);
+
 /* Diagnostics -------------------------------------------------------------- */
 /* Number of kernels this library has launched since it was loaded. */
 int64_t dpg_launch_count(void);

@@ -795,3 +795,163 @@ int dpg_unpack(const dpg_plan_t* plan, const void* flat_bf16, void* const* param
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// dpg_step_noalloc: the same fused pass and finalize, with the bucket tables
+// and the norm partials in one static device array instead of memory the plan
+// allocates.  For callers whose device memory the library must not allocate.
+// ---------------------------------------------------------------------------
+namespace dpg {
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[DPG_NOALLOC_SCRATCH_BYTES];
+
+static size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
+
+// Device address of g_noalloc_scratch on device `dev` (current), looked up
+// once per device: in host code the symbol's name is only a host-side stand-in.
+static int noalloc_scratch(int dev, unsigned char** out) {
+    static std::mutex mu;
+    static std::map<int, unsigned char*> addr;
+    std::lock_guard<std::mutex> g(mu);
+    auto it = addr.find(dev);
+    if (it == addr.end()) {
+        void* ptr = nullptr;
+        const cudaError_t e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
+        if (e != cudaSuccess || ptr == nullptr)
+            return fail(DPG_ERR_CUDA, "dpg_step_noalloc: cudaGetSymbolAddress failed on device %d: %s",
+                        dev, cudaGetErrorString(e));
+        it = addr.emplace(dev, static_cast<unsigned char*>(ptr)).first;
+    }
+    *out = it->second;
+    return DPG_OK;
+}
+
+static int step_noalloc(const dpg_plan_t* plan, const void* const* grads, int32_t grads_dtype,
+                        const void* const* last, const int64_t* tokens, int32_t n_counts,
+                        const dpg_hparams* hp, float* master, float* m, float* v,
+                        void* const* views, int32_t n_views, float* sqnorm, int64_t* nonfinite,
+                        void* stream) {
+    const char* who = "dpg_step_noalloc";
+    if (!plan) return fail(DPG_ERR_INVALID_ARG, "%s: plan is NULL", who);
+    const Plan& p = plan->p;
+    if (grads_dtype != DPG_BF16 && grads_dtype != DPG_F32)
+        return fail(DPG_ERR_INVALID_ARG, "%s: grads_dtype %d unknown", who, grads_dtype);
+    if (last && grads_dtype != DPG_F32)
+        return fail(DPG_ERR_INVALID_ARG, "%s: last_micro_bf16 needs fp32 accumulation grads", who);
+    if (n_views < 0 || n_views > DPG_MAX_VIEWS)
+        return fail(DPG_ERR_INVALID_ARG, "%s: n_views %d outside [0, %d]", who, n_views, DPG_MAX_VIEWS);
+    RsAdamArgs a{};
+    int st = adam_constants(hp, a);
+    if (st != DPG_OK) return st;
+    st = token_scale(tokens, n_counts, &a.scale);
+    if (st != DPG_OK) return st;
+
+    // layout of the static array: tables, then partials (256-byte sections)
+    const size_t nb1 = size_t(p.n_buckets) + 1;
+    const size_t n_part = size_t(p.n_tiles) * kWarps;
+    const size_t tab_bytes = round256(nb1 * sizeof(int64_t));
+    const size_t sq_bytes = round256(n_part * sizeof(float));
+    const size_t nf_bytes = round256(n_part * sizeof(int32_t));
+    const size_t need = 2 * tab_bytes + sq_bytes + nf_bytes;
+    if (need > size_t(DPG_NOALLOC_SCRATCH_BYTES))
+        return fail(DPG_ERR_INVALID_ARG,
+                    "%s: this plan (%d buckets, %lld tiles of %lld elements) needs %zu bytes of "
+                    "scratch; the library's static scratch holds %zu bytes (use dpg_step)",
+                    who, p.n_buckets, (long long)p.n_tiles, (long long)kTile, need,
+                    size_t(DPG_NOALLOC_SCRATCH_BYTES));
+    if (p.n_buckets == 0) return DPG_OK;
+    const bool want_norm = sqnorm || nonfinite;
+    const bool has_elems = p.total_padded > 0;
+    if (!has_elems && !want_norm) return DPG_OK;
+    if (!has_elems) n_views = 0;
+    if (has_elems && !grads) return fail(DPG_ERR_INVALID_ARG, "%s: grads is NULL", who);
+    if (has_elems && (!master || !m || !v))
+        return fail(DPG_ERR_INVALID_ARG, "%s: master/m/v must not be NULL", who);
+    if (n_views > 0 && !views) return fail(DPG_ERR_INVALID_ARG, "%s: param_views is NULL", who);
+    const uintptr_t galign = grads_dtype == DPG_BF16 ? 16 : 32;
+    for (int r = 0; has_elems && r < p.R; ++r) {
+        if (!grads[r]) return fail(DPG_ERR_INVALID_ARG, "%s: grads[%d] is NULL", who, r);
+        if (!aligned(grads[r], galign)) return fail(DPG_ERR_MISALIGNED, "%s: grads[%d] misaligned", who, r);
+        a.grads[r] = grads[r];
+        if (last) {
+            if (!last[r]) return fail(DPG_ERR_INVALID_ARG, "%s: last_micro_bf16[%d] is NULL", who, r);
+            if (!aligned(last[r], 16)) return fail(DPG_ERR_MISALIGNED, "%s: last_micro_bf16[%d] misaligned", who, r);
+            a.last[r] = last[r];
+        }
+    }
+    for (int k = 0; k < n_views; ++k) {
+        if (!views[k]) return fail(DPG_ERR_INVALID_ARG, "%s: param_views[%d] is NULL", who, k);
+        if (!aligned(views[k], 16)) return fail(DPG_ERR_MISALIGNED, "%s: param_views[%d] misaligned", who, k);
+        a.views[k] = views[k];
+    }
+    if (!aligned(master, 32) || !aligned(m, 32) || !aligned(v, 32))
+        return fail(DPG_ERR_MISALIGNED, "%s: fp32 buffers must be 32-byte aligned", who);
+
+    int dev = 0;
+    DPG_CUDA_TRY(cudaGetDevice(&dev));
+    unsigned char* base = nullptr;
+    st = noalloc_scratch(dev, &base);
+    if (st != DPG_OK) return st;
+    int64_t* d_bucket_offset = reinterpret_cast<int64_t*>(base);
+    int64_t* d_tile_begin = reinterpret_cast<int64_t*>(base + tab_bytes);
+    float* d_part_sq = reinterpret_cast<float*>(base + 2 * tab_bytes);
+    int32_t* d_part_nf = reinterpret_cast<int32_t*>(base + 2 * tab_bytes + sq_bytes);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    // the tables of this plan, in stream order ahead of the kernels that read them
+    DPG_CUDA_TRY(cudaMemcpyAsync(d_bucket_offset, p.bucket_offset.data(), nb1 * sizeof(int64_t),
+                                 cudaMemcpyHostToDevice, s));
+    DPG_CUDA_TRY(cudaMemcpyAsync(d_tile_begin, p.tile_begin.data(), nb1 * sizeof(int64_t),
+                                 cudaMemcpyHostToDevice, s));
+
+    a.master = master;
+    a.m = m;
+    a.v = v;
+    a.reduced = nullptr;
+    a.part_sq = want_norm ? d_part_sq : nullptr;
+    a.part_nf = want_norm ? d_part_nf : nullptr;
+    a.bucket_offset = d_bucket_offset;
+    a.tile_begin = d_tile_begin;
+    a.t0 = 0;
+    a.t1 = p.n_tiles;
+    a.b0 = 0;
+    a.b1 = p.n_buckets;
+    a.R = p.R;
+    a.n_views = n_views;
+    const int mode = grads_dtype == DPG_BF16 ? kInBf16 : (last ? kInF32PlusBf16 : kInF32);
+    RsKernel fn = mode == kInBf16 ? pick_rs_kernel<kInBf16>(p.R)
+                : mode == kInF32 ? pick_rs_kernel<kInF32>(p.R)
+                                 : pick_rs_kernel<kInF32PlusBf16>(p.R);
+    if (a.t1 > a.t0) {
+        int grid = 0;
+        st = grid_for(reinterpret_cast<const void*>(fn), kThreads, dev, a.t1 - a.t0, &grid);
+        if (st != DPG_OK) return st;
+        cudaEvent_t ev0 = t_fused_start, ev1 = t_fused_stop;
+        t_fused_start = t_fused_stop = nullptr;
+        if (ev0) DPG_CUDA_TRY(cudaEventRecord(ev0, s));
+        fn<<<grid, kThreads, 0, s>>>(a);
+        st = after_launch(who);
+        if (st != DPG_OK) return st;
+        if (ev1) DPG_CUDA_TRY(cudaEventRecord(ev1, s));
+    }
+    if (want_norm) {
+        k_norm_finalize<<<p.n_buckets, kFinalizeThreads, 0, s>>>(d_part_sq, d_part_nf, d_tile_begin,
+                                                                  0, sqnorm, nonfinite);
+        st = after_launch(who);
+        if (st != DPG_OK) return st;
+    }
+    return DPG_OK;
+}
+
+}  // namespace dpg
+
+extern "C" int dpg_step_noalloc(const dpg_plan_t* plan, const void* const* grads,
+                                int32_t grads_dtype, const void* const* last_micro_bf16,
+                                const int64_t* valid_tokens, int32_t n_counts,
+                                const dpg_hparams* hp, float* master, float* exp_avg,
+                                float* exp_avg_sq, void* const* param_views, int32_t n_views,
+                                float* bucket_sqnorm, int64_t* bucket_nonfinite, void* stream) {
+    dpg::clear_error();
+    return dpg::step_noalloc(plan, grads, grads_dtype, last_micro_bf16, valid_tokens, n_counts, hp,
+                             master, exp_avg, exp_avg_sq, param_views, n_views, bucket_sqnorm,
+                             bucket_nonfinite, stream);
+}
