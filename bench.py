@@ -54,6 +54,10 @@ def parse():
     ap.add_argument("--impl", default="dpg", choices=["dpg", "reference"])
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--kernels", action="store_true",
+                    help="time every kernel of the path on the workload, against its algorithmic bytes")
+    ap.add_argument("--hockney", action="store_true",
+                    help="bucket-cap sweep: per-bucket launches vs one fused launch, alpha-beta fit")
     a = ap.parse_args()
     if a.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -445,8 +449,162 @@ def run_reference(a):
     print(json.dumps(line), flush=True)
 
 
+# --------------------------------------------------------------------------
+# Hockney alpha-beta sweep ("Parallelisms", section "Gradient bucketing":
+# T(m) = alpha + beta m; K small operations cost K alpha + beta M, one fused
+# operation alpha + beta M)
+# --------------------------------------------------------------------------
+def run_hockney(a):
+    import torch
+    from zero_optimizer_step_gb300 import build as _build
+    _build.build()
+    import zero_optimizer_step_gb300 as dpg
+    cfg = CONFIGS["sweep"]
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    R = cfg.R
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)   # > L2 (129 MB)
+    points = []
+    for cap in cfg.cap_sweep:
+        plan = dpg.dpg_plan_buckets(cfg.numels, cap, R)
+        dpg.dpg_plan_upload(plan)
+        N = plan.total_padded
+        segs = segments(plan.param_offset, cfg.numels)
+        g = [flat_grads_bf16(segs, N, cfg.grad_std, stream_seed(cfg.seed, KIND_GRAD, r), device=dev)
+             for r in range(R)]
+        w = master_f32(N, stream_seed(cfg.seed, KIND_MASTER), device=dev)
+        m, v = torch.zeros(N, device=dev), torch.zeros(N, device=dev)
+        p = torch.empty(N, dtype=torch.bfloat16, device=dev)
+        tok = token_counts(cfg)
+        hp = dpg.HParams(step=1)
+        graphs = {}
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            for _ in range(2):     # warm the occupancy cache and the plan upload
+                dpg.dpg_reduce_scatter_adam(plan, g, tok, hp, w, m, v, [p])
+        torch.cuda.current_stream().wait_stream(s)
+        for mode in ("per_bucket", "fused"):
+            gr = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(gr):
+                if mode == "fused":
+                    dpg.dpg_reduce_scatter_adam(plan, g, tok, hp, w, m, v, [p])
+                else:
+                    for b in range(plan.n_buckets):
+                        dpg.dpg_reduce_scatter_adam(plan, g, tok, hp, w, m, v, [p], b0=b, b1=b + 1)
+            graphs[mode] = gr
+        res = {}
+        for mode, gr in graphs.items():
+            ts = []
+            for _ in range(max(3, a.steps)):
+                flush.zero_()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record()
+                gr.replay()
+                e1.record()
+                torch.cuda.synchronize()
+                ts.append(e0.elapsed_time(e1))
+            res[mode] = statistics.median(ts)
+        points.append({"cap_bytes": cap, "n_buckets": plan.n_buckets, "total_padded": N,
+                       "bytes": (2 * R + 26) * cfg.psi, "per_bucket_ms": res["per_bucket"],
+                       "fused_ms": res["fused"]})
+        del graphs, g, w, m, v, p
+        plan.destroy()
+    K = np.array([q["n_buckets"] for q in points], float)
+    T = np.array([q["per_bucket_ms"] for q in points], float) * 1e-3
+    Mb = np.array([q["bytes"] for q in points], float)
+    A = np.stack([K, Mb], axis=1)
+    (alpha, beta), *_ = np.linalg.lstsq(A, T, rcond=None)
+    fused = np.array([q["fused_ms"] for q in points]) * 1e-3
+    out = {"metric": "hockney alpha-beta fit of the fused reduce-scatter+Adam kernel over bucket caps",
+           "workload": f"sweep: {len(cfg.shapes)} tensors, psi={cfg.psi}, R={R}",
+           "points": points, "fit": {"alpha_us": alpha * 1e6, "inv_beta_gbs": 1.0 / beta / 1e9,
+                                     "model": "T_per_bucket = K*alpha + beta*M (least squares)"},
+           "fused_single_launch_ms": {"median": float(np.median(fused)) * 1e3,
+                                      "min": float(fused.min()) * 1e3, "max": float(fused.max()) * 1e3},
+           "timing": "CUDA graph replay, L2 flushed (256 MB write) before every replay"}
+    print(json.dumps(out), flush=True)
+
+
+# --------------------------------------------------------------------------
+# per-kernel table: each kernel of the path timed alone on the workload
+# --------------------------------------------------------------------------
+def run_kernel_table(a):
+    import torch
+    from zero_optimizer_step_gb300 import build as _build
+    _build.build()
+    import zero_optimizer_step_gb300 as dpg
+    cfg = CONFIGS[a.config]
+    cap = cap_of(cfg, a)
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    R = cfg.R
+    plan = dpg.dpg_plan_buckets(cfg.numels, cap, R)
+    dpg.dpg_plan_upload(plan)
+    N = plan.total_padded
+    segs = segments(plan.param_offset, cfg.numels)
+    psi = cfg.psi
+    peak, peak_kind = load_peak()
+    g = [flat_grads_bf16(segs, N, cfg.grad_std, stream_seed(cfg.seed, KIND_GRAD, r), device=dev)
+         for r in range(R)]
+    w = master_f32(N, stream_seed(cfg.seed, KIND_MASTER), device=dev)
+    m, v = torch.zeros(N, device=dev), torch.zeros(N, device=dev)
+    p = torch.empty(N, dtype=torch.bfloat16, device=dev)
+    sq = torch.empty(plan.n_buckets, device=dev)
+    acc = torch.empty(N, device=dev)
+    tok = token_counts(cfg)
+    # parameter-shaped gradients for pack/unpack (one replica)
+    pgrads = [g[0][int(o):int(o) + int(n)].clone() for o, n in zip(plan.param_offset, cfg.numels)]
+    flat = torch.empty(N, dtype=torch.bfloat16, device=dev)
+    state = {"t": 0}
+
+    def hp():
+        state["t"] += 1
+        return dpg.HParams(step=state["t"])
+
+    cases = [
+        ("k_pack (dpg_pack, one replica)", 4, lambda: dpg.dpg_pack(plan, pgrads, flat)),
+        ("k_pack unpack (dpg_unpack, one replica)", 4, lambda: dpg.dpg_unpack(plan, flat, pgrads)),
+        ("k_accumulate<first> (one replica)", 6, lambda: dpg.dpg_accumulate(plan, g[0], acc, True)),
+        ("k_accumulate (one replica)", 10, lambda: dpg.dpg_accumulate(plan, g[0], acc, False)),
+        ("k_allgather (one view)", 6, lambda: dpg.dpg_allgather_params(plan, w, [p])),
+        (f"k_rs_adam<R={R}> (dpg_reduce_scatter_adam, no norm)", 2 * R + 26,
+         lambda: dpg.dpg_reduce_scatter_adam(plan, g, tok, hp(), w, m, v, [p])),
+        (f"k_rs_adam<R={R}> + k_norm_finalize (dpg_step)", 2 * R + 26,
+         lambda: dpg.dpg_step(plan, g, tok, hp(), w, m, v, [p], bucket_sqnorm=sq)),
+        (f"k_rs_adam<R={R}> distinct views (n_views=R)", 4 * R + 24,
+         lambda: dpg.dpg_step(plan, g, tok, hp(), w, m, v, views)),
+    ]
+    views = [torch.empty(N, dtype=torch.bfloat16, device=dev) for _ in range(R)]
+    rows = []
+    for name, bpp, fn in cases:
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        ts = []
+        for _ in range(max(5, min(a.steps, 20))):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            fn()
+            e1.record()
+            torch.cuda.synchronize()
+            ts.append(e0.elapsed_time(e1))
+        ms = statistics.median(ts)
+        gbs = bpp * psi / (ms * 1e-3) / 1e9
+        rows.append({"kernel": name, "bytes_per_param": bpp, "ms": ms, "achieved_gbs": gbs,
+                     "frac": gbs / peak})
+    print(json.dumps({"metric": "per-kernel HBM roofline", "config": workload_desc(cfg, cap, plan.n_buckets, N),
+                      "peak_gbs": peak, "peak_kind": peak_kind, "rows": rows}), flush=True)
+
+
 def main():
     a = parse()
+    if a.kernels:
+        run_kernel_table(a)
+        return
+    if a.hockney:
+        run_hockney(a)
+        return
     if a.impl == "reference":
         run_reference(a)
     else:

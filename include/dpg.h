@@ -216,7 +216,8 @@ int dpg_step(const dpg_plan_t* plan, const void* const* grads, int32_t grads_dty
  * library, which every GPU that loads the library holds until the process
  * exits.  That array holds the bucket tables (16 bytes per bucket, copied in
  * from the plan's host tables on `stream` at every call) and the per-(tile,
- * warp) norm partials (64 bytes per 2048-element tile), each section rounded
+ * warp) norm partials (8 bytes per warp of each 4096-element tile, i.e. 32
+ * bytes per 1024 elements), each section rounded
  * up to 256 bytes.  A plan that does not fit is rejected with
  * DPG_ERR_INVALID_ARG before any device work.  Nothing in the array needs to
  * start at zero: each call rewrites the tables and every partial it reads.

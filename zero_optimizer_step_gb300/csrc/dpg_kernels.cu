@@ -46,7 +46,7 @@ struct F8 {
     float v[8];
 };
 
-// read-only gradient stream: bypass L1, first to leave L2
+// read-only gradient stream: bypass L1 (an L2 evict-first hint measured 0.4 % slower)
 __device__ __forceinline__ uint4 ld_grad_u4(const void* p) {
     uint4 r;
     asm("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
@@ -57,7 +57,7 @@ __device__ __forceinline__ uint4 ld_grad_u4(const void* p) {
 
 __device__ __forceinline__ F8 ld_grad_f8(const float* p) {
     F8 r;
-    asm("ld.global.nc.L1::no_allocate.L2::evict_first.v8.f32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+    asm("ld.global.nc.L1::no_allocate.v8.f32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
         : "=f"(r.v[0]), "=f"(r.v[1]), "=f"(r.v[2]), "=f"(r.v[3]), "=f"(r.v[4]), "=f"(r.v[5]),
           "=f"(r.v[6]), "=f"(r.v[7])
         : "l"(p));
@@ -67,7 +67,7 @@ __device__ __forceinline__ F8 ld_grad_f8(const float* p) {
 // read-modify-write state (master / m / v / accumulation buffer)
 __device__ __forceinline__ F8 ld_state_f8(const float* p) {
     F8 r;
-    asm("ld.global.L1::no_allocate.L2::evict_first.v8.f32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+    asm("ld.global.L1::no_allocate.v8.f32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
         : "=f"(r.v[0]), "=f"(r.v[1]), "=f"(r.v[2]), "=f"(r.v[3]), "=f"(r.v[4]), "=f"(r.v[5]),
           "=f"(r.v[6]), "=f"(r.v[7])
         : "l"(p));
@@ -204,7 +204,7 @@ __device__ __forceinline__ void reduce_vector(const RsAdamArgs& a, int64_t i, fl
 }
 
 template <int RT, int MODE>
-__global__ void __launch_bounds__(kThreads, 2) k_rs_adam(const __grid_constant__ RsAdamArgs a) {
+__global__ void __launch_bounds__(kThreads, 1) k_rs_adam(const __grid_constant__ RsAdamArgs a) {
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
     int b = a.b0;
