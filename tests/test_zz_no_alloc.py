@@ -88,16 +88,19 @@ def test_noalloc_matches_dpg_step_on_two_calls_in_a_row(name):
 
 
 def test_noalloc_refuses_plans_beyond_its_scratch():
-    # 2^28 elements = 131072 tiles -> 8 MiB of partials alone: over the limit
-    plan = dpg.dpg_plan_buckets([1 << 28], 1 << 40, 1)
-    fake = 1 << 20
+    # 2000 one-parameter buckets of 123 tiles each: every CTA visits hundreds of
+    # buckets, so the norm partials alone need tens of MB.  All buffers are NULL:
+    # the call must stop at the size check (and would stop at the NULL checks
+    # otherwise), so nothing can reach the device.
+    plan = dpg.dpg_plan_buckets([500_000] * 2000, 1 << 20, 1)
+    assert plan.n_buckets == 2000
     hp = dpg.HParams().c()
     tok = np.array([100], np.int64)
     before = dpg.dpg_launch_count()
-    rc = dpg.lib().dpg_step_noalloc(plan.handle, dpg._ptrs([fake]), dpg.DPG_BF16, None,
-                                    tok.ctypes.data, 1, ctypes.byref(hp), fake, fake, fake,
-                                    dpg._ptrs([fake]), 1, fake, None, None)
+    rc = dpg.lib().dpg_step_noalloc(plan.handle, dpg._ptrs([0]), dpg.DPG_BF16, None,
+                                    tok.ctypes.data, 1, ctypes.byref(hp), None, None, None,
+                                    dpg._ptrs([0]), 1, 1 << 20, None, None)
     assert rc == dpg.DPG_ERR_INVALID_ARG
     msg = dpg.lib().dpg_last_error().decode()
-    assert "scratch" in msg and str(dpg.DPG_NOALLOC_SCRATCH_BYTES) in msg
+    assert "scratch" in msg and str(dpg.DPG_NOALLOC_SCRATCH_BYTES) in msg, msg
     assert dpg.dpg_launch_count() == before

@@ -54,8 +54,14 @@ struct Plan {
     int64_t* d_bucket_offset = nullptr;
     int64_t* d_tile_begin = nullptr;
     PackItem* d_items = nullptr;
-    float* d_part_sq = nullptr;     // kWarps * n_tiles
-    int32_t* d_part_nf = nullptr;   // kWarps * n_tiles
+    // norm scratch: per-(CTA, bucket visit) partials of one fused launch
+    void* d_vis = nullptr;          // one allocation, sections below
+    double* d_vis_sq = nullptr;     // cap_visits * kWarps
+    int32_t* d_vis_nf = nullptr;    // cap_visits * kWarps
+    int32_t* d_vis_bucket = nullptr;// cap_visits
+    int32_t* d_vis_count = nullptr; // cap_ctas
+    int64_t cap_visits = 0;
+    int32_t cap_ctas = 0;
 };
 
 // thread-local error message

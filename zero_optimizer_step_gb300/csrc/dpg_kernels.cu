@@ -126,8 +126,11 @@ struct RsAdamArgs {
     float* m;
     float* v;
     float* reduced;      // nullable
-    float* part_sq;      // nullable (no norm requested)
-    int32_t* part_nf;
+    double* vis_sq;      // per-(CTA, bucket visit, warp) norm partials; NULL: no norm
+    int32_t* vis_nf;     // same layout, non-finite counts
+    int32_t* vis_bucket; // bucket of each (CTA, visit)
+    int32_t* vis_count;  // visits made by each CTA
+    int32_t vmax;        // visit slots per CTA
     const int64_t* bucket_offset;
     const int64_t* tile_begin;
     int64_t t0, t1;      // tile range of buckets [b0, b1)
@@ -203,18 +206,47 @@ __device__ __forceinline__ void reduce_vector(const RsAdamArgs& a, int64_t i, fl
     }
 }
 
-template <int RT, int MODE>
-__global__ void __launch_bounds__(kThreads, 1) k_rs_adam(const __grid_constant__ RsAdamArgs a) {
+// Per-bucket norm bookkeeping: a CTA's consecutive tiles of one bucket form a
+// "visit"; each thread keeps running sums over the visit (per-tile fp32 sums
+// of 8 squares, accumulated in double), and the warps reduce and store them
+// only when the CTA moves on to the next bucket -- once or twice per CTA for
+// large buckets, so no shuffle or store sits on the per-tile critical path.
+__device__ __forceinline__ void flush_visit(const RsAdamArgs& a, int bucket, int visit, double sq,
+                                            int nf) {
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        sq += __shfl_xor_sync(0xFFFFFFFFu, sq, o);
+        nf += __shfl_xor_sync(0xFFFFFFFFu, nf, o);
+    }
+    const int64_t slot = int64_t(blockIdx.x) * a.vmax + visit;
+    if (lane == 0) {
+        a.vis_sq[slot * kWarps + warp] = sq;
+        a.vis_nf[slot * kWarps + warp] = nf;
+    }
+    if (threadIdx.x == 0) a.vis_bucket[slot] = bucket;
+}
+
+template <int RT, int MODE>
+__global__ void __launch_bounds__(kThreads, 1) k_rs_adam(const __grid_constant__ RsAdamArgs a) {
+    const bool norm = a.vis_sq != nullptr;
     int b = a.b0;
+    int cur = -1;  // bucket of the running norm sums
+    int visit = 0;
+    double sq = 0.0;
+    int nf = 0;
     for (int64_t t = a.t0 + blockIdx.x; t < a.t1; t += gridDim.x) {
-        b = bucket_of_tile(a.tile_begin, b, a.b1, t);
+        b = bucket_of_tile(a.tile_begin, b, a.b1, t);  // CTA-uniform
+        if (norm && b != cur) {
+            if (cur >= 0) flush_visit(a, cur, visit++, sq, nf);
+            cur = b;
+            sq = 0.0;
+            nf = 0;
+        }
         const int64_t bucket_end = __ldg(a.bucket_offset + b + 1);
         const int64_t i = __ldg(a.bucket_offset + b) + (t - __ldg(a.tile_begin + b)) * kTile +
                           int64_t(threadIdx.x) * kVec;
-        float sq = 0.0f;
-        int nf = 0;
         if (i < bucket_end) {
             float s[8];
             reduce_vector<RT, MODE>(a, i, s);
@@ -222,6 +254,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_rs_adam(const __grid_constant__
             F8 m = ld_state_f8(a.m + i);
             F8 v = ld_state_f8(a.v + i);
             float g[8];
+            float tsq = 0.0f;
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
                 g[j] = __fmul_rn(s[j], a.scale);
@@ -236,9 +269,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_rs_adam(const __grid_constant__
                 w.v[j] = __fsub_rn(wj, __fmul_rn(a.lr, u));
                 m.v[j] = mj;
                 v.v[j] = vj;
-                sq = fmaf(g[j], g[j], sq);
+                tsq = fmaf(g[j], g[j], tsq);
                 nf += (__float_as_uint(g[j]) & 0x7F800000u) == 0x7F800000u;
             }
+            if (norm) sq += double(tsq);
             st_f8(a.master + i, w);
             st_f8(a.m + i, m);
             st_f8(a.v + i, v);
@@ -251,51 +285,47 @@ __global__ void __launch_bounds__(kThreads, 1) k_rs_adam(const __grid_constant__
                 st_f8(a.reduced + i, gg);
             }
         }
-        if (a.part_sq) {
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) {
-                sq += __shfl_xor_sync(0xFFFFFFFFu, sq, o);
-                nf += __shfl_xor_sync(0xFFFFFFFFu, nf, o);
-            }
-            if (lane == 0) {
-                a.part_sq[t * kWarps + warp] = sq;
-                a.part_nf[t * kWarps + warp] = nf;
-            }
-        }
+    }
+    if (norm) {
+        if (cur >= 0) flush_visit(a, cur, visit++, sq, nf);
+        if (threadIdx.x == 0) a.vis_count[blockIdx.x] = visit;
     }
 }
 
-// One CTA per bucket: sum the bucket's (tile, warp) partials in a fixed order,
-// so the result does not depend on scheduling.  A bucket's partials start at a
-// multiple of kWarps entries (32 bytes), so they are read as 16-byte vectors;
-// each thread keeps four independent fp32 sums (a handful of terms each) and
-// the block combines them in double.
-constexpr int kFinalizeThreads = 512;
+// One CTA per bucket: thread c (and c + 256, ...) finds CTA c's visit of the
+// bucket by binary search in that CTA's visit list (its buckets increase) and
+// adds the visit's warp partials in warp order; the block then combines the
+// threads in a fixed tree.  The order depends only on the launch geometry, so
+// the norms are the same from run to run.
+constexpr int kFinalizeThreads = 256;
 
 __global__ void __launch_bounds__(kFinalizeThreads)
-k_norm_finalize(const float* __restrict__ part_sq, const int32_t* __restrict__ part_nf,
-                const int64_t* __restrict__ tile_begin, int32_t b0, float* sqnorm,
-                int64_t* nonfinite) {
+k_norm_finalize(const double* __restrict__ vis_sq, const int32_t* __restrict__ vis_nf,
+                const int32_t* __restrict__ vis_bucket, const int32_t* __restrict__ vis_count,
+                int32_t n_cta, int32_t vmax, int32_t b0, float* sqnorm, int64_t* nonfinite) {
     __shared__ double s_sq[kFinalizeThreads];
     __shared__ long long s_nf[kFinalizeThreads];
     const int b = b0 + blockIdx.x;
-    const int64_t lo = tile_begin[b] * kWarps;
-    const int64_t n4 = (tile_begin[b + 1] * kWarps - lo) / 4;
-    const float4* sq4 = reinterpret_cast<const float4*>(part_sq + lo);
-    const int4* nf4 = reinterpret_cast<const int4*>(part_nf + lo);
-    float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+    double acc = 0.0;
     long long cnt = 0;
-#pragma unroll 4
-    for (int64_t k = threadIdx.x; k < n4; k += kFinalizeThreads) {
-        const float4 x = __ldg(sq4 + k);
-        const int4 c = __ldg(nf4 + k);
-        a0 += x.x;
-        a1 += x.y;
-        a2 += x.z;
-        a3 += x.w;
-        cnt += (long long)c.x + c.y + c.z + c.w;
+    for (int c = threadIdx.x; c < n_cta; c += kFinalizeThreads) {
+        const int32_t* vb = vis_bucket + int64_t(c) * vmax;
+        const int n = vis_count[c];
+        int lo = 0, hi = n;
+        while (lo < hi) {
+            const int mid = (lo + hi) >> 1;
+            if (vb[mid] < b) lo = mid + 1;
+            else hi = mid;
+        }
+        if (lo < n && vb[lo] == b) {
+            const int64_t slot = (int64_t(c) * vmax + lo) * kWarps;
+            for (int w = 0; w < kWarps; ++w) {
+                acc += vis_sq[slot + w];
+                cnt += vis_nf[slot + w];
+            }
+        }
     }
-    s_sq[threadIdx.x] = (double(a0) + double(a1)) + (double(a2) + double(a3));
+    s_sq[threadIdx.x] = acc;
     s_nf[threadIdx.x] = cnt;
     __syncthreads();
     for (int w = kFinalizeThreads / 2; w > 0; w >>= 1) {
@@ -361,31 +391,51 @@ struct PackArgs {
     int32_t unpack;
     const PackItem* items;
     int64_t item0;
+    int64_t n_items;
     uint16_t* flat;
 };
 
-__device__ __forceinline__ void copy_elems(uint16_t* dst, const uint16_t* src, int64_t n) {
+// Copy n bf16 elements.  When both ends are 16-byte aligned, each thread
+// issues four 16-byte loads before its four stores, so a CTA keeps 64 KB in
+// flight; otherwise (a parameter gradient at an odd 2-byte offset) it copies
+// element by element.
+__device__ __forceinline__ void copy_elems(uint16_t* __restrict__ dst,
+                                           const uint16_t* __restrict__ src, int64_t n) {
     const bool vec = ((reinterpret_cast<uintptr_t>(dst) | reinterpret_cast<uintptr_t>(src)) & 15) == 0;
     int64_t done = 0;
     if (vec) {
         const int64_t nv = n / kVec;
-        const uint4* s4 = reinterpret_cast<const uint4*>(src);
+        const int64_t bd = blockDim.x;
         uint4* d4 = reinterpret_cast<uint4*>(dst);
-        for (int64_t k = threadIdx.x; k < nv; k += blockDim.x) d4[k] = s4[k];
+        int64_t k = threadIdx.x;
+        for (; k + 3 * bd < nv; k += 4 * bd) {
+            const uint4 x0 = ld_grad_u4(src + (k) * kVec);
+            const uint4 x1 = ld_grad_u4(src + (k + bd) * kVec);
+            const uint4 x2 = ld_grad_u4(src + (k + 2 * bd) * kVec);
+            const uint4 x3 = ld_grad_u4(src + (k + 3 * bd) * kVec);
+            st_u4(d4 + k, x0);
+            st_u4(d4 + k + bd, x1);
+            st_u4(d4 + k + 2 * bd, x2);
+            st_u4(d4 + k + 3 * bd, x3);
+        }
+        for (; k < nv; k += bd) st_u4(d4 + k, ld_grad_u4(src + k * kVec));
         done = nv * kVec;
     }
     for (int64_t k = done + threadIdx.x; k < n; k += blockDim.x) dst[k] = src[k];
 }
 
+// Persistent: CTA c copies items c, c + grid, ... of the launch's window.
 __global__ void __launch_bounds__(256) k_pack(const __grid_constant__ PackArgs a) {
-    const PackItem it = a.items[a.item0 + blockIdx.x];
-    uint16_t* param = static_cast<uint16_t*>(const_cast<void*>(a.ptrs[it.param - a.p_base]));
-    uint16_t* flat = a.flat + it.flat_off;
-    if (!a.unpack) {
-        if (it.count > 0) copy_elems(flat, param + it.src_off, it.count);
-        for (int64_t k = threadIdx.x; k < it.tail; k += blockDim.x) flat[it.count + k] = 0;
-    } else if (it.count > 0) {
-        copy_elems(param + it.src_off, flat, it.count);
+    for (int64_t j = blockIdx.x; j < a.n_items; j += gridDim.x) {
+        const PackItem it = a.items[a.item0 + j];
+        uint16_t* param = static_cast<uint16_t*>(const_cast<void*>(a.ptrs[it.param - a.p_base]));
+        uint16_t* flat = a.flat + it.flat_off;
+        if (!a.unpack) {
+            if (it.count > 0) copy_elems(flat, param + it.src_off, it.count);
+            for (int64_t k = threadIdx.x; k < it.tail; k += blockDim.x) flat[it.count + k] = 0;
+        } else if (it.count > 0) {
+            copy_elems(param + it.src_off, flat, it.count);
+        }
     }
 }
 
@@ -439,6 +489,24 @@ static int after_launch(const char* what) {
     return DPG_OK;
 }
 
+static size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
+
+// Byte layout of a norm scratch with `visits` (CTA, bucket visit) slots for up
+// to `ctas` CTAs; every section starts on a 256-byte boundary.
+struct VisLayout {
+    size_t sq, nf, bucket, count, total;
+};
+
+static VisLayout vis_layout(int64_t visits, int64_t ctas) {
+    VisLayout L;
+    L.sq = 0;
+    L.nf = L.sq + round256(size_t(visits) * kWarps * sizeof(double));
+    L.bucket = L.nf + round256(size_t(visits) * kWarps * sizeof(int32_t));
+    L.count = L.bucket + round256(size_t(visits) * sizeof(int32_t));
+    L.total = L.count + round256(size_t(ctas) * sizeof(int32_t));
+    return L;
+}
+
 int upload(Plan& p) {
     std::lock_guard<std::mutex> g(p.mu);
     int dev = 0;
@@ -449,31 +517,47 @@ int upload(Plan& p) {
                         "plan tables live on device %d but device %d is current", p.device, dev);
         return DPG_OK;
     }
+    int sms = 0;
+    int st = sm_count(dev, &sms);
+    if (st != DPG_OK) return st;
+    // A fused launch over tiles T of buckets B with G CTAs uses G * min(B,
+    // ceil(T / G)) visit slots: at most T + G and at most G * B, G being at
+    // most the resident CTAs of the device (2048 threads per SM).
+    const int64_t cap_ctas = int64_t(sms) * (2048 / kThreads);
+    int64_t cap_visits = p.n_tiles + cap_ctas;
+    if (cap_ctas * p.n_buckets < cap_visits) cap_visits = cap_ctas * p.n_buckets;
+    if (cap_visits < 1) cap_visits = 1;
+    const VisLayout L = vis_layout(cap_visits, cap_ctas);
+
     const size_t nb1 = size_t(p.n_buckets) + 1;
     const size_t n_items = p.items.size() ? p.items.size() : 1;
-    const size_t n_part = size_t(p.n_tiles) * kWarps ? size_t(p.n_tiles) * kWarps : 1;
-    void *bo = nullptr, *tb = nullptr, *it = nullptr, *ps = nullptr, *pn = nullptr;
+    void *bo = nullptr, *tb = nullptr, *it = nullptr, *vis = nullptr;
     cudaError_t e = cudaSuccess;
     if (e == cudaSuccess) e = cudaMalloc(&bo, nb1 * sizeof(int64_t));
     if (e == cudaSuccess) e = cudaMalloc(&tb, nb1 * sizeof(int64_t));
     if (e == cudaSuccess) e = cudaMalloc(&it, n_items * sizeof(PackItem));
-    if (e == cudaSuccess) e = cudaMalloc(&ps, n_part * sizeof(float));
-    if (e == cudaSuccess) e = cudaMalloc(&pn, n_part * sizeof(int32_t));
+    if (e == cudaSuccess) e = cudaMalloc(&vis, L.total);
     if (e == cudaSuccess) e = cudaMemcpy(bo, p.bucket_offset.data(), nb1 * sizeof(int64_t), cudaMemcpyHostToDevice);
     if (e == cudaSuccess) e = cudaMemcpy(tb, p.tile_begin.data(), nb1 * sizeof(int64_t), cudaMemcpyHostToDevice);
     if (e == cudaSuccess && !p.items.empty())
         e = cudaMemcpy(it, p.items.data(), p.items.size() * sizeof(PackItem), cudaMemcpyHostToDevice);
     if (e != cudaSuccess) {
-        cudaFree(bo); cudaFree(tb); cudaFree(it); cudaFree(ps); cudaFree(pn);
+        cudaFree(bo); cudaFree(tb); cudaFree(it); cudaFree(vis);
         cudaGetLastError();
         return fail(e == cudaErrorMemoryAllocation ? DPG_ERR_OOM : DPG_ERR_CUDA,
                     "plan upload: %s", cudaGetErrorString(e));
     }
+    unsigned char* base = static_cast<unsigned char*>(vis);
     p.d_bucket_offset = static_cast<int64_t*>(bo);
     p.d_tile_begin = static_cast<int64_t*>(tb);
     p.d_items = static_cast<PackItem*>(it);
-    p.d_part_sq = static_cast<float*>(ps);
-    p.d_part_nf = static_cast<int32_t*>(pn);
+    p.d_vis = vis;
+    p.d_vis_sq = reinterpret_cast<double*>(base + L.sq);
+    p.d_vis_nf = reinterpret_cast<int32_t*>(base + L.nf);
+    p.d_vis_bucket = reinterpret_cast<int32_t*>(base + L.bucket);
+    p.d_vis_count = reinterpret_cast<int32_t*>(base + L.count);
+    p.cap_visits = cap_visits;
+    p.cap_ctas = int32_t(cap_ctas);
     p.device = dev;
     return DPG_OK;
 }
@@ -487,8 +571,7 @@ void release_device(Plan& p) {
         cudaFree(p.d_bucket_offset);
         cudaFree(p.d_tile_begin);
         cudaFree(p.d_items);
-        cudaFree(p.d_part_sq);
-        cudaFree(p.d_part_nf);
+        cudaFree(p.d_vis);
     }
     if (have_cur) cudaSetDevice(cur);
     cudaGetLastError();
@@ -540,6 +623,46 @@ static RsKernel pick_rs_kernel(int R) {
         case 8: return k_rs_adam<8, MODE>;
         default: return k_rs_adam<0, MODE>;
     }
+}
+
+// Grid of a fused launch over tiles [t0, t1) and the visit slots per CTA it
+// needs (a CTA visits at most every bucket of the range and at most one
+// bucket per tile it processes).
+static int fused_geometry(RsKernel fn, int dev, int64_t t0, int64_t t1, int32_t b0, int32_t b1,
+                          int* grid, int32_t* vmax) {
+    *grid = 0;
+    *vmax = 0;
+    if (t1 <= t0) return DPG_OK;
+    int st = grid_for(reinterpret_cast<const void*>(fn), kThreads, dev, t1 - t0, grid);
+    if (st != DPG_OK) return st;
+    const int64_t per_cta = (t1 - t0 + *grid - 1) / *grid;
+    const int64_t buckets = int64_t(b1) - b0;
+    *vmax = int32_t(per_cta < buckets ? per_cta : buckets);
+    return DPG_OK;
+}
+
+// Launch the fused pass described by `a` (tables and, when a norm output is
+// requested, norm scratch already filled in) on `grid` CTAs, then the norm
+// finalize of buckets [a.b0, a.b1).
+static int launch_fused(RsKernel fn, const RsAdamArgs& a, int grid, float* sqnorm,
+                        int64_t* nonfinite, cudaStream_t s, const char* who) {
+    int st = DPG_OK;
+    if (a.t1 > a.t0) {
+        cudaEvent_t ev0 = t_fused_start, ev1 = t_fused_stop;
+        t_fused_start = t_fused_stop = nullptr;
+        if (ev0) DPG_CUDA_TRY(cudaEventRecord(ev0, s));
+        fn<<<grid, kThreads, 0, s>>>(a);
+        st = after_launch(who);
+        if (st != DPG_OK) return st;
+        if (ev1) DPG_CUDA_TRY(cudaEventRecord(ev1, s));
+    }
+    if (sqnorm || nonfinite) {
+        const int32_t n_cta = a.t1 > a.t0 ? grid : 0;
+        k_norm_finalize<<<a.b1 - a.b0, kFinalizeThreads, 0, s>>>(
+            a.vis_sq, a.vis_nf, a.vis_bucket, a.vis_count, n_cta, a.vmax, a.b0, sqnorm, nonfinite);
+        st = after_launch(who);
+    }
+    return st;
 }
 
 static int rs_adam(const dpg_plan_t* plan, const void* const* grads, int32_t grads_dtype,
@@ -597,8 +720,6 @@ static int rs_adam(const dpg_plan_t* plan, const void* const* grads, int32_t gra
     a.m = m;
     a.v = v;
     a.reduced = reduced;
-    a.part_sq = want_norm ? p.d_part_sq : nullptr;
-    a.part_nf = want_norm ? p.d_part_nf : nullptr;
     a.bucket_offset = p.d_bucket_offset;
     a.tile_begin = p.d_tile_begin;
     a.t0 = p.tile_begin[b0];
@@ -611,26 +732,19 @@ static int rs_adam(const dpg_plan_t* plan, const void* const* grads, int32_t gra
     RsKernel fn = mode == kInBf16 ? pick_rs_kernel<kInBf16>(p.R)
                 : mode == kInF32 ? pick_rs_kernel<kInF32>(p.R)
                                  : pick_rs_kernel<kInF32PlusBf16>(p.R);
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (a.t1 > a.t0) {
-        int grid = 0;
-        st = grid_for(reinterpret_cast<const void*>(fn), kThreads, p.device, a.t1 - a.t0, &grid);
-        if (st != DPG_OK) return st;
-        cudaEvent_t ev0 = t_fused_start, ev1 = t_fused_stop;
-        t_fused_start = t_fused_stop = nullptr;
-        if (ev0) DPG_CUDA_TRY(cudaEventRecord(ev0, s));
-        fn<<<grid, kThreads, 0, s>>>(a);
-        st = after_launch(who);
-        if (st != DPG_OK) return st;
-        if (ev1) DPG_CUDA_TRY(cudaEventRecord(ev1, s));
-    }
+    int grid = 0;
+    st = fused_geometry(fn, p.device, a.t0, a.t1, b0, b1, &grid, &a.vmax);
+    if (st != DPG_OK) return st;
     if (want_norm) {
-        k_norm_finalize<<<b1 - b0, kFinalizeThreads, 0, s>>>(p.d_part_sq, p.d_part_nf,
-                                                              p.d_tile_begin, b0, sqnorm, nonfinite);
-        st = after_launch(who);
-        if (st != DPG_OK) return st;
+        if (grid > p.cap_ctas || int64_t(grid) * a.vmax > p.cap_visits)
+            return fail(DPG_ERR_CUDA, "%s: norm scratch too small (%d CTAs x %d visits)", who,
+                        grid, a.vmax);
+        a.vis_sq = p.d_vis_sq;
+        a.vis_nf = p.d_vis_nf;
+        a.vis_bucket = p.d_vis_bucket;
+        a.vis_count = p.d_vis_count;
     }
-    return DPG_OK;
+    return launch_fused(fn, a, grid, sqnorm, nonfinite, static_cast<cudaStream_t>(stream), who);
 }
 
 }  // namespace dpg
@@ -770,14 +884,14 @@ static int pack_common(const dpg_plan_t* plan, const void* const* ptrs, void* fl
         a.items = p.d_items;
         a.item0 = int64_t(i0);
         a.flat = static_cast<uint16_t*>(flat);
-        int64_t n = int64_t(i1 - i0);
-        for (int64_t off = 0; off < n; off += 65535 * 1024LL) {
-            const int64_t chunk = n - off < 65535 * 1024LL ? n - off : 65535 * 1024LL;
-            a.item0 = int64_t(i0) + off;
-            dpg::k_pack<<<dim3(unsigned(chunk)), 256, 0, s>>>(a);
-            st = dpg::after_launch(who);
-            if (st != DPG_OK) return st;
-        }
+        a.n_items = int64_t(i1 - i0);
+        int grid = 0;
+        st = dpg::grid_for(reinterpret_cast<const void*>(dpg::k_pack), 256, p.device, a.n_items,
+                           &grid);
+        if (st != DPG_OK) return st;
+        dpg::k_pack<<<grid, 256, 0, s>>>(a);
+        st = dpg::after_launch(who);
+        if (st != DPG_OK) return st;
         i0 = i1;
     }
     return DPG_OK;
@@ -804,8 +918,6 @@ int dpg_unpack(const dpg_plan_t* plan, const void* flat_bf16, void* const* param
 namespace dpg {
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[DPG_NOALLOC_SCRATCH_BYTES];
-
-static size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
 
 // Device address of g_noalloc_scratch on device `dev` (current), looked up
 // once per device: in host code the symbol's name is only a host-side stand-in.
@@ -845,25 +957,34 @@ static int step_noalloc(const dpg_plan_t* plan, const void* const* grads, int32_
     if (st != DPG_OK) return st;
     st = token_scale(tokens, n_counts, &a.scale);
     if (st != DPG_OK) return st;
-
-    // layout of the static array: tables, then partials (256-byte sections)
-    const size_t nb1 = size_t(p.n_buckets) + 1;
-    const size_t n_part = size_t(p.n_tiles) * kWarps;
-    const size_t tab_bytes = round256(nb1 * sizeof(int64_t));
-    const size_t sq_bytes = round256(n_part * sizeof(float));
-    const size_t nf_bytes = round256(n_part * sizeof(int32_t));
-    const size_t need = 2 * tab_bytes + sq_bytes + nf_bytes;
-    if (need > size_t(DPG_NOALLOC_SCRATCH_BYTES))
-        return fail(DPG_ERR_INVALID_ARG,
-                    "%s: this plan (%d buckets, %lld tiles of %lld elements) needs %zu bytes of "
-                    "scratch; the library's static scratch holds %zu bytes (use dpg_step)",
-                    who, p.n_buckets, (long long)p.n_tiles, (long long)kTile, need,
-                    size_t(DPG_NOALLOC_SCRATCH_BYTES));
     if (p.n_buckets == 0) return DPG_OK;
     const bool want_norm = sqnorm || nonfinite;
     const bool has_elems = p.total_padded > 0;
     if (!has_elems && !want_norm) return DPG_OK;
     if (!has_elems) n_views = 0;
+
+    // launch geometry, then the bytes of the static array it needs: the two
+    // bucket tables and, for a norm, the visit partials of this launch
+    const int mode = grads_dtype == DPG_BF16 ? kInBf16 : (last ? kInF32PlusBf16 : kInF32);
+    RsKernel fn = mode == kInBf16 ? pick_rs_kernel<kInBf16>(p.R)
+                : mode == kInF32 ? pick_rs_kernel<kInF32>(p.R)
+                                 : pick_rs_kernel<kInF32PlusBf16>(p.R);
+    int dev = 0;
+    DPG_CUDA_TRY(cudaGetDevice(&dev));
+    int grid = 0;
+    st = fused_geometry(fn, dev, 0, p.n_tiles, 0, p.n_buckets, &grid, &a.vmax);
+    if (st != DPG_OK) return st;
+    const size_t nb1 = size_t(p.n_buckets) + 1;
+    const size_t tab_bytes = round256(nb1 * sizeof(int64_t));
+    const VisLayout L = want_norm ? vis_layout(int64_t(grid) * a.vmax, grid) : vis_layout(0, 0);
+    const size_t need = 2 * tab_bytes + L.total;
+    if (need > size_t(DPG_NOALLOC_SCRATCH_BYTES))
+        return fail(DPG_ERR_INVALID_ARG,
+                    "%s: this plan (%d buckets, %lld tiles, %d CTAs x %d bucket visits) needs %zu "
+                    "bytes of scratch; the library's static scratch holds %zu bytes (use dpg_step)",
+                    who, p.n_buckets, (long long)p.n_tiles, grid, a.vmax, need,
+                    size_t(DPG_NOALLOC_SCRATCH_BYTES));
+
     if (has_elems && !grads) return fail(DPG_ERR_INVALID_ARG, "%s: grads is NULL", who);
     if (has_elems && (!master || !m || !v))
         return fail(DPG_ERR_INVALID_ARG, "%s: master/m/v must not be NULL", who);
@@ -887,28 +1008,22 @@ static int step_noalloc(const dpg_plan_t* plan, const void* const* grads, int32_
     if (!aligned(master, 32) || !aligned(m, 32) || !aligned(v, 32))
         return fail(DPG_ERR_MISALIGNED, "%s: fp32 buffers must be 32-byte aligned", who);
 
-    int dev = 0;
-    DPG_CUDA_TRY(cudaGetDevice(&dev));
     unsigned char* base = nullptr;
     st = noalloc_scratch(dev, &base);
     if (st != DPG_OK) return st;
     int64_t* d_bucket_offset = reinterpret_cast<int64_t*>(base);
     int64_t* d_tile_begin = reinterpret_cast<int64_t*>(base + tab_bytes);
-    float* d_part_sq = reinterpret_cast<float*>(base + 2 * tab_bytes);
-    int32_t* d_part_nf = reinterpret_cast<int32_t*>(base + 2 * tab_bytes + sq_bytes);
+    unsigned char* vis = base + 2 * tab_bytes;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     // the tables of this plan, in stream order ahead of the kernels that read them
     DPG_CUDA_TRY(cudaMemcpyAsync(d_bucket_offset, p.bucket_offset.data(), nb1 * sizeof(int64_t),
                                  cudaMemcpyHostToDevice, s));
     DPG_CUDA_TRY(cudaMemcpyAsync(d_tile_begin, p.tile_begin.data(), nb1 * sizeof(int64_t),
                                  cudaMemcpyHostToDevice, s));
-
     a.master = master;
     a.m = m;
     a.v = v;
     a.reduced = nullptr;
-    a.part_sq = want_norm ? d_part_sq : nullptr;
-    a.part_nf = want_norm ? d_part_nf : nullptr;
     a.bucket_offset = d_bucket_offset;
     a.tile_begin = d_tile_begin;
     a.t0 = 0;
@@ -917,29 +1032,13 @@ static int step_noalloc(const dpg_plan_t* plan, const void* const* grads, int32_
     a.b1 = p.n_buckets;
     a.R = p.R;
     a.n_views = n_views;
-    const int mode = grads_dtype == DPG_BF16 ? kInBf16 : (last ? kInF32PlusBf16 : kInF32);
-    RsKernel fn = mode == kInBf16 ? pick_rs_kernel<kInBf16>(p.R)
-                : mode == kInF32 ? pick_rs_kernel<kInF32>(p.R)
-                                 : pick_rs_kernel<kInF32PlusBf16>(p.R);
-    if (a.t1 > a.t0) {
-        int grid = 0;
-        st = grid_for(reinterpret_cast<const void*>(fn), kThreads, dev, a.t1 - a.t0, &grid);
-        if (st != DPG_OK) return st;
-        cudaEvent_t ev0 = t_fused_start, ev1 = t_fused_stop;
-        t_fused_start = t_fused_stop = nullptr;
-        if (ev0) DPG_CUDA_TRY(cudaEventRecord(ev0, s));
-        fn<<<grid, kThreads, 0, s>>>(a);
-        st = after_launch(who);
-        if (st != DPG_OK) return st;
-        if (ev1) DPG_CUDA_TRY(cudaEventRecord(ev1, s));
-    }
     if (want_norm) {
-        k_norm_finalize<<<p.n_buckets, kFinalizeThreads, 0, s>>>(d_part_sq, d_part_nf, d_tile_begin,
-                                                                  0, sqnorm, nonfinite);
-        st = after_launch(who);
-        if (st != DPG_OK) return st;
+        a.vis_sq = reinterpret_cast<double*>(vis + L.sq);
+        a.vis_nf = reinterpret_cast<int32_t*>(vis + L.nf);
+        a.vis_bucket = reinterpret_cast<int32_t*>(vis + L.bucket);
+        a.vis_count = reinterpret_cast<int32_t*>(vis + L.count);
     }
-    return DPG_OK;
+    return launch_fused(fn, a, grid, sqnorm, nonfinite, s, who);
 }
 
 }  // namespace dpg
