@@ -37,7 +37,8 @@ sys.path.insert(0, ROOT)
 from workloads import (CONFIGS, KIND_GRAD, KIND_MASTER, flat_grads_bf16, master_f32,  # noqa: E402
                        segments, stream_seed, token_counts)
 
-KERNEL_SRC = os.path.join(ROOT, "zero_optimizer_step_gb300", "csrc", "dpg_kernels.cu")
+KERNEL_SRCS = [os.path.join(ROOT, "zero_optimizer_step_gb300", "csrc", f)
+               for f in ("dpg_kernels.cu", "dpg_internal.h")]
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
 PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
 FALLBACK_HBM_GBS = 6800.0
@@ -214,6 +215,13 @@ def load_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+def kernel_source_sha256() -> str:
+    h = hashlib.sha256()
+    for f in KERNEL_SRCS:
+        h.update(open(f, "rb").read())
+    return h.hexdigest()
+
+
 def traffic_per_launch(cfg, cap, total_padded):
     """DRAM bytes per fused launch from the committed ncu summary, if it was
     taken on the current kernel source; scaled by elements if the capture ran
@@ -222,7 +230,7 @@ def traffic_per_launch(cfg, cap, total_padded):
         t = json.load(open(TRAFFIC_FILE))["k_rs_adam"]
     except (OSError, KeyError, ValueError):
         return None
-    src = hashlib.sha256(open(KERNEL_SRC, "rb").read()).hexdigest()
+    src = kernel_source_sha256()
     if t.get("source_sha256") != src or t.get("R") != cfg.R or t.get("K", 1) != cfg.K:
         return None
     return float(t["dram_bytes_per_launch"]) * total_padded / float(t["elements"])
