@@ -136,6 +136,29 @@ int dpg_unpack(const dpg_plan_t* plan, const void* flat_bf16, void* const* param
                void* stream);
 
 /* ---------------------------------------------------------------------------
+ * Checkpoint and resharding of the optimizer state  ["Distributed Training
+ *      and Parallelism" -- Reproduction and debugging: checkpoint ownership,
+ *      resumability, mesh reconfiguration]
+ * The canonical layout is independent of the plan: parameters back to back
+ * in REGISTRATION order, no padding, element j of parameter p at
+ * sum(numels[0..p)) + j.  A state exported under one plan imports under any
+ * plan of the same parameter list (another R or cap_bytes), which is how the
+ * state moves to a different data-parallel layout.
+ * flat[k] / canon[k], k < n_arrays (1..8): DEVICE pointers to fp32 arrays
+ * (e.g. master, exp_avg, exp_avg_sq); flat arrays hold total_padded elements
+ * (32-byte aligned), canonical arrays sum(numels) elements (4-byte aligned).
+ * dpg_export_state: canon[k][c_p + j] = flat[k][offset_p + j].
+ * dpg_import_state: flat[k][offset_p + j] = canon[k][c_p + j]; every padding
+ * slot of flat[k] is set to 0.
+ * The step counter t is the caller's (dpg_hparams.step) and travels with it.
+ * ------------------------------------------------------------------------- */
+#define DPG_MAX_STATE_ARRAYS 8
+int dpg_export_state(const dpg_plan_t* plan, const float* const* flat, float* const* canon,
+                     int32_t n_arrays, void* stream);
+int dpg_import_state(const dpg_plan_t* plan, const float* const* canon, float* const* flat,
+                     int32_t n_arrays, void* stream);
+
+/* ---------------------------------------------------------------------------
  * no_sync gradient accumulation (one replica)   ["Distributed Training and
  *                    Parallelism" -- Data parallelism and the global gradient]
  * acc_f32[i] = f32(g[i]) if first != 0, else acc_f32[i] + f32(g[i]) (binary32,

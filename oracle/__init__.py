@@ -64,6 +64,8 @@ def lib() -> ctypes.CDLL:
         L.oracle_pack.argtypes = [i32, P, P, P, i64, P]
         L.oracle_unpack.argtypes = [i32, P, P, P, P]
         L.oracle_accumulate.argtypes = [i64, P, P, i32]
+        L.oracle_export_state.argtypes = [i32, P, P, P, P]
+        L.oracle_import_state.argtypes = [i32, P, P, P, i64, P]
         L.oracle_grad_scale.argtypes = [P, i32, P]
         L.oracle_grad_scale.restype = ctypes.c_int
         L.oracle_reduce_range.argtypes = [i32, P, i32, P, f32, i64, i64, P]
@@ -174,6 +176,24 @@ def unpack(plan: Plan, flat: np.ndarray) -> list:
     lib().oracle_unpack(len(outs), _ptr(plan.numels), _ptr(plan.param_offset), _ptr(flat),
                         _ptr_array(outs))
     return outs
+
+
+def export_state(plan: Plan, flat: np.ndarray) -> np.ndarray:
+    """Canonical (registration-order, unpadded) copy of one fp32 flat array."""
+    flat = _c(flat, np.float32)
+    canon = np.empty(int(plan.numels.sum()), dtype=np.float32)
+    lib().oracle_export_state(plan.numels.size, _ptr(plan.numels), _ptr(plan.param_offset),
+                              _ptr(flat), _ptr(canon))
+    return canon
+
+
+def import_state(plan: Plan, canon: np.ndarray) -> np.ndarray:
+    """Flat fp32 array of the plan's layout from a canonical one (padding 0)."""
+    canon = _c(canon, np.float32)
+    flat = np.empty(plan.total_padded, dtype=np.float32)
+    lib().oracle_import_state(plan.numels.size, _ptr(plan.numels), _ptr(plan.param_offset),
+                              _ptr(canon), plan.total_padded, _ptr(flat))
+    return flat
 
 
 def accumulate(g_bf16: np.ndarray, acc: np.ndarray, first: bool) -> np.ndarray:

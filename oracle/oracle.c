@@ -195,6 +195,34 @@ void oracle_unpack(int32_t n, const int64_t* numels, const int64_t* param_offset
 }
 
 /* ------------------------------------------------------------------------ */
+/* Checkpoint layout  [P2 "Reproduction and debugging": checkpoint            */
+/* ownership, resumability, mesh reconfiguration]                            */
+/* ------------------------------------------------------------------------ */
+/*
+ * The canonical layout of a state array holds the parameters back to back in
+ * registration order with no padding; it does not depend on the bucket plan.
+ */
+void oracle_export_state(int32_t n, const int64_t* numels, const int64_t* param_offset,
+                         const float* flat, float* canon) {
+    int64_t c = 0;
+    for (int32_t p = 0; p < n; ++p) {
+        for (int64_t i = 0; i < numels[p]; ++i) canon[c + i] = flat[param_offset[p] + i];
+        c += numels[p];
+    }
+}
+
+/* flat = 0 everywhere, then every parameter's slice from the canonical array. */
+void oracle_import_state(int32_t n, const int64_t* numels, const int64_t* param_offset,
+                         const float* canon, int64_t total, float* flat) {
+    for (int64_t i = 0; i < total; ++i) flat[i] = 0.0f;
+    int64_t c = 0;
+    for (int32_t p = 0; p < n; ++p) {
+        for (int64_t i = 0; i < numels[p]; ++i) flat[param_offset[p] + i] = canon[c + i];
+        c += numels[p];
+    }
+}
+
+/* ------------------------------------------------------------------------ */
 /* Gradient accumulation without synchronisation  [P2 "Data parallelism and */
 /* the global gradient": no_sync on intermediate microbatches]               */
 /* ------------------------------------------------------------------------ */

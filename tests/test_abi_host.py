@@ -185,3 +185,19 @@ def test_other_entry_points_validation():
     assert L.dpg_pack(plan.handle, dpg._ptrs([FAKE] * 3), FAKE + 8, None) == dpg.DPG_ERR_MISALIGNED
     assert L.dpg_step(None, None, 0, None, None, 0, None, None, None, None, None, 0, None, None,
                       None) == dpg.DPG_ERR_INVALID_ARG
+
+
+def test_state_export_import_validation():
+    L = dpg.lib()
+    plan = dpg.dpg_plan_buckets([64, 32, 320], 2048, 4)
+    two = dpg._ptrs([FAKE, FAKE])
+    assert L.dpg_export_state(plan.handle, two, two, 0, None) == dpg.DPG_ERR_INVALID_ARG
+    assert L.dpg_export_state(plan.handle, two, two, 9, None) == dpg.DPG_ERR_INVALID_ARG
+    assert L.dpg_export_state(plan.handle, None, two, 1, None) == dpg.DPG_ERR_INVALID_ARG
+    assert L.dpg_export_state(plan.handle, dpg._ptrs([0]), two, 1, None) == dpg.DPG_ERR_INVALID_ARG
+    assert L.dpg_export_state(plan.handle, dpg._ptrs([FAKE + 16]), two, 1, None) == dpg.DPG_ERR_MISALIGNED
+    assert L.dpg_import_state(plan.handle, dpg._ptrs([FAKE + 2]), two, 1, None) == dpg.DPG_ERR_MISALIGNED
+    assert plan.canon_total == 416
+    # an empty plan has nothing to copy
+    empty = dpg.dpg_plan_buckets([], 1024, 2)
+    assert L.dpg_import_state(empty.handle, dpg._ptrs([0]), dpg._ptrs([0]), 1, None) == dpg.DPG_OK

@@ -60,6 +60,11 @@ MUTANTS = [
     ("norm_not_squared", "acc += gi * gi;", "acc += gi;", ["test_oracle_memory_and_step.py"]),
     ("shard_loop_ignores_owner", "int64_t lo = bucket_offset[b] + owner * shard;",
      "int64_t lo = bucket_offset[b];", ["test_oracle_memory_and_step.py"]),
+    ("export_wrong_slot", "for (int64_t i = 0; i < numels[p]; ++i) canon[c + i] = flat[param_offset[p] + i];",
+     "for (int64_t i = 0; i < numels[p]; ++i) canon[c + i] = flat[param_offset[p] + numels[p] - 1 - i];",
+     ["test_oracle_plan.py"]),
+    ("import_keeps_padding", "for (int64_t i = 0; i < total; ++i) flat[i] = 0.0f;",
+     "for (int64_t i = 0; i < total; ++i) flat[i] = flat[i];", ["test_oracle_plan.py"]),
     ("gather_truncates", "views[k][i] = oracle_f32_to_bf16(master[i]);\n    if (reduced)",
      "views[k][i] = (uint16_t)(f32_bits(master[i]) >> 16);\n    if (reduced)",
      ["test_oracle_memory_and_step.py"]),

@@ -184,3 +184,34 @@ def test_pack_unpack_bijection(oracle_lib, seed):
     assert hit.max(initial=0) <= 1
     assert np.all(flat[hit == 0] == 0)
     assert np.all(flat[hit == 1] != 0)
+
+
+@pytest.mark.parametrize("seed", range(8))
+def test_checkpoint_layout_bijection_and_reshard(oracle_lib, seed):
+    """Export/import of a state array ("Distributed Training and Parallelism",
+    Reproduction and debugging: resumability and mesh reconfiguration): the
+    canonical layout is the parameters back to back in registration order;
+    import after export restores every parameter slot and zeroes padding;
+    a state exported under one plan and imported under another (other R,
+    other cap) carries every parameter's values across unchanged."""
+    rng = np.random.Generator(np.random.Philox(700 + seed))
+    numels = random_param_list(rng, int(rng.integers(1, 80)), 3000)
+    pa = oracle_lib.plan_buckets(numels, int(rng.integers(16, 20000)), int(rng.choice([1, 2, 4, 8])))
+    pb = oracle_lib.plan_buckets(numels, int(rng.integers(16, 20000)), int(rng.choice([1, 3, 8, 16])))
+    flat = rng.standard_normal(pa.total_padded).astype(np.float32)
+    canon = oracle_lib.export_state(pa, flat)
+    assert canon.size == int(numels.sum())
+    # canonical order is registration order: parameter p's values start at sum(numels[:p])
+    c = 0
+    for p_, n in enumerate(numels):
+        np.testing.assert_array_equal(canon[c:c + n], flat[pa.param_offset[p_]:pa.param_offset[p_] + n])
+        c += int(n)
+    back = oracle_lib.import_state(pa, canon)
+    hit = np.zeros(pa.total_padded, bool)
+    for p_, n in enumerate(numels):
+        hit[pa.param_offset[p_]:pa.param_offset[p_] + n] = True
+    np.testing.assert_array_equal(back[hit], flat[hit])
+    assert not back[~hit].any()
+    # reshard: A -> canonical -> B -> canonical is the identity
+    flat_b = oracle_lib.import_state(pb, canon)
+    np.testing.assert_array_equal(oracle_lib.export_state(pb, flat_b), canon)

@@ -37,8 +37,9 @@ EXPORTED = (
     "dpg_plan_destroy", "dpg_plan_info", "dpg_plan_bucket", "dpg_plan_param",
     "dpg_plan_export", "dpg_plan_upload", "dpg_pack", "dpg_unpack", "dpg_accumulate",
     "dpg_reduce_scatter_adam", "dpg_allgather_params", "dpg_step", "dpg_launch_count",
-    "dpg_time_next_fused_launch", "dpg_step_noalloc",
+    "dpg_time_next_fused_launch", "dpg_step_noalloc", "dpg_export_state", "dpg_import_state",
 )
+DPG_MAX_STATE_ARRAYS = 8
 DPG_NOALLOC_SCRATCH_BYTES = 8 << 20
 
 
@@ -107,12 +108,14 @@ def lib() -> ctypes.CDLL:
         L.dpg_step.argtypes = [P, P, i32, P, P, i32, P, P, P, P, P, i32, P, P, P]
         L.dpg_step_noalloc.argtypes = [P, P, i32, P, P, i32, P, P, P, P, P, i32, P, P, P]
         L.dpg_launch_count.restype = i64
+        L.dpg_export_state.argtypes = [P, P, P, i32, P]
+        L.dpg_import_state.argtypes = [P, P, P, i32, P]
         L.dpg_time_next_fused_launch.argtypes = [P, P]
         L.dpg_time_next_fused_launch.restype = c_int
         for name in ("dpg_plan_buckets", "dpg_plan_info", "dpg_plan_bucket", "dpg_plan_param",
                      "dpg_plan_export", "dpg_plan_upload", "dpg_pack", "dpg_unpack",
                      "dpg_accumulate", "dpg_reduce_scatter_adam", "dpg_allgather_params",
-                     "dpg_step", "dpg_step_noalloc"):
+                     "dpg_step", "dpg_step_noalloc", "dpg_export_state", "dpg_import_state"):
             getattr(L, name).restype = c_int
         _lib = L
     return _lib
@@ -187,8 +190,9 @@ def _need(t, dtype_name: str, numel: int, what: str):
 class Plan:
     """Owning handle of a dpg_plan_t plus numpy copies of its maps."""
 
-    def __init__(self, handle: int):
+    def __init__(self, handle: int, numels=None):
         self._h = ctypes.c_void_p(handle)
+        self.numels = None if numels is None else np.asarray(numels, np.int64).copy()
         L = lib()
         n_params, n_buckets, R = ctypes.c_int32(), ctypes.c_int32(), ctypes.c_int32()
         total = ctypes.c_int64()
@@ -218,6 +222,11 @@ class Plan:
     def shard_numel(self) -> np.ndarray:
         return self.bucket_padded // self.R
 
+    @property
+    def canon_total(self) -> int:
+        """Elements of the canonical (registration-order, unpadded) layout."""
+        return int(self.numels.sum())
+
     def destroy(self):
         if getattr(self, "_h", None) is not None and _lib is not None:
             _lib.dpg_plan_destroy(self._h)
@@ -235,7 +244,7 @@ def dpg_plan_buckets(numels: Sequence[int], cap_bytes: int, R: int) -> Plan:
     out = ctypes.c_void_p()
     _check(lib().dpg_plan_buckets(n.ctypes.data if n.size else None, n.size, int(cap_bytes),
                                   int(R), ctypes.byref(out)))
-    return Plan(out.value)
+    return Plan(out.value, n)
 
 
 def dpg_plan_upload(plan: Plan):
@@ -273,6 +282,28 @@ def dpg_unpack(plan: Plan, flat_bf16: Ptr, param_grads: Sequence[Ptr], stream=No
     for k, g in enumerate(param_grads):
         _need(g, "bf16", 0, f"param_grads[{k}]")
     _check(lib().dpg_unpack(plan.handle, _ptr(flat_bf16), _ptrs(param_grads), _stream(stream)))
+
+
+def dpg_export_state(plan: Plan, flat: Sequence[Ptr], canon: Sequence[Ptr], stream=None):
+    """canon[k] <- flat[k] for the fp32 state arrays (see include/dpg.h)."""
+    if len(flat) != len(canon):
+        raise ValueError("flat and canon need the same number of arrays")
+    for k, (f, c) in enumerate(zip(flat, canon)):
+        _need(f, "f32", plan.total_padded, f"flat[{k}]")
+        _need(c, "f32", plan.canon_total, f"canon[{k}]")
+    _check(lib().dpg_export_state(plan.handle, _ptrs(flat), _ptrs(canon), len(flat),
+                                  _stream(stream)))
+
+
+def dpg_import_state(plan: Plan, canon: Sequence[Ptr], flat: Sequence[Ptr], stream=None):
+    """flat[k] <- canon[k] (padding zeroed) for the fp32 state arrays."""
+    if len(flat) != len(canon):
+        raise ValueError("flat and canon need the same number of arrays")
+    for k, (f, c) in enumerate(zip(flat, canon)):
+        _need(f, "f32", plan.total_padded, f"flat[{k}]")
+        _need(c, "f32", plan.canon_total, f"canon[{k}]")
+    _check(lib().dpg_import_state(plan.handle, _ptrs(canon), _ptrs(flat), len(flat),
+                                  _stream(stream)))
 
 
 def dpg_accumulate(plan: Plan, flat_bf16: Ptr, acc_f32: Ptr, first: bool, stream=None):

@@ -36,13 +36,15 @@ struct PackItem {
     int64_t src_off;   // element offset inside the parameter
     int64_t flat_off;  // element offset in the flat buffer
     int64_t count;     // elements copied
-    int64_t tail;      // zero elements written right after the copy (pack only)
+    int64_t tail;      // zero elements written right after the copy (pack, import)
+    int64_t canon_off; // element offset in the canonical (registration-order) layout
 };
 
 struct Plan {
     int32_t n_params = 0, n_buckets = 0, R = 1;
     int64_t cap_bytes = 0, total_padded = 0, n_tiles = 0;
     std::vector<int64_t> numels, param_offset;
+    int64_t canon_total = 0;             // sum of numels
     std::vector<int32_t> param_bucket;
     std::vector<int64_t> bucket_offset;  // n_buckets + 1 entries, last = total_padded
     std::vector<int64_t> tile_begin;     // n_buckets + 1 entries, last = n_tiles

@@ -440,6 +440,48 @@ __global__ void __launch_bounds__(256) k_pack(const __grid_constant__ PackArgs a
 }
 
 // ---------------------------------------------------------------------------
+// checkpoint: fp32 state between the flat bucket layout and the canonical
+// registration-order layout, one CTA per item (persistent)
+// ---------------------------------------------------------------------------
+struct StateArgs {
+    const float* src[DPG_MAX_STATE_ARRAYS];
+    float* dst[DPG_MAX_STATE_ARRAYS];
+    int32_t n_arrays;
+    int32_t to_flat;  // 1: canonical -> flat (import), 0: flat -> canonical
+    const PackItem* items;
+    int64_t n_items;
+};
+
+__device__ __forceinline__ void copy_f32(float* __restrict__ dst, const float* __restrict__ src,
+                                         int64_t n) {
+    const bool vec = ((reinterpret_cast<uintptr_t>(dst) | reinterpret_cast<uintptr_t>(src)) & 15) == 0;
+    int64_t done = 0;
+    if (vec) {
+        const int64_t n4 = n / 4;
+        const float4* s4 = reinterpret_cast<const float4*>(src);
+        float4* d4 = reinterpret_cast<float4*>(dst);
+        for (int64_t k = threadIdx.x; k < n4; k += blockDim.x) d4[k] = __ldg(s4 + k);
+        done = n4 * 4;
+    }
+    for (int64_t k = done + threadIdx.x; k < n; k += blockDim.x) dst[k] = __ldg(src + k);
+}
+
+__global__ void __launch_bounds__(256) k_state_copy(const __grid_constant__ StateArgs a) {
+    for (int64_t j = blockIdx.x; j < a.n_items; j += gridDim.x) {
+        const PackItem it = a.items[j];
+        for (int k = 0; k < a.n_arrays; ++k) {
+            if (a.to_flat) {
+                float* flat = a.dst[k] + it.flat_off;
+                if (it.count > 0) copy_f32(flat, a.src[k] + it.canon_off, it.count);
+                for (int64_t e = threadIdx.x; e < it.tail; e += blockDim.x) flat[it.count + e] = 0.0f;
+            } else if (it.count > 0) {
+                copy_f32(a.dst[k] + it.canon_off, a.src[k] + it.flat_off, it.count);
+            }
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
 // host helpers
 // ---------------------------------------------------------------------------
 static int sm_count(int dev, int* out) {
@@ -895,6 +937,52 @@ static int pack_common(const dpg_plan_t* plan, const void* const* ptrs, void* fl
         i0 = i1;
     }
     return DPG_OK;
+}
+
+static int state_common(const dpg_plan_t* plan, const float* const* src, float* const* dst,
+                        int32_t n_arrays, int to_flat, void* stream, const char* who) {
+    if (!plan) return fail(DPG_ERR_INVALID_ARG, "%s: plan is NULL", who);
+    dpg::Plan& p = const_cast<dpg_plan_t*>(plan)->p;
+    if (n_arrays < 1 || n_arrays > DPG_MAX_STATE_ARRAYS)
+        return fail(DPG_ERR_INVALID_ARG, "%s: n_arrays %d outside [1, %d]", who, n_arrays,
+                    DPG_MAX_STATE_ARRAYS);
+    if (!src || !dst) return fail(DPG_ERR_INVALID_ARG, "%s: array table is NULL", who);
+    if (p.items.empty() || p.total_padded == 0) return DPG_OK;
+    dpg::StateArgs a{};
+    for (int k = 0; k < n_arrays; ++k) {
+        const void* flat = to_flat ? static_cast<const void*>(dst[k]) : static_cast<const void*>(src[k]);
+        const void* canon = to_flat ? static_cast<const void*>(src[k]) : static_cast<const void*>(dst[k]);
+        if (!flat || (!canon && p.canon_total > 0))
+            return fail(DPG_ERR_INVALID_ARG, "%s: array %d is NULL", who, k);
+        if (!dpg::aligned(flat, 32) || !dpg::aligned(canon, 4))
+            return fail(DPG_ERR_MISALIGNED, "%s: array %d misaligned", who, k);
+        a.src[k] = src[k];
+        a.dst[k] = dst[k];
+    }
+    a.n_arrays = n_arrays;
+    a.to_flat = to_flat;
+    int st = dpg::upload(p);
+    if (st != DPG_OK) return st;
+    a.items = p.d_items;
+    a.n_items = int64_t(p.items.size());
+    int grid = 0;
+    st = dpg::grid_for(reinterpret_cast<const void*>(dpg::k_state_copy), 256, p.device, a.n_items,
+                       &grid);
+    if (st != DPG_OK) return st;
+    dpg::k_state_copy<<<grid, 256, 0, static_cast<cudaStream_t>(stream)>>>(a);
+    return dpg::after_launch(who);
+}
+
+int dpg_export_state(const dpg_plan_t* plan, const float* const* flat, float* const* canon,
+                     int32_t n_arrays, void* stream) {
+    dpg::clear_error();
+    return state_common(plan, flat, canon, n_arrays, 0, stream, "dpg_export_state");
+}
+
+int dpg_import_state(const dpg_plan_t* plan, const float* const* canon, float* const* flat,
+                     int32_t n_arrays, void* stream) {
+    dpg::clear_error();
+    return state_common(plan, canon, flat, n_arrays, 1, stream, "dpg_import_state");
 }
 
 int dpg_pack(const dpg_plan_t* plan, const void* const* param_grads, void* flat_bf16, void* stream) {

@@ -80,6 +80,9 @@ static void tile(Plan& p) {
 // gap up to the next slice (or to the end of its bucket).
 static void itemise(Plan& p) {
     p.items.clear();
+    std::vector<int64_t> canon(size_t(p.n_params) + 1, 0);
+    for (int32_t q = 0; q < p.n_params; ++q) canon[q + 1] = canon[q] + p.numels[q];
+    p.canon_total = canon[p.n_params];
     for (int32_t q = p.n_params - 1; q >= 0; --q) {
         const int64_t start = p.param_offset[q];
         const int64_t n = p.numels[q];
@@ -98,6 +101,7 @@ static void itemise(Plan& p) {
             it.count = std::min<int64_t>(kPackChunk, n - off);
             off += it.count;
             it.tail = (off == n) ? next - (start + n) : 0;
+            it.canon_off = canon[q] + it.src_off;
             p.items.push_back(it);
         } while (off < n);
     }
