@@ -226,6 +226,32 @@ int dpg_step(const dpg_plan_t* plan, const void* const* grads, int32_t grads_dty
              float* bucket_sqnorm, int64_t* bucket_nonfinite, void* stream);
 
 /* ---------------------------------------------------------------------------
+ * One whole step with global gradient-norm clipping   ["Parallelisms" --
+ *      ZeRO-2: clipping needs the norm over all gradient shards before any
+ *      weight is updated; only the local squared norms are all-reduced]
+ * Same arguments and semantics as dpg_step, except that the normalised
+ * reduced gradient g of every element is first multiplied by
+ *   coef = fp32( min(1, max_norm / (||g||_2 + 1e-6)) ),
+ * ||g||_2 over ALL buckets (squares of the fp32 g summed exactly in double,
+ * square root and quotient in double; a NaN norm gives a NaN coefficient).
+ * Pass 1 reduces and scales every element and sums its squares per bucket;
+ * the coefficient is computed on the device (no host synchronisation); pass
+ * 2 applies g * coef to Adam and writes the bf16 view(s).
+ * max_norm: finite, > 0.  bucket_sqnorm / bucket_nonfinite (nullable): of the
+ * UNclipped g.  reduced_grad (nullable, device, flat fp32, 32-byte aligned):
+ * when given, pass 1 stores g there and pass 2 reads it instead of reading
+ * the R replicas again ((2R+34) instead of (4R+26) bytes per parameter).
+ * clip_out (nullable, device float[2]): receives {||g||_2, coef}.
+ * Uses the plan's scratch like dpg_step (same no-overlap rule).
+ * ------------------------------------------------------------------------- */
+int dpg_step_clipped(const dpg_plan_t* plan, const void* const* grads, int32_t grads_dtype,
+                     const void* const* last_micro_bf16, const int64_t* valid_tokens,
+                     int32_t n_counts, const dpg_hparams* hp, double max_norm, float* master,
+                     float* exp_avg, float* exp_avg_sq, void* const* param_views, int32_t n_views,
+                     float* bucket_sqnorm, int64_t* bucket_nonfinite, float* reduced_grad,
+                     float* clip_out, void* stream);
+
+/* ---------------------------------------------------------------------------
  * dpg_step without any device allocation.  The pages have no counterpart to
  * this entry point: it exists for callers that must not have the library
  * allocate device memory -- for example code whose device memory is owned

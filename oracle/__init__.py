@@ -65,6 +65,8 @@ def lib() -> ctypes.CDLL:
         L.oracle_unpack.argtypes = [i32, P, P, P, P]
         L.oracle_accumulate.argtypes = [i64, P, P, i32]
         L.oracle_export_state.argtypes = [i32, P, P, P, P]
+        L.oracle_clip_coef.argtypes = [P, i64, f64, P, P]
+        L.oracle_scale_range.argtypes = [P, i64, f32]
         L.oracle_import_state.argtypes = [i32, P, P, P, i64, P]
         L.oracle_grad_scale.argtypes = [P, i32, P]
         L.oracle_grad_scale.restype = ctypes.c_int
@@ -244,6 +246,22 @@ def allreduce(grads: Sequence[np.ndarray], scale: float, last=None) -> list:
                            None if ls is None else _ptr_array(ls), float(scale),
                            _ptr_array(outs))
     return outs
+
+
+def clip_coef(g: np.ndarray, max_norm: float):
+    """(global L2 norm in binary64, binary32 clip coefficient)."""
+    g = _c(g, np.float32)
+    norm = ctypes.c_double(0.0)
+    coef = ctypes.c_float(0.0)
+    lib().oracle_clip_coef(_ptr(g), g.size, float(max_norm), ctypes.byref(norm), ctypes.byref(coef))
+    return norm.value, np.float32(coef.value)
+
+
+def scale(g: np.ndarray, coef) -> np.ndarray:
+    """A copy of g multiplied by coef in binary32."""
+    out = np.array(g, dtype=np.float32, copy=True)
+    lib().oracle_scale_range(_ptr(out), out.size, float(coef))
+    return out
 
 
 def adam(g, master, m, v, *, lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8, wd=0.0, t=1):

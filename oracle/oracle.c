@@ -313,6 +313,39 @@ void oracle_allreduce(int32_t R, int64_t n, const void* const* grads, int32_t dt
 }
 
 /* ------------------------------------------------------------------------ */
+/* Global gradient-norm clipping  [P1 "ZeRO-2": the norm over all gradient    */
+/* shards is needed before any weight is updated]                             */
+/* ------------------------------------------------------------------------ */
+/*
+ * ||g||_2 over every element of the normalised reduced gradient (squares of
+ * the binary32 values summed in binary64 in index order), and the clip
+ * coefficient min(1, max_norm / (||g|| + 1e-6)) computed in binary64 and
+ * rounded once to binary32 (the convention of torch.nn.utils.clip_grad_norm_;
+ * a NaN norm gives a NaN coefficient).
+ */
+void oracle_clip_coef(const float* g, int64_t n, double max_norm, double* norm_out,
+                      float* coef_out) {
+    double total = 0.0;
+    for (int64_t i = 0; i < n; ++i) {
+        double x = (double)g[i];
+        total += x * x;
+    }
+    double norm = sqrt(total);
+    double c = max_norm / (norm + 1e-6);
+    if (c > 1.0) c = 1.0;
+    *norm_out = norm;
+    *coef_out = (float)c;
+}
+
+/* g[i] = g[i] * coef (binary32). */
+void oracle_scale_range(float* g, int64_t n, float coef) {
+    for (int64_t i = 0; i < n; ++i) {
+        float y = g[i] * coef;
+        g[i] = y;
+    }
+}
+
+/* ------------------------------------------------------------------------ */
 /* Mixed-precision Adam on one shard  [P1 "ZeRO-1": m, v, step counter and   */
 /* fp32 master weight; KB Algorithm 1]                                        */
 /* ------------------------------------------------------------------------ */

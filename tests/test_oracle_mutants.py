@@ -65,6 +65,9 @@ MUTANTS = [
      ["test_oracle_plan.py"]),
     ("import_keeps_padding", "for (int64_t i = 0; i < total; ++i) flat[i] = 0.0f;",
      "for (int64_t i = 0; i < total; ++i) flat[i] = flat[i];", ["test_oracle_plan.py"]),
+    ("clip_unclamped", "if (c > 1.0) c = 1.0;\n    *norm_out", "*norm_out", ["test_oracle_clip.py"]),
+    ("clip_norm_squared", "double norm = sqrt(total);", "double norm = total;",
+     ["test_oracle_clip.py"]),
     ("gather_truncates", "views[k][i] = oracle_f32_to_bf16(master[i]);\n    if (reduced)",
      "views[k][i] = (uint16_t)(f32_bits(master[i]) >> 16);\n    if (reduced)",
      ["test_oracle_memory_and_step.py"]),

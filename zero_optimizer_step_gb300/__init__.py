@@ -38,6 +38,7 @@ EXPORTED = (
     "dpg_plan_export", "dpg_plan_upload", "dpg_pack", "dpg_unpack", "dpg_accumulate",
     "dpg_reduce_scatter_adam", "dpg_allgather_params", "dpg_step", "dpg_launch_count",
     "dpg_time_next_fused_launch", "dpg_step_noalloc", "dpg_export_state", "dpg_import_state",
+    "dpg_step_clipped",
 )
 DPG_MAX_STATE_ARRAYS = 8
 DPG_NOALLOC_SCRATCH_BYTES = 8 << 20
@@ -108,6 +109,8 @@ def lib() -> ctypes.CDLL:
         L.dpg_step.argtypes = [P, P, i32, P, P, i32, P, P, P, P, P, i32, P, P, P]
         L.dpg_step_noalloc.argtypes = [P, P, i32, P, P, i32, P, P, P, P, P, i32, P, P, P]
         L.dpg_launch_count.restype = i64
+        L.dpg_step_clipped.argtypes = [P, P, i32, P, P, i32, P, ctypes.c_double, P, P, P, P, i32,
+                                       P, P, P, P, P]
         L.dpg_export_state.argtypes = [P, P, P, i32, P]
         L.dpg_import_state.argtypes = [P, P, P, i32, P]
         L.dpg_time_next_fused_launch.argtypes = [P, P]
@@ -115,7 +118,8 @@ def lib() -> ctypes.CDLL:
         for name in ("dpg_plan_buckets", "dpg_plan_info", "dpg_plan_bucket", "dpg_plan_param",
                      "dpg_plan_export", "dpg_plan_upload", "dpg_pack", "dpg_unpack",
                      "dpg_accumulate", "dpg_reduce_scatter_adam", "dpg_allgather_params",
-                     "dpg_step", "dpg_step_noalloc", "dpg_export_state", "dpg_import_state"):
+                     "dpg_step", "dpg_step_noalloc", "dpg_export_state", "dpg_import_state",
+                     "dpg_step_clipped"):
             getattr(L, name).restype = c_int
         _lib = L
     return _lib
@@ -374,6 +378,36 @@ def dpg_step(plan: Plan, grads: Sequence[Ptr], valid_tokens, hp: HParams, master
         tok.ctypes.data, n_tok, ctypes.byref(hpc), _ptr(master), _ptr(exp_avg), _ptr(exp_avg_sq),
         _ptrs(param_views), len(param_views), _ptr(bucket_sqnorm), _ptr(bucket_nonfinite),
         _stream(stream)))
+
+
+def dpg_step_clipped(plan: Plan, grads: Sequence[Ptr], valid_tokens, hp: HParams, max_norm: float,
+                     master: Ptr, exp_avg: Ptr, exp_avg_sq: Ptr, param_views: Sequence[Ptr] = (),
+                     *, last_micro: Sequence[Ptr] = None, bucket_sqnorm: Ptr = None,
+                     bucket_nonfinite: Ptr = None, reduced_grad: Ptr = None, clip_out: Ptr = None,
+                     grads_dtype: Optional[int] = None, stream=None):
+    """dpg_step with global gradient-norm clipping (see include/dpg.h)."""
+    if len(grads) != plan.R:
+        raise ValueError(f"need R={plan.R} gradient buffers, got {len(grads)}")
+    gd = _grad_dtype(grads) if grads_dtype is None else grads_dtype
+    N = plan.total_padded
+    for k, g in enumerate(grads):
+        _need(g, "bf16" if gd == DPG_BF16 else "f32", N, f"grads[{k}]")
+    for k, g in enumerate(last_micro or ()):
+        _need(g, "bf16", N, f"last_micro[{k}]")
+    for name, t in (("master", master), ("exp_avg", exp_avg), ("exp_avg_sq", exp_avg_sq),
+                    ("reduced_grad", reduced_grad)):
+        _need(t, "f32", N, name)
+    for k, t in enumerate(param_views):
+        _need(t, "bf16", N, f"param_views[{k}]")
+    _need(bucket_sqnorm, "f32", plan.n_buckets, "bucket_sqnorm")
+    _need(clip_out, "f32", 2, "clip_out")
+    tok, n_tok = _tokens(valid_tokens)
+    hpc = hp.c()
+    _check(lib().dpg_step_clipped(
+        plan.handle, _ptrs(grads), gd, None if last_micro is None else _ptrs(last_micro),
+        tok.ctypes.data, n_tok, ctypes.byref(hpc), float(max_norm), _ptr(master), _ptr(exp_avg),
+        _ptr(exp_avg_sq), _ptrs(param_views), len(param_views), _ptr(bucket_sqnorm),
+        _ptr(bucket_nonfinite), _ptr(reduced_grad), _ptr(clip_out), _stream(stream)))
 
 
 def dpg_step_noalloc(plan: Plan, grads: Sequence[Ptr], valid_tokens, hp: HParams, master: Ptr,

@@ -64,6 +64,10 @@ struct Plan {
     int32_t* d_vis_count = nullptr; // cap_ctas
     int64_t cap_visits = 0;
     int32_t cap_ctas = 0;
+    // global-norm clipping: per-bucket fp64 squared norms and the coefficient
+    void* d_clip = nullptr;
+    double* d_bucket_sq64 = nullptr;  // n_buckets + 1
+    float* d_clip_coef = nullptr;     // 1
 };
 
 // thread-local error message

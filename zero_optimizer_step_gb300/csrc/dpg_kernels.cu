@@ -116,7 +116,13 @@ __device__ __forceinline__ uint4 narrow8(const float* f) {
 // ---------------------------------------------------------------------------
 // fused reduce-scatter -> scale -> Adam -> all-gather
 // ---------------------------------------------------------------------------
-enum : int { kInBf16 = 0, kInF32 = 1, kInF32PlusBf16 = 2 };
+enum : int { kInBf16 = 0, kInF32 = 1, kInF32PlusBf16 = 2, kInReduced = 3 };
+
+// Passes of the fused kernel.  kFull: reduce, scale, Adam, cast (the step).
+// With global norm clipping the step takes two passes: kNormOnly reduces and
+// scales, accumulates exact (fp64) squares and may store g; kUpdate then
+// multiplies g by the clip coefficient found on the device and runs Adam.
+enum : int { kFull = 0, kNormOnly = 1, kUpdate = 2 };
 
 struct RsAdamArgs {
     const void* grads[DPG_MAX_REPLICAS];
@@ -139,6 +145,8 @@ struct RsAdamArgs {
     float scale;         // fp32(1/G)
     float beta1, beta2, omb1, omb2, bias1, bias2, lr, eps, lr_wd;
     int32_t decay;
+    const float* g_in;      // kInReduced: the normalised reduced gradient
+    const float* clip_coef; // kUpdate: device scalar, g <- g * coef
 };
 
 // Bucket holding tile t, searching forward from bucket b (tile_begin[b] <= t
@@ -160,7 +168,11 @@ __device__ __forceinline__ int bucket_of_tile(const int64_t* tile_begin, int b, 
 template <int RT, int MODE>
 __device__ __forceinline__ void reduce_vector(const RsAdamArgs& a, int64_t i, float* s) {
     const int R = RT > 0 ? RT : a.R;
-    if constexpr (MODE == kInBf16) {
+    if constexpr (MODE == kInReduced) {
+        const F8 x = ld_grad_f8(a.g_in + i);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) s[j] = x.v[j];
+    } else if constexpr (MODE == kInBf16) {
         if constexpr (RT > 0) {
             uint4 x[RT];
 #pragma unroll
@@ -228,9 +240,11 @@ __device__ __forceinline__ void flush_visit(const RsAdamArgs& a, int bucket, int
     if (threadIdx.x == 0) a.vis_bucket[slot] = bucket;
 }
 
-template <int RT, int MODE>
+template <int RT, int MODE, int PHASE>
 __global__ void __launch_bounds__(kThreads, 1) k_rs_adam(const __grid_constant__ RsAdamArgs a) {
-    const bool norm = a.vis_sq != nullptr;
+    const bool norm = PHASE != kUpdate && a.vis_sq != nullptr;
+    float coef = 1.0f;
+    if constexpr (PHASE == kUpdate) coef = __ldg(a.clip_coef);
     int b = a.b0;
     int cur = -1;  // bucket of the running norm sums
     int visit = 0;
@@ -250,39 +264,59 @@ __global__ void __launch_bounds__(kThreads, 1) k_rs_adam(const __grid_constant__
         if (i < bucket_end) {
             float s[8];
             reduce_vector<RT, MODE>(a, i, s);
-            F8 w = ld_state_f8(a.master + i);
-            F8 m = ld_state_f8(a.m + i);
-            F8 v = ld_state_f8(a.v + i);
             float g[8];
-            float tsq = 0.0f;
+            if constexpr (PHASE == kNormOnly) {
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                g[j] = __fmul_rn(s[j], a.scale);
-                float wj = w.v[j];
-                if (a.decay) wj = __fsub_rn(wj, __fmul_rn(a.lr_wd, wj));
-                const float mj = __fadd_rn(__fmul_rn(a.beta1, m.v[j]), __fmul_rn(a.omb1, g[j]));
-                const float vj =
-                    __fadd_rn(__fmul_rn(a.beta2, v.v[j]), __fmul_rn(a.omb2, __fmul_rn(g[j], g[j])));
-                const float m_hat = __fdiv_rn(mj, a.bias1);
-                const float v_hat = __fdiv_rn(vj, a.bias2);
-                const float u = __fdiv_rn(m_hat, __fadd_rn(__fsqrt_rn(v_hat), a.eps));
-                w.v[j] = __fsub_rn(wj, __fmul_rn(a.lr, u));
-                m.v[j] = mj;
-                v.v[j] = vj;
-                tsq = fmaf(g[j], g[j], tsq);
-                nf += (__float_as_uint(g[j]) & 0x7F800000u) == 0x7F800000u;
-            }
-            if (norm) sq += double(tsq);
-            st_f8(a.master + i, w);
-            st_f8(a.m + i, m);
-            st_f8(a.v + i, v);
-            const uint4 p = narrow8(w.v);
-            for (int k = 0; k < a.n_views; ++k) st_u4(static_cast<uint16_t*>(a.views[k]) + i, p);
-            if (a.reduced) {
-                F8 gg;
+                for (int j = 0; j < 8; ++j) g[j] = __fmul_rn(s[j], a.scale);
+                // exact squares (a binary32 square is exact in binary64)
+                double tsq = 0.0;
 #pragma unroll
-                for (int j = 0; j < 8; ++j) gg.v[j] = g[j];
-                st_f8(a.reduced + i, gg);
+                for (int j = 0; j < 8; ++j) {
+                    tsq += double(g[j]) * double(g[j]);
+                    nf += (__float_as_uint(g[j]) & 0x7F800000u) == 0x7F800000u;
+                }
+                if (norm) sq += tsq;
+                if (a.reduced) {
+                    F8 gg;
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) gg.v[j] = g[j];
+                    st_f8(a.reduced + i, gg);
+                }
+            } else {
+                F8 w = ld_state_f8(a.master + i);
+                F8 m = ld_state_f8(a.m + i);
+                F8 v = ld_state_f8(a.v + i);
+                float tsq = 0.0f;
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    g[j] = MODE == kInReduced ? s[j] : __fmul_rn(s[j], a.scale);
+                    if constexpr (PHASE == kUpdate) g[j] = __fmul_rn(g[j], coef);
+                    float wj = w.v[j];
+                    if (a.decay) wj = __fsub_rn(wj, __fmul_rn(a.lr_wd, wj));
+                    const float mj = __fadd_rn(__fmul_rn(a.beta1, m.v[j]), __fmul_rn(a.omb1, g[j]));
+                    const float vj = __fadd_rn(__fmul_rn(a.beta2, v.v[j]),
+                                               __fmul_rn(a.omb2, __fmul_rn(g[j], g[j])));
+                    const float m_hat = __fdiv_rn(mj, a.bias1);
+                    const float v_hat = __fdiv_rn(vj, a.bias2);
+                    const float u = __fdiv_rn(m_hat, __fadd_rn(__fsqrt_rn(v_hat), a.eps));
+                    w.v[j] = __fsub_rn(wj, __fmul_rn(a.lr, u));
+                    m.v[j] = mj;
+                    v.v[j] = vj;
+                    tsq = fmaf(g[j], g[j], tsq);
+                    nf += (__float_as_uint(g[j]) & 0x7F800000u) == 0x7F800000u;
+                }
+                if (norm) sq += double(tsq);
+                st_f8(a.master + i, w);
+                st_f8(a.m + i, m);
+                st_f8(a.v + i, v);
+                const uint4 p = narrow8(w.v);
+                for (int k = 0; k < a.n_views; ++k) st_u4(static_cast<uint16_t*>(a.views[k]) + i, p);
+                if (PHASE == kFull && a.reduced) {
+                    F8 gg;
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) gg.v[j] = g[j];
+                    st_f8(a.reduced + i, gg);
+                }
             }
         }
     }
@@ -302,7 +336,8 @@ constexpr int kFinalizeThreads = 256;
 __global__ void __launch_bounds__(kFinalizeThreads)
 k_norm_finalize(const double* __restrict__ vis_sq, const int32_t* __restrict__ vis_nf,
                 const int32_t* __restrict__ vis_bucket, const int32_t* __restrict__ vis_count,
-                int32_t n_cta, int32_t vmax, int32_t b0, float* sqnorm, int64_t* nonfinite) {
+                int32_t n_cta, int32_t vmax, int32_t b0, float* sqnorm, int64_t* nonfinite,
+                double* sqnorm64) {
     __shared__ double s_sq[kFinalizeThreads];
     __shared__ long long s_nf[kFinalizeThreads];
     const int b = b0 + blockIdx.x;
@@ -338,6 +373,33 @@ k_norm_finalize(const double* __restrict__ vis_sq, const int32_t* __restrict__ v
     if (threadIdx.x == 0) {
         if (sqnorm) sqnorm[b] = float(s_sq[0]);
         if (nonfinite) nonfinite[b] = s_nf[0];
+        if (sqnorm64) sqnorm64[b] = s_sq[0];
+    }
+}
+
+// Global clip coefficient from the per-bucket squared norms (one CTA, fixed
+// order): norm = sqrt(sum), coef = min(1, max_norm / (norm + 1e-6)) in double,
+// stored as fp32; a NaN norm gives a NaN coefficient (it is not clamped away).
+__global__ void __launch_bounds__(256) k_clip_coef(const double* __restrict__ bucket_sq, int32_t nb,
+                                                   double max_norm, float* coef, float* out) {
+    __shared__ double sh[256];
+    double acc = 0.0;
+    for (int b = threadIdx.x; b < nb; b += 256) acc += bucket_sq[b];
+    sh[threadIdx.x] = acc;
+    __syncthreads();
+    for (int w = 128; w > 0; w >>= 1) {
+        if (threadIdx.x < w) sh[threadIdx.x] += sh[threadIdx.x + w];
+        __syncthreads();
+    }
+    if (threadIdx.x == 0) {
+        const double norm = sqrt(sh[0]);
+        double c = max_norm / (norm + 1e-6);
+        if (c > 1.0) c = 1.0;
+        *coef = float(c);
+        if (out) {
+            out[0] = float(norm);
+            out[1] = float(c);
+        }
     }
 }
 
@@ -579,12 +641,15 @@ int upload(Plan& p) {
     if (e == cudaSuccess) e = cudaMalloc(&tb, nb1 * sizeof(int64_t));
     if (e == cudaSuccess) e = cudaMalloc(&it, n_items * sizeof(PackItem));
     if (e == cudaSuccess) e = cudaMalloc(&vis, L.total);
+    const size_t clip_sq_bytes = round256(nb1 * sizeof(double));
+    void* clip = nullptr;
+    if (e == cudaSuccess) e = cudaMalloc(&clip, clip_sq_bytes + 256);
     if (e == cudaSuccess) e = cudaMemcpy(bo, p.bucket_offset.data(), nb1 * sizeof(int64_t), cudaMemcpyHostToDevice);
     if (e == cudaSuccess) e = cudaMemcpy(tb, p.tile_begin.data(), nb1 * sizeof(int64_t), cudaMemcpyHostToDevice);
     if (e == cudaSuccess && !p.items.empty())
         e = cudaMemcpy(it, p.items.data(), p.items.size() * sizeof(PackItem), cudaMemcpyHostToDevice);
     if (e != cudaSuccess) {
-        cudaFree(bo); cudaFree(tb); cudaFree(it); cudaFree(vis);
+        cudaFree(bo); cudaFree(tb); cudaFree(it); cudaFree(vis); cudaFree(clip);
         cudaGetLastError();
         return fail(e == cudaErrorMemoryAllocation ? DPG_ERR_OOM : DPG_ERR_CUDA,
                     "plan upload: %s", cudaGetErrorString(e));
@@ -598,6 +663,9 @@ int upload(Plan& p) {
     p.d_vis_nf = reinterpret_cast<int32_t*>(base + L.nf);
     p.d_vis_bucket = reinterpret_cast<int32_t*>(base + L.bucket);
     p.d_vis_count = reinterpret_cast<int32_t*>(base + L.count);
+    p.d_clip = clip;
+    p.d_bucket_sq64 = static_cast<double*>(clip);
+    p.d_clip_coef = reinterpret_cast<float*>(static_cast<unsigned char*>(clip) + clip_sq_bytes);
     p.cap_visits = cap_visits;
     p.cap_ctas = int32_t(cap_ctas);
     p.device = dev;
@@ -614,6 +682,7 @@ void release_device(Plan& p) {
         cudaFree(p.d_tile_begin);
         cudaFree(p.d_items);
         cudaFree(p.d_vis);
+        cudaFree(p.d_clip);
     }
     if (have_cur) cudaSetDevice(cur);
     cudaGetLastError();
@@ -656,15 +725,22 @@ static int token_scale(const int64_t* tokens, int32_t n, float* scale) {
 
 using RsKernel = void (*)(RsAdamArgs);
 
-template <int MODE>
+template <int MODE, int PHASE = kFull>
 static RsKernel pick_rs_kernel(int R) {
     switch (R) {
-        case 1: return k_rs_adam<1, MODE>;
-        case 2: return k_rs_adam<2, MODE>;
-        case 4: return k_rs_adam<4, MODE>;
-        case 8: return k_rs_adam<8, MODE>;
-        default: return k_rs_adam<0, MODE>;
+        case 1: return k_rs_adam<1, MODE, PHASE>;
+        case 2: return k_rs_adam<2, MODE, PHASE>;
+        case 4: return k_rs_adam<4, MODE, PHASE>;
+        case 8: return k_rs_adam<8, MODE, PHASE>;
+        default: return k_rs_adam<0, MODE, PHASE>;
     }
+}
+
+template <int PHASE>
+static RsKernel pick_rs_kernel_mode(int mode, int R) {
+    return mode == kInBf16 ? pick_rs_kernel<kInBf16, PHASE>(R)
+         : mode == kInF32  ? pick_rs_kernel<kInF32, PHASE>(R)
+                           : pick_rs_kernel<kInF32PlusBf16, PHASE>(R);
 }
 
 // Grid of a fused launch over tiles [t0, t1) and the visit slots per CTA it
@@ -687,7 +763,8 @@ static int fused_geometry(RsKernel fn, int dev, int64_t t0, int64_t t1, int32_t 
 // requested, norm scratch already filled in) on `grid` CTAs, then the norm
 // finalize of buckets [a.b0, a.b1).
 static int launch_fused(RsKernel fn, const RsAdamArgs& a, int grid, float* sqnorm,
-                        int64_t* nonfinite, cudaStream_t s, const char* who) {
+                        int64_t* nonfinite, cudaStream_t s, const char* who,
+                        double* sqnorm64 = nullptr) {
     int st = DPG_OK;
     if (a.t1 > a.t0) {
         cudaEvent_t ev0 = t_fused_start, ev1 = t_fused_stop;
@@ -698,10 +775,11 @@ static int launch_fused(RsKernel fn, const RsAdamArgs& a, int grid, float* sqnor
         if (st != DPG_OK) return st;
         if (ev1) DPG_CUDA_TRY(cudaEventRecord(ev1, s));
     }
-    if (sqnorm || nonfinite) {
+    if (sqnorm || nonfinite || sqnorm64) {
         const int32_t n_cta = a.t1 > a.t0 ? grid : 0;
         k_norm_finalize<<<a.b1 - a.b0, kFinalizeThreads, 0, s>>>(
-            a.vis_sq, a.vis_nf, a.vis_bucket, a.vis_count, n_cta, a.vmax, a.b0, sqnorm, nonfinite);
+            a.vis_sq, a.vis_nf, a.vis_bucket, a.vis_count, n_cta, a.vmax, a.b0, sqnorm, nonfinite,
+            sqnorm64);
         st = after_launch(who);
     }
     return st;
@@ -789,6 +867,125 @@ static int rs_adam(const dpg_plan_t* plan, const void* const* grads, int32_t gra
     return launch_fused(fn, a, grid, sqnorm, nonfinite, static_cast<cudaStream_t>(stream), who);
 }
 
+// Validate the per-call buffers of a whole-plan step and copy them into `a`.
+static int fill_step_args(const Plan& p, const void* const* grads, int32_t grads_dtype,
+                          const void* const* last, const dpg_hparams* hp, const int64_t* tokens,
+                          int32_t n_counts, float* master, float* m, float* v,
+                          void* const* views, int32_t n_views, RsAdamArgs& a, const char* who) {
+    if (grads_dtype != DPG_BF16 && grads_dtype != DPG_F32)
+        return fail(DPG_ERR_INVALID_ARG, "%s: grads_dtype %d unknown", who, grads_dtype);
+    if (last && grads_dtype != DPG_F32)
+        return fail(DPG_ERR_INVALID_ARG, "%s: last_micro_bf16 needs fp32 accumulation grads", who);
+    if (n_views < 0 || n_views > DPG_MAX_VIEWS)
+        return fail(DPG_ERR_INVALID_ARG, "%s: n_views %d outside [0, %d]", who, n_views, DPG_MAX_VIEWS);
+    int st = adam_constants(hp, a);
+    if (st != DPG_OK) return st;
+    st = token_scale(tokens, n_counts, &a.scale);
+    if (st != DPG_OK) return st;
+    const bool has_elems = p.total_padded > 0;
+    if (!has_elems) n_views = 0;
+    if (has_elems && !grads) return fail(DPG_ERR_INVALID_ARG, "%s: grads is NULL", who);
+    if (has_elems && (!master || !m || !v))
+        return fail(DPG_ERR_INVALID_ARG, "%s: master/m/v must not be NULL", who);
+    if (n_views > 0 && !views) return fail(DPG_ERR_INVALID_ARG, "%s: param_views is NULL", who);
+    const uintptr_t galign = grads_dtype == DPG_BF16 ? 16 : 32;
+    for (int r = 0; has_elems && r < p.R; ++r) {
+        if (!grads[r]) return fail(DPG_ERR_INVALID_ARG, "%s: grads[%d] is NULL", who, r);
+        if (!aligned(grads[r], galign)) return fail(DPG_ERR_MISALIGNED, "%s: grads[%d] misaligned", who, r);
+        a.grads[r] = grads[r];
+        if (last) {
+            if (!last[r]) return fail(DPG_ERR_INVALID_ARG, "%s: last_micro_bf16[%d] is NULL", who, r);
+            if (!aligned(last[r], 16)) return fail(DPG_ERR_MISALIGNED, "%s: last_micro_bf16[%d] misaligned", who, r);
+            a.last[r] = last[r];
+        }
+    }
+    for (int k = 0; k < n_views; ++k) {
+        if (!views[k]) return fail(DPG_ERR_INVALID_ARG, "%s: param_views[%d] is NULL", who, k);
+        if (!aligned(views[k], 16)) return fail(DPG_ERR_MISALIGNED, "%s: param_views[%d] misaligned", who, k);
+        a.views[k] = views[k];
+    }
+    if (!aligned(master, 32) || !aligned(m, 32) || !aligned(v, 32))
+        return fail(DPG_ERR_MISALIGNED, "%s: fp32 buffers must be 32-byte aligned", who);
+    a.master = master;
+    a.m = m;
+    a.v = v;
+    a.n_views = n_views;
+    a.R = p.R;
+    return DPG_OK;
+}
+
+// Whole step with global gradient-norm clipping: norm pass, coefficient on
+// the device, update pass (see dpg_step_clipped in include/dpg.h).
+static int step_clipped(const dpg_plan_t* plan, const void* const* grads, int32_t grads_dtype,
+                        const void* const* last, const int64_t* tokens, int32_t n_counts,
+                        const dpg_hparams* hp, double max_norm, float* master, float* m,
+                        float* v, void* const* views, int32_t n_views, float* sqnorm,
+                        int64_t* nonfinite, float* reduced, float* clip_out, void* stream) {
+    const char* who = "dpg_step_clipped";
+    if (!plan) return fail(DPG_ERR_INVALID_ARG, "%s: plan is NULL", who);
+    Plan& p = const_cast<dpg_plan_t*>(plan)->p;
+    if (!(max_norm > 0.0) || !std::isfinite(max_norm))
+        return fail(DPG_ERR_INVALID_ARG, "%s: max_norm must be finite and > 0", who);
+    RsAdamArgs a{};
+    int st = fill_step_args(p, grads, grads_dtype, last, hp, tokens, n_counts, master, m, v, views,
+                            n_views, a, who);
+    if (st != DPG_OK) return st;
+    if (!aligned(reduced, 32)) return fail(DPG_ERR_MISALIGNED, "%s: reduced_grad misaligned", who);
+    if (p.n_buckets == 0) return DPG_OK;
+    st = upload(p);
+    if (st != DPG_OK) return st;
+    a.bucket_offset = p.d_bucket_offset;
+    a.tile_begin = p.d_tile_begin;
+    a.t0 = 0;
+    a.t1 = p.n_tiles;
+    a.b0 = 0;
+    a.b1 = p.n_buckets;
+    const int mode = grads_dtype == DPG_BF16 ? kInBf16 : (last ? kInF32PlusBf16 : kInF32);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+
+    // pass 1: reduce, scale, exact squares per bucket (and g, when a buffer is given)
+    RsAdamArgs a1 = a;
+    a1.reduced = reduced;
+    RsKernel fn1 = pick_rs_kernel_mode<kNormOnly>(mode, p.R);
+    int grid1 = 0;
+    st = fused_geometry(fn1, p.device, a1.t0, a1.t1, 0, p.n_buckets, &grid1, &a1.vmax);
+    if (st != DPG_OK) return st;
+    if (grid1 > p.cap_ctas || int64_t(grid1) * a1.vmax > p.cap_visits)
+        return fail(DPG_ERR_CUDA, "%s: norm scratch too small", who);
+    a1.vis_sq = p.d_vis_sq;
+    a1.vis_nf = p.d_vis_nf;
+    a1.vis_bucket = p.d_vis_bucket;
+    a1.vis_count = p.d_vis_count;
+    if (a1.t1 > a1.t0) {
+        fn1<<<grid1, kThreads, 0, s>>>(a1);
+        st = after_launch(who);
+        if (st != DPG_OK) return st;
+    }
+    k_norm_finalize<<<p.n_buckets, kFinalizeThreads, 0, s>>>(
+        a1.vis_sq, a1.vis_nf, a1.vis_bucket, a1.vis_count, a1.t1 > a1.t0 ? grid1 : 0, a1.vmax, 0,
+        sqnorm, nonfinite, p.d_bucket_sq64);
+    st = after_launch(who);
+    if (st != DPG_OK) return st;
+    // the coefficient, on the device: no host synchronisation
+    k_clip_coef<<<1, 256, 0, s>>>(p.d_bucket_sq64, p.n_buckets, max_norm, p.d_clip_coef, clip_out);
+    st = after_launch(who);
+    if (st != DPG_OK) return st;
+    // pass 2: g * coef -> Adam -> bf16 views, from the stored g or the replicas again
+    RsAdamArgs a2 = a;
+    a2.clip_coef = p.d_clip_coef;
+    RsKernel fn2;
+    if (reduced) {
+        a2.g_in = reduced;
+        fn2 = k_rs_adam<1, kInReduced, kUpdate>;
+    } else {
+        fn2 = pick_rs_kernel_mode<kUpdate>(mode, p.R);
+    }
+    int grid2 = 0;
+    st = fused_geometry(fn2, p.device, a2.t0, a2.t1, 0, p.n_buckets, &grid2, &a2.vmax);
+    if (st != DPG_OK) return st;
+    return launch_fused(fn2, a2, grid2, nullptr, nullptr, s, who);
+}
+
 }  // namespace dpg
 
 using dpg::fail;
@@ -796,6 +993,18 @@ using dpg::fail;
 extern "C" {
 
 int64_t dpg_launch_count(void) { return dpg::g_launches.load(); }
+
+int dpg_step_clipped(const dpg_plan_t* plan, const void* const* grads, int32_t grads_dtype,
+                     const void* const* last_micro_bf16, const int64_t* valid_tokens,
+                     int32_t n_counts, const dpg_hparams* hp, double max_norm, float* master,
+                     float* exp_avg, float* exp_avg_sq, void* const* param_views, int32_t n_views,
+                     float* bucket_sqnorm, int64_t* bucket_nonfinite, float* reduced_grad,
+                     float* clip_out, void* stream) {
+    dpg::clear_error();
+    return dpg::step_clipped(plan, grads, grads_dtype, last_micro_bf16, valid_tokens, n_counts, hp,
+                             max_norm, master, exp_avg, exp_avg_sq, param_views, n_views,
+                             bucket_sqnorm, bucket_nonfinite, reduced_grad, clip_out, stream);
+}
 
 int dpg_time_next_fused_launch(void* start_event, void* stop_event) {
     dpg::clear_error();
