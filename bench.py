@@ -619,6 +619,10 @@ def run_kernel_table(a):
          lambda: dpg.dpg_step(plan, g, tok, hp(), w, m, v, [p], bucket_sqnorm=sq)),
         (f"k_rs_adam<R={R}> distinct views (n_views=R)", 4 * R + 24,
          lambda: dpg.dpg_step(plan, g, tok, hp(), w, m, v, views)),
+        ("dpg_step_clipped, g stored (norm pass + update pass)", 2 * R + 34,
+         lambda: dpg.dpg_step_clipped(plan, g, tok, hp(), 1e-6, w, m, v, [p], reduced_grad=acc)),
+        ("dpg_step_clipped, replicas re-read", 4 * R + 26,
+         lambda: dpg.dpg_step_clipped(plan, g, tok, hp(), 1e-6, w, m, v, [p])),
     ]
     views = [torch.empty(N, dtype=torch.bfloat16, device=dev) for _ in range(R)]
     rows = []
