@@ -53,6 +53,8 @@ def parse():
     ap.add_argument("--config", default="llama1b", choices=sorted(set(CONFIGS) - {"tiny"}))
     ap.add_argument("--cap-mib", type=float, default=None, help="override the bucket cap")
     ap.add_argument("--impl", default="dpg", choices=["dpg", "reference"])
+    ap.add_argument("--variant", default="direct", choices=["direct", "staged"],
+                    help="fused pass: direct vector loads, or bulk-copy staging in shared memory")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--kernels", action="store_true",
@@ -283,10 +285,15 @@ def run_dpg(a):
         if K > 1:
             dpg.dpg_step(plan, acc, tokens, hp, w, m, v, [param], last_micro=g,
                          bucket_sqnorm=sq, bucket_nonfinite=nf, stream=stream)
+        elif a.variant == "staged":
+            dpg.dpg_step_staged(plan, g, tokens, hp, w, m, v, [param], bucket_sqnorm=sq,
+                                bucket_nonfinite=nf, stream=stream)
         else:
             dpg.dpg_step(plan, g, tokens, hp, w, m, v, [param], bucket_sqnorm=sq,
                          bucket_nonfinite=nf, stream=stream)
 
+    if a.variant == "staged" and K > 1:
+        raise SystemExit("--variant staged covers bf16 gradients without accumulation")
     for _ in range(a.warmup):
         step()
     torch.cuda.synchronize()
@@ -617,6 +624,8 @@ def run_kernel_table(a):
          lambda: dpg.dpg_reduce_scatter_adam(plan, g, tok, hp(), w, m, v, [p])),
         (f"k_rs_adam<R={R}> + k_norm_finalize (dpg_step)", 2 * R + 26,
          lambda: dpg.dpg_step(plan, g, tok, hp(), w, m, v, [p], bucket_sqnorm=sq)),
+        (f"k_rs_adam_staged<R={R}> (dpg_step_staged, bulk-copy staging)", 2 * R + 26,
+         lambda: dpg.dpg_step_staged(plan, g, tok, hp(), w, m, v, [p], bucket_sqnorm=sq)),
         (f"k_rs_adam<R={R}> distinct views (n_views=R)", 4 * R + 24,
          lambda: dpg.dpg_step(plan, g, tok, hp(), w, m, v, views)),
         ("dpg_step_clipped, g stored (norm pass + update pass)", 2 * R + 34,

@@ -252,6 +252,26 @@ int dpg_step_clipped(const dpg_plan_t* plan, const void* const* grads, int32_t g
                      float* clip_out, void* stream);
 
 /* ---------------------------------------------------------------------------
+ * dpg_step through the STAGED variant of the fused pass: each CTA copies the
+ * R gradient tiles and the master/m/v tiles of the half-tiles it will
+ * process into shared memory with the bulk-copy engine (cp.async.bulk,
+ * completion counted in bytes on an mbarrier), several half-tiles ahead of
+ * its threads.  Same arguments and results as dpg_step for bf16 gradients
+ * (grads_dtype must be DPG_BF16, no last microbatch), R in {1, 2, 4, 8}.
+ * Every device-side wait is bounded (1 s); a wait that runs out makes the
+ * CTA wait (bounded) for its own copies in flight and return, and records
+ * DPG_ERR_DEVICE_TIMEOUT in the plan's status word: the outputs are then
+ * incomplete.  dpg_check_device_status() synchronises `stream` and returns
+ * that status (DPG_OK or DPG_ERR_DEVICE_TIMEOUT).
+ * ------------------------------------------------------------------------- */
+int dpg_step_staged(const dpg_plan_t* plan, const void* const* grads, int32_t grads_dtype,
+                    const int64_t* valid_tokens, int32_t n_counts, const dpg_hparams* hp,
+                    float* master, float* exp_avg, float* exp_avg_sq, void* const* param_views,
+                    int32_t n_views, float* bucket_sqnorm, int64_t* bucket_nonfinite,
+                    void* stream);
+int dpg_check_device_status(const dpg_plan_t* plan, void* stream);
+
+/* ---------------------------------------------------------------------------
  * dpg_step without any device allocation.  The pages have no counterpart to
  * this entry point: it exists for callers that must not have the library
  * allocate device memory -- for example code whose device memory is owned
@@ -296,6 +316,11 @@ int64_t dpg_launch_count(void);
  * the request is then cleared.  NULL, NULL clears a pending request.  Lets a
  * caller time the fused kernel alone inside a whole step. */
 int dpg_time_next_fused_launch(void* start_event, void* stop_event);
+/* Test-only fault injection for the staged step: its next launch by the
+ * calling thread never fetches half-tile `skip_unit` (-1: none), so the CTA
+ * that owns it must run out its wait, and every wait is bounded by
+ * `timeout_ns` (<= 0: the default 1 s).  Used to test the timeout path. */
+int dpg_set_staged_fault(int64_t skip_unit, int64_t timeout_ns);
 
 #ifdef __cplusplus
 }

@@ -38,7 +38,7 @@ EXPORTED = (
     "dpg_plan_export", "dpg_plan_upload", "dpg_pack", "dpg_unpack", "dpg_accumulate",
     "dpg_reduce_scatter_adam", "dpg_allgather_params", "dpg_step", "dpg_launch_count",
     "dpg_time_next_fused_launch", "dpg_step_noalloc", "dpg_export_state", "dpg_import_state",
-    "dpg_step_clipped",
+    "dpg_step_clipped", "dpg_step_staged", "dpg_check_device_status", "dpg_set_staged_fault",
 )
 DPG_MAX_STATE_ARRAYS = 8
 DPG_NOALLOC_SCRATCH_BYTES = 8 << 20
@@ -111,6 +111,9 @@ def lib() -> ctypes.CDLL:
         L.dpg_launch_count.restype = i64
         L.dpg_step_clipped.argtypes = [P, P, i32, P, P, i32, P, ctypes.c_double, P, P, P, P, i32,
                                        P, P, P, P, P]
+        L.dpg_step_staged.argtypes = [P, P, i32, P, i32, P, P, P, P, P, i32, P, P, P]
+        L.dpg_check_device_status.argtypes = [P, P]
+        L.dpg_set_staged_fault.argtypes = [i64, i64]
         L.dpg_export_state.argtypes = [P, P, P, i32, P]
         L.dpg_import_state.argtypes = [P, P, P, i32, P]
         L.dpg_time_next_fused_launch.argtypes = [P, P]
@@ -119,7 +122,8 @@ def lib() -> ctypes.CDLL:
                      "dpg_plan_export", "dpg_plan_upload", "dpg_pack", "dpg_unpack",
                      "dpg_accumulate", "dpg_reduce_scatter_adam", "dpg_allgather_params",
                      "dpg_step", "dpg_step_noalloc", "dpg_export_state", "dpg_import_state",
-                     "dpg_step_clipped"):
+                     "dpg_step_clipped", "dpg_step_staged", "dpg_check_device_status",
+                     "dpg_set_staged_fault"):
             getattr(L, name).restype = c_int
         _lib = L
     return _lib
@@ -408,6 +412,38 @@ def dpg_step_clipped(plan: Plan, grads: Sequence[Ptr], valid_tokens, hp: HParams
         tok.ctypes.data, n_tok, ctypes.byref(hpc), float(max_norm), _ptr(master), _ptr(exp_avg),
         _ptr(exp_avg_sq), _ptrs(param_views), len(param_views), _ptr(bucket_sqnorm),
         _ptr(bucket_nonfinite), _ptr(reduced_grad), _ptr(clip_out), _stream(stream)))
+
+
+def dpg_step_staged(plan: Plan, grads: Sequence[Ptr], valid_tokens, hp: HParams, master: Ptr,
+                    exp_avg: Ptr, exp_avg_sq: Ptr, param_views: Sequence[Ptr] = (), *,
+                    bucket_sqnorm: Ptr = None, bucket_nonfinite: Ptr = None, stream=None):
+    """dpg_step through the bulk-copy staged pass (bf16 gradients, R in 1/2/4/8)."""
+    if len(grads) != plan.R:
+        raise ValueError(f"need R={plan.R} gradient buffers, got {len(grads)}")
+    N = plan.total_padded
+    for k, g in enumerate(grads):
+        _need(g, "bf16", N, f"grads[{k}]")
+    for name, t in (("master", master), ("exp_avg", exp_avg), ("exp_avg_sq", exp_avg_sq)):
+        _need(t, "f32", N, name)
+    for k, t in enumerate(param_views):
+        _need(t, "bf16", N, f"param_views[{k}]")
+    _need(bucket_sqnorm, "f32", plan.n_buckets, "bucket_sqnorm")
+    tok, n_tok = _tokens(valid_tokens)
+    hpc = hp.c()
+    _check(lib().dpg_step_staged(
+        plan.handle, _ptrs(grads), DPG_BF16, tok.ctypes.data, n_tok, ctypes.byref(hpc),
+        _ptr(master), _ptr(exp_avg), _ptr(exp_avg_sq), _ptrs(param_views), len(param_views),
+        _ptr(bucket_sqnorm), _ptr(bucket_nonfinite), _stream(stream)))
+
+
+def dpg_check_device_status(plan: Plan, stream=None):
+    """Synchronise the stream; raise DpgError if the last staged step timed out."""
+    _check(lib().dpg_check_device_status(plan.handle, _stream(stream)))
+
+
+def dpg_set_staged_fault(skip_unit: int = -1, timeout_ns: int = 0):
+    """Test-only: the next staged launch skips fetching one half-tile."""
+    _check(lib().dpg_set_staged_fault(int(skip_unit), int(timeout_ns)))
 
 
 def dpg_step_noalloc(plan: Plan, grads: Sequence[Ptr], valid_tokens, hp: HParams, master: Ptr,

@@ -68,6 +68,7 @@ struct Plan {
     void* d_clip = nullptr;
     double* d_bucket_sq64 = nullptr;  // n_buckets + 1
     float* d_clip_coef = nullptr;     // 1
+    int32_t* d_status = nullptr;      // status word of the staged pass (0 = OK)
 };
 
 // thread-local error message

@@ -30,6 +30,10 @@ namespace dpg {
 
 static std::atomic<int64_t> g_launches{0};
 static thread_local cudaEvent_t t_fused_start = nullptr, t_fused_stop = nullptr;
+// test-only fault injection of the staged pass (consumed by its next launch)
+static thread_local int64_t t_staged_skip = -1;
+static thread_local int64_t t_staged_timeout_ns = 0;
+constexpr uint64_t kStagedTimeoutNs = 1000000000ull;   // 1 s per wait
 
 #define DPG_CUDA_TRY(call)                                                              \
     do {                                                                                \
@@ -324,6 +328,240 @@ __global__ void __launch_bounds__(kThreads, 1) k_rs_adam(const __grid_constant__
         if (cur >= 0) flush_visit(a, cur, visit++, sq, nf);
         if (threadIdx.x == 0) a.vis_count[blockIdx.x] = visit;
     }
+}
+
+// ---------------------------------------------------------------------------
+// Staged variant of the fused pass: the R gradient tiles and the master/m/v
+// tiles of a unit (half a 4096-element tile) are copied into shared memory by
+// the bulk-copy engine (cp.async.bulk, completion counted in bytes on an
+// mbarrier), S units ahead of the threads that consume them.  Every wait is
+// bounded by a global-timer deadline: a wait that runs out records
+// DPG_ERR_DEVICE_TIMEOUT in a status word, the CTA waits (again bounded) for
+// its own copies still in flight and returns.  bf16 gradients, R in {1,2,4,8}.
+// ---------------------------------------------------------------------------
+constexpr int kUnit = 2048;                 // elements per stage
+constexpr int kStagedThreads = 512;         // 4 elements per thread per unit
+constexpr int kMaxStages = 8;
+constexpr size_t kStagedSmemBudget = 200 * 1024;
+
+__host__ __device__ constexpr size_t staged_stage_bytes(int R) { return size_t(kUnit) * (2 * R + 12); }
+__host__ __device__ constexpr int staged_stages(int R) {
+    return int(kStagedSmemBudget / staged_stage_bytes(R)) < kMaxStages
+               ? int(kStagedSmemBudget / staged_stage_bytes(R)) : kMaxStages;
+}
+
+struct StagedArgs {
+    RsAdamArgs a;            // buffers, tables, constants, norm scratch
+    int32_t* status;         // device status word (0 = OK)
+    int64_t skip_unit;       // test-only: this unit is never fetched (-1: none)
+    uint64_t timeout_ns;     // bound of every wait
+};
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ uint64_t global_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t done;
+    asm volatile("{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+                 " selp.u32 %0, 1, 0, p;\n}"
+                 : "=r"(done) : "r"(bar), "r"(parity) : "memory");
+    return done != 0;
+}
+// true once the phase of `parity` completed, false if the deadline passed first
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, uint64_t deadline) {
+    while (!mbar_try_wait(bar, parity))
+        if (global_ns() > deadline) return false;
+    return true;
+}
+
+// element range [start, start + count) of unit u (count may be 0: the second
+// half of a partial tile); b is advanced to the unit's bucket
+__device__ __forceinline__ int64_t unit_range(const RsAdamArgs& a, int64_t u, int& b, int64_t* count) {
+    const int64_t t = u >> 1;
+    b = bucket_of_tile(a.tile_begin, b, a.b1, t);
+    const int64_t start = __ldg(a.bucket_offset + b) + (t - __ldg(a.tile_begin + b)) * kTile +
+                          (u & 1) * kUnit;
+    const int64_t end = __ldg(a.bucket_offset + b + 1);
+    const int64_t n = end - start;
+    *count = n <= 0 ? 0 : (n < kUnit ? n : kUnit);
+    return start;
+}
+
+template <int RT>
+__device__ __forceinline__ void issue_unit(const StagedArgs& sa, unsigned char* stage, uint32_t bar,
+                                           int64_t start, int64_t count) {
+    const RsAdamArgs& a = sa.a;
+    const uint32_t gbytes = uint32_t(count) * 2, sbytes = uint32_t(count) * 4;
+    uint64_t state;
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 %0, [%1], %2;"
+                 : "=l"(state) : "r"(bar), "r"(RT * gbytes + 3 * sbytes) : "memory");
+    (void)state;
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    if (count == 0) return;
+#pragma unroll
+    for (int r = 0; r < RT; ++r)
+        asm volatile("cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                     :: "r"(smem_u32(stage + size_t(r) * kUnit * 2)),
+                        "l"(static_cast<const uint16_t*>(a.grads[r]) + start), "r"(gbytes), "r"(bar)
+                     : "memory");
+    const float* src[3] = {a.master, a.m, a.v};
+#pragma unroll
+    for (int k = 0; k < 3; ++k)
+        asm volatile("cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                     :: "r"(smem_u32(stage + size_t(RT) * kUnit * 2 + size_t(k) * kUnit * 4)),
+                        "l"(src[k] + start), "r"(sbytes), "r"(bar)
+                     : "memory");
+}
+
+template <int RT>
+__global__ void __launch_bounds__(kStagedThreads, 1) k_rs_adam_staged(const __grid_constant__ StagedArgs sa) {
+    constexpr int S = staged_stages(RT);
+    constexpr size_t SB = staged_stage_bytes(RT);
+    extern __shared__ __align__(128) unsigned char smem[];
+    __shared__ __align__(8) uint64_t bars[kMaxStages];
+    const RsAdamArgs& a = sa.a;
+    const int64_t u0 = 2 * a.t0, u1 = 2 * a.t1;   // units of the launch
+    const int64_t n_mine = blockIdx.x < u1 - u0 ? (u1 - u0 - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
+    // producer bookkeeping (thread 0): which stages hold an armed, unconsumed unit
+    int b_prod = a.b0;
+    uint32_t armed = 0;      // bit s: stage s holds an armed, unconsumed unit
+    uint32_t armed_par = 0;  // bit s: phase parity that unit completes
+    if (threadIdx.x == 0) {
+        for (int k = 0; k < S; ++k)
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" :: "r"(smem_u32(&bars[k])) : "memory");
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        for (int64_t k = 0; k < S && k < n_mine; ++k) {
+            const int64_t u = u0 + blockIdx.x + k * gridDim.x;
+            int64_t cnt;
+            const int64_t st = unit_range(a, u, b_prod, &cnt);
+            if (u == sa.skip_unit) continue;
+            issue_unit<RT>(sa, smem + k * SB, smem_u32(&bars[k]), st, cnt);
+            armed |= 1u << k;   // parity 0: first phase of every stage
+        }
+    }
+    __syncthreads();
+
+    const bool norm = a.vis_sq != nullptr;
+    int b = a.b0, cur = -1, visit = 0;
+    double sq = 0.0;
+    int nf = 0;
+    bool aborted = false;
+    for (int64_t k = 0; k < n_mine; ++k) {
+        const int s = int(k % S);
+        const uint32_t parity = uint32_t((k / S) & 1);
+        const int64_t u = u0 + blockIdx.x + k * gridDim.x;
+        int64_t cnt;
+        const int64_t start = unit_range(a, u, b, &cnt);
+        const bool ok = mbar_wait_bounded(smem_u32(&bars[s]), parity, global_ns() + sa.timeout_ns);
+        if (__syncthreads_or(!ok)) {
+            aborted = true;
+            break;
+        }
+        if (norm && b != cur) {
+            if (cur >= 0) flush_visit(a, cur, visit++, sq, nf);
+            cur = b;
+            sq = 0.0;
+            nf = 0;
+        }
+        const int e = threadIdx.x * 4;
+        if (e < cnt) {
+            const unsigned char* stage = smem + s * SB;
+            float x[4];
+            {
+                const uint2 q = *reinterpret_cast<const uint2*>(stage + size_t(e) * 2);
+                widen2(q.x, x[0], x[1]);
+                widen2(q.y, x[2], x[3]);
+            }
+#pragma unroll
+            for (int r = 1; r < RT; ++r) {
+                const uint2 q = *reinterpret_cast<const uint2*>(stage + size_t(r) * kUnit * 2 + size_t(e) * 2);
+                float y[4];
+                widen2(q.x, y[0], y[1]);
+                widen2(q.y, y[2], y[3]);
+#pragma unroll
+                for (int j = 0; j < 4; ++j) x[j] = __fadd_rn(x[j], y[j]);
+            }
+            const float* sw = reinterpret_cast<const float*>(stage + size_t(RT) * kUnit * 2);
+            float4 w = *reinterpret_cast<const float4*>(sw + e);
+            float4 m = *reinterpret_cast<const float4*>(sw + kUnit + e);
+            float4 v = *reinterpret_cast<const float4*>(sw + 2 * kUnit + e);
+            float* wp = &w.x;
+            float* mp = &m.x;
+            float* vp = &v.x;
+            float tsq = 0.0f;
+            float g[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                g[j] = __fmul_rn(x[j], a.scale);
+                float wj = wp[j];
+                if (a.decay) wj = __fsub_rn(wj, __fmul_rn(a.lr_wd, wj));
+                const float mj = __fadd_rn(__fmul_rn(a.beta1, mp[j]), __fmul_rn(a.omb1, g[j]));
+                const float vj =
+                    __fadd_rn(__fmul_rn(a.beta2, vp[j]), __fmul_rn(a.omb2, __fmul_rn(g[j], g[j])));
+                const float m_hat = __fdiv_rn(mj, a.bias1);
+                const float v_hat = __fdiv_rn(vj, a.bias2);
+                const float uu = __fdiv_rn(m_hat, __fadd_rn(__fsqrt_rn(v_hat), a.eps));
+                wp[j] = __fsub_rn(wj, __fmul_rn(a.lr, uu));
+                mp[j] = mj;
+                vp[j] = vj;
+                tsq = fmaf(g[j], g[j], tsq);
+                nf += (__float_as_uint(g[j]) & 0x7F800000u) == 0x7F800000u;
+            }
+            if (norm) sq += double(tsq);
+            const int64_t i = start + e;
+            *reinterpret_cast<float4*>(a.master + i) = w;
+            *reinterpret_cast<float4*>(a.m + i) = m;
+            *reinterpret_cast<float4*>(a.v + i) = v;
+            __nv_bfloat162 h0 = __floats2bfloat162_rn(wp[0], wp[1]);
+            __nv_bfloat162 h1 = __floats2bfloat162_rn(wp[2], wp[3]);
+            uint2 pk;
+            pk.x = *reinterpret_cast<uint32_t*>(&h0);
+            pk.y = *reinterpret_cast<uint32_t*>(&h1);
+            for (int kv = 0; kv < a.n_views; ++kv)
+                *reinterpret_cast<uint2*>(static_cast<uint16_t*>(a.views[kv]) + i) = pk;
+        }
+        __syncthreads();   // every thread is done with stage s
+        if (threadIdx.x == 0) {
+            armed &= ~(1u << s);
+            const int64_t kn = k + S;
+            if (kn < n_mine) {
+                const int64_t un = u0 + blockIdx.x + kn * gridDim.x;
+                int64_t cn;
+                const int64_t sn = unit_range(a, un, b_prod, &cn);
+                if (un != sa.skip_unit) {
+                    issue_unit<RT>(sa, smem + s * SB, smem_u32(&bars[s]), sn, cn);
+                    armed |= 1u << s;
+                    armed_par = (armed_par & ~(1u << s)) | (uint32_t((kn / S) & 1) << s);
+                }
+            }
+        }
+    }
+    if (aborted) {
+        if (threadIdx.x == 0) {
+            atomicExch(sa.status, DPG_ERR_DEVICE_TIMEOUT);
+            // the visits flushed so far stay readable by the finalize
+            if (norm) a.vis_count[blockIdx.x] = visit;
+            // wait (bounded) for this CTA's copies still in flight before exiting
+            const uint64_t drain = global_ns() + sa.timeout_ns;
+            for (int s2 = 0; s2 < S; ++s2)
+                if (armed & (1u << s2))
+                    mbar_wait_bounded(smem_u32(&bars[s2]), (armed_par >> s2) & 1u, drain);
+        }
+        return;
+    }
+    if (norm) {
+        if (cur >= 0) flush_visit(a, cur, visit++, sq, nf);
+        if (threadIdx.x == 0) a.vis_count[blockIdx.x] = visit;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0)
+        for (int k = 0; k < S; ++k)
+            asm volatile("mbarrier.inval.shared::cta.b64 [%0];" :: "r"(smem_u32(&bars[k])) : "memory");
 }
 
 // One CTA per bucket: thread c (and c + 256, ...) finds CTA c's visit of the
@@ -628,7 +866,8 @@ int upload(Plan& p) {
     // ceil(T / G)) visit slots: at most T + G and at most G * B, G being at
     // most the resident CTAs of the device (2048 threads per SM).
     const int64_t cap_ctas = int64_t(sms) * (2048 / kThreads);
-    int64_t cap_visits = p.n_tiles + cap_ctas;
+    // (the staged pass works on half tiles: twice as many units)
+    int64_t cap_visits = 2 * p.n_tiles + cap_ctas;
     if (cap_ctas * p.n_buckets < cap_visits) cap_visits = cap_ctas * p.n_buckets;
     if (cap_visits < 1) cap_visits = 1;
     const VisLayout L = vis_layout(cap_visits, cap_ctas);
@@ -666,6 +905,7 @@ int upload(Plan& p) {
     p.d_clip = clip;
     p.d_bucket_sq64 = static_cast<double*>(clip);
     p.d_clip_coef = reinterpret_cast<float*>(static_cast<unsigned char*>(clip) + clip_sq_bytes);
+    p.d_status = reinterpret_cast<int32_t*>(static_cast<unsigned char*>(clip) + clip_sq_bytes + 128);
     p.cap_visits = cap_visits;
     p.cap_ctas = int32_t(cap_ctas);
     p.device = dev;
@@ -986,6 +1226,96 @@ static int step_clipped(const dpg_plan_t* plan, const void* const* grads, int32_
     return launch_fused(fn2, a2, grid2, nullptr, nullptr, s, who);
 }
 
+// Whole step through the staged (bulk-copy) variant of the fused pass.
+template <int RT>
+static int launch_staged(const StagedArgs& sa, int grid, cudaStream_t s) {
+    static std::mutex mu;
+    static bool attr_set = false;
+    const size_t smem = size_t(staged_stages(RT)) * staged_stage_bytes(RT);
+    {
+        std::lock_guard<std::mutex> g(mu);
+        if (!attr_set) {
+            DPG_CUDA_TRY(cudaFuncSetAttribute(k_rs_adam_staged<RT>,
+                                              cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)));
+            attr_set = true;
+        }
+    }
+    k_rs_adam_staged<RT><<<grid, kStagedThreads, smem, s>>>(sa);
+    return after_launch("dpg_step_staged");
+}
+
+static int step_staged(const dpg_plan_t* plan, const void* const* grads, int32_t grads_dtype,
+                       const int64_t* tokens, int32_t n_counts, const dpg_hparams* hp,
+                       float* master, float* m, float* v, void* const* views, int32_t n_views,
+                       float* sqnorm, int64_t* nonfinite, void* stream) {
+    const char* who = "dpg_step_staged";
+    if (!plan) return fail(DPG_ERR_INVALID_ARG, "%s: plan is NULL", who);
+    Plan& p = const_cast<dpg_plan_t*>(plan)->p;
+    if (grads_dtype != DPG_BF16)
+        return fail(DPG_ERR_INVALID_ARG, "%s: bf16 gradients only", who);
+    if (p.R != 1 && p.R != 2 && p.R != 4 && p.R != 8)
+        return fail(DPG_ERR_INVALID_ARG, "%s: R must be 1, 2, 4 or 8 (got %d)", who, p.R);
+    StagedArgs sa{};
+    RsAdamArgs& a = sa.a;
+    int st = fill_step_args(p, grads, grads_dtype, nullptr, hp, tokens, n_counts, master, m, v,
+                            views, n_views, a, who);
+    if (st != DPG_OK) return st;
+    const int64_t skip = t_staged_skip;
+    const int64_t tmo = t_staged_timeout_ns;
+    t_staged_skip = -1;
+    t_staged_timeout_ns = 0;
+    if (p.n_buckets == 0) return DPG_OK;
+    st = upload(p);
+    if (st != DPG_OK) return st;
+    a.bucket_offset = p.d_bucket_offset;
+    a.tile_begin = p.d_tile_begin;
+    a.t0 = 0;
+    a.t1 = p.n_tiles;
+    a.b0 = 0;
+    a.b1 = p.n_buckets;
+    int sms = 0;
+    st = sm_count(p.device, &sms);
+    if (st != DPG_OK) return st;
+    const int64_t units = 2 * p.n_tiles;
+    const int grid = int(units < sms ? (units > 0 ? units : 1) : sms);
+    const int64_t per_cta = (units + grid - 1) / grid;
+    a.vmax = int32_t(per_cta < p.n_buckets ? per_cta : p.n_buckets);
+    const bool want_norm = sqnorm || nonfinite;
+    if (want_norm) {
+        if (grid > p.cap_ctas || int64_t(grid) * a.vmax > p.cap_visits)
+            return fail(DPG_ERR_CUDA, "%s: norm scratch too small", who);
+        a.vis_sq = p.d_vis_sq;
+        a.vis_nf = p.d_vis_nf;
+        a.vis_bucket = p.d_vis_bucket;
+        a.vis_count = p.d_vis_count;
+    }
+    sa.status = p.d_status;
+    sa.skip_unit = skip;
+    sa.timeout_ns = tmo > 0 ? uint64_t(tmo) : kStagedTimeoutNs;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    DPG_CUDA_TRY(cudaMemsetAsync(p.d_status, 0, sizeof(int32_t), s));
+    if (units > 0) {
+        cudaEvent_t ev0 = t_fused_start, ev1 = t_fused_stop;
+        t_fused_start = t_fused_stop = nullptr;
+        if (ev0) DPG_CUDA_TRY(cudaEventRecord(ev0, s));
+        switch (p.R) {
+            case 1: st = launch_staged<1>(sa, grid, s); break;
+            case 2: st = launch_staged<2>(sa, grid, s); break;
+            case 4: st = launch_staged<4>(sa, grid, s); break;
+            default: st = launch_staged<8>(sa, grid, s); break;
+        }
+        if (st != DPG_OK) return st;
+        if (ev1) DPG_CUDA_TRY(cudaEventRecord(ev1, s));
+    }
+    if (want_norm) {
+        k_norm_finalize<<<p.n_buckets, kFinalizeThreads, 0, s>>>(
+            a.vis_sq, a.vis_nf, a.vis_bucket, a.vis_count, units > 0 ? grid : 0, a.vmax, 0, sqnorm,
+            nonfinite, nullptr);
+        st = after_launch(who);
+    }
+    return st;
+}
+
 }  // namespace dpg
 
 using dpg::fail;
@@ -993,6 +1323,38 @@ using dpg::fail;
 extern "C" {
 
 int64_t dpg_launch_count(void) { return dpg::g_launches.load(); }
+
+int dpg_step_staged(const dpg_plan_t* plan, const void* const* grads, int32_t grads_dtype,
+                    const int64_t* valid_tokens, int32_t n_counts, const dpg_hparams* hp,
+                    float* master, float* exp_avg, float* exp_avg_sq, void* const* param_views,
+                    int32_t n_views, float* bucket_sqnorm, int64_t* bucket_nonfinite,
+                    void* stream) {
+    dpg::clear_error();
+    return dpg::step_staged(plan, grads, grads_dtype, valid_tokens, n_counts, hp, master, exp_avg,
+                            exp_avg_sq, param_views, n_views, bucket_sqnorm, bucket_nonfinite,
+                            stream);
+}
+
+int dpg_check_device_status(const dpg_plan_t* plan, void* stream) {
+    dpg::clear_error();
+    if (!plan) return fail(DPG_ERR_INVALID_ARG, "dpg_check_device_status: plan is NULL");
+    const dpg::Plan& p = plan->p;
+    if (p.device < 0) return DPG_OK;   // nothing ran on a device yet
+    DPG_CUDA_TRY(cudaStreamSynchronize(static_cast<cudaStream_t>(stream)));
+    int32_t word = 0;
+    DPG_CUDA_TRY(cudaMemcpy(&word, p.d_status, sizeof word, cudaMemcpyDeviceToHost));
+    if (word != 0)
+        return fail(word, "dpg_check_device_status: a bounded device-side wait of the last staged "
+                          "step ran out; its results are incomplete");
+    return DPG_OK;
+}
+
+int dpg_set_staged_fault(int64_t skip_unit, int64_t timeout_ns) {
+    dpg::clear_error();
+    dpg::t_staged_skip = skip_unit;
+    dpg::t_staged_timeout_ns = timeout_ns;
+    return DPG_OK;
+}
 
 int dpg_step_clipped(const dpg_plan_t* plan, const void* const* grads, int32_t grads_dtype,
                      const void* const* last_micro_bf16, const int64_t* valid_tokens,
