@@ -123,9 +123,9 @@ __device__ __forceinline__ uint4 narrow8(const float* f) {
 enum : int { kInBf16 = 0, kInF32 = 1, kInF32PlusBf16 = 2, kInReduced = 3 };
 
 // Passes of the fused kernel.  kFull: reduce, scale, Adam, cast (the step).
-// With global norm clipping the step takes two passes: kNormOnly reduces and
-// scales, accumulates exact (fp64) squares and may store g; kUpdate then
-// multiplies g by the clip coefficient found on the device and runs Adam.
+// With global norm clipping the step takes two passes: the norm pass
+// (k_norm_pass) reduces, scales, sums the squares and may store g; kUpdate
+// then multiplies g by the clip coefficient found on the device and runs Adam.
 enum : int { kFull = 0, kNormOnly = 1, kUpdate = 2 };
 
 struct RsAdamArgs {
@@ -246,6 +246,7 @@ __device__ __forceinline__ void flush_visit(const RsAdamArgs& a, int bucket, int
 
 template <int RT, int MODE, int PHASE>
 __global__ void __launch_bounds__(kThreads, 1) k_rs_adam(const __grid_constant__ RsAdamArgs a) {
+    static_assert(PHASE != kNormOnly, "the norm pass is k_norm_pass");
     const bool norm = PHASE != kUpdate && a.vis_sq != nullptr;
     float coef = 1.0f;
     if constexpr (PHASE == kUpdate) coef = __ldg(a.clip_coef);
@@ -254,39 +255,30 @@ __global__ void __launch_bounds__(kThreads, 1) k_rs_adam(const __grid_constant__
     int visit = 0;
     double sq = 0.0;
     int nf = 0;
+    // the current bucket's table entries, reloaded only when a tile leaves it
+    // (per-tile lookups were half of the load requests of the lighter passes)
+    int64_t tb_lo = 0, tb_hi = -1, bo_lo = 0, bo_hi = 0;
     for (int64_t t = a.t0 + blockIdx.x; t < a.t1; t += gridDim.x) {
-        b = bucket_of_tile(a.tile_begin, b, a.b1, t);  // CTA-uniform
+        if (t >= tb_hi) {                                   // CTA-uniform
+            b = bucket_of_tile(a.tile_begin, b, a.b1, t);
+            tb_lo = __ldg(a.tile_begin + b);
+            tb_hi = __ldg(a.tile_begin + b + 1);
+            bo_lo = __ldg(a.bucket_offset + b);
+            bo_hi = __ldg(a.bucket_offset + b + 1);
+        }
         if (norm && b != cur) {
             if (cur >= 0) flush_visit(a, cur, visit++, sq, nf);
             cur = b;
             sq = 0.0;
             nf = 0;
         }
-        const int64_t bucket_end = __ldg(a.bucket_offset + b + 1);
-        const int64_t i = __ldg(a.bucket_offset + b) + (t - __ldg(a.tile_begin + b)) * kTile +
-                          int64_t(threadIdx.x) * kVec;
+        const int64_t bucket_end = bo_hi;
+        const int64_t i = bo_lo + (t - tb_lo) * kTile + int64_t(threadIdx.x) * kVec;
         if (i < bucket_end) {
             float s[8];
             reduce_vector<RT, MODE>(a, i, s);
             float g[8];
-            if constexpr (PHASE == kNormOnly) {
-#pragma unroll
-                for (int j = 0; j < 8; ++j) g[j] = __fmul_rn(s[j], a.scale);
-                // exact squares (a binary32 square is exact in binary64)
-                double tsq = 0.0;
-#pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    tsq += double(g[j]) * double(g[j]);
-                    nf += (__float_as_uint(g[j]) & 0x7F800000u) == 0x7F800000u;
-                }
-                if (norm) sq += tsq;
-                if (a.reduced) {
-                    F8 gg;
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) gg.v[j] = g[j];
-                    st_f8(a.reduced + i, gg);
-                }
-            } else {
+            {
                 F8 w = ld_state_f8(a.master + i);
                 F8 m = ld_state_f8(a.m + i);
                 F8 v = ld_state_f8(a.v + i);
@@ -328,6 +320,188 @@ __global__ void __launch_bounds__(kThreads, 1) k_rs_adam(const __grid_constant__
         if (cur >= 0) flush_visit(a, cur, visit++, sq, nf);
         if (threadIdx.x == 0) a.vis_count[blockIdx.x] = visit;
     }
+}
+
+// ---------------------------------------------------------------------------
+// Norm pass of the clipped step: reduce, scale, squares per bucket visit, and
+// optionally store g.  It moves only 2R (+4) bytes per element, so each
+// iteration handles two tiles (t and t + grid) with the loads of both in
+// flight before either is summed; the tile order, and with it the visits, is
+// that of the single-tile loop.
+// ---------------------------------------------------------------------------
+template <int RT, int MODE> struct Raw;
+template <int RT> struct Raw<RT, kInBf16> { uint4 x[RT]; };
+template <int RT> struct Raw<RT, kInF32> { F8 x[RT]; };
+template <int RT> struct Raw<RT, kInF32PlusBf16> { F8 x[RT]; uint4 l[RT]; };
+
+template <int RT, int MODE>
+__device__ __forceinline__ void load_raw(const RsAdamArgs& a, int64_t i, Raw<RT, MODE>& raw) {
+#pragma unroll
+    for (int r = 0; r < RT; ++r) {
+        if constexpr (MODE == kInBf16) {
+            raw.x[r] = ld_grad_u4(static_cast<const uint16_t*>(a.grads[r]) + i);
+        } else {
+            raw.x[r] = ld_grad_f8(static_cast<const float*>(a.grads[r]) + i);
+            if constexpr (MODE == kInF32PlusBf16)
+                raw.l[r] = ld_grad_u4(static_cast<const uint16_t*>(a.last[r]) + i);
+        }
+    }
+}
+
+// the same rank-ordered binary32 sum as reduce_vector
+template <int RT, int MODE>
+__device__ __forceinline__ void sum_raw(const Raw<RT, MODE>& raw, float* s) {
+#pragma unroll
+    for (int r = 0; r < RT; ++r) {
+        float x[8];
+        if constexpr (MODE == kInBf16) {
+            widen8(raw.x[r], x);
+        } else {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) x[j] = raw.x[r].v[j];
+            if constexpr (MODE == kInF32PlusBf16) {
+                float t[8];
+                widen8(raw.l[r], t);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) x[j] = __fadd_rn(x[j], t[j]);
+            }
+        }
+        if (r == 0) {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) s[j] = x[j];
+        } else {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) s[j] = __fadd_rn(s[j], x[j]);
+        }
+    }
+}
+
+// g = s * scale; its squares are added to a running double-float sum (hi, lo)
+// with binary32 operations only -- binary64 arithmetic is scarce on this GPU,
+// so the sum is widened to double once per bucket visit: p + e is g*g exactly
+// (FMA) and Knuth's TwoSum keeps the rounding error of hi in lo (about 2^-48
+// relative overall).  |g| >= 2^60, whose binary32 square would overflow, is
+// squared in binary64 (`big`).
+struct NormAcc {
+    float hi = 0.0f, lo = 0.0f;
+    double big = 0.0;
+    __device__ double value() const { return (double(hi) + double(lo)) + big; }
+};
+
+__device__ __forceinline__ void two_sum_square(NormAcc& acc, float x) {
+    const float p = __fmul_rn(x, x);
+    const float e = fmaf(x, x, -p);
+    const float t = __fadd_rn(acc.hi, p);
+    const float bp = __fsub_rn(t, acc.hi);
+    const float err = __fadd_rn(__fsub_rn(acc.hi, __fsub_rn(t, bp)), __fsub_rn(p, bp));
+    acc.hi = t;
+    acc.lo = __fadd_rn(acc.lo, __fadd_rn(err, e));
+}
+
+__device__ __forceinline__ void norm_vector(const RsAdamArgs& a, int64_t i, const float* s,
+                                            NormAcc& acc, int& nf) {
+    float g[8];
+    bool rare = false;   // a huge or non-finite value in this vector
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        g[j] = __fmul_rn(s[j], a.scale);
+        rare |= !(fabsf(g[j]) < 0x1p60f);
+    }
+    // a branch uniform over the active lanes (callers may be inside a partial
+    // tile's per-thread condition): the binary64 path must not be if-converted
+    // into predicated binary64 instructions issued for every element
+    if (__any_sync(__activemask(), rare)) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            if (fabsf(g[j]) < 0x1p60f) two_sum_square(acc, g[j]);
+            else acc.big += double(g[j]) * double(g[j]);
+            nf += (__float_as_uint(g[j]) & 0x7F800000u) == 0x7F800000u;
+        }
+    } else {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) two_sum_square(acc, g[j]);
+    }
+    if (a.reduced) {
+        F8 gg;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) gg.v[j] = g[j];
+        st_f8(a.reduced + i, gg);
+    }
+}
+
+// tiles per iteration of the norm pass: about 64 registers of loads in flight
+template <int RT, int MODE>
+constexpr int norm_tiles_per_iter() {
+    constexpr int regs = RT * (MODE == kInBf16 ? 4 : MODE == kInF32 ? 8 : 12);
+    return RT == 0 ? 1 : (64 / regs < 1 ? 1 : (64 / regs > 4 ? 4 : 64 / regs));
+}
+
+template <int RT, int MODE>
+__global__ void __launch_bounds__(kThreads, 1) k_norm_pass(const __grid_constant__ RsAdamArgs a) {
+    constexpr int TPI = norm_tiles_per_iter<RT, MODE>();
+    int b = a.b0, cur = -1, visit = 0;
+    NormAcc acc;
+    int nf = 0;
+    int64_t tb_lo = 0, tb_hi = -1, bo_lo = 0, bo_hi = 0;
+    const int64_t G = gridDim.x;
+    for (int64_t t = a.t0 + blockIdx.x; t < a.t1; t += TPI * G) {
+        int bu[TPI];
+        int64_t iu[TPI], eu[TPI];
+#pragma unroll
+        for (int u = 0; u < TPI; ++u) {
+            const int64_t tu = t + u * G;
+            bu[u] = -1;
+            iu[u] = 0;
+            eu[u] = 0;
+            if (tu < a.t1) {
+                if (tu >= tb_hi) {                      // CTA-uniform
+                    b = bucket_of_tile(a.tile_begin, b, a.b1, tu);
+                    tb_lo = __ldg(a.tile_begin + b);
+                    tb_hi = __ldg(a.tile_begin + b + 1);
+                    bo_lo = __ldg(a.bucket_offset + b);
+                    bo_hi = __ldg(a.bucket_offset + b + 1);
+                }
+                bu[u] = b;
+                eu[u] = bo_hi;
+                iu[u] = bo_lo + (tu - tb_lo) * kTile + int64_t(threadIdx.x) * kVec;
+            }
+        }
+        if constexpr (RT > 0) {
+            Raw<RT, MODE> raw[TPI];
+#pragma unroll
+            for (int u = 0; u < TPI; ++u)
+                if (iu[u] < eu[u]) load_raw<RT, MODE>(a, iu[u], raw[u]);
+#pragma unroll
+            for (int u = 0; u < TPI; ++u) {
+                if (bu[u] < 0) break;                   // past the end: CTA-uniform
+                if (bu[u] != cur) {
+                    if (cur >= 0) flush_visit(a, cur, visit++, acc.value(), nf);
+                    cur = bu[u];
+                    acc = NormAcc();
+                    nf = 0;
+                }
+                if (iu[u] < eu[u]) {
+                    float su[8];
+                    sum_raw<RT, MODE>(raw[u], su);
+                    norm_vector(a, iu[u], su, acc, nf);
+                }
+            }
+        } else {
+            if (bu[0] != cur) {
+                if (cur >= 0) flush_visit(a, cur, visit++, acc.value(), nf);
+                cur = bu[0];
+                acc = NormAcc();
+                nf = 0;
+            }
+            if (iu[0] < eu[0]) {
+                float su[8];
+                reduce_vector<RT, MODE>(a, iu[0], su);
+                norm_vector(a, iu[0], su, acc, nf);
+            }
+        }
+    }
+    if (cur >= 0) flush_visit(a, cur, visit++, acc.value(), nf);
+    if (threadIdx.x == 0) a.vis_count[blockIdx.x] = visit;
 }
 
 // ---------------------------------------------------------------------------
@@ -976,6 +1150,23 @@ static RsKernel pick_rs_kernel(int R) {
     }
 }
 
+template <int MODE>
+static RsKernel pick_norm_kernel_r(int R) {
+    switch (R) {
+        case 1: return k_norm_pass<1, MODE>;
+        case 2: return k_norm_pass<2, MODE>;
+        case 4: return k_norm_pass<4, MODE>;
+        case 8: return k_norm_pass<8, MODE>;
+        default: return k_norm_pass<0, MODE>;
+    }
+}
+
+static RsKernel pick_norm_kernel(int mode, int R) {
+    return mode == kInBf16 ? pick_norm_kernel_r<kInBf16>(R)
+         : mode == kInF32  ? pick_norm_kernel_r<kInF32>(R)
+                           : pick_norm_kernel_r<kInF32PlusBf16>(R);
+}
+
 template <int PHASE>
 static RsKernel pick_rs_kernel_mode(int mode, int R) {
     return mode == kInBf16 ? pick_rs_kernel<kInBf16, PHASE>(R)
@@ -1186,7 +1377,7 @@ static int step_clipped(const dpg_plan_t* plan, const void* const* grads, int32_
     // pass 1: reduce, scale, exact squares per bucket (and g, when a buffer is given)
     RsAdamArgs a1 = a;
     a1.reduced = reduced;
-    RsKernel fn1 = pick_rs_kernel_mode<kNormOnly>(mode, p.R);
+    RsKernel fn1 = pick_norm_kernel(mode, p.R);
     int grid1 = 0;
     st = fused_geometry(fn1, p.device, a1.t0, a1.t1, 0, p.n_buckets, &grid1, &a1.vmax);
     if (st != DPG_OK) return st;
