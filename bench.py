@@ -57,6 +57,8 @@ def parse():
                     help="fused pass: direct vector loads, or bulk-copy staging in shared memory")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-sample-elems", type=int, default=CPU_SAMPLE_ELEMS,
+                    help="elements of each oracle sample (CPU baseline and reference arm)")
     ap.add_argument("--kernels", action="store_true",
                     help="time every kernel of the path on the workload, against its algorithmic bytes")
     ap.add_argument("--hockney", action="store_true",
@@ -70,6 +72,24 @@ def parse():
 def dist_info():
     return (int(os.environ.get("RANK", 0)), int(os.environ.get("LOCAL_RANK", 0)),
             int(os.environ.get("WORLD_SIZE", 1)))
+
+
+def max_over_ranks(x: float, world: int, device) -> float:
+    """The largest value of x over all ranks (the job is as slow as its slowest
+    rank); a no-op for one rank."""
+    if world <= 1:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(units_per_rank: float, world: int, ms_slowest: float) -> float:
+    """Whole-job units per second: every rank processes units_per_rank units
+    in the slowest rank's time (weak scaling)."""
+    return units_per_rank * world / (ms_slowest * 1e-3)
 
 
 def cap_of(cfg, a) -> int:
@@ -322,10 +342,7 @@ def run_dpg(a):
     clk = clocks.stop()
     ms = ev_start.elapsed_time(ev_stop) / a.steps
     k_ms = statistics.mean(e0.elapsed_time(e1) for e0, e1 in ev_k)
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ms, world, dev)
 
     # end to end: host (pinned) gradients copied in, norms copied out, every step
     e2e = None
@@ -337,7 +354,7 @@ def run_dpg(a):
     peak, peak_kind = load_peak()
     achieved = bpp["fused"] * cfg.psi / (k_ms * 1e-3) / 1e9
     traffic = traffic_per_launch(cfg, cap, N)
-    value = cfg.psi * world / (ms * 1e-3)
+    value = job_throughput(cfg.psi, world, ms)
     line = {
         "metric": "params/s of the fused bucket reduce-scatter + Adam + all-gather step "
                   "(achieved HBM GB/s vs GB300 peak in roofline)",
@@ -441,12 +458,8 @@ def run_e2e(a, dpg, plan, g, acc, w, m, v, param, sq, nf, tokens, cfg, dev, stre
     e1.record(stream)
     torch.cuda.synchronize()
     ms = e0.elapsed_time(e1) / steps
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
-    return {"value": cfg.psi * world / (ms * 1e-3), "unit": "params/s", "steps": steps,
+    ms = max_over_ranks(ms, world, dev)
+    return {"value": job_throughput(cfg.psi, world, ms), "unit": "params/s", "steps": steps,
             "h2d_bytes_per_step": R * K * N * 2, "d2h_bytes_per_step": plan.n_buckets * 12,
             "ms_per_step": ms, "h2d_gbs": R * K * N * 2 / (ms * 1e-3) / 1e9,
             "how": (f"pinned host gradients copied in {len(bounds) - 1} bucket chunks on a copy "
@@ -471,7 +484,7 @@ def run_reference(a):
         os.sched_setaffinity(0, {sorted(os.sched_getaffinity(0))[0]})
     except (AttributeError, OSError):
         pass
-    n = CPU_SAMPLE_ELEMS
+    n = a.cpu_sample_elems
     grads, last, w, m, v = cpu_sample_inputs(cfg, n, "cpu")
     tokens = token_counts(cfg)
     t = 0
