@@ -61,6 +61,8 @@ def parse():
                     help="elements of each oracle sample (CPU baseline and reference arm)")
     ap.add_argument("--kernels", action="store_true",
                     help="time every kernel of the path on the workload, against its algorithmic bytes")
+    ap.add_argument("--schedules", action="store_true",
+                    help="DDP (all-reduce + R replica updates) against the ZeRO-2 step")
     ap.add_argument("--hockney", action="store_true",
                     help="bucket-cap sweep: per-bucket launches vs one fused launch, alpha-beta fit")
     a = ap.parse_args()
@@ -668,8 +670,83 @@ def run_kernel_table(a):
                       "peak_gbs": peak, "peak_kind": peak_kind, "rows": rows}), flush=True)
 
 
+# --------------------------------------------------------------------------
+# DDP against ZeRO-1/2 ("Parallelisms" -- ZeRO-1, ZeRO-2, FSDP NO_SHARD)
+# --------------------------------------------------------------------------
+def run_schedules(a):
+    import torch
+    from zero_optimizer_step_gb300 import build as _build
+    _build.build()
+    import zero_optimizer_step_gb300 as dpg
+    cfg = CONFIGS[a.config]
+    cap = cap_of(cfg, a)
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    R, psi = cfg.R, cfg.psi
+    plan = dpg.dpg_plan_buckets(cfg.numels, cap, R)
+    dpg.dpg_plan_upload(plan)
+    N = plan.total_padded
+    segs = segments(plan.param_offset, cfg.numels)
+    g = [flat_grads_bf16(segs, N, cfg.grad_std, stream_seed(cfg.seed, KIND_GRAD, r), device=dev)
+         for r in range(R)]
+    tok = token_counts(cfg)[:R]
+    w0 = master_f32(N, stream_seed(cfg.seed, KIND_MASTER), device=dev)
+    peak, peak_kind = load_peak()
+    state = {"t": 0}
+
+    def hp():
+        state["t"] += 1
+        return dpg.HParams(step=state["t"])
+
+    def timed(fn, reps=7):
+        for _ in range(2):
+            fn()
+        torch.cuda.synchronize()
+        ts = []
+        for _ in range(reps):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            fn()
+            e1.record()
+            torch.cuda.synchronize()
+            ts.append(e0.elapsed_time(e1))
+        return statistics.median(ts)
+
+    rows = []
+    z = [w0.clone(), torch.zeros(N, device=dev), torch.zeros(N, device=dev)]
+    zp = torch.empty(N, dtype=torch.bfloat16, device=dev)
+    ms = timed(lambda: dpg.dpg_step(plan, g, tok, hp(), *z, [zp]))
+    for name, mem in (("ZeRO-2", 2 + 14 / R), ("ZeRO-1", 4 + 12 / R)):
+        rows.append({"schedule": name, "ms": ms, "bytes_per_param": 2 * R + 26,
+                     "achieved_gbs": (2 * R + 26) * psi / (ms * 1e-3) / 1e9,
+                     "model_state_bytes_per_param_per_replica": mem,
+                     "note": "same fused pass; ZeRO-1 also keeps the full bf16 gradients"})
+    del z
+    reps = [[w0.clone(), torch.zeros(N, device=dev), torch.zeros(N, device=dev)] for _ in range(R)]
+    rp = [torch.empty(N, dtype=torch.bfloat16, device=dev) for _ in range(R)]
+    red = torch.empty(N, device=dev)
+
+    def ddp():
+        h = hp()
+        dpg.dpg_allreduce_grads(plan, g, tok, red)
+        for r in range(R):
+            dpg.dpg_adam_from_reduced(plan, red, h, *reps[r], [rp[r]])
+
+    ms = timed(ddp)
+    bpp = 2 * R + 4 + R * 30
+    rows.append({"schedule": "DDP (NO_SHARD)", "ms": ms, "bytes_per_param": bpp,
+                 "achieved_gbs": bpp * psi / (ms * 1e-3) / 1e9,
+                 "model_state_bytes_per_param_per_replica": 16,
+                 "note": "all-reduce, then each of the R replicas updates its own full state"})
+    print(json.dumps({"metric": "DDP vs ZeRO-1/2 schedules", "config": workload_desc(cfg, cap, plan.n_buckets, N),
+                      "peak_gbs": peak, "peak_kind": peak_kind, "rows": rows}), flush=True)
+
+
 def main():
     a = parse()
+    if a.schedules:
+        run_schedules(a)
+        return
     if a.kernels:
         run_kernel_table(a)
         return

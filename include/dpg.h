@@ -226,6 +226,30 @@ int dpg_step(const dpg_plan_t* plan, const void* const* grads, int32_t grads_dty
              float* bucket_sqnorm, int64_t* bucket_nonfinite, void* stream);
 
 /* ---------------------------------------------------------------------------
+ * DDP / FSDP NO_SHARD schedule, buckets [b0, b1)   ["Parallelisms" -- Data
+ *      parallel; FSDP (NO_SHARD all-reduces gradients like DDP); "Parallelism
+ *      Strategies in Distributed Computing" -- DP and DDP]
+ * dpg_allreduce_grads: reduced_grad[i] = (x_0 + ... + x_{R-1}) * fp32(1/G)
+ *   for every element (x_r as in dpg_reduce_scatter_adam; rank order,
+ *   binary32): the all-reduce result that every DDP replica receives.
+ *   reduced_grad: device, flat fp32 (32-byte aligned).  bucket_sqnorm /
+ *   bucket_nonfinite (nullable) as in dpg_reduce_scatter_adam.
+ * dpg_adam_from_reduced: one replica's optimizer step on its own full copy
+ *   of master/exp_avg/exp_avg_sq from reduced_grad (Adam as in
+ *   dpg_reduce_scatter_adam, bf16 views written).  Under DDP each of the R
+ *   replicas calls it on its own state: R times the optimizer traffic of the
+ *   ZeRO-2 step, with bit-identical results (the test suite checks it).
+ * ------------------------------------------------------------------------- */
+int dpg_allreduce_grads(const dpg_plan_t* plan, const void* const* grads, int32_t grads_dtype,
+                        const void* const* last_micro_bf16, const int64_t* valid_tokens,
+                        int32_t n_counts, float* reduced_grad, float* bucket_sqnorm,
+                        int64_t* bucket_nonfinite, int32_t b0, int32_t b1, void* stream);
+int dpg_adam_from_reduced(const dpg_plan_t* plan, const float* reduced_grad, const dpg_hparams* hp,
+                          float* master, float* exp_avg, float* exp_avg_sq,
+                          void* const* param_views, int32_t n_views, float* bucket_sqnorm,
+                          int64_t* bucket_nonfinite, int32_t b0, int32_t b1, void* stream);
+
+/* ---------------------------------------------------------------------------
  * One whole step with global gradient-norm clipping   ["Parallelisms" --
  *      ZeRO-2: clipping needs the norm over all gradient shards before any
  *      weight is updated; only the local squared norms are all-reduced]

@@ -39,6 +39,7 @@ EXPORTED = (
     "dpg_reduce_scatter_adam", "dpg_allgather_params", "dpg_step", "dpg_launch_count",
     "dpg_time_next_fused_launch", "dpg_step_noalloc", "dpg_export_state", "dpg_import_state",
     "dpg_step_clipped", "dpg_step_staged", "dpg_check_device_status", "dpg_set_staged_fault",
+    "dpg_allreduce_grads", "dpg_adam_from_reduced",
 )
 DPG_MAX_STATE_ARRAYS = 8
 DPG_NOALLOC_SCRATCH_BYTES = 8 << 20
@@ -112,6 +113,8 @@ def lib() -> ctypes.CDLL:
         L.dpg_step_clipped.argtypes = [P, P, i32, P, P, i32, P, ctypes.c_double, P, P, P, P, i32,
                                        P, P, P, P, P]
         L.dpg_step_staged.argtypes = [P, P, i32, P, i32, P, P, P, P, P, i32, P, P, P]
+        L.dpg_allreduce_grads.argtypes = [P, P, i32, P, P, i32, P, P, P, i32, i32, P]
+        L.dpg_adam_from_reduced.argtypes = [P, P, P, P, P, P, P, i32, P, P, i32, i32, P]
         L.dpg_check_device_status.argtypes = [P, P]
         L.dpg_set_staged_fault.argtypes = [i64, i64]
         L.dpg_export_state.argtypes = [P, P, P, i32, P]
@@ -123,7 +126,7 @@ def lib() -> ctypes.CDLL:
                      "dpg_accumulate", "dpg_reduce_scatter_adam", "dpg_allgather_params",
                      "dpg_step", "dpg_step_noalloc", "dpg_export_state", "dpg_import_state",
                      "dpg_step_clipped", "dpg_step_staged", "dpg_check_device_status",
-                     "dpg_set_staged_fault"):
+                     "dpg_set_staged_fault", "dpg_allreduce_grads", "dpg_adam_from_reduced"):
             getattr(L, name).restype = c_int
         _lib = L
     return _lib
@@ -444,6 +447,47 @@ def dpg_check_device_status(plan: Plan, stream=None):
 def dpg_set_staged_fault(skip_unit: int = -1, timeout_ns: int = 0):
     """Test-only: the next staged launch skips fetching one half-tile."""
     _check(lib().dpg_set_staged_fault(int(skip_unit), int(timeout_ns)))
+
+
+def dpg_allreduce_grads(plan: Plan, grads: Sequence[Ptr], valid_tokens, reduced_grad: Ptr, *,
+                        last_micro: Sequence[Ptr] = None, bucket_sqnorm: Ptr = None,
+                        bucket_nonfinite: Ptr = None, b0: int = 0, b1: Optional[int] = None,
+                        grads_dtype: Optional[int] = None, stream=None):
+    """DDP all-reduce: reduced_grad = rank-ordered sum x fp32(1/G), every element."""
+    if len(grads) != plan.R:
+        raise ValueError(f"need R={plan.R} gradient buffers, got {len(grads)}")
+    gd = _grad_dtype(grads) if grads_dtype is None else grads_dtype
+    N = plan.total_padded
+    for k, g in enumerate(grads):
+        _need(g, "bf16" if gd == DPG_BF16 else "f32", N, f"grads[{k}]")
+    for k, g in enumerate(last_micro or ()):
+        _need(g, "bf16", N, f"last_micro[{k}]")
+    _need(reduced_grad, "f32", N, "reduced_grad")
+    _need(bucket_sqnorm, "f32", plan.n_buckets, "bucket_sqnorm")
+    tok, n_tok = _tokens(valid_tokens)
+    _check(lib().dpg_allreduce_grads(
+        plan.handle, _ptrs(grads), gd, None if last_micro is None else _ptrs(last_micro),
+        tok.ctypes.data, n_tok, _ptr(reduced_grad), _ptr(bucket_sqnorm), _ptr(bucket_nonfinite),
+        b0, plan.n_buckets if b1 is None else b1, _stream(stream)))
+
+
+def dpg_adam_from_reduced(plan: Plan, reduced_grad: Ptr, hp: HParams, master: Ptr, exp_avg: Ptr,
+                          exp_avg_sq: Ptr, param_views: Sequence[Ptr] = (), *,
+                          bucket_sqnorm: Ptr = None, bucket_nonfinite: Ptr = None, b0: int = 0,
+                          b1: Optional[int] = None, stream=None):
+    """One DDP replica's Adam step on its full state from the all-reduced gradient."""
+    N = plan.total_padded
+    for name, t in (("reduced_grad", reduced_grad), ("master", master), ("exp_avg", exp_avg),
+                    ("exp_avg_sq", exp_avg_sq)):
+        _need(t, "f32", N, name)
+    for k, t in enumerate(param_views):
+        _need(t, "bf16", N, f"param_views[{k}]")
+    _need(bucket_sqnorm, "f32", plan.n_buckets, "bucket_sqnorm")
+    hpc = hp.c()
+    _check(lib().dpg_adam_from_reduced(
+        plan.handle, _ptr(reduced_grad), ctypes.byref(hpc), _ptr(master), _ptr(exp_avg),
+        _ptr(exp_avg_sq), _ptrs(param_views), len(param_views), _ptr(bucket_sqnorm),
+        _ptr(bucket_nonfinite), b0, plan.n_buckets if b1 is None else b1, _stream(stream)))
 
 
 def dpg_step_noalloc(plan: Plan, grads: Sequence[Ptr], valid_tokens, hp: HParams, master: Ptr,

@@ -399,13 +399,22 @@ __device__ __forceinline__ void two_sum_square(NormAcc& acc, float x) {
 }
 
 __device__ __forceinline__ void norm_vector(const RsAdamArgs& a, int64_t i, const float* s,
-                                            NormAcc& acc, int& nf) {
+                                            NormAcc& acc, int& nf, bool squares) {
     float g[8];
     bool rare = false;   // a huge or non-finite value in this vector
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
         g[j] = __fmul_rn(s[j], a.scale);
         rare |= !(fabsf(g[j]) < 0x1p60f);
+    }
+    if (!squares) {      // all-reduce only: no norm requested
+        if (a.reduced) {
+            F8 gg;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) gg.v[j] = g[j];
+            st_f8(a.reduced + i, gg);
+        }
+        return;
     }
     // a branch uniform over the active lanes (callers may be inside a partial
     // tile's per-thread condition): the binary64 path must not be if-converted
@@ -439,6 +448,7 @@ constexpr int norm_tiles_per_iter() {
 template <int RT, int MODE>
 __global__ void __launch_bounds__(kThreads, 1) k_norm_pass(const __grid_constant__ RsAdamArgs a) {
     constexpr int TPI = norm_tiles_per_iter<RT, MODE>();
+    const bool norm = a.vis_sq != nullptr;
     int b = a.b0, cur = -1, visit = 0;
     NormAcc acc;
     int nf = 0;
@@ -474,7 +484,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_norm_pass(const __grid_constant
 #pragma unroll
             for (int u = 0; u < TPI; ++u) {
                 if (bu[u] < 0) break;                   // past the end: CTA-uniform
-                if (bu[u] != cur) {
+                if (norm && bu[u] != cur) {
                     if (cur >= 0) flush_visit(a, cur, visit++, acc.value(), nf);
                     cur = bu[u];
                     acc = NormAcc();
@@ -483,11 +493,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_norm_pass(const __grid_constant
                 if (iu[u] < eu[u]) {
                     float su[8];
                     sum_raw<RT, MODE>(raw[u], su);
-                    norm_vector(a, iu[u], su, acc, nf);
+                    norm_vector(a, iu[u], su, acc, nf, norm);
                 }
             }
         } else {
-            if (bu[0] != cur) {
+            if (norm && bu[0] != cur) {
                 if (cur >= 0) flush_visit(a, cur, visit++, acc.value(), nf);
                 cur = bu[0];
                 acc = NormAcc();
@@ -496,12 +506,14 @@ __global__ void __launch_bounds__(kThreads, 1) k_norm_pass(const __grid_constant
             if (iu[0] < eu[0]) {
                 float su[8];
                 reduce_vector<RT, MODE>(a, iu[0], su);
-                norm_vector(a, iu[0], su, acc, nf);
+                norm_vector(a, iu[0], su, acc, nf, norm);
             }
         }
     }
-    if (cur >= 0) flush_visit(a, cur, visit++, acc.value(), nf);
-    if (threadIdx.x == 0) a.vis_count[blockIdx.x] = visit;
+    if (norm) {
+        if (cur >= 0) flush_visit(a, cur, visit++, acc.value(), nf);
+        if (threadIdx.x == 0) a.vis_count[blockIdx.x] = visit;
+    }
 }
 
 // ---------------------------------------------------------------------------
@@ -1417,6 +1429,134 @@ static int step_clipped(const dpg_plan_t* plan, const void* const* grads, int32_
     return launch_fused(fn2, a2, grid2, nullptr, nullptr, s, who);
 }
 
+// All-reduce of the replica gradients (DDP): every element's rank-ordered
+// sum times fp32(1/G), written to `reduced`; optional per-bucket norms.
+static int allreduce_grads(const dpg_plan_t* plan, const void* const* grads, int32_t grads_dtype,
+                           const void* const* last, const int64_t* tokens, int32_t n_counts,
+                           float* reduced, float* sqnorm, int64_t* nonfinite, int32_t b0,
+                           int32_t b1, void* stream) {
+    const char* who = "dpg_allreduce_grads";
+    if (!plan) return fail(DPG_ERR_INVALID_ARG, "%s: plan is NULL", who);
+    Plan& p = const_cast<dpg_plan_t*>(plan)->p;
+    if (b0 < 0 || b1 < b0 || b1 > p.n_buckets)
+        return fail(DPG_ERR_INVALID_ARG, "%s: bucket range [%d, %d) outside [0, %d]", who, b0, b1,
+                    p.n_buckets);
+    if (grads_dtype != DPG_BF16 && grads_dtype != DPG_F32)
+        return fail(DPG_ERR_INVALID_ARG, "%s: grads_dtype %d unknown", who, grads_dtype);
+    if (last && grads_dtype != DPG_F32)
+        return fail(DPG_ERR_INVALID_ARG, "%s: last_micro_bf16 needs fp32 accumulation grads", who);
+    RsAdamArgs a{};
+    int st = token_scale(tokens, n_counts, &a.scale);
+    if (st != DPG_OK) return st;
+    if (b0 == b1) return DPG_OK;
+    const bool want_norm = sqnorm || nonfinite;
+    const bool has_elems = p.bucket_offset[b1] > p.bucket_offset[b0];
+    if (!has_elems && !want_norm) return DPG_OK;
+    if (has_elems) {
+        if (!grads) return fail(DPG_ERR_INVALID_ARG, "%s: grads is NULL", who);
+        if (!reduced) return fail(DPG_ERR_INVALID_ARG, "%s: reduced_grad is NULL", who);
+        if (!aligned(reduced, 32)) return fail(DPG_ERR_MISALIGNED, "%s: reduced_grad misaligned", who);
+        const uintptr_t galign = grads_dtype == DPG_BF16 ? 16 : 32;
+        for (int r = 0; r < p.R; ++r) {
+            if (!grads[r]) return fail(DPG_ERR_INVALID_ARG, "%s: grads[%d] is NULL", who, r);
+            if (!aligned(grads[r], galign)) return fail(DPG_ERR_MISALIGNED, "%s: grads[%d] misaligned", who, r);
+            a.grads[r] = grads[r];
+            if (last) {
+                if (!last[r]) return fail(DPG_ERR_INVALID_ARG, "%s: last_micro_bf16[%d] is NULL", who, r);
+                if (!aligned(last[r], 16)) return fail(DPG_ERR_MISALIGNED, "%s: last_micro_bf16[%d] misaligned", who, r);
+                a.last[r] = last[r];
+            }
+        }
+    }
+    st = upload(p);
+    if (st != DPG_OK) return st;
+    a.reduced = reduced;
+    a.bucket_offset = p.d_bucket_offset;
+    a.tile_begin = p.d_tile_begin;
+    a.t0 = p.tile_begin[b0];
+    a.t1 = p.tile_begin[b1];
+    a.b0 = b0;
+    a.b1 = b1;
+    a.R = p.R;
+    const int mode = grads_dtype == DPG_BF16 ? kInBf16 : (last ? kInF32PlusBf16 : kInF32);
+    RsKernel fn = pick_norm_kernel(mode, p.R);
+    int grid = 0;
+    st = fused_geometry(fn, p.device, a.t0, a.t1, b0, b1, &grid, &a.vmax);
+    if (st != DPG_OK) return st;
+    if (want_norm) {
+        if (grid > p.cap_ctas || int64_t(grid) * a.vmax > p.cap_visits)
+            return fail(DPG_ERR_CUDA, "%s: norm scratch too small", who);
+        a.vis_sq = p.d_vis_sq;
+        a.vis_nf = p.d_vis_nf;
+        a.vis_bucket = p.d_vis_bucket;
+        a.vis_count = p.d_vis_count;
+    }
+    return launch_fused(fn, a, grid, sqnorm, nonfinite, static_cast<cudaStream_t>(stream), who);
+}
+
+// One replica's optimizer step from an already-reduced gradient (DDP /
+// NO_SHARD: every replica updates its own full copy of the state).
+static int adam_from_reduced(const dpg_plan_t* plan, const float* reduced, const dpg_hparams* hp,
+                             float* master, float* m, float* v, void* const* views,
+                             int32_t n_views, float* sqnorm, int64_t* nonfinite, int32_t b0,
+                             int32_t b1, void* stream) {
+    const char* who = "dpg_adam_from_reduced";
+    if (!plan) return fail(DPG_ERR_INVALID_ARG, "%s: plan is NULL", who);
+    Plan& p = const_cast<dpg_plan_t*>(plan)->p;
+    if (b0 < 0 || b1 < b0 || b1 > p.n_buckets)
+        return fail(DPG_ERR_INVALID_ARG, "%s: bucket range [%d, %d) outside [0, %d]", who, b0, b1,
+                    p.n_buckets);
+    if (n_views < 0 || n_views > DPG_MAX_VIEWS)
+        return fail(DPG_ERR_INVALID_ARG, "%s: n_views %d outside [0, %d]", who, n_views, DPG_MAX_VIEWS);
+    RsAdamArgs a{};
+    int st = adam_constants(hp, a);
+    if (st != DPG_OK) return st;
+    if (b0 == b1) return DPG_OK;
+    const bool want_norm = sqnorm || nonfinite;
+    const bool has_elems = p.bucket_offset[b1] > p.bucket_offset[b0];
+    if (!has_elems && !want_norm) return DPG_OK;
+    if (!has_elems) n_views = 0;
+    if (has_elems) {
+        if (!reduced || !master || !m || !v)
+            return fail(DPG_ERR_INVALID_ARG, "%s: reduced_grad/master/m/v must not be NULL", who);
+        if (!aligned(reduced, 32) || !aligned(master, 32) || !aligned(m, 32) || !aligned(v, 32))
+            return fail(DPG_ERR_MISALIGNED, "%s: fp32 buffers must be 32-byte aligned", who);
+    }
+    if (n_views > 0 && !views) return fail(DPG_ERR_INVALID_ARG, "%s: param_views is NULL", who);
+    for (int k = 0; k < n_views; ++k) {
+        if (!views[k]) return fail(DPG_ERR_INVALID_ARG, "%s: param_views[%d] is NULL", who, k);
+        if (!aligned(views[k], 16)) return fail(DPG_ERR_MISALIGNED, "%s: param_views[%d] misaligned", who, k);
+        a.views[k] = views[k];
+    }
+    st = upload(p);
+    if (st != DPG_OK) return st;
+    a.g_in = reduced;
+    a.master = master;
+    a.m = m;
+    a.v = v;
+    a.n_views = n_views;
+    a.bucket_offset = p.d_bucket_offset;
+    a.tile_begin = p.d_tile_begin;
+    a.t0 = p.tile_begin[b0];
+    a.t1 = p.tile_begin[b1];
+    a.b0 = b0;
+    a.b1 = b1;
+    a.R = p.R;
+    RsKernel fn = k_rs_adam<1, kInReduced, kFull>;
+    int grid = 0;
+    st = fused_geometry(fn, p.device, a.t0, a.t1, b0, b1, &grid, &a.vmax);
+    if (st != DPG_OK) return st;
+    if (want_norm) {
+        if (grid > p.cap_ctas || int64_t(grid) * a.vmax > p.cap_visits)
+            return fail(DPG_ERR_CUDA, "%s: norm scratch too small", who);
+        a.vis_sq = p.d_vis_sq;
+        a.vis_nf = p.d_vis_nf;
+        a.vis_bucket = p.d_vis_bucket;
+        a.vis_count = p.d_vis_count;
+    }
+    return launch_fused(fn, a, grid, sqnorm, nonfinite, static_cast<cudaStream_t>(stream), who);
+}
+
 // Whole step through the staged (bulk-copy) variant of the fused pass.
 template <int RT>
 static int launch_staged(const StagedArgs& sa, int grid, cudaStream_t s) {
@@ -1524,6 +1664,24 @@ int dpg_step_staged(const dpg_plan_t* plan, const void* const* grads, int32_t gr
     return dpg::step_staged(plan, grads, grads_dtype, valid_tokens, n_counts, hp, master, exp_avg,
                             exp_avg_sq, param_views, n_views, bucket_sqnorm, bucket_nonfinite,
                             stream);
+}
+
+int dpg_allreduce_grads(const dpg_plan_t* plan, const void* const* grads, int32_t grads_dtype,
+                        const void* const* last_micro_bf16, const int64_t* valid_tokens,
+                        int32_t n_counts, float* reduced_grad, float* bucket_sqnorm,
+                        int64_t* bucket_nonfinite, int32_t b0, int32_t b1, void* stream) {
+    dpg::clear_error();
+    return dpg::allreduce_grads(plan, grads, grads_dtype, last_micro_bf16, valid_tokens, n_counts,
+                                reduced_grad, bucket_sqnorm, bucket_nonfinite, b0, b1, stream);
+}
+
+int dpg_adam_from_reduced(const dpg_plan_t* plan, const float* reduced_grad, const dpg_hparams* hp,
+                          float* master, float* exp_avg, float* exp_avg_sq,
+                          void* const* param_views, int32_t n_views, float* bucket_sqnorm,
+                          int64_t* bucket_nonfinite, int32_t b0, int32_t b1, void* stream) {
+    dpg::clear_error();
+    return dpg::adam_from_reduced(plan, reduced_grad, hp, master, exp_avg, exp_avg_sq, param_views,
+                                  n_views, bucket_sqnorm, bucket_nonfinite, b0, b1, stream);
 }
 
 int dpg_check_device_status(const dpg_plan_t* plan, void* stream) {
