@@ -276,11 +276,12 @@ int dpg_step_clipped(const dpg_plan_t* plan, const void* const* grads, int32_t g
                      float* clip_out, void* stream);
 
 /* ---------------------------------------------------------------------------
- * dpg_step through the STAGED variant of the fused pass: each CTA copies the
- * R gradient tiles and the master/m/v tiles of the half-tiles it will
- * process into shared memory with the bulk-copy engine (cp.async.bulk,
- * completion counted in bytes on an mbarrier), several half-tiles ahead of
- * its threads.  Same arguments and results as dpg_step for bf16 gradients
+ * dpg_step through the STAGED variant of the fused pass: in each CTA a
+ * producer warp copies the R gradient tiles and the master/m/v tiles of the
+ * half-tiles it will process into a ring of shared-memory stages with the
+ * bulk-copy engine (cp.async.bulk, completion counted in bytes on a "full"
+ * mbarrier per stage), refilling a stage as soon as the consumer warps have
+ * released it on its "empty" mbarrier.  Same arguments and results as dpg_step for bf16 gradients
  * (grads_dtype must be DPG_BF16, no last microbatch), R in {1, 2, 4, 8}.
  * Every device-side wait is bounded (1 s); a wait that runs out makes the
  * CTA wait (bounded) for its own copies in flight and return, and records

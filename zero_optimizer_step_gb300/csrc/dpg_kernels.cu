@@ -604,34 +604,72 @@ __device__ __forceinline__ void issue_unit(const StagedArgs& sa, unsigned char* 
                      : "memory");
 }
 
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    uint64_t state;
+    asm volatile("mbarrier.arrive.shared::cta.b64 %0, [%1];" : "=l"(state) : "r"(bar) : "memory");
+    (void)state;
+}
+
+// Warp-specialised: warps 0..15 consume (512 threads, 4 elements each per
+// unit), warp 16 produces.  full[s] completes when stage s's copies have
+// landed (the producer arms it with the byte count); empty[s] completes when
+// the 16 consumer warps have finished reading it, and the producer refills it
+// only then.  All waits are bounded.
 template <int RT>
-__global__ void __launch_bounds__(kStagedThreads, 1) k_rs_adam_staged(const __grid_constant__ StagedArgs sa) {
+__global__ void __launch_bounds__(kStagedThreads + 32, 1) k_rs_adam_staged(const __grid_constant__ StagedArgs sa) {
     constexpr int S = staged_stages(RT);
     constexpr size_t SB = staged_stage_bytes(RT);
+    constexpr int kConsumerWarps = kStagedThreads / 32;
     extern __shared__ __align__(128) unsigned char smem[];
-    __shared__ __align__(8) uint64_t bars[kMaxStages];
+    __shared__ __align__(8) uint64_t full[kMaxStages];
+    __shared__ __align__(8) uint64_t empty[kMaxStages];
     const RsAdamArgs& a = sa.a;
     const int64_t u0 = 2 * a.t0, u1 = 2 * a.t1;   // units of the launch
     const int64_t n_mine = blockIdx.x < u1 - u0 ? (u1 - u0 - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
-    // producer bookkeeping (thread 0): which stages hold an armed, unconsumed unit
-    int b_prod = a.b0;
-    uint32_t armed = 0;      // bit s: stage s holds an armed, unconsumed unit
-    uint32_t armed_par = 0;  // bit s: phase parity that unit completes
     if (threadIdx.x == 0) {
-        for (int k = 0; k < S; ++k)
-            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" :: "r"(smem_u32(&bars[k])) : "memory");
-        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-        for (int64_t k = 0; k < S && k < n_mine; ++k) {
-            const int64_t u = u0 + blockIdx.x + k * gridDim.x;
-            int64_t cnt;
-            const int64_t st = unit_range(a, u, b_prod, &cnt);
-            if (u == sa.skip_unit) continue;
-            issue_unit<RT>(sa, smem + k * SB, smem_u32(&bars[k]), st, cnt);
-            armed |= 1u << k;   // parity 0: first phase of every stage
+        for (int k = 0; k < S; ++k) {
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" :: "r"(smem_u32(&full[k])) : "memory");
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;"
+                         :: "r"(smem_u32(&empty[k])), "r"(kConsumerWarps) : "memory");
         }
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     __syncthreads();
 
+    if (threadIdx.x >= kStagedThreads) {
+        // ---------------- producer warp: one lane issues ----------------
+        if (threadIdx.x != kStagedThreads) return;
+        int b_prod = a.b0;
+        uint32_t armed = 0, armed_par = 0;   // stages armed at least once, parity of the last arm
+        bool aborted = false;
+        for (int64_t k = 0; k < n_mine; ++k) {
+            const int s = int(k % S);
+            if (k >= S &&
+                !mbar_wait_bounded(smem_u32(&empty[s]), uint32_t((k / S - 1) & 1),
+                                   global_ns() + sa.timeout_ns)) {
+                aborted = true;
+                break;
+            }
+            const int64_t u = u0 + blockIdx.x + k * gridDim.x;
+            int64_t cnt;
+            const int64_t st = unit_range(a, u, b_prod, &cnt);
+            if (u == sa.skip_unit) continue;          // test hook: never fetched
+            issue_unit<RT>(sa, smem + s * SB, smem_u32(&full[s]), st, cnt);
+            armed |= 1u << s;
+            armed_par = (armed_par & ~(1u << s)) | (uint32_t((k / S) & 1) << s);
+        }
+        if (aborted) atomicExch(sa.status, DPG_ERR_DEVICE_TIMEOUT);
+        // no copy may still be in flight when this CTA exits: wait (bounded)
+        // until the last phase armed on every stage has landed
+        const uint64_t drain = global_ns() + sa.timeout_ns;
+        for (int s2 = 0; s2 < S; ++s2)
+            if (armed & (1u << s2))
+                mbar_wait_bounded(smem_u32(&full[s2]), (armed_par >> s2) & 1u, drain);
+        return;
+    }
+
+    // ---------------- consumer warps ----------------
+    const int lane = threadIdx.x & 31;
     const bool norm = a.vis_sq != nullptr;
     int b = a.b0, cur = -1, visit = 0;
     double sq = 0.0;
@@ -643,8 +681,9 @@ __global__ void __launch_bounds__(kStagedThreads, 1) k_rs_adam_staged(const __gr
         const int64_t u = u0 + blockIdx.x + k * gridDim.x;
         int64_t cnt;
         const int64_t start = unit_range(a, u, b, &cnt);
-        const bool ok = mbar_wait_bounded(smem_u32(&bars[s]), parity, global_ns() + sa.timeout_ns);
-        if (__syncthreads_or(!ok)) {
+        bool ok = mbar_wait_bounded(smem_u32(&full[s]), parity, global_ns() + sa.timeout_ns);
+        ok = __all_sync(0xFFFFFFFFu, ok);     // warp-uniform decision
+        if (!ok) {
             aborted = true;
             break;
         }
@@ -655,9 +694,11 @@ __global__ void __launch_bounds__(kStagedThreads, 1) k_rs_adam_staged(const __gr
             nf = 0;
         }
         const int e = threadIdx.x * 4;
-        if (e < cnt) {
+        const bool mine = e < cnt;
+        float x[4];
+        float4 w, m, v;
+        if (mine) {
             const unsigned char* stage = smem + s * SB;
-            float x[4];
             {
                 const uint2 q = *reinterpret_cast<const uint2*>(stage + size_t(e) * 2);
                 widen2(q.x, x[0], x[1]);
@@ -673,9 +714,14 @@ __global__ void __launch_bounds__(kStagedThreads, 1) k_rs_adam_staged(const __gr
                 for (int j = 0; j < 4; ++j) x[j] = __fadd_rn(x[j], y[j]);
             }
             const float* sw = reinterpret_cast<const float*>(stage + size_t(RT) * kUnit * 2);
-            float4 w = *reinterpret_cast<const float4*>(sw + e);
-            float4 m = *reinterpret_cast<const float4*>(sw + kUnit + e);
-            float4 v = *reinterpret_cast<const float4*>(sw + 2 * kUnit + e);
+            w = *reinterpret_cast<const float4*>(sw + e);
+            m = *reinterpret_cast<const float4*>(sw + kUnit + e);
+            v = *reinterpret_cast<const float4*>(sw + 2 * kUnit + e);
+        }
+        // the warp has read stage s: release it to the producer, then compute
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&empty[s]));
+        if (mine) {
             float* wp = &w.x;
             float* mp = &m.x;
             float* vp = &v.x;
@@ -711,43 +757,12 @@ __global__ void __launch_bounds__(kStagedThreads, 1) k_rs_adam_staged(const __gr
             for (int kv = 0; kv < a.n_views; ++kv)
                 *reinterpret_cast<uint2*>(static_cast<uint16_t*>(a.views[kv]) + i) = pk;
         }
-        __syncthreads();   // every thread is done with stage s
-        if (threadIdx.x == 0) {
-            armed &= ~(1u << s);
-            const int64_t kn = k + S;
-            if (kn < n_mine) {
-                const int64_t un = u0 + blockIdx.x + kn * gridDim.x;
-                int64_t cn;
-                const int64_t sn = unit_range(a, un, b_prod, &cn);
-                if (un != sa.skip_unit) {
-                    issue_unit<RT>(sa, smem + s * SB, smem_u32(&bars[s]), sn, cn);
-                    armed |= 1u << s;
-                    armed_par = (armed_par & ~(1u << s)) | (uint32_t((kn / S) & 1) << s);
-                }
-            }
-        }
     }
-    if (aborted) {
-        if (threadIdx.x == 0) {
-            atomicExch(sa.status, DPG_ERR_DEVICE_TIMEOUT);
-            // the visits flushed so far stay readable by the finalize
-            if (norm) a.vis_count[blockIdx.x] = visit;
-            // wait (bounded) for this CTA's copies still in flight before exiting
-            const uint64_t drain = global_ns() + sa.timeout_ns;
-            for (int s2 = 0; s2 < S; ++s2)
-                if (armed & (1u << s2))
-                    mbar_wait_bounded(smem_u32(&bars[s2]), (armed_par >> s2) & 1u, drain);
-        }
-        return;
-    }
+    if (aborted && lane == 0) atomicExch(sa.status, DPG_ERR_DEVICE_TIMEOUT);
     if (norm) {
         if (cur >= 0) flush_visit(a, cur, visit++, sq, nf);
         if (threadIdx.x == 0) a.vis_count[blockIdx.x] = visit;
     }
-    __syncthreads();
-    if (threadIdx.x == 0)
-        for (int k = 0; k < S; ++k)
-            asm volatile("mbarrier.inval.shared::cta.b64 [%0];" :: "r"(smem_u32(&bars[k])) : "memory");
 }
 
 // One CTA per bucket: thread c (and c + 256, ...) finds CTA c's visit of the
@@ -1571,7 +1586,7 @@ static int launch_staged(const StagedArgs& sa, int grid, cudaStream_t s) {
             attr_set = true;
         }
     }
-    k_rs_adam_staged<RT><<<grid, kStagedThreads, smem, s>>>(sa);
+    k_rs_adam_staged<RT><<<grid, kStagedThreads + 32, smem, s>>>(sa);
     return after_launch("dpg_step_staged");
 }
 
