@@ -742,7 +742,28 @@ def run_schedules(a):
                  "achieved_gbs": bpp * psi / (ms * 1e-3) / 1e9,
                  "model_state_bytes_per_param_per_replica": 16,
                  "note": "all-reduce, then each of the R replicas updates its own full state"})
-    print(json.dumps({"metric": "DDP vs ZeRO-1/2 schedules", "config": workload_desc(cfg, cap, plan.n_buckets, N),
+    del reps
+    # ZeRO-3: the step writes only the sharded bf16 parameters; every layer is
+    # all-gathered from the shards before forward and again before backward
+    z = [w0.clone(), torch.zeros(N, device=dev), torch.zeros(N, device=dev)]
+    shards = torch.empty(N, dtype=torch.bfloat16, device=dev)
+    ms_step = timed(lambda: dpg.dpg_step(plan, g, tok, hp(), *z, [shards]))
+
+    def gathers():
+        for _ in range(2):
+            for b in range(plan.n_buckets):
+                dpg.dpg_gather_params_bf16(plan, shards, rp, b0=b, b1=b + 1)
+
+    ms_gather = timed(gathers)
+    bpp = 2 * R + 26 + 2 * (2 + 2 * R)
+    rows.append({"schedule": "ZeRO-3", "ms": ms_step + ms_gather, "ms_step": ms_step,
+                 "ms_gathers": ms_gather, "bytes_per_param": bpp,
+                 "achieved_gbs": bpp * psi / ((ms_step + ms_gather) * 1e-3) / 1e9,
+                 "gather_gbs": 2 * (2 + 2 * R) * psi / (ms_gather * 1e-3) / 1e9,
+                 "model_state_bytes_per_param_per_replica": 16 / R,
+                 "note": "same fused pass writing one sharded bf16 buffer, then two "
+                         "layer-by-layer parameter all-gathers (forward, backward)"})
+    print(json.dumps({"metric": "DDP vs ZeRO-1/2/3 schedules", "config": workload_desc(cfg, cap, plan.n_buckets, N),
                       "peak_gbs": peak, "peak_kind": peak_kind, "rows": rows}), flush=True)
 
 

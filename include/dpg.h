@@ -214,6 +214,22 @@ int dpg_allgather_params(const dpg_plan_t* plan, const float* master,
                          void* stream);
 
 /* ---------------------------------------------------------------------------
+ * ZeRO-3 parameter all-gather, buckets [b0, b1)   ["Parallelisms" -- ZeRO-3:
+ *      before a layer runs in forward, and again in backward, workers
+ *      all-gather its parameter shards; "Parallelism Strategies in
+ *      Distributed Computing" -- ZeRO and FSDP]
+ * param_bf16: the flat bf16 parameter buffer in which every rank's shard of
+ * every bucket lives in place (shard r of bucket b at its shard range);
+ * views[k][i] = param_bf16[i] for every element of the buckets: each
+ * replica's full copy of the layer, assembled from all shards.  Under ZeRO-3
+ * the step itself then writes only the sharded parameters (n_views = 1 on the
+ * shared buffer), and layers are gathered before use.
+ * ------------------------------------------------------------------------- */
+int dpg_gather_params_bf16(const dpg_plan_t* plan, const void* param_bf16,
+                           void* const* param_views, int32_t n_views, int32_t b0, int32_t b1,
+                           void* stream);
+
+/* ---------------------------------------------------------------------------
  * One whole optimizer step over every bucket (one fused launch plus, when a
  * norm output is requested, one small finalize launch).  Same arguments and
  * semantics as dpg_reduce_scatter_adam with b0 = 0, b1 = n_buckets and no

@@ -180,6 +180,17 @@ def test_other_entry_points_validation():
     assert L.dpg_allgather_params(plan.handle, FAKE, dpg._ptrs([FAKE]), 65, 0, 1, None) == dpg.DPG_ERR_INVALID_ARG
     assert L.dpg_allgather_params(plan.handle, FAKE + 4, dpg._ptrs([FAKE]), 1, 0, 1, None) == dpg.DPG_ERR_MISALIGNED
     assert L.dpg_allgather_params(plan.handle, FAKE, dpg._ptrs([FAKE]), 1, 1, 1, None) == dpg.DPG_OK
+    G = L.dpg_gather_params_bf16
+    assert G(None, FAKE, dpg._ptrs([FAKE]), 1, 0, 1, None) == dpg.DPG_ERR_INVALID_ARG
+    assert G(plan.handle, FAKE, dpg._ptrs([FAKE]), 1, 0, 3, None) == dpg.DPG_ERR_INVALID_ARG
+    assert G(plan.handle, FAKE, dpg._ptrs([FAKE]), 1, 1, 0, None) == dpg.DPG_ERR_INVALID_ARG
+    assert G(plan.handle, FAKE, dpg._ptrs([FAKE]), 65, 0, 1, None) == dpg.DPG_ERR_INVALID_ARG
+    assert G(plan.handle, None, dpg._ptrs([FAKE]), 1, 0, 1, None) == dpg.DPG_ERR_INVALID_ARG
+    assert G(plan.handle, FAKE, dpg._ptrs([0]), 1, 0, 1, None) == dpg.DPG_ERR_INVALID_ARG
+    assert G(plan.handle, FAKE + 2, dpg._ptrs([FAKE]), 1, 0, 1, None) == dpg.DPG_ERR_MISALIGNED
+    assert G(plan.handle, FAKE, dpg._ptrs([FAKE, FAKE + 8]), 2, 0, 1, None) == dpg.DPG_ERR_MISALIGNED
+    assert G(plan.handle, FAKE, dpg._ptrs([FAKE]), 1, 1, 1, None) == dpg.DPG_OK
+    assert G(plan.handle, None, None, 0, 0, 1, None) == dpg.DPG_OK
     assert L.dpg_pack(plan.handle, dpg._ptrs([FAKE, 0, FAKE]), FAKE, None) == dpg.DPG_ERR_INVALID_ARG
     assert L.dpg_pack(plan.handle, dpg._ptrs([FAKE, FAKE + 1, FAKE]), FAKE, None) == dpg.DPG_ERR_MISALIGNED
     assert L.dpg_pack(plan.handle, dpg._ptrs([FAKE] * 3), FAKE + 8, None) == dpg.DPG_ERR_MISALIGNED

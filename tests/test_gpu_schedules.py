@@ -122,3 +122,52 @@ def test_ddp_replicas_equal_zero2_bit_for_bit():
         for a, b in zip(reps[r], z):
             assert torch.equal(a.view(torch.int32), b.view(torch.int32))
         assert torch.equal(rp[r].view(torch.int16), zp.view(torch.int16))
+
+
+def test_zero3_gather_copies_bucket_range_only():
+    plan, op, _, _, _ = _setup(2, "bf16", seed=13)
+    N = op.total_padded
+    g = torch.Generator().manual_seed(13)
+    param = torch.randn(N, generator=g).to(torch.bfloat16).cuda()
+    nan_bits = torch.tensor(0x7FC1, dtype=torch.int16)
+    views = [torch.full((N,), int(nan_bits), dtype=torch.int16, device="cuda") for _ in range(3)]
+    b0, b1 = 1, max(2, op.n_buckets - 1)
+    dpg.dpg_gather_params_bf16(plan, param, [v.view(torch.bfloat16) for v in views], b0=b0, b1=b1)
+    torch.cuda.synchronize()
+    lo, hi = op.bucket_offset[b0], op.bucket_offset[b1 - 1] + op.bucket_padded[b1 - 1]
+    pb = param.view(torch.int16).cpu()
+    for v in views:
+        h = v.cpu()
+        assert torch.equal(h[lo:hi], pb[lo:hi])
+        assert bool((h[:lo] == nan_bits).all()) and bool((h[hi:] == nan_bits).all())
+
+
+def test_zero3_schedule_equals_zero2_views():
+    """ZeRO-3: the step writes only the sharded bf16 parameters (one buffer);
+    before use, every replica all-gathers the full layer from the shards.
+    Each gathered replica equals the ZeRO-2 step's own per-replica view and
+    the oracle's cast of the master weights."""
+    R = 4
+    plan, op, grads, _, tok = _setup(R, "bf16", seed=17)
+    N = op.total_padded
+    dg = [g.cuda() for g in grads]
+    w0 = master_f32(N, stream_seed(17, KIND_MASTER), device="cuda")
+    z2 = [w0.clone(), torch.zeros(N, device="cuda"), torch.zeros(N, device="cuda")]
+    z2v = [torch.empty(N, dtype=torch.bfloat16, device="cuda") for _ in range(R)]
+    z3 = [w0.clone(), torch.zeros(N, device="cuda"), torch.zeros(N, device="cuda")]
+    shards = torch.empty(N, dtype=torch.bfloat16, device="cuda")
+    z3v = [torch.full((N,), float("nan"), dtype=torch.bfloat16, device="cuda") for _ in range(R)]
+    for t in (1, 2):
+        dpg.dpg_step(plan, dg, tok, dpg.HParams(step=t), *z2, z2v)
+        dpg.dpg_step(plan, dg, tok, dpg.HParams(step=t), *z3, [shards])
+        for b in range(op.n_buckets):  # layer by layer, as a forward pass would
+            dpg.dpg_gather_params_bf16(plan, shards, z3v, b0=b, b1=b + 1)
+    torch.cuda.synchronize()
+    w, m, v = np_f32(w0).copy(), np.zeros(N, np.float32), np.zeros(N, np.float32)
+    for t in (1, 2):
+        oracle.step(op.bucket_offset, op.bucket_padded, [np_bf16(g) for g in grads], tok, w, m, v,
+                    n_views=1, t=t)
+    ref = oracle.f32_to_bf16(w)
+    for a, b in zip(z2v, z3v):
+        assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+        np.testing.assert_array_equal(np_bf16(b), ref)

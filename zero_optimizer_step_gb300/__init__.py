@@ -39,7 +39,7 @@ EXPORTED = (
     "dpg_reduce_scatter_adam", "dpg_allgather_params", "dpg_step", "dpg_launch_count",
     "dpg_time_next_fused_launch", "dpg_step_noalloc", "dpg_export_state", "dpg_import_state",
     "dpg_step_clipped", "dpg_step_staged", "dpg_check_device_status", "dpg_set_staged_fault",
-    "dpg_allreduce_grads", "dpg_adam_from_reduced",
+    "dpg_allreduce_grads", "dpg_adam_from_reduced", "dpg_gather_params_bf16",
 )
 DPG_MAX_STATE_ARRAYS = 8
 DPG_NOALLOC_SCRATCH_BYTES = 8 << 20
@@ -114,6 +114,7 @@ def lib() -> ctypes.CDLL:
                                        P, P, P, P, P]
         L.dpg_step_staged.argtypes = [P, P, i32, P, i32, P, P, P, P, P, i32, P, P, P]
         L.dpg_allreduce_grads.argtypes = [P, P, i32, P, P, i32, P, P, P, i32, i32, P]
+        L.dpg_gather_params_bf16.argtypes = [P, P, P, i32, i32, i32, P]
         L.dpg_adam_from_reduced.argtypes = [P, P, P, P, P, P, P, i32, P, P, i32, i32, P]
         L.dpg_check_device_status.argtypes = [P, P]
         L.dpg_set_staged_fault.argtypes = [i64, i64]
@@ -126,7 +127,8 @@ def lib() -> ctypes.CDLL:
                      "dpg_accumulate", "dpg_reduce_scatter_adam", "dpg_allgather_params",
                      "dpg_step", "dpg_step_noalloc", "dpg_export_state", "dpg_import_state",
                      "dpg_step_clipped", "dpg_step_staged", "dpg_check_device_status",
-                     "dpg_set_staged_fault", "dpg_allreduce_grads", "dpg_adam_from_reduced"):
+                     "dpg_set_staged_fault", "dpg_allreduce_grads", "dpg_adam_from_reduced",
+                     "dpg_gather_params_bf16"):
             getattr(L, name).restype = c_int
         _lib = L
     return _lib
@@ -529,6 +531,17 @@ def dpg_allgather_params(plan: Plan, master: Ptr, param_views: Sequence[Ptr], *,
     _check(lib().dpg_allgather_params(plan.handle, _ptr(master), _ptrs(param_views),
                                       len(param_views), b0,
                                       plan.n_buckets if b1 is None else b1, _stream(stream)))
+
+
+def dpg_gather_params_bf16(plan: Plan, param_bf16: Ptr, param_views: Sequence[Ptr], *, b0: int = 0,
+                           b1: Optional[int] = None, stream=None):
+    """ZeRO-3 all-gather of the bf16 parameter shards into full replica views."""
+    _need(param_bf16, "bf16", plan.total_padded, "param_bf16")
+    for k, t in enumerate(param_views):
+        _need(t, "bf16", plan.total_padded, f"param_views[{k}]")
+    _check(lib().dpg_gather_params_bf16(plan.handle, _ptr(param_bf16), _ptrs(param_views),
+                                        len(param_views), b0, plan.n_buckets if b1 is None else b1,
+                                        _stream(stream)))
 
 
 def dpg_launch_count() -> int:

@@ -883,6 +883,19 @@ __global__ void __launch_bounds__(256) k_allgather(const float* __restrict__ mas
     }
 }
 
+// ZeRO-3 parameter all-gather: the bf16 shards (laid out in place in the flat
+// parameter buffer) copied into every replica's full view; read once, written
+// n_views times.
+__global__ void __launch_bounds__(256) k_gather_bf16(const uint16_t* __restrict__ param,
+                                                     const __grid_constant__ ViewArgs va,
+                                                     int64_t lo_vec, int64_t hi_vec) {
+    for (int64_t k = lo_vec + int64_t(blockIdx.x) * blockDim.x + threadIdx.x; k < hi_vec;
+         k += int64_t(gridDim.x) * blockDim.x) {
+        const uint4 x = ld_grad_u4(param + k * kVec);
+        for (int v = 0; v < va.n_views; ++v) st_u4(static_cast<uint16_t*>(va.views[v]) + k * kVec, x);
+    }
+}
+
 // ---------------------------------------------------------------------------
 // pack / unpack: one CTA per item (<= kPackChunk elements of one parameter)
 // ---------------------------------------------------------------------------
@@ -1829,6 +1842,42 @@ int dpg_allgather_params(const dpg_plan_t* plan, const float* master, void* cons
     if (st != DPG_OK) return st;
     dpg::k_allgather<<<grid, 256, 0, static_cast<cudaStream_t>(stream)>>>(master, va, lo, hi);
     return dpg::after_launch("dpg_allgather_params");
+}
+
+int dpg_gather_params_bf16(const dpg_plan_t* plan, const void* param_bf16, void* const* views,
+                           int32_t n_views, int32_t b0, int32_t b1, void* stream) {
+    dpg::clear_error();
+    if (!plan) return fail(DPG_ERR_INVALID_ARG, "dpg_gather_params_bf16: plan is NULL");
+    const dpg::Plan& p = plan->p;
+    if (b0 < 0 || b1 < b0 || b1 > p.n_buckets)
+        return fail(DPG_ERR_INVALID_ARG, "dpg_gather_params_bf16: bucket range [%d, %d) outside [0, %d]",
+                    b0, b1, p.n_buckets);
+    if (n_views < 0 || n_views > DPG_MAX_VIEWS)
+        return fail(DPG_ERR_INVALID_ARG, "dpg_gather_params_bf16: n_views %d outside [0, %d]", n_views,
+                    DPG_MAX_VIEWS);
+    if (b0 == b1 || n_views == 0 || p.bucket_offset[b1] == p.bucket_offset[b0]) return DPG_OK;
+    if (!param_bf16) return fail(DPG_ERR_INVALID_ARG, "dpg_gather_params_bf16: param is NULL");
+    if (!dpg::aligned(param_bf16, 16))
+        return fail(DPG_ERR_MISALIGNED, "dpg_gather_params_bf16: param misaligned");
+    if (!views) return fail(DPG_ERR_INVALID_ARG, "dpg_gather_params_bf16: views is NULL");
+    dpg::ViewArgs va{};
+    va.n_views = n_views;
+    for (int k = 0; k < n_views; ++k) {
+        if (!views[k]) return fail(DPG_ERR_INVALID_ARG, "dpg_gather_params_bf16: views[%d] is NULL", k);
+        if (!dpg::aligned(views[k], 16))
+            return fail(DPG_ERR_MISALIGNED, "dpg_gather_params_bf16: views[%d] misaligned", k);
+        va.views[k] = views[k];
+    }
+    const int64_t lo = p.bucket_offset[b0] / dpg::kVec, hi = p.bucket_offset[b1] / dpg::kVec;
+    int dev = 0;
+    DPG_CUDA_TRY(cudaGetDevice(&dev));
+    int grid = 0;
+    int st = dpg::grid_for(reinterpret_cast<const void*>(dpg::k_gather_bf16), 256, dev,
+                           (hi - lo + 255) / 256, &grid);
+    if (st != DPG_OK) return st;
+    dpg::k_gather_bf16<<<grid, 256, 0, static_cast<cudaStream_t>(stream)>>>(
+        static_cast<const uint16_t*>(param_bf16), va, lo, hi);
+    return dpg::after_launch("dpg_gather_params_bf16");
 }
 
 static int pack_common(const dpg_plan_t* plan, const void* const* ptrs, void* flat, int unpack,
