@@ -207,6 +207,21 @@ def cpu_sample_inputs(cfg, n, device):
     return grads, last, w, np.zeros(n, np.float32), np.zeros(n, np.float32)
 
 
+def host_cpu() -> str:
+    """Machine, core count and CPU model of the host the oracle is timed on."""
+    import platform
+    model = ""
+    try:
+        for ln in open("/proc/cpuinfo"):
+            k, _, val = ln.partition(":")
+            if k.strip() in ("model name", "CPU part") and val.strip():
+                model = val.strip()
+                break
+    except OSError:
+        pass
+    return f"{platform.machine()}, {os.cpu_count()} cores, {model or 'model unknown'}"
+
+
 def cpu_baseline(cfg, device, target_s=12.0) -> dict:
     """Time the oracle, as it stands, on one host core over a bounded sample."""
     import oracle
@@ -228,6 +243,7 @@ def cpu_baseline(cfg, device, target_s=12.0) -> dict:
     dt = time.perf_counter() - t0
     cores = 1
     return {"value": reps * n / dt, "unit": "params/s", "cores": cores, "kind": "oracle",
+            "host": host_cpu(),
             "sample": f"{reps} oracle steps over the first {n} elements of the workload "
                       f"(elementwise reduce+scale+Adam+bf16 cast; fixed-order fp32), one pinned core"}
 
@@ -347,7 +363,9 @@ def run_dpg(a):
         dist.barrier()
     clk = clocks.stop()
     ms = ev_start.elapsed_time(ev_stop) / a.steps
-    k_ms = statistics.mean(e0.elapsed_time(e1) for e0, e1 in ev_k)
+    k_all = sorted(e0.elapsed_time(e1) for e0, e1 in ev_k)
+    k_ms = statistics.mean(k_all)
+    k_pct = [k_all[int(round(q * (len(k_all) - 1)))] for q in (0.1, 0.5, 0.9)]
     ms = max_over_ranks(ms, world, dev)
 
     # end to end: host (pinned) gradients copied in, norms copied out, every step
@@ -373,7 +391,7 @@ def run_dpg(a):
                      "peak": peak, "peak_kind": f"{peak_kind} (copy bandwidth)", "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic,
                      "algorithmic_bytes_per_launch": bpp["fused"] * cfg.psi,
-                     "kernel_ms": k_ms},
+                     "kernel_ms": k_ms, "kernel_ms_p10_p50_p90": k_pct},
         "gpu_launches": int(launches),
         "clocks": clk,
         "e2e": e2e,
@@ -514,7 +532,7 @@ def run_reference(a):
             "config": workload_desc(cfg, cap, plan.n_buckets, plan.total_padded),
             "impl": "reference",
             "cpu_baseline": {"value": value, "unit": "params/s", "cores": 1, "kind": "oracle",
-                             "sample": sample},
+                             "host": host_cpu(), "sample": sample},
             "e2e": {"value": value, "unit": "params/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
