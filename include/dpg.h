@@ -39,6 +39,15 @@
  *     that before capturing a stream into a CUDA graph.  A plan serves one
  *     device.  Calls that use the norm scratch of the same plan must not
  *     overlap on the GPU (issue them on one stream).
+ *   - Gradient INPUTS (grads, last_micro, the accumulate source) of
+ *     dpg_accumulate, dpg_reduce_scatter_adam, dpg_step, dpg_step_clipped
+ *     and dpg_allreduce_grads may instead be page-locked host memory
+ *     (cudaHostAlloc / cudaMallocHost, or host-registered) at its own
+ *     address, which unified addressing maps into the device: the kernels
+ *     then read it over the host link with the same loads, so no staging
+ *     copy or device gradient buffer is needed and the results are the
+ *     same bits.  The pass then runs at the link's bandwidth, not HBM's.
+ *     The staged and allocation-free steps take device memory only.
  */
 #ifndef DPG_H
 #define DPG_H

@@ -171,3 +171,29 @@ def test_zero3_schedule_equals_zero2_views():
     for a, b in zip(z2v, z3v):
         assert torch.equal(a.view(torch.int16), b.view(torch.int16))
         np.testing.assert_array_equal(np_bf16(b), ref)
+
+
+def test_pinned_host_gradients_read_in_place():
+    """Gradient inputs in page-locked host memory are read by the kernels over
+    the host link; every output equals the device-resident run bit for bit
+    (fused step with and without accumulation, all-reduce)."""
+    R = 4
+    plan, op, grads, last, tok = _setup(R, "acc", seed=19)
+    N = op.total_padded
+    w0 = master_f32(N, stream_seed(19, KIND_MASTER), device="cuda")
+    h_acc = [x.pin_memory() for x in grads]
+    h_last = [x.pin_memory() for x in last]
+    outs = []
+    for acc, last in (([x.cuda() for x in h_acc], [x.cuda() for x in h_last]), (h_acc, h_last)):
+        d = [w0.clone(), torch.zeros(N, device="cuda"), torch.zeros(N, device="cuda")]
+        p = torch.empty(N, dtype=torch.bfloat16, device="cuda")
+        sq = torch.empty(op.n_buckets, device="cuda")
+        red = torch.empty(N, device="cuda")
+        a0 = torch.empty(N, device="cuda")
+        dpg.dpg_accumulate(plan, last[0], a0, first=True)
+        dpg.dpg_step(plan, acc, tok, dpg.HParams(), *d, [p], last_micro=last, bucket_sqnorm=sq)
+        dpg.dpg_allreduce_grads(plan, acc, tok, red, last_micro=last)
+        torch.cuda.synchronize()
+        outs.append([*d, p, sq, red, a0])
+    for a, b in zip(*outs):
+        assert torch.equal(a.view(torch.uint8), b.view(torch.uint8))

@@ -197,6 +197,20 @@ def _need(t, dtype_name: str, numel: int, what: str):
         raise ValueError(f"{what}: needs >= {numel} elements, has {t.numel()}")
 
 
+def _need_in(t, dtype_name: str, numel: int, what: str):
+    """Gradient inputs may also be page-locked host tensors: under unified
+    addressing the kernels read them over the host link at the same address."""
+    if t is not None and not isinstance(t, int) and not t.is_cuda and t.is_pinned():
+        import torch
+        want = {"bf16": torch.bfloat16, "f32": torch.float32}[dtype_name]
+        if t.dtype != want:
+            raise TypeError(f"{what}: expected {want}, got {t.dtype}")
+        if not t.is_contiguous() or t.numel() < numel:
+            raise ValueError(f"{what}: needs a contiguous tensor of >= {numel} elements")
+        return
+    _need(t, dtype_name, numel, what)
+
+
 # --------------------------------------------------------------------------
 # plan
 # --------------------------------------------------------------------------
@@ -320,7 +334,7 @@ def dpg_import_state(plan: Plan, canon: Sequence[Ptr], flat: Sequence[Ptr], stre
 
 
 def dpg_accumulate(plan: Plan, flat_bf16: Ptr, acc_f32: Ptr, first: bool, stream=None):
-    _need(flat_bf16, "bf16", plan.total_padded, "flat_bf16")
+    _need_in(flat_bf16, "bf16", plan.total_padded, "flat_bf16")
     _need(acc_f32, "f32", plan.total_padded, "acc_f32")
     _check(lib().dpg_accumulate(plan.handle, _ptr(flat_bf16), _ptr(acc_f32), 1 if first else 0,
                                 _stream(stream)))
@@ -345,9 +359,9 @@ def dpg_reduce_scatter_adam(plan: Plan, grads: Sequence[Ptr], valid_tokens, hp: 
     gd = _grad_dtype(grads) if grads_dtype is None else grads_dtype
     N = plan.total_padded
     for k, g in enumerate(grads):
-        _need(g, "bf16" if gd == DPG_BF16 else "f32", N, f"grads[{k}]")
+        _need_in(g, "bf16" if gd == DPG_BF16 else "f32", N, f"grads[{k}]")
     for k, g in enumerate(last_micro or ()):
-        _need(g, "bf16", N, f"last_micro[{k}]")
+        _need_in(g, "bf16", N, f"last_micro[{k}]")
     for name, t in (("master", master), ("exp_avg", exp_avg), ("exp_avg_sq", exp_avg_sq),
                     ("reduced_grad", reduced_grad)):
         _need(t, "f32", N, name)
@@ -372,9 +386,9 @@ def dpg_step(plan: Plan, grads: Sequence[Ptr], valid_tokens, hp: HParams, master
     gd = _grad_dtype(grads) if grads_dtype is None else grads_dtype
     N = plan.total_padded
     for k, g in enumerate(grads):
-        _need(g, "bf16" if gd == DPG_BF16 else "f32", N, f"grads[{k}]")
+        _need_in(g, "bf16" if gd == DPG_BF16 else "f32", N, f"grads[{k}]")
     for k, g in enumerate(last_micro or ()):
-        _need(g, "bf16", N, f"last_micro[{k}]")
+        _need_in(g, "bf16", N, f"last_micro[{k}]")
     for name, t in (("master", master), ("exp_avg", exp_avg), ("exp_avg_sq", exp_avg_sq)):
         _need(t, "f32", N, name)
     for k, t in enumerate(param_views):
@@ -400,9 +414,9 @@ def dpg_step_clipped(plan: Plan, grads: Sequence[Ptr], valid_tokens, hp: HParams
     gd = _grad_dtype(grads) if grads_dtype is None else grads_dtype
     N = plan.total_padded
     for k, g in enumerate(grads):
-        _need(g, "bf16" if gd == DPG_BF16 else "f32", N, f"grads[{k}]")
+        _need_in(g, "bf16" if gd == DPG_BF16 else "f32", N, f"grads[{k}]")
     for k, g in enumerate(last_micro or ()):
-        _need(g, "bf16", N, f"last_micro[{k}]")
+        _need_in(g, "bf16", N, f"last_micro[{k}]")
     for name, t in (("master", master), ("exp_avg", exp_avg), ("exp_avg_sq", exp_avg_sq),
                     ("reduced_grad", reduced_grad)):
         _need(t, "f32", N, name)
@@ -461,9 +475,9 @@ def dpg_allreduce_grads(plan: Plan, grads: Sequence[Ptr], valid_tokens, reduced_
     gd = _grad_dtype(grads) if grads_dtype is None else grads_dtype
     N = plan.total_padded
     for k, g in enumerate(grads):
-        _need(g, "bf16" if gd == DPG_BF16 else "f32", N, f"grads[{k}]")
+        _need_in(g, "bf16" if gd == DPG_BF16 else "f32", N, f"grads[{k}]")
     for k, g in enumerate(last_micro or ()):
-        _need(g, "bf16", N, f"last_micro[{k}]")
+        _need_in(g, "bf16", N, f"last_micro[{k}]")
     _need(reduced_grad, "f32", N, "reduced_grad")
     _need(bucket_sqnorm, "f32", plan.n_buckets, "bucket_sqnorm")
     tok, n_tok = _tokens(valid_tokens)
