@@ -699,6 +699,18 @@ def run_kernel_table(a):
          lambda: dpg.dpg_step_clipped(plan, g, tok, hp(), 1e-6, w, m, v, [p], reduced_grad=acc)),
         ("dpg_step_clipped, replicas re-read", 4 * R + 26,
          lambda: dpg.dpg_step_clipped(plan, g, tok, hp(), 1e-6, w, m, v, [p])),
+        ("k_gather_bf16 (dpg_gather_params_bf16, one view, one launch)", 4,
+         lambda: dpg.dpg_gather_params_bf16(plan, p, views[:1])),
+        (f"k_gather_bf16 (dpg_gather_params_bf16, {R} views, one launch)", 2 + 2 * R,
+         lambda: dpg.dpg_gather_params_bf16(plan, p, views)),
+        (f"k_gather_bf16 ({R} views, one launch per bucket)", 2 + 2 * R,
+         lambda: [dpg.dpg_gather_params_bf16(plan, p, views, b0=b, b1=b + 1)
+                  for b in range(plan.n_buckets)]),
+        # calibration (torch's own kernels, not this library): the mix of reads
+        # and writes sets the ceiling; the denominator is a 1:1 copy
+        ("calibration: torch fill_ (write only, 4 B/param)", 4, lambda: acc.fill_(0.5)),
+        ("calibration: torch copy_ (fp32 1:1 copy, 8 B/param)", 8, lambda: acc.copy_(w)),
+        ("calibration: torch sum (read only, 4 B/param)", 4, lambda: torch.sum(w)),
     ]
     views = [torch.empty(N, dtype=torch.bfloat16, device=dev) for _ in range(R)]
     rows = []
