@@ -52,6 +52,8 @@ def parse():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--config", default="llama1b", choices=sorted(set(CONFIGS) - {"tiny"}))
     ap.add_argument("--cap-mib", type=float, default=None, help="override the bucket cap")
+    ap.add_argument("--hockney-config", default="sweep", choices=["sweep", "llama1b"],
+                    help="parameter list of the --hockney cap sweep")
     ap.add_argument("--impl", default="dpg", choices=["dpg", "reference"])
     ap.add_argument("--variant", default="direct", choices=["direct", "staged"],
                     help="fused pass: direct vector loads, or bulk-copy staging in shared memory")
@@ -578,7 +580,7 @@ def run_hockney(a):
     from zero_optimizer_step_gb300 import build as _build
     _build.build()
     import zero_optimizer_step_gb300 as dpg
-    cfg = CONFIGS["sweep"]
+    cfg = CONFIGS[a.hockney_config]
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
     R = cfg.R
@@ -624,9 +626,11 @@ def run_hockney(a):
                 torch.cuda.synchronize()
                 ts.append(e0.elapsed_time(e1))
             res[mode] = statistics.median(ts)
+            res[mode + "_range"] = [min(ts), max(ts)]
         points.append({"cap_bytes": cap, "n_buckets": plan.n_buckets, "total_padded": N,
                        "bytes": (2 * R + 26) * cfg.psi, "per_bucket_ms": res["per_bucket"],
-                       "fused_ms": res["fused"]})
+                       "fused_ms": res["fused"], "per_bucket_ms_range": res["per_bucket_range"],
+                       "fused_ms_range": res["fused_range"]})
         del graphs, g, w, m, v, p
         plan.destroy()
     K = np.array([q["n_buckets"] for q in points], float)
@@ -636,7 +640,7 @@ def run_hockney(a):
     (alpha, beta), *_ = np.linalg.lstsq(A, T, rcond=None)
     fused = np.array([q["fused_ms"] for q in points]) * 1e-3
     out = {"metric": "hockney alpha-beta fit of the fused reduce-scatter+Adam kernel over bucket caps",
-           "workload": f"sweep: {len(cfg.shapes)} tensors, psi={cfg.psi}, R={R}",
+           "workload": f"{cfg.name}: {len(cfg.shapes)} tensors, psi={cfg.psi}, R={R}",
            "points": points, "fit": {"alpha_us": alpha * 1e6, "inv_beta_gbs": 1.0 / beta / 1e9,
                                      "model": "T_per_bucket = K*alpha + beta*M (least squares)"},
            "fused_single_launch_ms": {"median": float(np.median(fused)) * 1e3,
