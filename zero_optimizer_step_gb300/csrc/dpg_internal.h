@@ -8,8 +8,18 @@
 #include <vector>
 
 #include "dpg.h"
+#include <nvtx3/nvToolsExt.h>
 
 namespace dpg {
+
+// NVTX range around one C-ABI call, so that a timeline (Nsight Systems, or
+// any NVTX-aware tool) shows each call by name; a no-op with no tool attached.
+struct Trace {
+    explicit Trace(const char* name) { nvtxRangePushA(name); }
+    ~Trace() { nvtxRangePop(); }
+    Trace(const Trace&) = delete;
+    Trace& operator=(const Trace&) = delete;
+};
 
 // Geometry of the fused pass.  One thread owns one 8-element vector (16 bytes
 // of bf16 gradient per replica, 32 bytes of each fp32 state array); a CTA of

@@ -1689,6 +1689,7 @@ int dpg_step_staged(const dpg_plan_t* plan, const void* const* grads, int32_t gr
                     int32_t n_views, float* bucket_sqnorm, int64_t* bucket_nonfinite,
                     void* stream) {
     dpg::clear_error();
+    const dpg::Trace trace("dpg_step_staged");
     return dpg::step_staged(plan, grads, grads_dtype, valid_tokens, n_counts, hp, master, exp_avg,
                             exp_avg_sq, param_views, n_views, bucket_sqnorm, bucket_nonfinite,
                             stream);
@@ -1699,6 +1700,7 @@ int dpg_allreduce_grads(const dpg_plan_t* plan, const void* const* grads, int32_
                         int32_t n_counts, float* reduced_grad, float* bucket_sqnorm,
                         int64_t* bucket_nonfinite, int32_t b0, int32_t b1, void* stream) {
     dpg::clear_error();
+    const dpg::Trace trace("dpg_allreduce_grads");
     return dpg::allreduce_grads(plan, grads, grads_dtype, last_micro_bf16, valid_tokens, n_counts,
                                 reduced_grad, bucket_sqnorm, bucket_nonfinite, b0, b1, stream);
 }
@@ -1708,6 +1710,7 @@ int dpg_adam_from_reduced(const dpg_plan_t* plan, const float* reduced_grad, con
                           void* const* param_views, int32_t n_views, float* bucket_sqnorm,
                           int64_t* bucket_nonfinite, int32_t b0, int32_t b1, void* stream) {
     dpg::clear_error();
+    const dpg::Trace trace("dpg_adam_from_reduced");
     return dpg::adam_from_reduced(plan, reduced_grad, hp, master, exp_avg, exp_avg_sq, param_views,
                                   n_views, bucket_sqnorm, bucket_nonfinite, b0, b1, stream);
 }
@@ -1740,6 +1743,7 @@ int dpg_step_clipped(const dpg_plan_t* plan, const void* const* grads, int32_t g
                      float* bucket_sqnorm, int64_t* bucket_nonfinite, float* reduced_grad,
                      float* clip_out, void* stream) {
     dpg::clear_error();
+    const dpg::Trace trace("dpg_step_clipped");
     return dpg::step_clipped(plan, grads, grads_dtype, last_micro_bf16, valid_tokens, n_counts, hp,
                              max_norm, master, exp_avg, exp_avg_sq, param_views, n_views,
                              bucket_sqnorm, bucket_nonfinite, reduced_grad, clip_out, stream);
@@ -1767,6 +1771,7 @@ int dpg_reduce_scatter_adam(const dpg_plan_t* plan, const void* const* grads, in
                             int32_t n_views, float* bucket_sqnorm, int64_t* bucket_nonfinite,
                             float* reduced_grad, int32_t b0, int32_t b1, void* stream) {
     dpg::clear_error();
+    const dpg::Trace trace("dpg_reduce_scatter_adam");
     return dpg::rs_adam(plan, grads, grads_dtype, last_micro_bf16, valid_tokens, n_counts, hp,
                         master, exp_avg, exp_avg_sq, param_views, n_views, bucket_sqnorm,
                         bucket_nonfinite, reduced_grad, b0, b1, stream, "dpg_reduce_scatter_adam");
@@ -1778,6 +1783,7 @@ int dpg_step(const dpg_plan_t* plan, const void* const* grads, int32_t grads_dty
              void* const* param_views, int32_t n_views, float* bucket_sqnorm,
              int64_t* bucket_nonfinite, void* stream) {
     dpg::clear_error();
+    const dpg::Trace trace("dpg_step");
     if (!plan) return fail(DPG_ERR_INVALID_ARG, "dpg_step: plan is NULL");
     return dpg::rs_adam(plan, grads, grads_dtype, last_micro_bf16, valid_tokens, n_counts, hp,
                         master, exp_avg, exp_avg_sq, param_views, n_views, bucket_sqnorm,
@@ -1787,6 +1793,7 @@ int dpg_step(const dpg_plan_t* plan, const void* const* grads, int32_t grads_dty
 int dpg_accumulate(const dpg_plan_t* plan, const void* flat_bf16, float* acc_f32, int32_t first,
                    void* stream) {
     dpg::clear_error();
+    const dpg::Trace trace("dpg_accumulate");
     if (!plan) return fail(DPG_ERR_INVALID_ARG, "dpg_accumulate: plan is NULL");
     if (plan->p.total_padded == 0) return DPG_OK;
     if (!flat_bf16 || !acc_f32) return fail(DPG_ERR_INVALID_ARG, "dpg_accumulate: NULL buffer");
@@ -1812,6 +1819,7 @@ int dpg_accumulate(const dpg_plan_t* plan, const void* flat_bf16, float* acc_f32
 int dpg_allgather_params(const dpg_plan_t* plan, const float* master, void* const* views,
                          int32_t n_views, int32_t b0, int32_t b1, void* stream) {
     dpg::clear_error();
+    const dpg::Trace trace("dpg_allgather_params");
     if (!plan) return fail(DPG_ERR_INVALID_ARG, "dpg_allgather_params: plan is NULL");
     const dpg::Plan& p = plan->p;
     if (b0 < 0 || b1 < b0 || b1 > p.n_buckets)
@@ -1847,6 +1855,7 @@ int dpg_allgather_params(const dpg_plan_t* plan, const float* master, void* cons
 int dpg_gather_params_bf16(const dpg_plan_t* plan, const void* param_bf16, void* const* views,
                            int32_t n_views, int32_t b0, int32_t b1, void* stream) {
     dpg::clear_error();
+    const dpg::Trace trace("dpg_gather_params_bf16");
     if (!plan) return fail(DPG_ERR_INVALID_ARG, "dpg_gather_params_bf16: plan is NULL");
     const dpg::Plan& p = plan->p;
     if (b0 < 0 || b1 < b0 || b1 > p.n_buckets)
@@ -1960,22 +1969,26 @@ static int state_common(const dpg_plan_t* plan, const float* const* src, float* 
 int dpg_export_state(const dpg_plan_t* plan, const float* const* flat, float* const* canon,
                      int32_t n_arrays, void* stream) {
     dpg::clear_error();
+    const dpg::Trace trace("dpg_export_state");
     return state_common(plan, flat, canon, n_arrays, 0, stream, "dpg_export_state");
 }
 
 int dpg_import_state(const dpg_plan_t* plan, const float* const* canon, float* const* flat,
                      int32_t n_arrays, void* stream) {
     dpg::clear_error();
+    const dpg::Trace trace("dpg_import_state");
     return state_common(plan, canon, flat, n_arrays, 1, stream, "dpg_import_state");
 }
 
 int dpg_pack(const dpg_plan_t* plan, const void* const* param_grads, void* flat_bf16, void* stream) {
     dpg::clear_error();
+    const dpg::Trace trace("dpg_pack");
     return pack_common(plan, param_grads, flat_bf16, 0, stream, "dpg_pack");
 }
 
 int dpg_unpack(const dpg_plan_t* plan, const void* flat_bf16, void* const* param_grads, void* stream) {
     dpg::clear_error();
+    const dpg::Trace trace("dpg_unpack");
     return pack_common(plan, const_cast<const void* const*>(param_grads), const_cast<void*>(flat_bf16),
                        1, stream, "dpg_unpack");
 }
