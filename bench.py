@@ -57,6 +57,9 @@ def parse():
     ap.add_argument("--impl", default="dpg", choices=["dpg", "reference"])
     ap.add_argument("--variant", default="direct", choices=["direct", "staged"],
                     help="fused pass: direct vector loads, or bulk-copy staging in shared memory")
+    ap.add_argument("--fold2", action="store_true",
+                    help="K >= 3: paired accumulation (two bf16 gradient buffers per replica), "
+                         "the last two microbatches folded into the fused step")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-sample-elems", type=int, default=CPU_SAMPLE_ELEMS,
@@ -104,17 +107,40 @@ def cap_of(cfg, a) -> int:
     return int(a.cap_mib * (1 << 20)) if a.cap_mib else cfg.cap_bytes
 
 
-def workload_desc(cfg, cap, plan_nb, total) -> dict:
-    return {"workload": f"{cfg.name}: {len(cfg.shapes)} tensors, psi={cfg.psi}, R={cfg.R} simulated "
-                        f"replicas, {cap / (1 << 20):g} MiB buckets, K={cfg.K} microbatch(es), ZeRO-2 "
-                        f"fused reduce-scatter+Adam+all-gather",
-            "psi": cfg.psi, "R": cfg.R, "K": cfg.K, "cap_bytes": cap, "n_buckets": plan_nb,
-            "total_padded": total, "grad_dtype": "bf16", "state_dtype": "f32",
-            "param_views": 1, "l2": "inputs larger than L2 (no flush)"}
+def workload_desc(cfg, cap, plan_nb, total, fold2=False) -> dict:
+    d = {"workload": f"{cfg.name}: {len(cfg.shapes)} tensors, psi={cfg.psi}, R={cfg.R} simulated "
+                     f"replicas, {cap / (1 << 20):g} MiB buckets, K={cfg.K} microbatch(es), ZeRO-2 "
+                     f"fused reduce-scatter+Adam+all-gather",
+         "psi": cfg.psi, "R": cfg.R, "K": cfg.K, "cap_bytes": cap, "n_buckets": plan_nb,
+         "total_padded": total, "grad_dtype": "bf16", "state_dtype": "f32",
+         "param_views": 1, "l2": "inputs larger than L2 (no flush)"}
+    if cfg.K > 1:
+        d["accumulation"] = ("paired: two bf16 gradient buffers per replica; microbatches folded "
+                             "into the fp32 buffers two at a time, the last two into the fused "
+                             "step" if fold2 else
+                             "one fp32 pass per microbatch, the last folded into the fused step")
+    return d
 
 
-def algorithmic_bytes_per_param(cfg) -> dict:
+def fold2_schedule(K: int):
+    """Microbatches 0..K-3 as (first, pair?) accumulation passes; the last two
+    are folded into the fused step."""
+    out, k = [], 0
+    while k + 1 < K - 2:
+        out.append((k, True))
+        k += 2
+    if k < K - 2:
+        out.append((k, False))
+    return out
+
+
+def algorithmic_bytes_per_param(cfg, fold2=False) -> dict:
     R, K = cfg.R, cfg.K
+    if K > 1 and fold2:
+        fused = 8 * R + 26
+        acc = sum((8 if k == 0 else 12) * R if pair else (6 if k == 0 else 10) * R
+                  for k, pair in fold2_schedule(K))
+        return {"fused": fused, "step": fused + acc}
     fused = (6 * R + 26) if K > 1 else (2 * R + 26)
     step = fused + ((6 * R + (K - 2) * 10 * R) if K > 1 else 0)
     return {"fused": fused, "step": step}
@@ -308,6 +334,10 @@ def run_dpg(a):
     g = [flat_grads_bf16(segs, N, cfg.grad_std, stream_seed(cfg.seed, KIND_GRAD, r, 0), device=dev)
          for r in range(R)]
     acc = [torch.empty(N, device=dev) for _ in range(R)] if K > 1 else None
+    fold2 = bool(a.fold2) and K >= 3
+    # paired accumulation keeps a second bf16 gradient buffer per replica
+    g2 = ([flat_grads_bf16(segs, N, cfg.grad_std, stream_seed(cfg.seed, KIND_GRAD, r, 1), device=dev)
+           for r in range(R)] if fold2 else None)
     w = master_f32(N, stream_seed(cfg.seed, KIND_MASTER), device=dev)
     m = torch.zeros(N, device=dev)
     v = torch.zeros(N, device=dev)
@@ -320,6 +350,19 @@ def run_dpg(a):
     def step(ev_pair=None):
         state["t"] += 1
         hp = dpg.HParams(step=state["t"])
+        if fold2:
+            for k, pair in fold2_schedule(K):
+                for r in range(R):
+                    if pair:
+                        dpg.dpg_accumulate_pair(plan, g[r], g2[r], acc[r], first=(k == 0),
+                                                stream=stream)
+                    else:
+                        dpg.dpg_accumulate(plan, g[r], acc[r], first=(k == 0), stream=stream)
+            if ev_pair is not None:
+                dpg.dpg_time_next_fused_launch(*ev_pair)
+            dpg.dpg_step_fold2(plan, acc, g, g2, tokens, hp, w, m, v, [param], bucket_sqnorm=sq,
+                               bucket_nonfinite=nf, stream=stream)
+            return
         if K > 1:
             for k in range(K - 1):
                 for r in range(R):
@@ -374,9 +417,9 @@ def run_dpg(a):
     e2e = None
     if not a.no_e2e:
         e2e = run_e2e(a, dpg, plan, g, acc, w, m, v, param, sq, nf, tokens, cfg, dev, stream,
-                      state, world)
+                      state, world, fold2)
 
-    bpp = algorithmic_bytes_per_param(cfg)
+    bpp = algorithmic_bytes_per_param(cfg, fold2)
     peak, peak_kind = load_peak()
     achieved = bpp["fused"] * cfg.psi / (k_ms * 1e-3) / 1e9
     traffic = traffic_per_launch(cfg, cap, N)
@@ -387,7 +430,7 @@ def run_dpg(a):
         "value": value, "unit": "params/s", "n_gpus": world, "steps": a.steps,
         "warmup": a.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": workload_desc(cfg, cap, plan.n_buckets, N),
+        "config": workload_desc(cfg, cap, plan.n_buckets, N, fold2),
         "hbm_gbs_step": bpp["step"] * cfg.psi / (ms * 1e-3) / 1e9,
         "roofline": {"bound": "hbm", "kernel": f"k_rs_adam<R={R}>", "achieved": achieved,
                      "peak": peak, "peak_kind": f"{peak_kind} (copy bandwidth)", "unit": "GB/s",
@@ -407,7 +450,8 @@ def run_dpg(a):
         dist.destroy_process_group()
 
 
-def run_e2e(a, dpg, plan, g, acc, w, m, v, param, sq, nf, tokens, cfg, dev, stream, state, world):
+def run_e2e(a, dpg, plan, g, acc, w, m, v, param, sq, nf, tokens, cfg, dev, stream, state, world,
+            fold2=False):
     import torch
     R, K = cfg.R, cfg.K
     N = plan.total_padded
@@ -474,6 +518,21 @@ def run_e2e(a, dpg, plan, g, acc, w, m, v, param, sq, nf, tokens, cfg, dev, stre
         # the kernels read the pinned host gradients in place over the host link
         state["t"] += 1
         hp = dpg.HParams(step=state["t"])
+        if fold2:
+            for k, pair in fold2_schedule(K):
+                for r in range(R):
+                    if pair:
+                        dpg.dpg_accumulate_pair(plan, h_in[r][k], h_in[r][k + 1], acc[r],
+                                                first=(k == 0), stream=stream)
+                    else:
+                        dpg.dpg_accumulate(plan, h_in[r][k], acc[r], first=(k == 0),
+                                           stream=stream)
+            dpg.dpg_step_fold2(plan, acc, [h_in[r][K - 2] for r in range(R)],
+                               [h_in[r][K - 1] for r in range(R)], tokens, hp, w, m, v, [param],
+                               bucket_sqnorm=sq, bucket_nonfinite=nf, stream=stream)
+            h_sq.copy_(sq, non_blocking=True)
+            h_nf.copy_(nf, non_blocking=True)
+            return
         for k in range(K - 1):
             for r in range(R):
                 dpg.dpg_accumulate(plan, h_in[r][k], acc[r], first=(k == 0), stream=stream)
@@ -507,6 +566,8 @@ def run_e2e(a, dpg, plan, g, acc, w, m, v, param, sq, nf, tokens, cfg, dev, stre
     how = {
         "zero_copy": "the kernels read the pinned host gradients in place over the host link "
                      "(unified addressing; no staging copy)" + ("" if K == 1 else
+                     ", paired accumulations then the fused step with the last two microbatches"
+                     if fold2 else
                      ", K-1 accumulations then the fused step with the last microbatch") +
                      "; norms read back",
         "copy": (f"pinned host gradients copied in {len(bounds) - 1} bucket chunks on a copy "
@@ -515,7 +576,9 @@ def run_e2e(a, dpg, plan, g, acc, w, m, v, param, sq, nf, tokens, cfg, dev, stre
                  "pinned host gradients copied in per microbatch, accumulated, fused step; "
                  "norms read back"),
     }
-    modes = {"zero_copy": time_mode(e2e_step_zero_copy), "copy": time_mode(e2e_step)}
+    modes = {"zero_copy": time_mode(e2e_step_zero_copy)}
+    if not fold2:
+        modes["copy"] = time_mode(e2e_step)
     best = min(modes, key=modes.get)
     ms = modes[best]
     return {"value": job_throughput(cfg.psi, world, ms), "unit": "params/s", "steps": steps,

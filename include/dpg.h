@@ -178,6 +178,36 @@ int dpg_accumulate(const dpg_plan_t* plan, const void* flat_bf16, float* acc_f32
                    int32_t first, void* stream);
 
 /* ---------------------------------------------------------------------------
+ * Paired no_sync accumulation (no counterpart on the pages: a schedule of the
+ * same sums for a caller that keeps TWO bf16 gradient buffers per replica)
+ * acc_f32[i] = f32(a[i]) + f32(b[i]) if first != 0, else
+ * (acc_f32[i] + f32(a[i])) + f32(b[i]): exactly the two binary32 additions of
+ * dpg_accumulate(a) then dpg_accumulate(b), in that order, with the fp32
+ * buffer read and written once instead of twice (8 or 12 bytes per element
+ * instead of 16 or 20).  micro_a is the earlier microbatch.
+ * ------------------------------------------------------------------------- */
+int dpg_accumulate_pair(const dpg_plan_t* plan, const void* micro_a_bf16,
+                        const void* micro_b_bf16, float* acc_f32, int32_t first, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * Whole step with the LAST TWO microbatches folded into the reduction (same
+ * schedule note as dpg_accumulate_pair)
+ * Replica r's contribution is x_r = (acc_f32[r] + f32(micro_a[r])) +
+ * f32(micro_b[r]) -- what dpg_accumulate(micro_a) followed by dpg_step with
+ * last_micro_bf16 = micro_b computes, bit for bit -- then the rank-ordered
+ * sum, scale, Adam and cast exactly as dpg_step.  micro_a/micro_b: R
+ * DEVICE (or page-locked host) bf16 flat buffers, 16-byte aligned;
+ * acc_f32: R fp32 flat buffers, 32-byte aligned.  valid_tokens counts every
+ * microbatch of the cycle (R*K counts).  Norm outputs as dpg_step.
+ * ------------------------------------------------------------------------- */
+int dpg_step_fold2(const dpg_plan_t* plan, const float* const* acc_f32,
+                   const void* const* micro_a_bf16, const void* const* micro_b_bf16,
+                   const int64_t* valid_tokens, int32_t n_counts, const dpg_hparams* hp,
+                   float* master, float* exp_avg, float* exp_avg_sq, void* const* param_views,
+                   int32_t n_views, float* bucket_sqnorm, int64_t* bucket_nonfinite,
+                   void* stream);
+
+/* ---------------------------------------------------------------------------
  * Fused reduce-scatter + normalisation + Adam + all-gather, buckets [b0, b1)
  *      ["Parallelisms" -- ZeRO-1, ZeRO-2; "Parallelism Starts With the
  *       Bottleneck" -- Allreduce equals reducescatter plus allgather;

@@ -180,6 +180,28 @@ def test_other_entry_points_validation():
     assert L.dpg_allgather_params(plan.handle, FAKE, dpg._ptrs([FAKE]), 65, 0, 1, None) == dpg.DPG_ERR_INVALID_ARG
     assert L.dpg_allgather_params(plan.handle, FAKE + 4, dpg._ptrs([FAKE]), 1, 0, 1, None) == dpg.DPG_ERR_MISALIGNED
     assert L.dpg_allgather_params(plan.handle, FAKE, dpg._ptrs([FAKE]), 1, 1, 1, None) == dpg.DPG_OK
+    A2 = L.dpg_accumulate_pair
+    assert A2(None, FAKE, FAKE, FAKE, 1, None) == dpg.DPG_ERR_INVALID_ARG
+    assert A2(plan.handle, FAKE, None, FAKE, 1, None) == dpg.DPG_ERR_INVALID_ARG
+    assert A2(plan.handle, FAKE, FAKE + 2, FAKE, 1, None) == dpg.DPG_ERR_MISALIGNED
+    assert A2(plan.handle, FAKE, FAKE, FAKE + 16, 0, None) == dpg.DPG_ERR_MISALIGNED
+    F2 = L.dpg_step_fold2
+    tok = (ctypes.c_int64 * 4)(100, 80, 120, 60)
+    hp = dpg.HParams().c()
+    four = dpg._ptrs([FAKE] * 4)
+    assert F2(plan.handle, four, None, four, tok, 4, ctypes.byref(hp), FAKE, FAKE, FAKE, None, 0,
+              None, None, None) == dpg.DPG_ERR_INVALID_ARG
+    assert F2(plan.handle, four, four, None, tok, 4, ctypes.byref(hp), FAKE, FAKE, FAKE, None, 0,
+              None, None, None) == dpg.DPG_ERR_INVALID_ARG
+    assert F2(plan.handle, four, four, dpg._ptrs([FAKE, FAKE, FAKE, FAKE + 2]), tok, 4,
+              ctypes.byref(hp), FAKE, FAKE, FAKE, None, 0, None, None,
+              None) == dpg.DPG_ERR_MISALIGNED
+    assert F2(plan.handle, four, four, dpg._ptrs([FAKE, 0, FAKE, FAKE]), tok, 4,
+              ctypes.byref(hp), FAKE, FAKE, FAKE, None, 0, None, None,
+              None) == dpg.DPG_ERR_INVALID_ARG
+    zero = (ctypes.c_int64 * 4)(0, 0, 0, 0)
+    assert F2(plan.handle, four, four, four, zero, 4, ctypes.byref(hp), FAKE, FAKE, FAKE, None, 0,
+              None, None, None) == dpg.DPG_ERR_ZERO_TOKENS
     G = L.dpg_gather_params_bf16
     assert G(None, FAKE, dpg._ptrs([FAKE]), 1, 0, 1, None) == dpg.DPG_ERR_INVALID_ARG
     assert G(plan.handle, FAKE, dpg._ptrs([FAKE]), 1, 0, 3, None) == dpg.DPG_ERR_INVALID_ARG

@@ -40,6 +40,7 @@ EXPORTED = (
     "dpg_time_next_fused_launch", "dpg_step_noalloc", "dpg_export_state", "dpg_import_state",
     "dpg_step_clipped", "dpg_step_staged", "dpg_check_device_status", "dpg_set_staged_fault",
     "dpg_allreduce_grads", "dpg_adam_from_reduced", "dpg_gather_params_bf16",
+    "dpg_accumulate_pair", "dpg_step_fold2",
 )
 DPG_MAX_STATE_ARRAYS = 8
 DPG_NOALLOC_SCRATCH_BYTES = 8 << 20
@@ -104,6 +105,8 @@ def lib() -> ctypes.CDLL:
         L.dpg_pack.argtypes = [P, P, P, P]
         L.dpg_unpack.argtypes = [P, P, P, P]
         L.dpg_accumulate.argtypes = [P, P, P, i32, P]
+        L.dpg_accumulate_pair.argtypes = [P, P, P, P, i32, P]
+        L.dpg_step_fold2.argtypes = [P, P, P, P, P, i32, P, P, P, P, P, i32, P, P, P]
         L.dpg_reduce_scatter_adam.argtypes = [P, P, i32, P, P, i32, P, P, P, P, P, i32, P, P, P,
                                               i32, i32, P]
         L.dpg_allgather_params.argtypes = [P, P, P, i32, i32, i32, P]
@@ -128,7 +131,7 @@ def lib() -> ctypes.CDLL:
                      "dpg_step", "dpg_step_noalloc", "dpg_export_state", "dpg_import_state",
                      "dpg_step_clipped", "dpg_step_staged", "dpg_check_device_status",
                      "dpg_set_staged_fault", "dpg_allreduce_grads", "dpg_adam_from_reduced",
-                     "dpg_gather_params_bf16"):
+                     "dpg_gather_params_bf16", "dpg_accumulate_pair", "dpg_step_fold2"):
             getattr(L, name).restype = c_int
         _lib = L
     return _lib
@@ -338,6 +341,42 @@ def dpg_accumulate(plan: Plan, flat_bf16: Ptr, acc_f32: Ptr, first: bool, stream
     _need(acc_f32, "f32", plan.total_padded, "acc_f32")
     _check(lib().dpg_accumulate(plan.handle, _ptr(flat_bf16), _ptr(acc_f32), 1 if first else 0,
                                 _stream(stream)))
+
+
+def dpg_accumulate_pair(plan: Plan, micro_a_bf16: Ptr, micro_b_bf16: Ptr, acc_f32: Ptr,
+                        first: bool, stream=None):
+    """acc <- (acc + a) + b (or a + b when first): two microbatches in one pass."""
+    _need_in(micro_a_bf16, "bf16", plan.total_padded, "micro_a_bf16")
+    _need_in(micro_b_bf16, "bf16", plan.total_padded, "micro_b_bf16")
+    _need(acc_f32, "f32", plan.total_padded, "acc_f32")
+    _check(lib().dpg_accumulate_pair(plan.handle, _ptr(micro_a_bf16), _ptr(micro_b_bf16),
+                                     _ptr(acc_f32), 1 if first else 0, _stream(stream)))
+
+
+def dpg_step_fold2(plan: Plan, acc_f32: Sequence[Ptr], micro_a: Sequence[Ptr],
+                   micro_b: Sequence[Ptr], valid_tokens, hp: HParams, master: Ptr, exp_avg: Ptr,
+                   exp_avg_sq: Ptr, param_views: Sequence[Ptr] = (), *, bucket_sqnorm: Ptr = None,
+                   bucket_nonfinite: Ptr = None, stream=None):
+    """Whole step with the last two bf16 microbatches folded into the reduction."""
+    for name, xs in (("acc_f32", acc_f32), ("micro_a", micro_a), ("micro_b", micro_b)):
+        if len(xs) != plan.R:
+            raise ValueError(f"{name}: need R={plan.R} buffers, got {len(xs)}")
+    N = plan.total_padded
+    for k in range(plan.R):
+        _need_in(acc_f32[k], "f32", N, f"acc_f32[{k}]")
+        _need_in(micro_a[k], "bf16", N, f"micro_a[{k}]")
+        _need_in(micro_b[k], "bf16", N, f"micro_b[{k}]")
+    for name, t in (("master", master), ("exp_avg", exp_avg), ("exp_avg_sq", exp_avg_sq)):
+        _need(t, "f32", N, name)
+    for k, t in enumerate(param_views):
+        _need(t, "bf16", N, f"param_views[{k}]")
+    _need(bucket_sqnorm, "f32", plan.n_buckets, "bucket_sqnorm")
+    tok, n_tok = _tokens(valid_tokens)
+    hpc = hp.c()
+    _check(lib().dpg_step_fold2(
+        plan.handle, _ptrs(acc_f32), _ptrs(micro_a), _ptrs(micro_b), tok.ctypes.data, n_tok,
+        ctypes.byref(hpc), _ptr(master), _ptr(exp_avg), _ptr(exp_avg_sq), _ptrs(param_views),
+        len(param_views), _ptr(bucket_sqnorm), _ptr(bucket_nonfinite), _stream(stream)))
 
 
 def _grad_dtype(grads) -> int:

@@ -120,7 +120,9 @@ __device__ __forceinline__ uint4 narrow8(const float* f) {
 // ---------------------------------------------------------------------------
 // fused reduce-scatter -> scale -> Adam -> all-gather
 // ---------------------------------------------------------------------------
-enum : int { kInBf16 = 0, kInF32 = 1, kInF32PlusBf16 = 2, kInReduced = 3 };
+// kInF32PlusBf16x2: fp32 accumulation buffers plus the last TWO bf16
+// microbatches, folded in microbatch order.
+enum : int { kInBf16 = 0, kInF32 = 1, kInF32PlusBf16 = 2, kInReduced = 3, kInF32PlusBf16x2 = 4 };
 
 // Passes of the fused kernel.  kFull: reduce, scale, Adam, cast (the step).
 // With global norm clipping the step takes two passes: the norm pass
@@ -131,6 +133,7 @@ enum : int { kFull = 0, kNormOnly = 1, kUpdate = 2 };
 struct RsAdamArgs {
     const void* grads[DPG_MAX_REPLICAS];
     const void* last[DPG_MAX_REPLICAS];
+    const void* last2[DPG_MAX_REPLICAS];  // kInF32PlusBf16x2: the final microbatch
     void* views[DPG_MAX_VIEWS];
     float* master;
     float* m;
@@ -205,9 +208,15 @@ __device__ __forceinline__ void reduce_vector(const RsAdamArgs& a, int64_t i, fl
 #pragma unroll(RT > 0 ? RT : 2)
         for (int r = 0; r < R; ++r) {
             F8 x = ld_grad_f8(static_cast<const float*>(a.grads[r]) + i);
-            if constexpr (MODE == kInF32PlusBf16) {
+            if constexpr (MODE == kInF32PlusBf16 || MODE == kInF32PlusBf16x2) {
                 float t[8];
                 widen8(ld_grad_u4(static_cast<const uint16_t*>(a.last[r]) + i), t);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) x.v[j] = __fadd_rn(x.v[j], t[j]);
+            }
+            if constexpr (MODE == kInF32PlusBf16x2) {
+                float t[8];
+                widen8(ld_grad_u4(static_cast<const uint16_t*>(a.last2[r]) + i), t);
 #pragma unroll
                 for (int j = 0; j < 8; ++j) x.v[j] = __fadd_rn(x.v[j], t[j]);
             }
@@ -866,6 +875,33 @@ __global__ void __launch_bounds__(256) k_accumulate(const uint16_t* __restrict__
     }
 }
 
+// Two microbatches folded into the fp32 buffer in one pass, in microbatch
+// order: acc <- (acc + f32(a)) + f32(b), or f32(a) + f32(b) for the first
+// pair -- the same two binary32 additions as two k_accumulate launches, with
+// the accumulator read and written once instead of twice.
+template <bool FIRST>
+__global__ void __launch_bounds__(256) k_accumulate_pair(const uint16_t* __restrict__ ga,
+                                                         const uint16_t* __restrict__ gb,
+                                                         float* __restrict__ acc, int64_t n_vec) {
+    for (int64_t k = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; k < n_vec;
+         k += int64_t(gridDim.x) * blockDim.x) {
+        const int64_t i = k * kVec;
+        float xa[8], xb[8];
+        widen8(ld_grad_u4(ga + i), xa);
+        widen8(ld_grad_u4(gb + i), xb);
+        F8 r;
+        if (FIRST) {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) r.v[j] = __fadd_rn(xa[j], xb[j]);
+        } else {
+            const F8 a = ld_state_f8(acc + i);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) r.v[j] = __fadd_rn(__fadd_rn(a.v[j], xa[j]), xb[j]);
+        }
+        st_f8(acc + i, r);
+    }
+}
+
 struct ViewArgs {
     void* views[DPG_MAX_VIEWS];
     int32_t n_views;
@@ -1260,7 +1296,8 @@ static int rs_adam(const dpg_plan_t* plan, const void* const* grads, int32_t gra
                    const void* const* last, const int64_t* tokens, int32_t n_counts,
                    const dpg_hparams* hp, float* master, float* m, float* v,
                    void* const* views, int32_t n_views, float* sqnorm, int64_t* nonfinite,
-                   float* reduced, int32_t b0, int32_t b1, void* stream, const char* who) {
+                   float* reduced, int32_t b0, int32_t b1, void* stream, const char* who,
+                   const void* const* last2 = nullptr) {
     if (!plan) return fail(DPG_ERR_INVALID_ARG, "%s: plan is NULL", who);
     Plan& p = const_cast<dpg_plan_t*>(plan)->p;
     if (b0 < 0 || b1 < b0 || b1 > p.n_buckets)
@@ -1270,6 +1307,8 @@ static int rs_adam(const dpg_plan_t* plan, const void* const* grads, int32_t gra
         return fail(DPG_ERR_INVALID_ARG, "%s: grads_dtype %d unknown", who, grads_dtype);
     if (last && grads_dtype != DPG_F32)
         return fail(DPG_ERR_INVALID_ARG, "%s: last_micro_bf16 needs fp32 accumulation grads", who);
+    if (last2 && !last)
+        return fail(DPG_ERR_INVALID_ARG, "%s: the final microbatch needs the one before it", who);
     if (n_views < 0 || n_views > DPG_MAX_VIEWS)
         return fail(DPG_ERR_INVALID_ARG, "%s: n_views %d outside [0, %d]", who, n_views, DPG_MAX_VIEWS);
     RsAdamArgs a{};
@@ -1296,6 +1335,11 @@ static int rs_adam(const dpg_plan_t* plan, const void* const* grads, int32_t gra
             if (!aligned(last[r], 16)) return fail(DPG_ERR_MISALIGNED, "%s: last_micro_bf16[%d] misaligned", who, r);
             a.last[r] = last[r];
         }
+        if (last2) {
+            if (!last2[r]) return fail(DPG_ERR_INVALID_ARG, "%s: final microbatch[%d] is NULL", who, r);
+            if (!aligned(last2[r], 16)) return fail(DPG_ERR_MISALIGNED, "%s: final microbatch[%d] misaligned", who, r);
+            a.last2[r] = last2[r];
+        }
     }
     for (int k = 0; k < n_views; ++k) {
         if (!views[k]) return fail(DPG_ERR_INVALID_ARG, "%s: param_views[%d] is NULL", who, k);
@@ -1319,10 +1363,12 @@ static int rs_adam(const dpg_plan_t* plan, const void* const* grads, int32_t gra
     a.b1 = b1;
     a.R = p.R;
     a.n_views = n_views;
-    const int mode = grads_dtype == DPG_BF16 ? kInBf16 : (last ? kInF32PlusBf16 : kInF32);
+    const int mode = grads_dtype == DPG_BF16 ? kInBf16
+                   : last2 ? kInF32PlusBf16x2 : (last ? kInF32PlusBf16 : kInF32);
     RsKernel fn = mode == kInBf16 ? pick_rs_kernel<kInBf16>(p.R)
                 : mode == kInF32 ? pick_rs_kernel<kInF32>(p.R)
-                                 : pick_rs_kernel<kInF32PlusBf16>(p.R);
+                : mode == kInF32PlusBf16 ? pick_rs_kernel<kInF32PlusBf16>(p.R)
+                                         : pick_rs_kernel<kInF32PlusBf16x2>(p.R);
     int grid = 0;
     st = fused_geometry(fn, p.device, a.t0, a.t1, b0, b1, &grid, &a.vmax);
     if (st != DPG_OK) return st;
@@ -1814,6 +1860,50 @@ int dpg_accumulate(const dpg_plan_t* plan, const void* flat_bf16, float* acc_f32
     if (first) dpg::k_accumulate<true><<<grid, 256, 0, s>>>(g, acc_f32, n_vec);
     else dpg::k_accumulate<false><<<grid, 256, 0, s>>>(g, acc_f32, n_vec);
     return dpg::after_launch("dpg_accumulate");
+}
+
+int dpg_accumulate_pair(const dpg_plan_t* plan, const void* micro_a_bf16, const void* micro_b_bf16,
+                        float* acc_f32, int32_t first, void* stream) {
+    dpg::clear_error();
+    const dpg::Trace trace("dpg_accumulate_pair");
+    if (!plan) return fail(DPG_ERR_INVALID_ARG, "dpg_accumulate_pair: plan is NULL");
+    if (plan->p.total_padded == 0) return DPG_OK;
+    if (!micro_a_bf16 || !micro_b_bf16 || !acc_f32)
+        return fail(DPG_ERR_INVALID_ARG, "dpg_accumulate_pair: NULL buffer");
+    if (!dpg::aligned(micro_a_bf16, 16) || !dpg::aligned(micro_b_bf16, 16) || !dpg::aligned(acc_f32, 32))
+        return fail(DPG_ERR_MISALIGNED, "dpg_accumulate_pair: misaligned buffer");
+    const dpg::Plan& p = plan->p;
+    const int64_t n_vec = p.total_padded / dpg::kVec;
+    int dev = 0;
+    DPG_CUDA_TRY(cudaGetDevice(&dev));
+    const void* fn = first ? reinterpret_cast<const void*>(dpg::k_accumulate_pair<true>)
+                           : reinterpret_cast<const void*>(dpg::k_accumulate_pair<false>);
+    int grid = 0;
+    int st = dpg::grid_for(fn, 256, dev, (n_vec + 255) / 256, &grid);
+    if (st != DPG_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const uint16_t* ga = static_cast<const uint16_t*>(micro_a_bf16);
+    const uint16_t* gb = static_cast<const uint16_t*>(micro_b_bf16);
+    if (first) dpg::k_accumulate_pair<true><<<grid, 256, 0, s>>>(ga, gb, acc_f32, n_vec);
+    else dpg::k_accumulate_pair<false><<<grid, 256, 0, s>>>(ga, gb, acc_f32, n_vec);
+    return dpg::after_launch("dpg_accumulate_pair");
+}
+
+int dpg_step_fold2(const dpg_plan_t* plan, const float* const* acc_f32,
+                   const void* const* micro_a_bf16, const void* const* micro_b_bf16,
+                   const int64_t* valid_tokens, int32_t n_counts, const dpg_hparams* hp,
+                   float* master, float* exp_avg, float* exp_avg_sq, void* const* param_views,
+                   int32_t n_views, float* bucket_sqnorm, int64_t* bucket_nonfinite,
+                   void* stream) {
+    dpg::clear_error();
+    const dpg::Trace trace("dpg_step_fold2");
+    if (!plan) return fail(DPG_ERR_INVALID_ARG, "dpg_step_fold2: plan is NULL");
+    if (!micro_a_bf16 || !micro_b_bf16)
+        return fail(DPG_ERR_INVALID_ARG, "dpg_step_fold2: microbatch tables must not be NULL");
+    return dpg::rs_adam(plan, reinterpret_cast<const void* const*>(acc_f32), DPG_F32, micro_a_bf16,
+                        valid_tokens, n_counts, hp, master, exp_avg, exp_avg_sq, param_views,
+                        n_views, bucket_sqnorm, bucket_nonfinite, nullptr, 0, plan->p.n_buckets,
+                        stream, "dpg_step_fold2", micro_b_bf16);
 }
 
 int dpg_allgather_params(const dpg_plan_t* plan, const float* master, void* const* views,
