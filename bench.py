@@ -57,6 +57,10 @@ def parse():
     ap.add_argument("--impl", default="dpg", choices=["dpg", "reference"])
     ap.add_argument("--variant", default="direct", choices=["direct", "staged"],
                     help="fused pass: direct vector loads, or bulk-copy staging in shared memory")
+    ap.add_argument("--traffic-from", default=None, metavar="CSV",
+                    help="no GPU: read an ncu launch list (--csv with dram__bytes_read.sum and "
+                         "dram__bytes_write.sum) of this bench's --config run and write the "
+                         "fused kernel's mean DRAM bytes per launch to profiles/traffic.json")
     ap.add_argument("--fold2", action="store_true",
                     help="K >= 3: paired accumulation (two bf16 gradient buffers per replica), "
                          "the last two microbatches folded into the fused step")
@@ -306,6 +310,38 @@ def traffic_per_launch(cfg, cap, total_padded):
     if t.get("source_sha256") != src or t.get("R") != cfg.R or t.get("K", 1) != cfg.K:
         return None
     return float(t["dram_bytes_per_launch"]) * total_padded / float(t["elements"])
+
+
+def write_traffic(a):
+    """profiles/traffic.json from an ncu launch list of the fused kernel."""
+    import csv
+    cfg = CONFIGS[a.config]
+    per = {}
+    with open(a.traffic_from, newline="") as fh:
+        rows = [r for r in csv.reader(fh) if len(r) > 14 and r[0].isdigit()]
+    for r in rows:
+        name, metric, value = r[4], r[12], float(r[14].replace(",", ""))
+        if not name.startswith("void k_rs_adam<") or "staged" in name:
+            continue
+        per.setdefault(r[0], {})[metric] = value
+    launches = [d for d in per.values()
+                if "dram__bytes_read.sum" in d and "dram__bytes_write.sum" in d]
+    if not launches:
+        raise SystemExit(f"{a.traffic_from}: no k_rs_adam launch with DRAM byte counts")
+    rd = statistics.mean(d["dram__bytes_read.sum"] for d in launches)
+    wr = statistics.mean(d["dram__bytes_write.sum"] for d in launches)
+    out = {"k_rs_adam": {
+        "workload": f"{cfg.name} ({cfg.psi:,} params, R={cfg.R}, "
+                    f"{cap_of(cfg, a) / (1 << 20):g} MiB buckets), full size",
+        "R": cfg.R, "K": cfg.K, "elements": cfg.psi,
+        "dram_bytes_read": rd, "dram_bytes_write": wr, "dram_bytes_per_launch": rd + wr,
+        "launches": len(launches), "source_sha256": kernel_source_sha256(),
+        "how": "ncu --metrics gpu__time_duration.sum,dram__bytes_read.sum,dram__bytes_write.sum "
+               "--clock-control none -k regex:\"k_rs_adam|k_norm_finalize\" on python bench.py "
+               "--no-e2e --no-cpu-baseline (one pass, full-size workload); mean per launch"}}
+    with open(TRAFFIC_FILE, "w") as fh:
+        json.dump(out, fh, indent=1)
+    print(json.dumps(out), flush=True)
 
 
 def run_dpg(a):
@@ -976,6 +1012,9 @@ def main():
     a = parse()
     if a.overlap:
         run_overlap(a)
+        return
+    if a.traffic_from:
+        write_traffic(a)
         return
     if a.schedules:
         run_schedules(a)
