@@ -47,7 +47,10 @@
  *     then read it over the host link with the same loads, so no staging
  *     copy or device gradient buffer is needed and the results are the
  *     same bits.  The pass then runs at the link's bandwidth, not HBM's.
- *     The staged and allocation-free steps take device memory only.
+ *     The staged and allocation-free steps take device memory only.  The
+ *     library does not query pointer kinds (that would cost a driver call
+ *     per pointer per launch): every other pointer must be device memory,
+ *     and pageable (unregistered) host memory is not a valid input.
  */
 #ifndef DPG_H
 #define DPG_H
