@@ -89,6 +89,10 @@ class StepCase:
     warm: bool = False           # non-zero m, v
     t: int = 1
     wd: float = 0.0
+    lr: float = 1e-3
+    beta1: float = 0.9
+    beta2: float = 0.999
+    eps: float = 1e-8
     n_views: int = 1
     grad_std: float = 1e-2
     seed: int = 1234
@@ -153,7 +157,7 @@ def run_case(c: StepCase) -> StepResult:
     d_nf = torch.full((max(1, plan.n_buckets),), -1, dtype=torch.int64, device=dev)
     d_red = torch.full((N,), float("nan"), device=dev)
     d_micro = [[micro[r][k].to(dev) for k in range(K)] for r in range(R)]
-    hp = dpg.HParams(step=c.t, weight_decay=c.wd)
+    hp = dpg.HParams(step=c.t, weight_decay=c.wd, lr=c.lr, beta1=c.beta1, beta2=c.beta2, eps=c.eps)
     acc_after = []
     if K > 1:
         d_acc = [torch.full((N,), float("nan"), device=dev) for _ in range(R)]
@@ -194,7 +198,8 @@ def run_case(c: StepCase) -> StepResult:
     else:
         ograds, olast = [h_micro[r][0] for r in range(R)], None
     views, red, sq = oracle.step(oplan.bucket_offset, oplan.bucket_padded, ograds, tokens, w, m, v,
-                                 last=olast, n_views=c.n_views, wd=c.wd, t=c.t, want_reduced=True)
+                                 last=olast, n_views=c.n_views, wd=c.wd, t=c.t, lr=c.lr,
+                                 beta1=c.beta1, beta2=c.beta2, eps=c.eps, want_reduced=True)
     nf = np.array([int(np.sum(~np.isfinite(red[o:o + p])))
                    for o, p in zip(oplan.bucket_offset, oplan.bucket_padded)], np.int64)
     res.ref = dict(master=w, m=m, v=v, views=views, sq=sq, nf=nf, reduced=red,

@@ -66,6 +66,14 @@ CASES = {
                         grad_std=1e-37),
     "R8_acc_K3_nan": dict(numels=_ragged(15, 10, 10_000), cap_bytes=1 << 15, R=8, K=3,
                           inject="nan"),
+    # other hyper-parameters: a large step (bias corrections near 1), a small
+    # beta2 and eps where eps matters, AdamW with a large lr
+    "R8_hp_late_step": dict(numels=_ragged(16, 20, 40_000), cap_bytes=1 << 18, R=8, warm=True,
+                            t=100_000, lr=3e-4, beta1=0.95, beta2=0.98, eps=1e-6),
+    "R4_hp_eps_dominant": dict(numels=_ragged(17, 20, 40_000), cap_bytes=1 << 18, R=4,
+                               grad_std=1e-9, eps=1e-5, lr=1e-2),
+    "R2_hp_adamw": dict(numels=_ragged(18, 20, 40_000), cap_bytes=1 << 18, R=2, warm=True, t=9,
+                        lr=5e-2, wd=0.3, beta1=0.5, beta2=0.9),
 }
 
 

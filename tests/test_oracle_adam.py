@@ -33,28 +33,44 @@ def torch_adam_trajectory(w0, grads, wd=0.0, **hp):
     return out
 
 
+HP_SETS = {
+    "default": HP,
+    "small_betas_large_lr": dict(lr=5e-2, beta1=0.5, beta2=0.9, eps=1e-6),
+    "high_beta1": dict(lr=3e-4, beta1=0.95, beta2=0.98, eps=1e-6),
+}
+
+
+@pytest.mark.parametrize("hp_name", sorted(HP_SETS))
 @pytest.mark.parametrize("wd", [0.0, 0.1])
-def test_matches_torch_adam_binary64(oracle_lib, wd):
+def test_matches_torch_adam_binary64(oracle_lib, wd, hp_name):
+    hp = HP_SETS[hp_name]
     rng = np.random.Generator(np.random.Philox(42))
     n, T = 20_000, 10
     w0 = (rng.standard_normal(n) * 0.02).astype(np.float32)
     # magnitudes from 1e-9 (around eps) to 1e-1
     mag = 10.0 ** rng.uniform(-9, -1, n)
     grads = [(rng.standard_normal(n) * mag).astype(np.float32) for _ in range(T)]
-    ref = torch_adam_trajectory(w0, grads, wd=wd, **HP)
+    ref = torch_adam_trajectory(w0, grads, wd=wd, **hp)
     w, m, v = w0.copy(), np.zeros(n, np.float32), np.zeros(n, np.float32)
     m_mag = np.zeros(n)      # sum of |terms| of the m recurrence (cancellation-free)
+    # |u| = |m_hat| / (sqrt(v_hat) + eps) <= (1-b1)/sqrt(1-b2) when b1^2 < b2
+    # (Kingma & Ba, the bound on the effective step)
+    assert hp["beta1"] ** 2 < hp["beta2"]
+    ub = (1 - hp["beta1"]) / np.sqrt(1 - hp["beta2"])
     for t, g in enumerate(grads, start=1):
-        oracle_lib.adam(g, w, m, v, wd=wd, t=t, **HP)
+        oracle_lib.adam(g, w, m, v, wd=wd, t=t, **hp)
         rw, rm, rv = ref[t - 1]
-        m_mag = HP["beta1"] * m_mag + (1 - HP["beta1"]) * np.abs(g.astype(np.float64))
+        m_mag = hp["beta1"] * m_mag + (1 - hp["beta1"]) * np.abs(g.astype(np.float64))
         # m, v: chains of binary32 multiply-adds; error a few t * 2^-24 of the
         # magnitude of the terms (v has only non-negative terms)
         assert np.all(np.abs(m - rm) <= 4 * t * 2.0 ** -24 * m_mag + 1e-45)
         np.testing.assert_allclose(v, rv, rtol=4 * t * 2.0 ** -24, atol=1e-45)
-        # weight: one rounding of the weight per step (half an ulp of |w| <= 0.2)
-        # plus lr * |u| * (relative error of u); |u| <= (1-b1)/sqrt(1-b2) ~ 3.2
-        bound = t * (0.5 * np.spacing(np.float32(0.2)) + HP["lr"] * 3.2 * 64 * t * 2.0 ** -24)
+        # weight: one rounding of the weight per step (half an ulp of the
+        # largest |w| reached; two with decoupled decay, whose subtraction
+        # rounds w once more) plus lr * |u| * (relative error of u)
+        wmax = np.float32(np.max(np.abs(w0)) + t * hp["lr"] * ub)
+        roundings = 2 if wd else 1
+        bound = t * (0.5 * roundings * np.spacing(wmax) + hp["lr"] * ub * 64 * t * 2.0 ** -24)
         assert np.max(np.abs(w.astype(np.float64) - rw)) <= bound
 
 
