@@ -142,7 +142,7 @@ def test_multi_step_trajectory():
 def test_pack_unpack_bit_exact(seed):
     rng = np.random.Generator(np.random.Philox(300 + seed))
     numels = random_param_list(rng, int(rng.integers(1, 300)), 20_000)
-    numels[0] = 3 * 8192 + 5            # several pack items for one parameter
+    numels[0] = 3 * 32768 + 5           # several pack items (32768 elements each) for one parameter
     R = int(rng.choice([1, 2, 4, 8]))
     cap = int(rng.integers(64, 1 << 17))
     plan = dpg.dpg_plan_buckets(numels, cap, R)
@@ -160,6 +160,36 @@ def test_pack_unpack_bit_exact(seed):
     dpg.dpg_pack(plan, grads, flat)
     oplan = oracle.plan_buckets(numels, cap, R)
     np.testing.assert_array_equal(oplan.param_offset, plan.param_offset)
+    ref = oracle.pack(oplan, h_grads)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(np_bf16(flat), ref)
+    outs = [torch.full((int(n),), float("nan"), dtype=torch.bfloat16, device="cuda") for n in numels]
+    dpg.dpg_unpack(plan, flat, outs)
+    torch.cuda.synchronize()
+    for o, h in zip(outs, h_grads):
+        np.testing.assert_array_equal(np_bf16(o), h)
+
+
+def test_pack_unpack_many_parameters():
+    """2600 parameters: the pointer table travels 1024 parameters per launch,
+    so pack and unpack run three launches over the item list."""
+    rng = np.random.Generator(np.random.Philox(377))
+    numels = rng.integers(1, 65, 2600)
+    numels[1500] = 70_000               # one parameter split into several items mid-list
+    R, cap = 4, 1 << 12
+    plan = dpg.dpg_plan_buckets(numels, cap, R)
+    store = torch.randn(int(numels.sum()), generator=torch.Generator().manual_seed(377)).to(torch.bfloat16)
+    d_store = store.cuda()
+    grads, h_grads, off = [], [], 0
+    for n in numels:
+        grads.append(d_store[off:off + int(n)])
+        h_grads.append(np_bf16(store[off:off + int(n)]))
+        off += int(n)
+    flat = torch.full((plan.total_padded,), float("nan"), dtype=torch.bfloat16, device="cuda")
+    before = dpg.dpg_launch_count()
+    dpg.dpg_pack(plan, grads, flat)
+    assert dpg.dpg_launch_count() - before == 3
+    oplan = oracle.plan_buckets(numels, cap, R)
     ref = oracle.pack(oplan, h_grads)
     torch.cuda.synchronize()
     np.testing.assert_array_equal(np_bf16(flat), ref)
