@@ -71,6 +71,12 @@ MUTANTS = [
     ("gather_truncates", "views[k][i] = oracle_f32_to_bf16(master[i]);\n    if (reduced)",
      "views[k][i] = (uint16_t)(f32_bits(master[i]) >> 16);\n    if (reduced)",
      ["test_oracle_memory_and_step.py"]),
+    ("clip_no_eps", "double c = max_norm / (norm + 1e-6);", "double c = max_norm / norm;",
+     ["test_oracle_clip.py"]),
+    ("m_uses_beta2", "float m_old = c.beta1 * m[i];", "float m_old = c.beta2 * m[i];",
+     ["test_oracle_adam.py"]),
+    ("allreduce_rank0_only", "for (int32_t dst = 0; dst < R; ++dst)\n        oracle_reduce_range(",
+     "for (int32_t dst = 0; dst < 1; ++dst)\n        oracle_reduce_range(", ["test_oracle_reduce.py"]),
 ]
 
 
