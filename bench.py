@@ -23,6 +23,7 @@ from __future__ import annotations
 import argparse
 import hashlib
 import json
+import math
 import os
 import statistics
 import subprocess
@@ -74,6 +75,16 @@ def parse():
                     help="DDP (all-reduce + R replica updates) against the ZeRO-2 step")
     ap.add_argument("--overlap", action="store_true",
                     help="bucket updates overlapped with a simulated backward, exposed tail vs cap")
+    ap.add_argument("--backward-kind", default="spin", choices=["spin", "gemm"],
+                    help="--overlap: backward simulated by one-CTA spin kernels, or by the bf16 "
+                         "GEMMs of each weight's dW and dX over --tokens tokens")
+    ap.add_argument("--tokens", type=int, default=4096, help="--backward-kind gemm: tokens per rank")
+    ap.add_argument("--overlap-caps-mib", default="1,4,25,100,400,1048576",
+                    help="--overlap: bucket caps in MiB")
+    ap.add_argument("--overlap-max-ctas", default="0",
+                    help="--overlap: fused-pass grid caps to sweep (0: one CTA per SM)")
+    ap.add_argument("--backward-priority", action="store_true",
+                    help="--overlap: give the backward stream the higher priority")
     ap.add_argument("--backward-ms", type=float, default=30.0,
                     help="duration of the simulated backward (--overlap)")
     ap.add_argument("--hockney", action="store_true",
@@ -935,6 +946,41 @@ def run_schedules(a):
 # Gradient bucketing; "Distributed Training and Parallelism" -- DDP buckets:
 # small buckets start early but pay more startup, large ones leave a tail)
 # --------------------------------------------------------------------------
+def make_gemm_backward(cfg, plan, grad0, weight, tokens, dev):
+    """A stand-in backward made of real GEMMs: for every weight, in
+    backward-ready order, dW = dY^T X written straight into replica 0's flat
+    gradient slice (gradients produced in the communication buffers) and
+    dX = dY W into scratch; 1-D weights get a token reduction.  Returns a
+    function that issues bucket b's work on the current stream."""
+    import torch
+    shapes = [tuple(s) for _, s in cfg.shapes]
+    rows = max(s[0] for s in shapes)
+    cols = max(s[-1] for s in shapes)
+    gen = torch.Generator(device=dev).manual_seed(7)
+    dy_all = (torch.randn(tokens, rows, device=dev, generator=gen) * 1e-3).to(torch.bfloat16)
+    x_all = torch.randn(tokens, cols, device=dev, generator=gen).to(torch.bfloat16)
+    dx_flat = torch.empty(tokens * cols, dtype=torch.bfloat16, device=dev)
+    by_bucket = [[] for _ in range(plan.n_buckets)]
+    for q in range(len(shapes) - 1, -1, -1):            # backward-ready order
+        if shapes[q] and math.prod(shapes[q]) > 0:
+            by_bucket[int(plan.param_bucket[q])].append(q)
+
+    def run(b):
+        for q in by_bucket[b]:
+            off = int(plan.param_offset[q])
+            shp = shapes[q]
+            if len(shp) == 2:
+                o, i = shp
+                dw = grad0[off:off + o * i].view(o, i)
+                torch.mm(dy_all[:, :o].t(), x_all[:, :i], out=dw)
+                torch.mm(dy_all[:, :o], weight[off:off + o * i].view(o, i),
+                         out=dx_flat[:tokens * i].view(tokens, i))
+            else:
+                n = int(math.prod(shp))
+                grad0[off:off + n].copy_((dy_all[:, :n].float() * x_all[:, :n].float()).sum(0))
+    return run
+
+
 def run_overlap(a):
     import torch
     from zero_optimizer_step_gb300 import build as _build
@@ -945,9 +991,12 @@ def run_overlap(a):
     torch.cuda.set_device(dev)
     R, psi = cfg.R, cfg.psi
     sm_mhz = 2070.0       # the spin kernel counts SM clocks; the measured time is reported
-    caps = [1 << 20, 4 << 20, 25 << 20, 100 << 20, 400 << 20, 1 << 40]
+    caps = [int(float(c) * (1 << 20)) for c in a.overlap_caps_mib.split(",")]
+    grid_caps = [int(x) for x in a.overlap_max_ctas.split(",")]
     rows = []
-    bwd_stream, upd_stream = torch.cuda.Stream(), torch.cuda.Stream()
+    lo_pri, hi_pri = torch.cuda.Stream.priority_range()   # (lowest, greatest)
+    bwd_stream = torch.cuda.Stream(priority=hi_pri if a.backward_priority else 0)
+    upd_stream = torch.cuda.Stream(priority=lo_pri if a.backward_priority else 0)
     for cap in caps:
         plan = dpg.dpg_plan_buckets(cfg.numels, cap, R)
         dpg.dpg_plan_upload(plan)
@@ -962,6 +1011,8 @@ def run_overlap(a):
         # backward of bucket b takes a share of the backward time proportional
         # to its parameters; buckets are produced in plan order (last layers first)
         cycles = [int(a.backward_ms * 1e3 * sm_mhz * float(pb) / N) for pb in plan.bucket_padded]
+        gemm_bucket = make_gemm_backward(cfg, plan, g[0], p, a.tokens, dev) \
+            if a.backward_kind == "gemm" else None
 
         def one(overlap: bool):
             torch.cuda.synchronize()
@@ -973,7 +1024,10 @@ def run_overlap(a):
             evs = []
             with torch.cuda.stream(bwd_stream):
                 for b in range(plan.n_buckets):
-                    torch.cuda._sleep(cycles[b])
+                    if gemm_bucket is None:
+                        torch.cuda._sleep(cycles[b])
+                    else:
+                        gemm_bucket(b)
                     ev = torch.cuda.Event()
                     ev.record(bwd_stream)
                     evs.append(ev)
@@ -989,22 +1043,35 @@ def run_overlap(a):
             torch.cuda.synchronize()
             return e0.elapsed_time(eb), e0.elapsed_time(eu)
 
-        one(True)
-        res = {}
-        for mode in (True, False):
-            ts = sorted(one(mode) for _ in range(5))
-            res[mode] = ts[len(ts) // 2]
-        bwd, tot = res[True]
-        _, serial = res[False]
-        rows.append({"cap_bytes": cap, "n_buckets": plan.n_buckets, "backward_ms": bwd,
-                     "overlapped_total_ms": tot, "exposed_tail_ms": tot - bwd,
-                     "serial_total_ms": serial, "update_alone_ms": serial - bwd})
-        del g, w, m, v, p
+        for gc in grid_caps:
+            dpg.dpg_set_fused_max_ctas(gc)
+            try:
+                one(True)
+                res = {}
+                for mode in (True, False):
+                    ts = sorted(one(mode) for _ in range(5))
+                    res[mode] = ts[len(ts) // 2]
+            finally:
+                dpg.dpg_set_fused_max_ctas(0)
+            bwd, tot = res[True]
+            _, serial = res[False]
+            bwd_alone = res[False][0]
+            rows.append({"cap_bytes": cap, "n_buckets": plan.n_buckets, "fused_max_ctas": gc,
+                         "backward_ms": bwd_alone, "backward_ms_overlapped": bwd,
+                         "overlapped_total_ms": tot, "exposed_tail_ms": tot - bwd,
+                         "serial_total_ms": serial, "update_alone_ms": serial - bwd_alone,
+                         "saved_vs_serial_ms": serial - tot})
+        del g, w, m, v, p, gemm_bucket
         plan.destroy()
+    backward = (f"{a.backward_ms} ms of spin kernels (one CTA), split over buckets in proportion "
+                f"to their parameters, in backward-ready order" if a.backward_kind == "spin" else
+                f"bf16 GEMMs per weight in backward-ready order: dW = dY^T X written into replica "
+                f"0's flat gradient slice, dX = dY W, {a.tokens} tokens (4 * tokens * psi flops); "
+                f"the other replicas' gradients are resident synthetic data")
     print(json.dumps({"metric": "exposed update tail behind a simulated backward",
-                      "workload": f"{cfg.name}: psi={psi}, R={R}",
-                      "backward": f"{a.backward_ms} ms of spin kernels (one CTA), split over buckets "
-                                  f"in proportion to their parameters, in backward-ready order",
+                      "workload": f"{cfg.name}: psi={psi}, R={R}", "backward": backward,
+                      "streams": "backward high priority, updates low" if a.backward_priority
+                                 else "equal priority",
                       "rows": rows}), flush=True)
 
 

@@ -39,9 +39,10 @@
  *     that before capturing a stream into a CUDA graph.  A plan serves one
  *     device.  Calls that use the norm scratch of the same plan must not
  *     overlap on the GPU (issue them on one stream).
- *   - Gradient INPUTS (grads, last_micro, the accumulate source) of
- *     dpg_accumulate, dpg_reduce_scatter_adam, dpg_step, dpg_step_clipped
- *     and dpg_allreduce_grads may instead be page-locked host memory
+ *   - Gradient INPUTS (grads, last_micro, the accumulate sources) of
+ *     dpg_accumulate, dpg_accumulate_pair, dpg_reduce_scatter_adam, dpg_step,
+ *     dpg_step_fold2, dpg_step_clipped and dpg_allreduce_grads may instead be
+ *     page-locked host memory
  *     (cudaHostAlloc / cudaMallocHost, or host-registered) at its own
  *     address, which unified addressing maps into the device: the kernels
  *     then read it over the host link with the same loads, so no staging
@@ -389,6 +390,18 @@ int dpg_step_noalloc(const dpg_plan_t* plan, const void* const* grads, int32_t g
                      int32_t n_counts, const dpg_hparams* hp, float* master, float* exp_avg,
                      float* exp_avg_sq, void* const* param_views, int32_t n_views,
                      float* bucket_sqnorm, int64_t* bucket_nonfinite, void* stream);
+
+/* Launch shape -------------------------------------------------------------- */
+/* At most max_ctas CTAs (0: the default, one per SM) for the direct fused
+ * passes (dpg_step, dpg_reduce_scatter_adam, dpg_step_fold2, dpg_step_clipped,
+ * dpg_allreduce_grads, dpg_adam_from_reduced, dpg_step_noalloc) launched
+ * later by the CALLING THREAD.  A smaller grid leaves SMs free for work
+ * running concurrently on other streams (e.g. the backward GEMMs that bucket
+ * updates overlap with) at the cost of the pass's own bandwidth.  Results
+ * are the same bits for any grid; only the per-bucket norms' summation
+ * grouping changes (within their documented tolerance).  Negative:
+ * DPG_ERR_INVALID_ARG. */
+int dpg_set_fused_max_ctas(int32_t max_ctas);
 
 /* Diagnostics -------------------------------------------------------------- */
 /* Number of kernels this library has launched since it was loaded. */

@@ -180,6 +180,8 @@ def test_other_entry_points_validation():
     assert L.dpg_allgather_params(plan.handle, FAKE, dpg._ptrs([FAKE]), 65, 0, 1, None) == dpg.DPG_ERR_INVALID_ARG
     assert L.dpg_allgather_params(plan.handle, FAKE + 4, dpg._ptrs([FAKE]), 1, 0, 1, None) == dpg.DPG_ERR_MISALIGNED
     assert L.dpg_allgather_params(plan.handle, FAKE, dpg._ptrs([FAKE]), 1, 1, 1, None) == dpg.DPG_OK
+    assert L.dpg_set_fused_max_ctas(-1) == dpg.DPG_ERR_INVALID_ARG
+    assert L.dpg_set_fused_max_ctas(0) == dpg.DPG_OK
     A2 = L.dpg_accumulate_pair
     assert A2(None, FAKE, FAKE, FAKE, 1, None) == dpg.DPG_ERR_INVALID_ARG
     assert A2(plan.handle, FAKE, None, FAKE, 1, None) == dpg.DPG_ERR_INVALID_ARG

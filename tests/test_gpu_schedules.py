@@ -197,3 +197,34 @@ def test_pinned_host_gradients_read_in_place():
         outs.append([*d, p, sq, red, a0])
     for a, b in zip(*outs):
         assert torch.equal(a.view(torch.uint8), b.view(torch.uint8))
+
+
+@pytest.mark.parametrize("max_ctas", [1, 7, 40])
+def test_fused_grid_cap_gives_the_same_bits(max_ctas):
+    """A capped grid changes only which CTA visits which tile: every output
+    is the same bits, and the per-bucket norms stay within their bar."""
+    R = 4
+    plan, op, grads, _, tok = _setup(R, "bf16", seed=23)
+    N = op.total_padded
+    dg = [g.cuda() for g in grads]
+    w0 = master_f32(N, stream_seed(23, KIND_MASTER), device="cuda")
+    outs = []
+    for cap in (0, max_ctas):
+        dpg.dpg_set_fused_max_ctas(cap)
+        try:
+            d = [w0.clone(), torch.zeros(N, device="cuda"), torch.zeros(N, device="cuda")]
+            p = torch.empty(N, dtype=torch.bfloat16, device="cuda")
+            sq = torch.empty(op.n_buckets, device="cuda")
+            red = torch.empty(N, device="cuda")
+            dpg.dpg_reduce_scatter_adam(plan, dg, tok, dpg.HParams(), *d, [p], bucket_sqnorm=sq,
+                                        reduced_grad=red)
+            torch.cuda.synchronize()
+        finally:
+            dpg.dpg_set_fused_max_ctas(0)
+        outs.append((d, p, sq, red))
+    (d0, p0, sq0, r0), (d1, p1, sq1, r1) = outs
+    for a, b in zip(d0 + [p0, r0], d1 + [p1, r1]):
+        assert torch.equal(a.view(torch.uint8), b.view(torch.uint8))
+    ref = oracle.reduce([np_bf16(x) for x in grads], oracle.grad_scale(tok))
+    check_norms(np_f32(sq1), np.array([np.sum(ref[o:o + q].astype(np.float64) ** 2)
+                                       for o, q in zip(op.bucket_offset, op.bucket_padded)]))

@@ -40,7 +40,7 @@ EXPORTED = (
     "dpg_time_next_fused_launch", "dpg_step_noalloc", "dpg_export_state", "dpg_import_state",
     "dpg_step_clipped", "dpg_step_staged", "dpg_check_device_status", "dpg_set_staged_fault",
     "dpg_allreduce_grads", "dpg_adam_from_reduced", "dpg_gather_params_bf16",
-    "dpg_accumulate_pair", "dpg_step_fold2",
+    "dpg_accumulate_pair", "dpg_step_fold2", "dpg_set_fused_max_ctas",
 )
 DPG_MAX_STATE_ARRAYS = 8
 DPG_NOALLOC_SCRATCH_BYTES = 8 << 20
@@ -106,6 +106,7 @@ def lib() -> ctypes.CDLL:
         L.dpg_unpack.argtypes = [P, P, P, P]
         L.dpg_accumulate.argtypes = [P, P, P, i32, P]
         L.dpg_accumulate_pair.argtypes = [P, P, P, P, i32, P]
+        L.dpg_set_fused_max_ctas.argtypes = [i32]
         L.dpg_step_fold2.argtypes = [P, P, P, P, P, i32, P, P, P, P, P, i32, P, P, P]
         L.dpg_reduce_scatter_adam.argtypes = [P, P, i32, P, P, i32, P, P, P, P, P, i32, P, P, P,
                                               i32, i32, P]
@@ -131,7 +132,8 @@ def lib() -> ctypes.CDLL:
                      "dpg_step", "dpg_step_noalloc", "dpg_export_state", "dpg_import_state",
                      "dpg_step_clipped", "dpg_step_staged", "dpg_check_device_status",
                      "dpg_set_staged_fault", "dpg_allreduce_grads", "dpg_adam_from_reduced",
-                     "dpg_gather_params_bf16", "dpg_accumulate_pair", "dpg_step_fold2"):
+                     "dpg_gather_params_bf16", "dpg_accumulate_pair", "dpg_step_fold2",
+                     "dpg_set_fused_max_ctas"):
             getattr(L, name).restype = c_int
         _lib = L
     return _lib
@@ -595,6 +597,11 @@ def dpg_gather_params_bf16(plan: Plan, param_bf16: Ptr, param_views: Sequence[Pt
     _check(lib().dpg_gather_params_bf16(plan.handle, _ptr(param_bf16), _ptrs(param_views),
                                         len(param_views), b0, plan.n_buckets if b1 is None else b1,
                                         _stream(stream)))
+
+
+def dpg_set_fused_max_ctas(max_ctas: int = 0):
+    """Cap the CTAs of later fused passes from this thread (0: one per SM)."""
+    _check(lib().dpg_set_fused_max_ctas(int(max_ctas)))
 
 
 def dpg_launch_count() -> int:

@@ -32,6 +32,9 @@ static std::atomic<int64_t> g_launches{0};
 static thread_local cudaEvent_t t_fused_start = nullptr, t_fused_stop = nullptr;
 // test-only fault injection of the staged pass (consumed by its next launch)
 static thread_local int64_t t_staged_skip = -1;
+// Upper bound on the CTAs of the fused passes launched from this thread
+// (0: one per SM, the default).  A smaller grid leaves SMs to concurrent work.
+static thread_local int32_t t_fused_max_ctas = 0;
 static thread_local int64_t t_staged_timeout_ns = 0;
 constexpr uint64_t kStagedTimeoutNs = 1000000000ull;   // 1 s per wait
 
@@ -1260,6 +1263,7 @@ static int fused_geometry(RsKernel fn, int dev, int64_t t0, int64_t t1, int32_t 
     if (t1 <= t0) return DPG_OK;
     int st = grid_for(reinterpret_cast<const void*>(fn), kThreads, dev, t1 - t0, grid);
     if (st != DPG_OK) return st;
+    if (t_fused_max_ctas > 0 && *grid > t_fused_max_ctas) *grid = t_fused_max_ctas;
     const int64_t per_cta = (t1 - t0 + *grid - 1) / *grid;
     const int64_t buckets = int64_t(b1) - b0;
     *vmax = int32_t(per_cta < buckets ? per_cta : buckets);
@@ -1793,6 +1797,13 @@ int dpg_step_clipped(const dpg_plan_t* plan, const void* const* grads, int32_t g
     return dpg::step_clipped(plan, grads, grads_dtype, last_micro_bf16, valid_tokens, n_counts, hp,
                              max_norm, master, exp_avg, exp_avg_sq, param_views, n_views,
                              bucket_sqnorm, bucket_nonfinite, reduced_grad, clip_out, stream);
+}
+
+int dpg_set_fused_max_ctas(int32_t max_ctas) {
+    dpg::clear_error();
+    if (max_ctas < 0) return fail(DPG_ERR_INVALID_ARG, "dpg_set_fused_max_ctas: %d < 0", max_ctas);
+    dpg::t_fused_max_ctas = max_ctas;
+    return DPG_OK;
 }
 
 int dpg_time_next_fused_launch(void* start_event, void* stop_event) {
