@@ -537,12 +537,16 @@ __global__ void __launch_bounds__(kThreads, 1) k_norm_pass(const __grid_constant
 // DPG_ERR_DEVICE_TIMEOUT in a status word, the CTA waits (again bounded) for
 // its own copies still in flight and returns.  bf16 gradients, R in {1,2,4,8}.
 // ---------------------------------------------------------------------------
-constexpr int kUnit = 2048;                 // elements per stage
-constexpr int kStagedThreads = 512;         // 4 elements per thread per unit
+// A unit (one ring stage) is half a tile for R = 8 and a whole tile for
+// R <= 4, so that a stage holds 40-64 KB and its consumers -- one thread per
+// 8-element vector -- have enough warps for the Adam arithmetic of a unit
+// within the time its bytes take to stream in.
 constexpr int kMaxStages = 8;
 constexpr size_t kStagedSmemBudget = 200 * 1024;
 
-__host__ __device__ constexpr size_t staged_stage_bytes(int R) { return size_t(kUnit) * (2 * R + 12); }
+__host__ __device__ constexpr int staged_unit(int R) { return R >= 8 ? kTile / 2 : kTile; }
+__host__ __device__ constexpr int staged_consumers(int R) { return staged_unit(R) / kVec; }
+__host__ __device__ constexpr size_t staged_stage_bytes(int R) { return size_t(staged_unit(R)) * (2 * R + 12); }
 __host__ __device__ constexpr int staged_stages(int R) {
     return int(kStagedSmemBudget / staged_stage_bytes(R)) < kMaxStages
                ? int(kStagedSmemBudget / staged_stage_bytes(R)) : kMaxStages;
@@ -570,29 +574,51 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
                  : "=r"(done) : "r"(bar), "r"(parity) : "memory");
     return done != 0;
 }
-// true once the phase of `parity` completed, false if the deadline passed first
-__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, uint64_t deadline) {
+// true once the phase of `parity` completed, false if the absolute deadline
+// passed first
+__device__ __forceinline__ bool mbar_wait_until(uint32_t bar, uint32_t parity, uint64_t deadline) {
     while (!mbar_try_wait(bar, parity))
         if (global_ns() > deadline) return false;
     return true;
 }
+// the same with a relative bound, started only if the first poll fails (the
+// common case -- the stage has already landed -- reads no timer)
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, uint64_t timeout_ns) {
+    if (mbar_try_wait(bar, parity)) return true;
+    return mbar_wait_until(bar, parity, global_ns() + timeout_ns);
+}
 
-// element range [start, start + count) of unit u (count may be 0: the second
-// half of a partial tile); b is advanced to the unit's bucket
-__device__ __forceinline__ int64_t unit_range(const RsAdamArgs& a, int64_t u, int& b, int64_t* count) {
-    const int64_t t = u >> 1;
-    b = bucket_of_tile(a.tile_begin, b, a.b1, t);
-    const int64_t start = __ldg(a.bucket_offset + b) + (t - __ldg(a.tile_begin + b)) * kTile +
-                          (u & 1) * kUnit;
-    const int64_t end = __ldg(a.bucket_offset + b + 1);
-    const int64_t n = end - start;
-    *count = n <= 0 ? 0 : (n < kUnit ? n : kUnit);
+// The current bucket's table entries, reloaded only when a unit leaves it.
+struct BucketCursor {
+    int b;
+    int64_t tb_lo = 0, tb_hi = -1, bo_lo = 0, bo_hi = 0;
+};
+
+// element range [start, start + count) of unit u of U elements (count may be
+// 0: the second half of a partial tile); the cursor is advanced to the
+// unit's bucket
+template <int U>
+__device__ __forceinline__ int64_t unit_range(const RsAdamArgs& a, int64_t u, BucketCursor& c,
+                                              int64_t* count) {
+    constexpr int UPT = kTile / U;
+    const int64_t t = u / UPT;
+    if (t >= c.tb_hi) {
+        c.b = bucket_of_tile(a.tile_begin, c.b, a.b1, t);
+        c.tb_lo = __ldg(a.tile_begin + c.b);
+        c.tb_hi = __ldg(a.tile_begin + c.b + 1);
+        c.bo_lo = __ldg(a.bucket_offset + c.b);
+        c.bo_hi = __ldg(a.bucket_offset + c.b + 1);
+    }
+    const int64_t start = c.bo_lo + (t - c.tb_lo) * kTile + (u % UPT) * U;
+    const int64_t n = c.bo_hi - start;
+    *count = n <= 0 ? 0 : (n < U ? n : U);
     return start;
 }
 
 template <int RT>
 __device__ __forceinline__ void issue_unit(const StagedArgs& sa, unsigned char* stage, uint32_t bar,
                                            int64_t start, int64_t count) {
+    constexpr int kUnit = staged_unit(RT);
     const RsAdamArgs& a = sa.a;
     const uint32_t gbytes = uint32_t(count) * 2, sbytes = uint32_t(count) * 4;
     uint64_t state;
@@ -622,21 +648,41 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
     (void)state;
 }
 
-// Warp-specialised: warps 0..15 consume (512 threads, 4 elements each per
-// unit), warp 16 produces.  full[s] completes when stage s's copies have
-// landed (the producer arms it with the byte count); empty[s] completes when
-// the 16 consumer warps have finished reading it, and the producer refills it
-// only then.  All waits are bounded.
+// flush_visit for a CTA with fewer warps than the kWarps partial slots per
+// visit that k_norm_finalize adds up: the slots of absent warps get zeros.
+template <int kConsumerWarps>
+__device__ __forceinline__ void flush_visit_staged(const RsAdamArgs& a, int bucket, int visit,
+                                                   double sq, int nf) {
+    flush_visit(a, bucket, visit, sq, nf);
+    const int64_t slot = int64_t(blockIdx.x) * a.vmax + visit;
+    if ((threadIdx.x & 31) == 0)
+        for (int w2 = (threadIdx.x >> 5) + kConsumerWarps; w2 < kWarps; w2 += kConsumerWarps) {
+            a.vis_sq[slot * kWarps + w2] = 0.0;
+            a.vis_nf[slot * kWarps + w2] = 0;
+        }
+}
+
+// Warp-specialised: the consumer warps (8 for R = 8, 16 for R <= 4; one
+// thread per 8-element vector of the unit) compute, the last warp produces.
+// full[s] completes when stage s's copies have landed (the producer arms it
+// with the byte count); empty[s] completes when every consumer warp has
+// finished reading it, and the producer refills it only then.  All waits are
+// bounded.
 template <int RT>
-__global__ void __launch_bounds__(kStagedThreads + 32, 1) k_rs_adam_staged(const __grid_constant__ StagedArgs sa) {
+__global__ void __launch_bounds__(staged_consumers(RT) + 32, 1) k_rs_adam_staged(const __grid_constant__ StagedArgs sa) {
     constexpr int S = staged_stages(RT);
     constexpr size_t SB = staged_stage_bytes(RT);
+    constexpr int kUnit = staged_unit(RT);
+    constexpr int kStagedThreads = staged_consumers(RT);
     constexpr int kConsumerWarps = kStagedThreads / 32;
+    constexpr int UPT = kTile / kUnit;
+    static_assert(kStagedThreads * kVec == kUnit, "one 8-element vector per consumer thread");
+    static_assert(kConsumerWarps <= kWarps, "norm partial slots per visit");
     extern __shared__ __align__(128) unsigned char smem[];
     __shared__ __align__(8) uint64_t full[kMaxStages];
     __shared__ __align__(8) uint64_t empty[kMaxStages];
     const RsAdamArgs& a = sa.a;
-    const int64_t u0 = 2 * a.t0, u1 = 2 * a.t1;   // units of the launch
+    const int64_t u0 = UPT * a.t0, u1 = UPT * a.t1;   // units of the launch
     const int64_t n_mine = blockIdx.x < u1 - u0 ? (u1 - u0 - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
     if (threadIdx.x == 0) {
         for (int k = 0; k < S; ++k) {
@@ -651,20 +697,19 @@ __global__ void __launch_bounds__(kStagedThreads + 32, 1) k_rs_adam_staged(const
     if (threadIdx.x >= kStagedThreads) {
         // ---------------- producer warp: one lane issues ----------------
         if (threadIdx.x != kStagedThreads) return;
-        int b_prod = a.b0;
+        BucketCursor cur_p{a.b0};
         uint32_t armed = 0, armed_par = 0;   // stages armed at least once, parity of the last arm
         bool aborted = false;
         for (int64_t k = 0; k < n_mine; ++k) {
             const int s = int(k % S);
             if (k >= S &&
-                !mbar_wait_bounded(smem_u32(&empty[s]), uint32_t((k / S - 1) & 1),
-                                   global_ns() + sa.timeout_ns)) {
+                !mbar_wait_bounded(smem_u32(&empty[s]), uint32_t((k / S - 1) & 1), sa.timeout_ns)) {
                 aborted = true;
                 break;
             }
             const int64_t u = u0 + blockIdx.x + k * gridDim.x;
             int64_t cnt;
-            const int64_t st = unit_range(a, u, b_prod, &cnt);
+            const int64_t st = unit_range<kUnit>(a, u, cur_p, &cnt);
             if (u == sa.skip_unit) continue;          // test hook: never fetched
             issue_unit<RT>(sa, smem + s * SB, smem_u32(&full[s]), st, cnt);
             armed |= 1u << s;
@@ -676,103 +721,95 @@ __global__ void __launch_bounds__(kStagedThreads + 32, 1) k_rs_adam_staged(const
         const uint64_t drain = global_ns() + sa.timeout_ns;
         for (int s2 = 0; s2 < S; ++s2)
             if (armed & (1u << s2))
-                mbar_wait_bounded(smem_u32(&full[s2]), (armed_par >> s2) & 1u, drain);
+                mbar_wait_until(smem_u32(&full[s2]), (armed_par >> s2) & 1u, drain);
         return;
     }
 
     // ---------------- consumer warps ----------------
     const int lane = threadIdx.x & 31;
     const bool norm = a.vis_sq != nullptr;
-    int b = a.b0, cur = -1, visit = 0;
+    BucketCursor cur_c{a.b0};
+    int cur = -1, visit = 0;
     double sq = 0.0;
     int nf = 0;
     bool aborted = false;
+    const int e = threadIdx.x * kVec;
     for (int64_t k = 0; k < n_mine; ++k) {
         const int s = int(k % S);
         const uint32_t parity = uint32_t((k / S) & 1);
         const int64_t u = u0 + blockIdx.x + k * gridDim.x;
         int64_t cnt;
-        const int64_t start = unit_range(a, u, b, &cnt);
-        bool ok = mbar_wait_bounded(smem_u32(&full[s]), parity, global_ns() + sa.timeout_ns);
+        const int64_t start = unit_range<kUnit>(a, u, cur_c, &cnt);
+        bool ok = mbar_wait_bounded(smem_u32(&full[s]), parity, sa.timeout_ns);
         ok = __all_sync(0xFFFFFFFFu, ok);     // warp-uniform decision
         if (!ok) {
             aborted = true;
             break;
         }
-        if (norm && b != cur) {
-            if (cur >= 0) flush_visit(a, cur, visit++, sq, nf);
-            cur = b;
+        if (norm && cur_c.b != cur) {
+            if (cur >= 0) flush_visit_staged<kConsumerWarps>(a, cur, visit++, sq, nf);
+            cur = cur_c.b;
             sq = 0.0;
             nf = 0;
         }
-        const int e = threadIdx.x * 4;
-        const bool mine = e < cnt;
-        float x[4];
-        float4 w, m, v;
+        const bool mine = e < cnt;             // counts are whole 8-element vectors
+        float x[8];
+        F8 w, m, v;
         if (mine) {
             const unsigned char* stage = smem + s * SB;
-            {
-                const uint2 q = *reinterpret_cast<const uint2*>(stage + size_t(e) * 2);
-                widen2(q.x, x[0], x[1]);
-                widen2(q.y, x[2], x[3]);
-            }
+            widen8(*reinterpret_cast<const uint4*>(stage + size_t(e) * 2), x);
 #pragma unroll
             for (int r = 1; r < RT; ++r) {
-                const uint2 q = *reinterpret_cast<const uint2*>(stage + size_t(r) * kUnit * 2 + size_t(e) * 2);
-                float y[4];
-                widen2(q.x, y[0], y[1]);
-                widen2(q.y, y[2], y[3]);
+                float y[8];
+                widen8(*reinterpret_cast<const uint4*>(stage + size_t(r) * kUnit * 2 + size_t(e) * 2), y);
 #pragma unroll
-                for (int j = 0; j < 4; ++j) x[j] = __fadd_rn(x[j], y[j]);
+                for (int j = 0; j < 8; ++j) x[j] = __fadd_rn(x[j], y[j]);
             }
             const float* sw = reinterpret_cast<const float*>(stage + size_t(RT) * kUnit * 2);
-            w = *reinterpret_cast<const float4*>(sw + e);
-            m = *reinterpret_cast<const float4*>(sw + kUnit + e);
-            v = *reinterpret_cast<const float4*>(sw + 2 * kUnit + e);
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const float4 w4 = *reinterpret_cast<const float4*>(sw + e + 4 * h);
+                const float4 m4 = *reinterpret_cast<const float4*>(sw + kUnit + e + 4 * h);
+                const float4 v4 = *reinterpret_cast<const float4*>(sw + 2 * kUnit + e + 4 * h);
+                w.v[4 * h] = w4.x; w.v[4 * h + 1] = w4.y; w.v[4 * h + 2] = w4.z; w.v[4 * h + 3] = w4.w;
+                m.v[4 * h] = m4.x; m.v[4 * h + 1] = m4.y; m.v[4 * h + 2] = m4.z; m.v[4 * h + 3] = m4.w;
+                v.v[4 * h] = v4.x; v.v[4 * h + 1] = v4.y; v.v[4 * h + 2] = v4.z; v.v[4 * h + 3] = v4.w;
+            }
         }
         // the warp has read stage s: release it to the producer, then compute
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&empty[s]));
         if (mine) {
-            float* wp = &w.x;
-            float* mp = &m.x;
-            float* vp = &v.x;
             float tsq = 0.0f;
-            float g[4];
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                g[j] = __fmul_rn(x[j], a.scale);
-                float wj = wp[j];
+            for (int j = 0; j < 8; ++j) {
+                const float g = __fmul_rn(x[j], a.scale);
+                float wj = w.v[j];
                 if (a.decay) wj = __fsub_rn(wj, __fmul_rn(a.lr_wd, wj));
-                const float mj = __fadd_rn(__fmul_rn(a.beta1, mp[j]), __fmul_rn(a.omb1, g[j]));
+                const float mj = __fadd_rn(__fmul_rn(a.beta1, m.v[j]), __fmul_rn(a.omb1, g));
                 const float vj =
-                    __fadd_rn(__fmul_rn(a.beta2, vp[j]), __fmul_rn(a.omb2, __fmul_rn(g[j], g[j])));
+                    __fadd_rn(__fmul_rn(a.beta2, v.v[j]), __fmul_rn(a.omb2, __fmul_rn(g, g)));
                 const float m_hat = __fdiv_rn(mj, a.bias1);
                 const float v_hat = __fdiv_rn(vj, a.bias2);
                 const float uu = __fdiv_rn(m_hat, __fadd_rn(__fsqrt_rn(v_hat), a.eps));
-                wp[j] = __fsub_rn(wj, __fmul_rn(a.lr, uu));
-                mp[j] = mj;
-                vp[j] = vj;
-                tsq = fmaf(g[j], g[j], tsq);
-                nf += (__float_as_uint(g[j]) & 0x7F800000u) == 0x7F800000u;
+                w.v[j] = __fsub_rn(wj, __fmul_rn(a.lr, uu));
+                m.v[j] = mj;
+                v.v[j] = vj;
+                tsq = fmaf(g, g, tsq);
+                nf += (__float_as_uint(g) & 0x7F800000u) == 0x7F800000u;
             }
             if (norm) sq += double(tsq);
             const int64_t i = start + e;
-            *reinterpret_cast<float4*>(a.master + i) = w;
-            *reinterpret_cast<float4*>(a.m + i) = m;
-            *reinterpret_cast<float4*>(a.v + i) = v;
-            __nv_bfloat162 h0 = __floats2bfloat162_rn(wp[0], wp[1]);
-            __nv_bfloat162 h1 = __floats2bfloat162_rn(wp[2], wp[3]);
-            uint2 pk;
-            pk.x = *reinterpret_cast<uint32_t*>(&h0);
-            pk.y = *reinterpret_cast<uint32_t*>(&h1);
-            for (int kv = 0; kv < a.n_views; ++kv)
-                *reinterpret_cast<uint2*>(static_cast<uint16_t*>(a.views[kv]) + i) = pk;
+            st_f8(a.master + i, w);
+            st_f8(a.m + i, m);
+            st_f8(a.v + i, v);
+            const uint4 pk = narrow8(w.v);
+            for (int kv = 0; kv < a.n_views; ++kv) st_u4(static_cast<uint16_t*>(a.views[kv]) + i, pk);
         }
     }
     if (aborted && lane == 0) atomicExch(sa.status, DPG_ERR_DEVICE_TIMEOUT);
     if (norm) {
-        if (cur >= 0) flush_visit(a, cur, visit++, sq, nf);
+        if (cur >= 0) flush_visit_staged<kConsumerWarps>(a, cur, visit++, sq, nf);
         if (threadIdx.x == 0) a.vis_count[blockIdx.x] = visit;
     }
 }
@@ -1649,7 +1686,7 @@ static int launch_staged(const StagedArgs& sa, int grid, cudaStream_t s) {
             attr_set = true;
         }
     }
-    k_rs_adam_staged<RT><<<grid, kStagedThreads + 32, smem, s>>>(sa);
+    k_rs_adam_staged<RT><<<grid, staged_consumers(RT) + 32, smem, s>>>(sa);
     return after_launch("dpg_step_staged");
 }
 
@@ -1685,7 +1722,7 @@ static int step_staged(const dpg_plan_t* plan, const void* const* grads, int32_t
     int sms = 0;
     st = sm_count(p.device, &sms);
     if (st != DPG_OK) return st;
-    const int64_t units = 2 * p.n_tiles;
+    const int64_t units = int64_t(kTile / staged_unit(p.R)) * p.n_tiles;
     const int grid = int(units < sms ? (units > 0 ? units : 1) : sms);
     const int64_t per_cta = (units + grid - 1) / grid;
     a.vmax = int32_t(per_cta < p.n_buckets ? per_cta : p.n_buckets);
