@@ -336,8 +336,9 @@ int dpg_step_clipped(const dpg_plan_t* plan, const void* const* grads, int32_t g
 
 /* ---------------------------------------------------------------------------
  * dpg_step through the STAGED variant of the fused pass: in each CTA a
- * producer warp copies the R gradient tiles and the master/m/v tiles of the
- * half-tiles it will process into a ring of shared-memory stages with the
+ * producer warp copies the R gradient slices and the master/m/v slices of the
+ * units it will process (half a 4096-element tile at R = 8, a whole tile at
+ * R <= 4) into a ring of shared-memory stages with the
  * bulk-copy engine (cp.async.bulk, completion counted in bytes on a "full"
  * mbarrier per stage), refilling a stage as soon as the consumer warps have
  * released it on its "empty" mbarrier.  Same arguments and results as dpg_step for bf16 gradients
@@ -413,7 +414,7 @@ int64_t dpg_launch_count(void);
  * caller time the fused kernel alone inside a whole step. */
 int dpg_time_next_fused_launch(void* start_event, void* stop_event);
 /* Test-only fault injection for the staged step: its next launch by the
- * calling thread never fetches half-tile `skip_unit` (-1: none), so the CTA
+ * calling thread never fetches unit `skip_unit` (-1: none), so the CTA
  * that owns it must run out its wait, and every wait is bounded by
  * `timeout_ns` (<= 0: the default 1 s).  Used to test the timeout path. */
 int dpg_set_staged_fault(int64_t skip_unit, int64_t timeout_ns);
