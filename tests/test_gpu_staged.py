@@ -2,9 +2,10 @@
 
 * Parity: dpg_step_staged against the oracle on the same inputs, bit-exact
   expected (bars: 2 ulp fp32, 1 ulp bf16, norms 1e-5), for R = 1, 2, 4, 8,
-  ragged buckets (partial half-tiles, empty second halves), several views.
+  ragged buckets (partial units, empty second halves of tiles at R = 8),
+  several views.
 * Failure detection without a GPU fault: a test-only hook makes one CTA's
-  half-tile never be fetched, so its bounded wait (50 ms here) runs out; the
+  unit never be fetched, so its bounded wait (50 ms here) runs out; the
   kernel records DPG_ERR_DEVICE_TIMEOUT, drains its copies in flight and
   returns; dpg_check_device_status reports it, and the next call on the same
   context runs normally and is exact again.

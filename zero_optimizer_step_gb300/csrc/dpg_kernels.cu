@@ -529,8 +529,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_norm_pass(const __grid_constant
 }
 
 // ---------------------------------------------------------------------------
-// Staged variant of the fused pass: the R gradient tiles and the master/m/v
-// tiles of a unit (half a 4096-element tile) are copied into shared memory by
+// Staged variant of the fused pass: the R gradient slices and the master/m/v
+// slices of a unit (a tile or half of one, by R) are copied into shared memory by
 // the bulk-copy engine (cp.async.bulk, completion counted in bytes on an
 // mbarrier), S units ahead of the threads that consume them.  Every wait is
 // bounded by a global-timer deadline: a wait that runs out records
@@ -1156,7 +1156,7 @@ int upload(Plan& p) {
     // ceil(T / G)) visit slots: at most T + G and at most G * B, G being at
     // most the resident CTAs of the device (2048 threads per SM).
     const int64_t cap_ctas = int64_t(sms) * (2048 / kThreads);
-    // (the staged pass works on half tiles: twice as many units)
+    // (the staged pass works on up to two units per tile: twice as many)
     int64_t cap_visits = 2 * p.n_tiles + cap_ctas;
     if (cap_ctas * p.n_buckets < cap_visits) cap_visits = cap_ctas * p.n_buckets;
     if (cap_visits < 1) cap_visits = 1;
