@@ -303,9 +303,15 @@ def load_peak():
 
 
 def kernel_source_sha256() -> str:
+    """Hash of the kernel sources' code: comments and whitespace removed, so a
+    stored capture stays valid across edits that change no code."""
+    import re
     h = hashlib.sha256()
     for f in KERNEL_SRCS:
-        h.update(open(f, "rb").read())
+        src = open(f).read()
+        src = re.sub(r"/\*.*?\*/", " ", src, flags=re.S)
+        src = re.sub(r"//[^\n]*", " ", src)
+        h.update(" ".join(src.split()).encode())
     return h.hexdigest()
 
 
