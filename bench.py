@@ -353,6 +353,7 @@ def write_traffic(a):
         "R": cfg.R, "K": cfg.K, "elements": cfg.psi,
         "dram_bytes_read": rd, "dram_bytes_write": wr, "dram_bytes_per_launch": rd + wr,
         "launches": len(launches), "source_sha256": kernel_source_sha256(),
+        "hash": "sha256 of dpg_kernels.cu + dpg_internal.h with comments and whitespace removed",
         "how": "ncu --metrics gpu__time_duration.sum,dram__bytes_read.sum,dram__bytes_write.sum "
                "--clock-control none -k regex:\"k_rs_adam|k_norm_finalize\" on python bench.py "
                "--no-e2e --no-cpu-baseline (one pass, full-size workload); mean per launch"}}
