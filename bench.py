@@ -855,6 +855,8 @@ def run_kernel_table(a):
         ("calibration: torch fill_ (write only, 4 B/param)", 4, lambda: acc.fill_(0.5)),
         ("calibration: torch copy_ (fp32 1:1 copy, 8 B/param)", 8, lambda: acc.copy_(w)),
         ("calibration: torch sum (read only, 4 B/param)", 4, lambda: torch.sum(w)),
+        ("calibration: torch add (2 reads : 1 write, 12 B/param)", 12,
+         lambda: torch.add(w, m, out=acc)),
     ]
     views = [torch.empty(N, dtype=torch.bfloat16, device=dev) for _ in range(R)]
     rows = []

@@ -74,6 +74,12 @@ struct Plan {
     int32_t* d_vis_count = nullptr; // cap_ctas
     int64_t cap_visits = 0;
     int32_t cap_ctas = 0;
+    // chunked launches: tile -> bucket map (n_tiles) and per-chunk norm
+    // partials (chunks_per_tile * n_tiles each), one allocation
+    void* d_chunk = nullptr;
+    int32_t* d_tile_bucket = nullptr;
+    double* d_chunk_sq = nullptr;
+    int32_t* d_chunk_nf = nullptr;
     // global-norm clipping: per-bucket fp64 squared norms and the coefficient
     void* d_clip = nullptr;
     double* d_bucket_sq64 = nullptr;  // n_buckets + 1

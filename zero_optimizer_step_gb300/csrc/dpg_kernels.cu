@@ -157,6 +157,11 @@ struct RsAdamArgs {
     int32_t decay;
     const float* g_in;      // kInReduced: the normalised reduced gradient
     const float* clip_coef; // kUpdate: device scalar, g <- g * coef
+    // chunked launches (one CTA per chunk): tile -> bucket map and the
+    // per-chunk norm partials (NULL: no norm)
+    const int32_t* tile_bucket;
+    double* chunk_sq;
+    int32_t* chunk_nf;
 };
 
 // Bucket holding tile t, searching forward from bucket b (tile_begin[b] <= t
@@ -865,6 +870,149 @@ k_norm_finalize(const double* __restrict__ vis_sq, const int32_t* __restrict__ v
     }
 }
 
+// ---------------------------------------------------------------------------
+// Chunked launch of the fused pass: one 128-thread CTA per 1024-element chunk
+// (a quarter tile), one 8-element vector per thread, no grid-stride loop.  The
+// SM keeps several such CTAs resident at different points of their
+// load -> Adam -> store sequence, so DRAM stays busy while some of them do
+// arithmetic; a persistent CTA of 16 warps that load and compute in step
+// leaves it idle meanwhile.  Norms: each CTA writes one (sum of squares,
+// non-finite count) partial per chunk; k_chunk_finalize adds a bucket's
+// chunks in a fixed order.
+// ---------------------------------------------------------------------------
+constexpr int kChunkThreads = 128;
+constexpr int kChunk = kChunkThreads * kVec;
+constexpr int kChunksPerTile = int(kTile / kChunk);
+
+template <int RT, int MODE, int PHASE>
+__global__ void __launch_bounds__(kChunkThreads) k_rs_adam_chunk(const __grid_constant__ RsAdamArgs a) {
+    static_assert(PHASE != kNormOnly, "the norm pass is k_norm_pass");
+    const int64_t c = blockIdx.x;                         // chunk of this launch
+    const int64_t t = a.t0 + c / kChunksPerTile;
+    const int b = __ldg(a.tile_bucket + t);
+    const int64_t i = __ldg(a.bucket_offset + b) + (t - __ldg(a.tile_begin + b)) * kTile +
+                      (c % kChunksPerTile) * kChunk + int64_t(threadIdx.x) * kVec;
+    double sq = 0.0;
+    int nf = 0;
+    if (i < __ldg(a.bucket_offset + b + 1)) {
+        float coef = 1.0f;
+        if constexpr (PHASE == kUpdate) coef = __ldg(a.clip_coef);
+        float s[8];
+        reduce_vector<RT, MODE>(a, i, s);
+        F8 w = ld_state_f8(a.master + i);
+        F8 m = ld_state_f8(a.m + i);
+        F8 v = ld_state_f8(a.v + i);
+        float g[8];
+        float tsq = 0.0f;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            g[j] = MODE == kInReduced ? s[j] : __fmul_rn(s[j], a.scale);
+            if constexpr (PHASE == kUpdate) g[j] = __fmul_rn(g[j], coef);
+            float wj = w.v[j];
+            if (a.decay) wj = __fsub_rn(wj, __fmul_rn(a.lr_wd, wj));
+            const float mj = __fadd_rn(__fmul_rn(a.beta1, m.v[j]), __fmul_rn(a.omb1, g[j]));
+            const float vj = __fadd_rn(__fmul_rn(a.beta2, v.v[j]),
+                                       __fmul_rn(a.omb2, __fmul_rn(g[j], g[j])));
+            const float m_hat = __fdiv_rn(mj, a.bias1);
+            const float v_hat = __fdiv_rn(vj, a.bias2);
+            const float u = __fdiv_rn(m_hat, __fadd_rn(__fsqrt_rn(v_hat), a.eps));
+            w.v[j] = __fsub_rn(wj, __fmul_rn(a.lr, u));
+            m.v[j] = mj;
+            v.v[j] = vj;
+            tsq = fmaf(g[j], g[j], tsq);
+            nf += (__float_as_uint(g[j]) & 0x7F800000u) == 0x7F800000u;
+        }
+        sq = double(tsq);
+        st_f8(a.master + i, w);
+        st_f8(a.m + i, m);
+        st_f8(a.v + i, v);
+        const uint4 p = narrow8(w.v);
+        for (int k = 0; k < a.n_views; ++k) st_u4(static_cast<uint16_t*>(a.views[k]) + i, p);
+        if (PHASE == kFull && a.reduced) {
+            F8 gg;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) gg.v[j] = g[j];
+            st_f8(a.reduced + i, gg);
+        }
+    }
+    if (a.chunk_sq != nullptr) {                          // uniform over the launch
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            sq += __shfl_xor_sync(0xFFFFFFFFu, sq, o);
+            nf += __shfl_xor_sync(0xFFFFFFFFu, nf, o);
+        }
+        __shared__ double w_sq[kChunkThreads / 32];
+        __shared__ int w_nf[kChunkThreads / 32];
+        if ((threadIdx.x & 31) == 0) {
+            w_sq[threadIdx.x >> 5] = sq;
+            w_nf[threadIdx.x >> 5] = nf;
+        }
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            double tot = 0.0;
+            int cnt = 0;
+#pragma unroll
+            for (int k = 0; k < kChunkThreads / 32; ++k) {
+                tot += w_sq[k];
+                cnt += w_nf[k];
+            }
+            a.chunk_sq[c] = tot;
+            a.chunk_nf[c] = cnt;
+        }
+    }
+}
+
+// One CTA per bucket of a chunked launch starting at tile t0.  A bucket of a
+// large plan has 10^5 chunk partials and there are only tens of buckets, so
+// each thread keeps 8 loads in flight: thread j adds chunks j + 1024 k in
+// increasing k (8 at a time, in order), then a fixed tree combines the
+// threads -- the same order on every run.
+constexpr int kChunkFinalizeThreads = 1024;
+
+__global__ void __launch_bounds__(kChunkFinalizeThreads)
+k_chunk_finalize(const double* __restrict__ chunk_sq, const int32_t* __restrict__ chunk_nf,
+                 const int64_t* __restrict__ tile_begin, int64_t t0, int32_t b0, float* sqnorm,
+                 int64_t* nonfinite, double* sqnorm64) {
+    constexpr int T = kChunkFinalizeThreads, U = 8;
+    __shared__ double s_sq[T];
+    __shared__ long long s_nf[T];
+    const int b = b0 + blockIdx.x;
+    const int64_t c0 = (__ldg(tile_begin + b) - t0) * kChunksPerTile;
+    const int64_t c1 = (__ldg(tile_begin + b + 1) - t0) * kChunksPerTile;
+    double acc = 0.0;
+    long long cnt = 0;
+    for (int64_t c = c0 + threadIdx.x; c < c1; c += int64_t(T) * U) {
+        double x[U];
+        int y[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int64_t k = c + int64_t(u) * T;
+            x[u] = k < c1 ? chunk_sq[k] : 0.0;
+            y[u] = k < c1 ? chunk_nf[k] : 0;
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            acc += x[u];
+            cnt += y[u];
+        }
+    }
+    s_sq[threadIdx.x] = acc;
+    s_nf[threadIdx.x] = cnt;
+    __syncthreads();
+    for (int w = T / 2; w > 0; w >>= 1) {
+        if (threadIdx.x < w) {
+            s_sq[threadIdx.x] += s_sq[threadIdx.x + w];
+            s_nf[threadIdx.x] += s_nf[threadIdx.x + w];
+        }
+        __syncthreads();
+    }
+    if (threadIdx.x == 0) {
+        if (sqnorm) sqnorm[b] = float(s_sq[0]);
+        if (nonfinite) nonfinite[b] = s_nf[0];
+        if (sqnorm64) sqnorm64[b] = s_sq[0];
+    }
+}
+
 // Global clip coefficient from the per-bucket squared norms (one CTA, fixed
 // order): norm = sqrt(sum), coef = min(1, max_norm / (norm + 1e-6)) in double,
 // stored as fp32; a NaN norm gives a NaN coefficient (it is not clamped away).
@@ -1173,12 +1321,24 @@ int upload(Plan& p) {
     const size_t clip_sq_bytes = round256(nb1 * sizeof(double));
     void* clip = nullptr;
     if (e == cudaSuccess) e = cudaMalloc(&clip, clip_sq_bytes + 256);
+    // chunked launches: tile -> bucket map, then the per-chunk norm partials
+    const size_t n_tiles1 = size_t(p.n_tiles > 0 ? p.n_tiles : 1);
+    const size_t n_chunks1 = n_tiles1 * kChunksPerTile;
+    const size_t tb_bytes = round256(n_tiles1 * sizeof(int32_t));
+    const size_t csq_bytes = round256(n_chunks1 * sizeof(double));
+    void* chunk = nullptr;
+    if (e == cudaSuccess) e = cudaMalloc(&chunk, tb_bytes + csq_bytes + n_chunks1 * sizeof(int32_t));
+    std::vector<int32_t> tile_bucket(n_tiles1, 0);
+    for (int32_t b = 0; b < p.n_buckets; ++b)
+        for (int64_t t = p.tile_begin[b]; t < p.tile_begin[b + 1]; ++t) tile_bucket[size_t(t)] = b;
+    if (e == cudaSuccess)
+        e = cudaMemcpy(chunk, tile_bucket.data(), n_tiles1 * sizeof(int32_t), cudaMemcpyHostToDevice);
     if (e == cudaSuccess) e = cudaMemcpy(bo, p.bucket_offset.data(), nb1 * sizeof(int64_t), cudaMemcpyHostToDevice);
     if (e == cudaSuccess) e = cudaMemcpy(tb, p.tile_begin.data(), nb1 * sizeof(int64_t), cudaMemcpyHostToDevice);
     if (e == cudaSuccess && !p.items.empty())
         e = cudaMemcpy(it, p.items.data(), p.items.size() * sizeof(PackItem), cudaMemcpyHostToDevice);
     if (e != cudaSuccess) {
-        cudaFree(bo); cudaFree(tb); cudaFree(it); cudaFree(vis); cudaFree(clip);
+        cudaFree(bo); cudaFree(tb); cudaFree(it); cudaFree(vis); cudaFree(clip); cudaFree(chunk);
         cudaGetLastError();
         return fail(e == cudaErrorMemoryAllocation ? DPG_ERR_OOM : DPG_ERR_CUDA,
                     "plan upload: %s", cudaGetErrorString(e));
@@ -1196,6 +1356,10 @@ int upload(Plan& p) {
     p.d_bucket_sq64 = static_cast<double*>(clip);
     p.d_clip_coef = reinterpret_cast<float*>(static_cast<unsigned char*>(clip) + clip_sq_bytes);
     p.d_status = reinterpret_cast<int32_t*>(static_cast<unsigned char*>(clip) + clip_sq_bytes + 128);
+    p.d_chunk = chunk;
+    p.d_tile_bucket = static_cast<int32_t*>(chunk);
+    p.d_chunk_sq = reinterpret_cast<double*>(static_cast<unsigned char*>(chunk) + tb_bytes);
+    p.d_chunk_nf = reinterpret_cast<int32_t*>(static_cast<unsigned char*>(chunk) + tb_bytes + csq_bytes);
     p.cap_visits = cap_visits;
     p.cap_ctas = int32_t(cap_ctas);
     p.device = dev;
@@ -1213,6 +1377,7 @@ void release_device(Plan& p) {
         cudaFree(p.d_items);
         cudaFree(p.d_vis);
         cudaFree(p.d_clip);
+        cudaFree(p.d_chunk);
     }
     if (have_cur) cudaSetDevice(cur);
     cudaGetLastError();
@@ -1333,6 +1498,46 @@ static int launch_fused(RsKernel fn, const RsAdamArgs& a, int grid, float* sqnor
     return st;
 }
 
+template <int MODE, int PHASE = kFull>
+static RsKernel pick_chunk_kernel(int R) {
+    switch (R) {
+        case 1: return k_rs_adam_chunk<1, MODE, PHASE>;
+        case 2: return k_rs_adam_chunk<2, MODE, PHASE>;
+        case 4: return k_rs_adam_chunk<4, MODE, PHASE>;
+        case 8: return k_rs_adam_chunk<8, MODE, PHASE>;
+        default: return k_rs_adam_chunk<0, MODE, PHASE>;
+    }
+}
+
+// Chunked launch of the fused pass over tiles [a.t0, a.t1) (tables already in
+// `a`), then, when a norm output is requested, the per-bucket finalize.
+static int launch_chunked(RsKernel fn, RsAdamArgs a, const Plan& p, bool want_norm, float* sqnorm,
+                          int64_t* nonfinite, cudaStream_t s, const char* who,
+                          double* sqnorm64 = nullptr) {
+    a.tile_bucket = p.d_tile_bucket;
+    a.chunk_sq = want_norm ? p.d_chunk_sq : nullptr;
+    a.chunk_nf = want_norm ? p.d_chunk_nf : nullptr;
+    const int64_t n_chunks = (a.t1 - a.t0) * kChunksPerTile;
+    if (n_chunks > 0x7FFFFFFF) return fail(DPG_ERR_INVALID_ARG, "%s: %lld chunks in one launch", who,
+                                           (long long)n_chunks);
+    int st = DPG_OK;
+    if (n_chunks > 0) {
+        cudaEvent_t ev0 = t_fused_start, ev1 = t_fused_stop;
+        t_fused_start = t_fused_stop = nullptr;
+        if (ev0) DPG_CUDA_TRY(cudaEventRecord(ev0, s));
+        fn<<<unsigned(n_chunks), kChunkThreads, 0, s>>>(a);
+        st = after_launch(who);
+        if (st != DPG_OK) return st;
+        if (ev1) DPG_CUDA_TRY(cudaEventRecord(ev1, s));
+    }
+    if (want_norm) {
+        k_chunk_finalize<<<a.b1 - a.b0, kChunkFinalizeThreads, 0, s>>>(
+            p.d_chunk_sq, p.d_chunk_nf, p.d_tile_begin, a.t0, a.b0, sqnorm, nonfinite, sqnorm64);
+        st = after_launch(who);
+    }
+    return st;
+}
+
 static int rs_adam(const dpg_plan_t* plan, const void* const* grads, int32_t grads_dtype,
                    const void* const* last, const int64_t* tokens, int32_t n_counts,
                    const dpg_hparams* hp, float* master, float* m, float* v,
@@ -1406,6 +1611,15 @@ static int rs_adam(const dpg_plan_t* plan, const void* const* grads, int32_t gra
     a.n_views = n_views;
     const int mode = grads_dtype == DPG_BF16 ? kInBf16
                    : last2 ? kInF32PlusBf16x2 : (last ? kInF32PlusBf16 : kInF32);
+    if (t_fused_max_ctas == 0) {
+        RsKernel fc = mode == kInBf16 ? pick_chunk_kernel<kInBf16>(p.R)
+                    : mode == kInF32 ? pick_chunk_kernel<kInF32>(p.R)
+                    : mode == kInF32PlusBf16 ? pick_chunk_kernel<kInF32PlusBf16>(p.R)
+                                             : pick_chunk_kernel<kInF32PlusBf16x2>(p.R);
+        return launch_chunked(fc, a, p, want_norm, sqnorm, nonfinite,
+                              static_cast<cudaStream_t>(stream), who);
+    }
+    // a grid cap asks for the persistent kernel, whose CTA count it bounds
     RsKernel fn = mode == kInBf16 ? pick_rs_kernel<kInBf16>(p.R)
                 : mode == kInF32 ? pick_rs_kernel<kInF32>(p.R)
                 : mode == kInF32PlusBf16 ? pick_rs_kernel<kInF32PlusBf16>(p.R)
@@ -1657,6 +1871,9 @@ static int adam_from_reduced(const dpg_plan_t* plan, const float* reduced, const
     a.b0 = b0;
     a.b1 = b1;
     a.R = p.R;
+    if (t_fused_max_ctas == 0)
+        return launch_chunked(k_rs_adam_chunk<1, kInReduced, kFull>, a, p, want_norm, sqnorm,
+                              nonfinite, static_cast<cudaStream_t>(stream), who);
     RsKernel fn = k_rs_adam<1, kInReduced, kFull>;
     int grid = 0;
     st = fused_geometry(fn, p.device, a.t0, a.t1, b0, b1, &grid, &a.vmax);
