@@ -332,6 +332,13 @@ def traffic_per_launch(cfg, cap, total_padded):
     return float(t["dram_bytes_per_launch"]) * total_padded / float(t["elements"])
 
 
+def fused_kernel_name(a, R, K) -> str:
+    """The fused kernel the timed step launches (for the roofline label)."""
+    if getattr(a, "variant", "direct") == "staged":
+        return f"k_rs_adam_staged<R={R}>"
+    return f"k_rs_adam_chunk<R={R}>" + ("" if K == 1 else " (fp32 accumulators + last microbatch)")
+
+
 def write_traffic(a):
     """profiles/traffic.json from an ncu launch list of the fused kernel."""
     import csv
@@ -341,7 +348,7 @@ def write_traffic(a):
         rows = [r for r in csv.reader(fh) if len(r) > 14 and r[0].isdigit()]
     for r in rows:
         name, metric, value = r[4], r[12], float(r[14].replace(",", ""))
-        if not name.startswith("void k_rs_adam<") or "staged" in name:
+        if not name.startswith(("void k_rs_adam<", "void k_rs_adam_chunk<")) or "staged" in name:
             continue
         per.setdefault(r[0], {})[metric] = value
     launches = [d for d in per.values()
@@ -358,7 +365,7 @@ def write_traffic(a):
         "launches": len(launches), "source_sha256": kernel_source_sha256(),
         "hash": "sha256 of dpg_kernels.cu + dpg_internal.h with comments and whitespace removed",
         "how": "ncu --metrics gpu__time_duration.sum,dram__bytes_read.sum,dram__bytes_write.sum "
-               "--clock-control none -k regex:\"k_rs_adam|k_norm_finalize\" on python bench.py "
+               "--clock-control none -k regex:\"k_rs_adam|finalize\" on python bench.py "
                "--no-e2e --no-cpu-baseline (one pass, full-size workload); mean per launch"}}
     with open(TRAFFIC_FILE, "w") as fh:
         json.dump(out, fh, indent=1)
@@ -489,7 +496,7 @@ def run_dpg(a):
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": workload_desc(cfg, cap, plan.n_buckets, N, fold2),
         "hbm_gbs_step": bpp["step"] * cfg.psi / (ms * 1e-3) / 1e9,
-        "roofline": {"bound": "hbm", "kernel": f"k_rs_adam<R={R}>", "achieved": achieved,
+        "roofline": {"bound": "hbm", "kernel": fused_kernel_name(a, R, K), "achieved": achieved,
                      "peak": peak, "peak_kind": f"{peak_kind} (copy bandwidth)", "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic,
                      "algorithmic_bytes_per_launch": bpp["fused"] * cfg.psi,
@@ -831,13 +838,13 @@ def run_kernel_table(a):
         ("k_accumulate<first> (one replica)", 6, lambda: dpg.dpg_accumulate(plan, g[0], acc, True)),
         ("k_accumulate (one replica)", 10, lambda: dpg.dpg_accumulate(plan, g[0], acc, False)),
         ("k_allgather (one view)", 6, lambda: dpg.dpg_allgather_params(plan, w, [p])),
-        (f"k_rs_adam<R={R}> (dpg_reduce_scatter_adam, no norm)", 2 * R + 26,
+        (f"k_rs_adam_chunk<R={R}> (dpg_reduce_scatter_adam, no norm)", 2 * R + 26,
          lambda: dpg.dpg_reduce_scatter_adam(plan, g, tok, hp(), w, m, v, [p])),
-        (f"k_rs_adam<R={R}> + k_norm_finalize (dpg_step)", 2 * R + 26,
+        (f"k_rs_adam_chunk<R={R}> + k_chunk_finalize (dpg_step)", 2 * R + 26,
          lambda: dpg.dpg_step(plan, g, tok, hp(), w, m, v, [p], bucket_sqnorm=sq)),
         (f"k_rs_adam_staged<R={R}> (dpg_step_staged, bulk-copy staging)", 2 * R + 26,
          lambda: dpg.dpg_step_staged(plan, g, tok, hp(), w, m, v, [p], bucket_sqnorm=sq)),
-        (f"k_rs_adam<R={R}> distinct views (n_views=R)", 4 * R + 24,
+        (f"k_rs_adam_chunk<R={R}> distinct views (n_views=R)", 4 * R + 24,
          lambda: dpg.dpg_step(plan, g, tok, hp(), w, m, v, views)),
         ("dpg_step_clipped, g stored (norm pass + update pass)", 2 * R + 34,
          lambda: dpg.dpg_step_clipped(plan, g, tok, hp(), 1e-6, w, m, v, [p], reduced_grad=acc)),

@@ -936,11 +936,13 @@ __global__ void __launch_bounds__(kChunkThreads) k_rs_adam_chunk(const __grid_co
         }
     }
     if (a.chunk_sq != nullptr) {                          // uniform over the launch
+        // a warp's 256 squares summed in fp32 (relative error ~1e-7), the
+        // CTA's four warps and the bucket's chunks in double
+        float fs = float(sq);
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            sq += __shfl_xor_sync(0xFFFFFFFFu, sq, o);
-            nf += __shfl_xor_sync(0xFFFFFFFFu, nf, o);
-        }
+        for (int o = 16; o > 0; o >>= 1) fs += __shfl_xor_sync(0xFFFFFFFFu, fs, o);
+        sq = fs;
+        nf = __reduce_add_sync(0xFFFFFFFFu, nf);
         __shared__ double w_sq[kChunkThreads / 32];
         __shared__ int w_nf[kChunkThreads / 32];
         if ((threadIdx.x & 31) == 0) {
