@@ -393,15 +393,18 @@ int dpg_step_noalloc(const dpg_plan_t* plan, const void* const* grads, int32_t g
                      float* bucket_sqnorm, int64_t* bucket_nonfinite, void* stream);
 
 /* Launch shape -------------------------------------------------------------- */
-/* At most max_ctas CTAs (0: the default, one per SM) for the direct fused
- * passes (dpg_step, dpg_reduce_scatter_adam, dpg_step_fold2, dpg_step_clipped,
- * dpg_allreduce_grads, dpg_adam_from_reduced, dpg_step_noalloc) launched
- * later by the CALLING THREAD.  A smaller grid leaves SMs free for work
- * running concurrently on other streams (e.g. the backward GEMMs that bucket
- * updates overlap with) at the cost of the pass's own bandwidth.  Results
- * are the same bits for any grid; only the per-bucket norms' summation
- * grouping changes (within their documented tolerance).  Negative:
- * DPG_ERR_INVALID_ARG. */
+/* By default the fused passes (dpg_step, dpg_reduce_scatter_adam,
+ * dpg_step_fold2, dpg_adam_from_reduced and the update pass of
+ * dpg_step_clipped) launch one small CTA per 1024-element chunk, which keeps
+ * the most bytes in flight.  max_ctas > 0 makes later launches from the
+ * CALLING THREAD use instead a persistent grid of at most max_ctas CTAs
+ * (grid-stride over 4096-element tiles), leaving SMs free for work running
+ * concurrently on other streams at the cost of the pass's own bandwidth; the
+ * clipped step's norm pass, dpg_allreduce_grads and dpg_step_noalloc always
+ * use the persistent grid and honour the bound too.  0 restores the default.
+ * Results are the same bits for any launch shape; only the per-bucket norms'
+ * summation grouping changes (within their documented tolerance).
+ * Negative: DPG_ERR_INVALID_ARG. */
 int dpg_set_fused_max_ctas(int32_t max_ctas);
 
 /* Diagnostics -------------------------------------------------------------- */

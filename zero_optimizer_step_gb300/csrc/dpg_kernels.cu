@@ -892,7 +892,7 @@ __global__ void __launch_bounds__(kChunkThreads) k_rs_adam_chunk(const __grid_co
     const int b = __ldg(a.tile_bucket + t);
     const int64_t i = __ldg(a.bucket_offset + b) + (t - __ldg(a.tile_begin + b)) * kTile +
                       (c % kChunksPerTile) * kChunk + int64_t(threadIdx.x) * kVec;
-    double sq = 0.0;
+    float sq = 0.0f;
     int nf = 0;
     if (i < __ldg(a.bucket_offset + b + 1)) {
         float coef = 1.0f;
@@ -922,7 +922,7 @@ __global__ void __launch_bounds__(kChunkThreads) k_rs_adam_chunk(const __grid_co
             tsq = fmaf(g[j], g[j], tsq);
             nf += (__float_as_uint(g[j]) & 0x7F800000u) == 0x7F800000u;
         }
-        sq = double(tsq);
+        sq = tsq;
         st_f8(a.master + i, w);
         st_f8(a.m + i, m);
         st_f8(a.v + i, v);
@@ -938,15 +938,13 @@ __global__ void __launch_bounds__(kChunkThreads) k_rs_adam_chunk(const __grid_co
     if (a.chunk_sq != nullptr) {                          // uniform over the launch
         // a warp's 256 squares summed in fp32 (relative error ~1e-7), the
         // CTA's four warps and the bucket's chunks in double
-        float fs = float(sq);
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) fs += __shfl_xor_sync(0xFFFFFFFFu, fs, o);
-        sq = fs;
+        for (int o = 16; o > 0; o >>= 1) sq += __shfl_xor_sync(0xFFFFFFFFu, sq, o);
         nf = __reduce_add_sync(0xFFFFFFFFu, nf);
         __shared__ double w_sq[kChunkThreads / 32];
         __shared__ int w_nf[kChunkThreads / 32];
         if ((threadIdx.x & 31) == 0) {
-            w_sq[threadIdx.x >> 5] = sq;
+            w_sq[threadIdx.x >> 5] = double(sq);
             w_nf[threadIdx.x >> 5] = nf;
         }
         __syncthreads();
@@ -1747,6 +1745,18 @@ static int step_clipped(const dpg_plan_t* plan, const void* const* grads, int32_
     // pass 2: g * coef -> Adam -> bf16 views, from the stored g or the replicas again
     RsAdamArgs a2 = a;
     a2.clip_coef = p.d_clip_coef;
+    if (t_fused_max_ctas == 0) {
+        RsKernel fc;
+        if (reduced) {
+            a2.g_in = reduced;
+            fc = k_rs_adam_chunk<1, kInReduced, kUpdate>;
+        } else {
+            fc = mode == kInBf16 ? pick_chunk_kernel<kInBf16, kUpdate>(p.R)
+               : mode == kInF32  ? pick_chunk_kernel<kInF32, kUpdate>(p.R)
+                                 : pick_chunk_kernel<kInF32PlusBf16, kUpdate>(p.R);
+        }
+        return launch_chunked(fc, a2, p, false, nullptr, nullptr, s, who);
+    }
     RsKernel fn2;
     if (reduced) {
         a2.g_in = reduced;
