@@ -1236,6 +1236,17 @@ static int sm_count(int dev, int* out) {
     return DPG_OK;
 }
 
+// One CTA per `work_ctas` unit of work: the streaming kernels (accumulate,
+// all-gather, gathers, pack, state copy) keep more bytes in flight with many
+// short CTAs, several resident per SM at different points of their loads and
+// stores, than with a resident-sized grid that strides over the work.
+static int grid_cover(int64_t work_ctas, int* grid, const char* who) {
+    if (work_ctas > 0x7FFFFFFF)
+        return fail(DPG_ERR_INVALID_ARG, "%s: %lld CTAs in one launch", who, (long long)work_ctas);
+    *grid = int(work_ctas > 0 ? work_ctas : 1);
+    return DPG_OK;
+}
+
 // persistent-grid size: SM count x resident CTAs of `fn` (cached per device)
 static int grid_for(const void* fn, int threads, int dev, int64_t work_ctas, int* grid) {
     static std::mutex mu;
@@ -2125,12 +2136,8 @@ int dpg_accumulate(const dpg_plan_t* plan, const void* flat_bf16, float* acc_f32
     dpg::Plan& p = const_cast<dpg_plan_t*>(plan)->p;
     const int64_t n_vec = p.total_padded / dpg::kVec;
     if (n_vec == 0) return DPG_OK;
-    int dev = 0;
-    DPG_CUDA_TRY(cudaGetDevice(&dev));
-    const void* fn = first ? reinterpret_cast<const void*>(dpg::k_accumulate<true>)
-                           : reinterpret_cast<const void*>(dpg::k_accumulate<false>);
     int grid = 0;
-    int st = dpg::grid_for(fn, 256, dev, (n_vec + 255) / 256, &grid);
+    int st = dpg::grid_cover((n_vec + 255) / 256, &grid, "dpg_accumulate");
     if (st != DPG_OK) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const uint16_t* g = static_cast<const uint16_t*>(flat_bf16);
@@ -2151,12 +2158,8 @@ int dpg_accumulate_pair(const dpg_plan_t* plan, const void* micro_a_bf16, const 
         return fail(DPG_ERR_MISALIGNED, "dpg_accumulate_pair: misaligned buffer");
     const dpg::Plan& p = plan->p;
     const int64_t n_vec = p.total_padded / dpg::kVec;
-    int dev = 0;
-    DPG_CUDA_TRY(cudaGetDevice(&dev));
-    const void* fn = first ? reinterpret_cast<const void*>(dpg::k_accumulate_pair<true>)
-                           : reinterpret_cast<const void*>(dpg::k_accumulate_pair<false>);
     int grid = 0;
-    int st = dpg::grid_for(fn, 256, dev, (n_vec + 255) / 256, &grid);
+    int st = dpg::grid_cover((n_vec + 255) / 256, &grid, "dpg_accumulate_pair");
     if (st != DPG_OK) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const uint16_t* ga = static_cast<const uint16_t*>(micro_a_bf16);
@@ -2209,11 +2212,8 @@ int dpg_allgather_params(const dpg_plan_t* plan, const float* master, void* cons
     }
     const int64_t lo = p.bucket_offset[b0] / dpg::kVec, hi = p.bucket_offset[b1] / dpg::kVec;
     if (hi <= lo || n_views == 0) return DPG_OK;
-    int dev = 0;
-    DPG_CUDA_TRY(cudaGetDevice(&dev));
     int grid = 0;
-    int st = dpg::grid_for(reinterpret_cast<const void*>(dpg::k_allgather), 256, dev,
-                           (hi - lo + 255) / 256, &grid);
+    int st = dpg::grid_cover((hi - lo + 255) / 256, &grid, "dpg_allgather_params");
     if (st != DPG_OK) return st;
     dpg::k_allgather<<<grid, 256, 0, static_cast<cudaStream_t>(stream)>>>(master, va, lo, hi);
     return dpg::after_launch("dpg_allgather_params");
@@ -2245,11 +2245,8 @@ int dpg_gather_params_bf16(const dpg_plan_t* plan, const void* param_bf16, void*
         va.views[k] = views[k];
     }
     const int64_t lo = p.bucket_offset[b0] / dpg::kVec, hi = p.bucket_offset[b1] / dpg::kVec;
-    int dev = 0;
-    DPG_CUDA_TRY(cudaGetDevice(&dev));
     int grid = 0;
-    int st = dpg::grid_for(reinterpret_cast<const void*>(dpg::k_gather_bf16), 256, dev,
-                           (hi - lo + 255) / 256, &grid);
+    int st = dpg::grid_cover((hi - lo + 255) / 256, &grid, "dpg_gather_params_bf16");
     if (st != DPG_OK) return st;
     dpg::k_gather_bf16<<<grid, 256, 0, static_cast<cudaStream_t>(stream)>>>(
         static_cast<const uint16_t*>(param_bf16), va, lo, hi);
@@ -2288,8 +2285,7 @@ static int pack_common(const dpg_plan_t* plan, const void* const* ptrs, void* fl
         a.flat = static_cast<uint16_t*>(flat);
         a.n_items = int64_t(i1 - i0);
         int grid = 0;
-        st = dpg::grid_for(reinterpret_cast<const void*>(dpg::k_pack), 256, p.device, a.n_items,
-                           &grid);
+        st = dpg::grid_cover(a.n_items, &grid, who);
         if (st != DPG_OK) return st;
         dpg::k_pack<<<grid, 256, 0, s>>>(a);
         st = dpg::after_launch(who);
@@ -2326,8 +2322,7 @@ static int state_common(const dpg_plan_t* plan, const float* const* src, float* 
     a.items = p.d_items;
     a.n_items = int64_t(p.items.size());
     int grid = 0;
-    st = dpg::grid_for(reinterpret_cast<const void*>(dpg::k_state_copy), 256, p.device, a.n_items,
-                       &grid);
+    st = dpg::grid_cover(a.n_items, &grid, who);
     if (st != DPG_OK) return st;
     dpg::k_state_copy<<<grid, 256, 0, static_cast<cudaStream_t>(stream)>>>(a);
     return dpg::after_launch(who);
