@@ -142,7 +142,7 @@ def test_multi_step_trajectory():
 def test_pack_unpack_bit_exact(seed):
     rng = np.random.Generator(np.random.Philox(300 + seed))
     numels = random_param_list(rng, int(rng.integers(1, 300)), 20_000)
-    numels[0] = 3 * 32768 + 5           # several pack items (32768 elements each) for one parameter
+    numels[0] = 3 * 65536 + 5           # several pack items (65536 elements each) for one parameter
     R = int(rng.choice([1, 2, 4, 8]))
     cap = int(rng.integers(64, 1 << 17))
     plan = dpg.dpg_plan_buckets(numels, cap, R)

@@ -37,7 +37,7 @@ constexpr int64_t kTile = int64_t(kThreads) * kVec;
 // Pack/unpack work is cut into items of at most kPackChunk elements; one CTA
 // copies one item.  kPackPtrs parameter pointers travel in one launch's
 // argument block.
-constexpr int64_t kPackChunk = 32768;
+constexpr int64_t kPackChunk = 65536;
 constexpr int kPackPtrs = 1024;
 
 struct PackItem {
