@@ -364,7 +364,9 @@ int dpg_check_device_status(const dpg_plan_t* plan, void* stream);
  * budget), or that cannot accept the implicit synchronisation of
  * cudaMalloc/cudaFree in the middle of a training step.
  *
- * Same arguments, semantics and results as dpg_step.  Instead of the plan's
+ * Same arguments, semantics and results as dpg_step (it runs the persistent
+ * grid-stride form of the fused pass, so its per-bucket norms are summed in
+ * another grouping, within their tolerance).  Instead of the plan's
  * device copy and norm scratch (which dpg_step allocates on first use), it
  * uses one static device array of DPG_NOALLOC_SCRATCH_BYTES compiled into the
  * library, which every GPU that loads the library holds until the process
