@@ -884,9 +884,52 @@ constexpr int kChunkThreads = 128;
 constexpr int kChunk = kChunkThreads * kVec;
 constexpr int kChunksPerTile = int(kTile / kChunk);
 
+// Adam on one 8-element vector of the chunked pass: s is the rank-ordered
+// sum; adds the vector's squares and non-finite count to sq / nf.
+template <int MODE, int PHASE>
+__device__ __forceinline__ void adam_vector(const RsAdamArgs& a, int64_t i, const float* s,
+                                            float coef, float& sq, int& nf) {
+    F8 w = ld_state_f8(a.master + i);
+    F8 m = ld_state_f8(a.m + i);
+    F8 v = ld_state_f8(a.v + i);
+    float g[8];
+    float tsq = 0.0f;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        g[j] = MODE == kInReduced ? s[j] : __fmul_rn(s[j], a.scale);
+        if constexpr (PHASE == kUpdate) g[j] = __fmul_rn(g[j], coef);
+        float wj = w.v[j];
+        if (a.decay) wj = __fsub_rn(wj, __fmul_rn(a.lr_wd, wj));
+        const float mj = __fadd_rn(__fmul_rn(a.beta1, m.v[j]), __fmul_rn(a.omb1, g[j]));
+        const float vj = __fadd_rn(__fmul_rn(a.beta2, v.v[j]),
+                                   __fmul_rn(a.omb2, __fmul_rn(g[j], g[j])));
+        const float m_hat = __fdiv_rn(mj, a.bias1);
+        const float v_hat = __fdiv_rn(vj, a.bias2);
+        const float u = __fdiv_rn(m_hat, __fadd_rn(__fsqrt_rn(v_hat), a.eps));
+        w.v[j] = __fsub_rn(wj, __fmul_rn(a.lr, u));
+        m.v[j] = mj;
+        v.v[j] = vj;
+        tsq = fmaf(g[j], g[j], tsq);
+        nf += (__float_as_uint(g[j]) & 0x7F800000u) == 0x7F800000u;
+    }
+    sq = tsq;
+    st_f8(a.master + i, w);
+    st_f8(a.m + i, m);
+    st_f8(a.v + i, v);
+    const uint4 p = narrow8(w.v);
+    for (int k = 0; k < a.n_views; ++k) st_u4(static_cast<uint16_t*>(a.views[k]) + i, p);
+    if (PHASE == kFull && a.reduced) {
+        F8 gg;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) gg.v[j] = g[j];
+        st_f8(a.reduced + i, gg);
+    }
+}
+
 template <int RT, int MODE, int PHASE>
 __global__ void __launch_bounds__(kChunkThreads) k_rs_adam_chunk(const __grid_constant__ RsAdamArgs a) {
-    static_assert(PHASE != kNormOnly, "the norm pass is k_norm_pass");
+    // kNormOnly: reduce and scale only -- g to a.reduced, norm partials, no
+    // Adam (the all-reduce of the DDP schedule)
     const int64_t c = blockIdx.x;                         // chunk of this launch
     const int64_t t = a.t0 + c / kChunksPerTile;
     const int b = __ldg(a.tile_bucket + t);
@@ -899,40 +942,19 @@ __global__ void __launch_bounds__(kChunkThreads) k_rs_adam_chunk(const __grid_co
         if constexpr (PHASE == kUpdate) coef = __ldg(a.clip_coef);
         float s[8];
         reduce_vector<RT, MODE>(a, i, s);
-        F8 w = ld_state_f8(a.master + i);
-        F8 m = ld_state_f8(a.m + i);
-        F8 v = ld_state_f8(a.v + i);
-        float g[8];
-        float tsq = 0.0f;
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            g[j] = MODE == kInReduced ? s[j] : __fmul_rn(s[j], a.scale);
-            if constexpr (PHASE == kUpdate) g[j] = __fmul_rn(g[j], coef);
-            float wj = w.v[j];
-            if (a.decay) wj = __fsub_rn(wj, __fmul_rn(a.lr_wd, wj));
-            const float mj = __fadd_rn(__fmul_rn(a.beta1, m.v[j]), __fmul_rn(a.omb1, g[j]));
-            const float vj = __fadd_rn(__fmul_rn(a.beta2, v.v[j]),
-                                       __fmul_rn(a.omb2, __fmul_rn(g[j], g[j])));
-            const float m_hat = __fdiv_rn(mj, a.bias1);
-            const float v_hat = __fdiv_rn(vj, a.bias2);
-            const float u = __fdiv_rn(m_hat, __fadd_rn(__fsqrt_rn(v_hat), a.eps));
-            w.v[j] = __fsub_rn(wj, __fmul_rn(a.lr, u));
-            m.v[j] = mj;
-            v.v[j] = vj;
-            tsq = fmaf(g[j], g[j], tsq);
-            nf += (__float_as_uint(g[j]) & 0x7F800000u) == 0x7F800000u;
-        }
-        sq = tsq;
-        st_f8(a.master + i, w);
-        st_f8(a.m + i, m);
-        st_f8(a.v + i, v);
-        const uint4 p = narrow8(w.v);
-        for (int k = 0; k < a.n_views; ++k) st_u4(static_cast<uint16_t*>(a.views[k]) + i, p);
-        if (PHASE == kFull && a.reduced) {
+        if constexpr (PHASE == kNormOnly) {
             F8 gg;
+            float tsq = 0.0f;
 #pragma unroll
-            for (int j = 0; j < 8; ++j) gg.v[j] = g[j];
+            for (int j = 0; j < 8; ++j) {
+                gg.v[j] = __fmul_rn(s[j], a.scale);
+                tsq = fmaf(gg.v[j], gg.v[j], tsq);
+                nf += (__float_as_uint(gg.v[j]) & 0x7F800000u) == 0x7F800000u;
+            }
+            sq = tsq;
             st_f8(a.reduced + i, gg);
+        } else {
+            adam_vector<MODE, PHASE>(a, i, s, coef, sq, nf);
         }
     }
     if (a.chunk_sq != nullptr) {                          // uniform over the launch
@@ -1831,6 +1853,13 @@ static int allreduce_grads(const dpg_plan_t* plan, const void* const* grads, int
     a.b1 = b1;
     a.R = p.R;
     const int mode = grads_dtype == DPG_BF16 ? kInBf16 : (last ? kInF32PlusBf16 : kInF32);
+    if (t_fused_max_ctas == 0 && has_elems) {
+        RsKernel fc = mode == kInBf16 ? pick_chunk_kernel<kInBf16, kNormOnly>(p.R)
+                    : mode == kInF32  ? pick_chunk_kernel<kInF32, kNormOnly>(p.R)
+                                      : pick_chunk_kernel<kInF32PlusBf16, kNormOnly>(p.R);
+        return launch_chunked(fc, a, p, want_norm, sqnorm, nonfinite,
+                              static_cast<cudaStream_t>(stream), who);
+    }
     RsKernel fn = pick_norm_kernel(mode, p.R);
     int grid = 0;
     st = fused_geometry(fn, p.device, a.t0, a.t1, b0, b1, &grid, &a.vmax);
