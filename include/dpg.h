@@ -396,14 +396,16 @@ int dpg_step_noalloc(const dpg_plan_t* plan, const void* const* grads, int32_t g
 
 /* Launch shape -------------------------------------------------------------- */
 /* By default the fused passes (dpg_step, dpg_reduce_scatter_adam,
- * dpg_step_fold2, dpg_adam_from_reduced, dpg_allreduce_grads and the update
- * pass of dpg_step_clipped) launch one small CTA per 1024-element chunk, which keeps
+ * dpg_step_fold2, dpg_adam_from_reduced, dpg_allreduce_grads and
+ * dpg_step_clipped -- whose norm pass stays on the persistent grid when it
+ * only re-reads R <= 4 replicas) launch one small CTA per 1024-element chunk,
+ * which keeps
  * the most bytes in flight.  max_ctas > 0 makes later launches from the
  * CALLING THREAD use instead a persistent grid of at most max_ctas CTAs
  * (grid-stride over 4096-element tiles), leaving SMs free for work running
- * concurrently on other streams at the cost of the pass's own bandwidth; the
- * clipped step's norm pass and dpg_step_noalloc always use the persistent
- * grid and honour the bound too.  0 restores the default.
+ * concurrently on other streams at the cost of the pass's own bandwidth;
+ * dpg_step_noalloc always uses the persistent grid and honours the bound
+ * too.  0 restores the default.
  * Results are the same bits for any launch shape; only the per-bucket norms'
  * summation grouping changes (within their documented tolerance).
  * Negative: DPG_ERR_INVALID_ARG. */

@@ -131,3 +131,20 @@ def test_no_clip_equals_dpg_step():
     for k in ("w", "m", "v"):
         np.testing.assert_array_equal(a[k].view(np.uint32), b[k].view(np.uint32))
     np.testing.assert_array_equal(a["p"], b["p"])
+
+
+@pytest.mark.parametrize("name", ["R8_clip_stored_g", "R4_acc_K3_clip_warm"])
+def test_clipped_step_parity_on_the_persistent_grid(name):
+    """With a grid cap the clipped step runs its persistent norm and update
+    passes; the coefficient and every output are the oracle's as before."""
+    c = CASES[name]
+    dpg.dpg_set_fused_max_ctas(40)
+    try:
+        got, ref = _run(c)
+    finally:
+        dpg.dpg_set_fused_max_ctas(0)
+    assert got["clip"][1] == ref["coef"]
+    for k in ("w", "m", "v"):
+        assert ulp_f32(got[k], ref[k]) <= F32_ULP, k
+    assert ulp_bf16(got["p"], ref["p"]) <= BF16_ULP
+    check_norms(got["sq"], ref["sq"])

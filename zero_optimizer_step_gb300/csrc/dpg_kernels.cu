@@ -984,6 +984,66 @@ __global__ void __launch_bounds__(kChunkThreads) k_rs_adam_chunk(const __grid_co
     }
 }
 
+// Chunked norm pass of the clipped step: reduce, scale, optionally store g,
+// and sum the squares near-exactly (fp32 double-float per thread, see
+// two_sum_square), one double partial per chunk.  The warps combine their
+// double-float pairs with fp32 TwoSum; the rare binary64 term (huge or
+// non-finite values) is combined only when some lane of the warp has one, so
+// the per-element path issues no binary64 instruction.
+template <int RT, int MODE, int NT>
+__global__ void __launch_bounds__(NT) k_norm_chunk(const __grid_constant__ RsAdamArgs a) {
+    constexpr int CH = NT * kVec;                         // elements per chunk
+    constexpr int CPT = int(kTile / CH);
+    static_assert(CPT >= 1 && CPT * CH == kTile, "a tile holds a whole number of chunks");
+    const int64_t c = blockIdx.x;
+    const int64_t t = a.t0 + c / CPT;
+    const int b = __ldg(a.tile_bucket + t);
+    const int64_t i = __ldg(a.bucket_offset + b) + (t - __ldg(a.tile_begin + b)) * kTile +
+                      (c % CPT) * CH + int64_t(threadIdx.x) * kVec;
+    const bool norm = a.chunk_sq != nullptr;
+    NormAcc acc;
+    int nf = 0;
+    if (i < __ldg(a.bucket_offset + b + 1)) {
+        float s[8];
+        reduce_vector<RT, MODE>(a, i, s);
+        norm_vector(a, i, s, acc, nf, norm);
+    }
+    if (!norm) return;                                    // uniform over the launch
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const float ohi = __shfl_xor_sync(0xFFFFFFFFu, acc.hi, o);
+        const float olo = __shfl_xor_sync(0xFFFFFFFFu, acc.lo, o);
+        const float sh = __fadd_rn(acc.hi, ohi);
+        const float bp = __fsub_rn(sh, acc.hi);
+        const float err = __fadd_rn(__fsub_rn(acc.hi, __fsub_rn(sh, bp)), __fsub_rn(ohi, bp));
+        acc.hi = sh;
+        acc.lo = __fadd_rn(__fadd_rn(acc.lo, olo), err);
+    }
+    if (__any_sync(0xFFFFFFFFu, acc.big != 0.0)) {
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) acc.big += __shfl_xor_sync(0xFFFFFFFFu, acc.big, o);
+    }
+    nf = __reduce_add_sync(0xFFFFFFFFu, nf);
+    __shared__ double w_sq[NT / 32];
+    __shared__ int w_nf[NT / 32];
+    if ((threadIdx.x & 31) == 0) {
+        w_sq[threadIdx.x >> 5] = acc.value();
+        w_nf[threadIdx.x >> 5] = nf;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        double tot = 0.0;
+        int cnt = 0;
+#pragma unroll
+        for (int k = 0; k < NT / 32; ++k) {
+            tot += w_sq[k];
+            cnt += w_nf[k];
+        }
+        a.chunk_sq[c] = tot;
+        a.chunk_nf[c] = cnt;
+    }
+}
+
 // One CTA per bucket of a chunked launch starting at tile t0.  A bucket of a
 // large plan has 10^5 chunk partials and there are only tens of buckets, so
 // each thread keeps 8 loads in flight: thread j adds chunks j + 1024 k in
@@ -993,14 +1053,14 @@ constexpr int kChunkFinalizeThreads = 1024;
 
 __global__ void __launch_bounds__(kChunkFinalizeThreads)
 k_chunk_finalize(const double* __restrict__ chunk_sq, const int32_t* __restrict__ chunk_nf,
-                 const int64_t* __restrict__ tile_begin, int64_t t0, int32_t b0, float* sqnorm,
-                 int64_t* nonfinite, double* sqnorm64) {
+                 const int64_t* __restrict__ tile_begin, int64_t t0, int32_t cpt, int32_t b0,
+                 float* sqnorm, int64_t* nonfinite, double* sqnorm64) {
     constexpr int T = kChunkFinalizeThreads, U = 8;
     __shared__ double s_sq[T];
     __shared__ long long s_nf[T];
     const int b = b0 + blockIdx.x;
-    const int64_t c0 = (__ldg(tile_begin + b) - t0) * kChunksPerTile;
-    const int64_t c1 = (__ldg(tile_begin + b + 1) - t0) * kChunksPerTile;
+    const int64_t c0 = (__ldg(tile_begin + b) - t0) * cpt;
+    const int64_t c1 = (__ldg(tile_begin + b + 1) - t0) * cpt;
     double acc = 0.0;
     long long cnt = 0;
     for (int64_t c = c0 + threadIdx.x; c < c1; c += int64_t(T) * U) {
@@ -1542,15 +1602,31 @@ static RsKernel pick_chunk_kernel(int R) {
     }
 }
 
+// CTA size of the chunked norm pass (128, 256 and 512 threads measured; the
+// smallest is fastest, as for the fused pass).
+constexpr int kNormChunkThreads = 128;
+
+template <int MODE>
+static RsKernel pick_norm_chunk_kernel(int R) {
+    switch (R) {
+        case 1: return k_norm_chunk<1, MODE, kNormChunkThreads>;
+        case 2: return k_norm_chunk<2, MODE, kNormChunkThreads>;
+        case 4: return k_norm_chunk<4, MODE, kNormChunkThreads>;
+        case 8: return k_norm_chunk<8, MODE, kNormChunkThreads>;
+        default: return k_norm_chunk<0, MODE, kNormChunkThreads>;
+    }
+}
+
 // Chunked launch of the fused pass over tiles [a.t0, a.t1) (tables already in
 // `a`), then, when a norm output is requested, the per-bucket finalize.
 static int launch_chunked(RsKernel fn, RsAdamArgs a, const Plan& p, bool want_norm, float* sqnorm,
                           int64_t* nonfinite, cudaStream_t s, const char* who,
-                          double* sqnorm64 = nullptr) {
+                          double* sqnorm64 = nullptr, int threads = kChunkThreads) {
+    const int cpt = int(kTile / (int64_t(threads) * kVec));   // chunks per tile
     a.tile_bucket = p.d_tile_bucket;
     a.chunk_sq = want_norm ? p.d_chunk_sq : nullptr;
     a.chunk_nf = want_norm ? p.d_chunk_nf : nullptr;
-    const int64_t n_chunks = (a.t1 - a.t0) * kChunksPerTile;
+    const int64_t n_chunks = (a.t1 - a.t0) * cpt;
     if (n_chunks > 0x7FFFFFFF) return fail(DPG_ERR_INVALID_ARG, "%s: %lld chunks in one launch", who,
                                            (long long)n_chunks);
     int st = DPG_OK;
@@ -1558,14 +1634,14 @@ static int launch_chunked(RsKernel fn, RsAdamArgs a, const Plan& p, bool want_no
         cudaEvent_t ev0 = t_fused_start, ev1 = t_fused_stop;
         t_fused_start = t_fused_stop = nullptr;
         if (ev0) DPG_CUDA_TRY(cudaEventRecord(ev0, s));
-        fn<<<unsigned(n_chunks), kChunkThreads, 0, s>>>(a);
+        fn<<<unsigned(n_chunks), threads, 0, s>>>(a);
         st = after_launch(who);
         if (st != DPG_OK) return st;
         if (ev1) DPG_CUDA_TRY(cudaEventRecord(ev1, s));
     }
     if (want_norm) {
         k_chunk_finalize<<<a.b1 - a.b0, kChunkFinalizeThreads, 0, s>>>(
-            p.d_chunk_sq, p.d_chunk_nf, p.d_tile_begin, a.t0, a.b0, sqnorm, nonfinite, sqnorm64);
+            p.d_chunk_sq, p.d_chunk_nf, p.d_tile_begin, a.t0, cpt, a.b0, sqnorm, nonfinite, sqnorm64);
         st = after_launch(who);
     }
     return st;
@@ -1751,25 +1827,38 @@ static int step_clipped(const dpg_plan_t* plan, const void* const* grads, int32_
     // pass 1: reduce, scale, exact squares per bucket (and g, when a buffer is given)
     RsAdamArgs a1 = a;
     a1.reduced = reduced;
-    RsKernel fn1 = pick_norm_kernel(mode, p.R);
-    int grid1 = 0;
-    st = fused_geometry(fn1, p.device, a1.t0, a1.t1, 0, p.n_buckets, &grid1, &a1.vmax);
-    if (st != DPG_OK) return st;
-    if (grid1 > p.cap_ctas || int64_t(grid1) * a1.vmax > p.cap_visits)
-        return fail(DPG_ERR_CUDA, "%s: norm scratch too small", who);
-    a1.vis_sq = p.d_vis_sq;
-    a1.vis_nf = p.d_vis_nf;
-    a1.vis_bucket = p.d_vis_bucket;
-    a1.vis_count = p.d_vis_count;
-    if (a1.t1 > a1.t0) {
-        fn1<<<grid1, kThreads, 0, s>>>(a1);
-        st = after_launch(who);
+    // Chunked unless a grid cap is set -- or when the pass only reads the
+    // replicas (no g stored) and R <= 4: then it moves just 2R bytes per
+    // element, and the persistent pass, which keeps up to four tiles' loads
+    // in flight per thread, is faster (4.5B, R = 4: 27.3 against 28.5 ms
+    // for the whole step).
+    if (t_fused_max_ctas == 0 && (reduced != nullptr || p.R >= 8)) {
+        RsKernel fc1 = mode == kInBf16 ? pick_norm_chunk_kernel<kInBf16>(p.R)
+                     : mode == kInF32  ? pick_norm_chunk_kernel<kInF32>(p.R)
+                                       : pick_norm_chunk_kernel<kInF32PlusBf16>(p.R);
+        st = launch_chunked(fc1, a1, p, true, sqnorm, nonfinite, s, who, p.d_bucket_sq64,
+                            kNormChunkThreads);
+    } else {   // the persistent norm pass
+        RsKernel fn1 = pick_norm_kernel(mode, p.R);
+        int grid1 = 0;
+        st = fused_geometry(fn1, p.device, a1.t0, a1.t1, 0, p.n_buckets, &grid1, &a1.vmax);
         if (st != DPG_OK) return st;
+        if (grid1 > p.cap_ctas || int64_t(grid1) * a1.vmax > p.cap_visits)
+            return fail(DPG_ERR_CUDA, "%s: norm scratch too small", who);
+        a1.vis_sq = p.d_vis_sq;
+        a1.vis_nf = p.d_vis_nf;
+        a1.vis_bucket = p.d_vis_bucket;
+        a1.vis_count = p.d_vis_count;
+        if (a1.t1 > a1.t0) {
+            fn1<<<grid1, kThreads, 0, s>>>(a1);
+            st = after_launch(who);
+            if (st != DPG_OK) return st;
+        }
+        k_norm_finalize<<<p.n_buckets, kFinalizeThreads, 0, s>>>(
+            a1.vis_sq, a1.vis_nf, a1.vis_bucket, a1.vis_count, a1.t1 > a1.t0 ? grid1 : 0, a1.vmax, 0,
+            sqnorm, nonfinite, p.d_bucket_sq64);
+        st = after_launch(who);
     }
-    k_norm_finalize<<<p.n_buckets, kFinalizeThreads, 0, s>>>(
-        a1.vis_sq, a1.vis_nf, a1.vis_bucket, a1.vis_count, a1.t1 > a1.t0 ? grid1 : 0, a1.vmax, 0,
-        sqnorm, nonfinite, p.d_bucket_sq64);
-    st = after_launch(who);
     if (st != DPG_OK) return st;
     // the coefficient, on the device: no host synchronisation
     k_clip_coef<<<1, 256, 0, s>>>(p.d_bucket_sq64, p.n_buckets, max_norm, p.d_clip_coef, clip_out);
