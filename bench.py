@@ -39,7 +39,8 @@ from workloads import (CONFIGS, KIND_GRAD, KIND_MASTER, flat_grads_bf16, master_
                        segments, stream_seed, token_counts)
 
 KERNEL_SRCS = [os.path.join(ROOT, "zero_optimizer_step_gb300", "csrc", f)
-               for f in ("dpg_kernels.cu", "dpg_internal.h")]
+               for f in ("dpg_device.cuh", "dpg_fused.cu", "dpg_host.h", "dpg_internal.h",
+                         "dpg_runtime.cu", "dpg_staged.cu", "dpg_stream.cu")]
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
 PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
 FALLBACK_HBM_GBS = 6800.0
@@ -363,7 +364,7 @@ def write_traffic(a):
         "R": cfg.R, "K": cfg.K, "elements": cfg.psi,
         "dram_bytes_read": rd, "dram_bytes_write": wr, "dram_bytes_per_launch": rd + wr,
         "launches": len(launches), "source_sha256": kernel_source_sha256(),
-        "hash": "sha256 of dpg_kernels.cu + dpg_internal.h with comments and whitespace removed",
+        "hash": "sha256 of the library's CUDA sources and headers with comments and whitespace removed",
         "how": "ncu --metrics gpu__time_duration.sum,dram__bytes_read.sum,dram__bytes_write.sum "
                "--clock-control none -k regex:\"k_rs_adam|finalize\" on python bench.py "
                "--no-e2e --no-cpu-baseline (one pass, full-size workload); mean per launch"}}

@@ -40,8 +40,8 @@ def sources():
 
 
 def _inputs():
-    return sources() + glob.glob(os.path.join(CSRC, "*.h")) + [os.path.join(INCLUDE, "dpg.h"),
-                                                               os.path.abspath(__file__)]
+    return (sources() + glob.glob(os.path.join(CSRC, "*.h")) + glob.glob(os.path.join(CSRC, "*.cuh"))
+            + [os.path.join(INCLUDE, "dpg.h"), os.path.abspath(__file__)])
 
 
 def up_to_date() -> bool:

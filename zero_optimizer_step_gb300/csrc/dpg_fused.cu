@@ -1,0 +1,1346 @@
+// dpg_fused.cu -- the fused reduce-scatter + normalisation + Adam + bf16
+// all-gather pass and its variants: the chunked kernels (one small CTA per
+// 1024-element chunk, the default), the persistent grid-stride kernels (a
+// grid cap, the allocation-free step, the clipped norm pass over R <= 4
+// re-read replicas), the clipped step's norm pass, the per-bucket norm
+// finalizes, and their C entry points.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <map>
+#include <mutex>
+
+#include "dpg_host.h"
+
+namespace dpg {
+
+template <int RT, int MODE, int PHASE>
+__global__ void __launch_bounds__(kThreads, 1) k_rs_adam(const __grid_constant__ RsAdamArgs a) {
+    static_assert(PHASE != kNormOnly, "the norm pass is k_norm_pass");
+    const bool norm = PHASE != kUpdate && a.vis_sq != nullptr;
+    float coef = 1.0f;
+    if constexpr (PHASE == kUpdate) coef = __ldg(a.clip_coef);
+    int b = a.b0;
+    int cur = -1;  // bucket of the running norm sums
+    int visit = 0;
+    double sq = 0.0;
+    int nf = 0;
+    // the current bucket's table entries, reloaded only when a tile leaves it
+    // (per-tile lookups were half of the load requests of the lighter passes)
+    int64_t tb_lo = 0, tb_hi = -1, bo_lo = 0, bo_hi = 0;
+    for (int64_t t = a.t0 + blockIdx.x; t < a.t1; t += gridDim.x) {
+        if (t >= tb_hi) {                                   // CTA-uniform
+            b = bucket_of_tile(a.tile_begin, b, a.b1, t);
+            tb_lo = __ldg(a.tile_begin + b);
+            tb_hi = __ldg(a.tile_begin + b + 1);
+            bo_lo = __ldg(a.bucket_offset + b);
+            bo_hi = __ldg(a.bucket_offset + b + 1);
+        }
+        if (norm && b != cur) {
+            if (cur >= 0) flush_visit(a, cur, visit++, sq, nf);
+            cur = b;
+            sq = 0.0;
+            nf = 0;
+        }
+        const int64_t bucket_end = bo_hi;
+        const int64_t i = bo_lo + (t - tb_lo) * kTile + int64_t(threadIdx.x) * kVec;
+        if (i < bucket_end) {
+            float s[8];
+            reduce_vector<RT, MODE>(a, i, s);
+            float g[8];
+            {
+                F8 w = ld_state_f8(a.master + i);
+                F8 m = ld_state_f8(a.m + i);
+                F8 v = ld_state_f8(a.v + i);
+                float tsq = 0.0f;
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    g[j] = MODE == kInReduced ? s[j] : __fmul_rn(s[j], a.scale);
+                    if constexpr (PHASE == kUpdate) g[j] = __fmul_rn(g[j], coef);
+                    float wj = w.v[j];
+                    if (a.decay) wj = __fsub_rn(wj, __fmul_rn(a.lr_wd, wj));
+                    const float mj = __fadd_rn(__fmul_rn(a.beta1, m.v[j]), __fmul_rn(a.omb1, g[j]));
+                    const float vj = __fadd_rn(__fmul_rn(a.beta2, v.v[j]),
+                                               __fmul_rn(a.omb2, __fmul_rn(g[j], g[j])));
+                    const float m_hat = __fdiv_rn(mj, a.bias1);
+                    const float v_hat = __fdiv_rn(vj, a.bias2);
+                    const float u = __fdiv_rn(m_hat, __fadd_rn(__fsqrt_rn(v_hat), a.eps));
+                    w.v[j] = __fsub_rn(wj, __fmul_rn(a.lr, u));
+                    m.v[j] = mj;
+                    v.v[j] = vj;
+                    tsq = fmaf(g[j], g[j], tsq);
+                    nf += (__float_as_uint(g[j]) & 0x7F800000u) == 0x7F800000u;
+                }
+                if (norm) sq += double(tsq);
+                st_f8(a.master + i, w);
+                st_f8(a.m + i, m);
+                st_f8(a.v + i, v);
+                const uint4 p = narrow8(w.v);
+                for (int k = 0; k < a.n_views; ++k) st_u4(static_cast<uint16_t*>(a.views[k]) + i, p);
+                if (PHASE == kFull && a.reduced) {
+                    F8 gg;
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) gg.v[j] = g[j];
+                    st_f8(a.reduced + i, gg);
+                }
+            }
+        }
+    }
+    if (norm) {
+        if (cur >= 0) flush_visit(a, cur, visit++, sq, nf);
+        if (threadIdx.x == 0) a.vis_count[blockIdx.x] = visit;
+    }
+}
+
+
+// ---------------------------------------------------------------------------
+// Norm pass of the clipped step: reduce, scale, squares per bucket visit, and
+// optionally store g.  It moves only 2R (+4) bytes per element, so each
+// iteration handles two tiles (t and t + grid) with the loads of both in
+// flight before either is summed; the tile order, and with it the visits, is
+// that of the single-tile loop.
+// ---------------------------------------------------------------------------
+template <int RT, int MODE> struct Raw;
+template <int RT> struct Raw<RT, kInBf16> { uint4 x[RT]; };
+template <int RT> struct Raw<RT, kInF32> { F8 x[RT]; };
+template <int RT> struct Raw<RT, kInF32PlusBf16> { F8 x[RT]; uint4 l[RT]; };
+
+template <int RT, int MODE>
+__device__ __forceinline__ void load_raw(const RsAdamArgs& a, int64_t i, Raw<RT, MODE>& raw) {
+#pragma unroll
+    for (int r = 0; r < RT; ++r) {
+        if constexpr (MODE == kInBf16) {
+            raw.x[r] = ld_grad_u4(static_cast<const uint16_t*>(a.grads[r]) + i);
+        } else {
+            raw.x[r] = ld_grad_f8(static_cast<const float*>(a.grads[r]) + i);
+            if constexpr (MODE == kInF32PlusBf16)
+                raw.l[r] = ld_grad_u4(static_cast<const uint16_t*>(a.last[r]) + i);
+        }
+    }
+}
+
+// the same rank-ordered binary32 sum as reduce_vector
+template <int RT, int MODE>
+__device__ __forceinline__ void sum_raw(const Raw<RT, MODE>& raw, float* s) {
+#pragma unroll
+    for (int r = 0; r < RT; ++r) {
+        float x[8];
+        if constexpr (MODE == kInBf16) {
+            widen8(raw.x[r], x);
+        } else {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) x[j] = raw.x[r].v[j];
+            if constexpr (MODE == kInF32PlusBf16) {
+                float t[8];
+                widen8(raw.l[r], t);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) x[j] = __fadd_rn(x[j], t[j]);
+            }
+        }
+        if (r == 0) {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) s[j] = x[j];
+        } else {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) s[j] = __fadd_rn(s[j], x[j]);
+        }
+    }
+}
+
+// g = s * scale; its squares are added to a running double-float sum (hi, lo)
+// with binary32 operations only -- binary64 arithmetic is scarce on this GPU,
+// so the sum is widened to double once per bucket visit: p + e is g*g exactly
+// (FMA) and Knuth's TwoSum keeps the rounding error of hi in lo (about 2^-48
+// relative overall).  |g| >= 2^60, whose binary32 square would overflow, is
+// squared in binary64 (`big`).
+struct NormAcc {
+    float hi = 0.0f, lo = 0.0f;
+    double big = 0.0;
+    __device__ double value() const { return (double(hi) + double(lo)) + big; }
+};
+
+__device__ __forceinline__ void two_sum_square(NormAcc& acc, float x) {
+    const float p = __fmul_rn(x, x);
+    const float e = fmaf(x, x, -p);
+    const float t = __fadd_rn(acc.hi, p);
+    const float bp = __fsub_rn(t, acc.hi);
+    const float err = __fadd_rn(__fsub_rn(acc.hi, __fsub_rn(t, bp)), __fsub_rn(p, bp));
+    acc.hi = t;
+    acc.lo = __fadd_rn(acc.lo, __fadd_rn(err, e));
+}
+
+__device__ __forceinline__ void norm_vector(const RsAdamArgs& a, int64_t i, const float* s,
+                                            NormAcc& acc, int& nf, bool squares) {
+    float g[8];
+    bool rare = false;   // a huge or non-finite value in this vector
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        g[j] = __fmul_rn(s[j], a.scale);
+        rare |= !(fabsf(g[j]) < 0x1p60f);
+    }
+    if (!squares) {      // all-reduce only: no norm requested
+        if (a.reduced) {
+            F8 gg;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) gg.v[j] = g[j];
+            st_f8(a.reduced + i, gg);
+        }
+        return;
+    }
+    // a branch uniform over the active lanes (callers may be inside a partial
+    // tile's per-thread condition): the binary64 path must not be if-converted
+    // into predicated binary64 instructions issued for every element
+    if (__any_sync(__activemask(), rare)) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            if (fabsf(g[j]) < 0x1p60f) two_sum_square(acc, g[j]);
+            else acc.big += double(g[j]) * double(g[j]);
+            nf += (__float_as_uint(g[j]) & 0x7F800000u) == 0x7F800000u;
+        }
+    } else {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) two_sum_square(acc, g[j]);
+    }
+    if (a.reduced) {
+        F8 gg;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) gg.v[j] = g[j];
+        st_f8(a.reduced + i, gg);
+    }
+}
+
+// tiles per iteration of the norm pass: about 64 registers of loads in flight
+template <int RT, int MODE>
+constexpr int norm_tiles_per_iter() {
+    constexpr int regs = RT * (MODE == kInBf16 ? 4 : MODE == kInF32 ? 8 : 12);
+    return RT == 0 ? 1 : (64 / regs < 1 ? 1 : (64 / regs > 4 ? 4 : 64 / regs));
+}
+
+template <int RT, int MODE>
+__global__ void __launch_bounds__(kThreads, 1) k_norm_pass(const __grid_constant__ RsAdamArgs a) {
+    constexpr int TPI = norm_tiles_per_iter<RT, MODE>();
+    const bool norm = a.vis_sq != nullptr;
+    int b = a.b0, cur = -1, visit = 0;
+    NormAcc acc;
+    int nf = 0;
+    int64_t tb_lo = 0, tb_hi = -1, bo_lo = 0, bo_hi = 0;
+    const int64_t G = gridDim.x;
+    for (int64_t t = a.t0 + blockIdx.x; t < a.t1; t += TPI * G) {
+        int bu[TPI];
+        int64_t iu[TPI], eu[TPI];
+#pragma unroll
+        for (int u = 0; u < TPI; ++u) {
+            const int64_t tu = t + u * G;
+            bu[u] = -1;
+            iu[u] = 0;
+            eu[u] = 0;
+            if (tu < a.t1) {
+                if (tu >= tb_hi) {                      // CTA-uniform
+                    b = bucket_of_tile(a.tile_begin, b, a.b1, tu);
+                    tb_lo = __ldg(a.tile_begin + b);
+                    tb_hi = __ldg(a.tile_begin + b + 1);
+                    bo_lo = __ldg(a.bucket_offset + b);
+                    bo_hi = __ldg(a.bucket_offset + b + 1);
+                }
+                bu[u] = b;
+                eu[u] = bo_hi;
+                iu[u] = bo_lo + (tu - tb_lo) * kTile + int64_t(threadIdx.x) * kVec;
+            }
+        }
+        if constexpr (RT > 0) {
+            Raw<RT, MODE> raw[TPI];
+#pragma unroll
+            for (int u = 0; u < TPI; ++u)
+                if (iu[u] < eu[u]) load_raw<RT, MODE>(a, iu[u], raw[u]);
+#pragma unroll
+            for (int u = 0; u < TPI; ++u) {
+                if (bu[u] < 0) break;                   // past the end: CTA-uniform
+                if (norm && bu[u] != cur) {
+                    if (cur >= 0) flush_visit(a, cur, visit++, acc.value(), nf);
+                    cur = bu[u];
+                    acc = NormAcc();
+                    nf = 0;
+                }
+                if (iu[u] < eu[u]) {
+                    float su[8];
+                    sum_raw<RT, MODE>(raw[u], su);
+                    norm_vector(a, iu[u], su, acc, nf, norm);
+                }
+            }
+        } else {
+            if (norm && bu[0] != cur) {
+                if (cur >= 0) flush_visit(a, cur, visit++, acc.value(), nf);
+                cur = bu[0];
+                acc = NormAcc();
+                nf = 0;
+            }
+            if (iu[0] < eu[0]) {
+                float su[8];
+                reduce_vector<RT, MODE>(a, iu[0], su);
+                norm_vector(a, iu[0], su, acc, nf, norm);
+            }
+        }
+    }
+    if (norm) {
+        if (cur >= 0) flush_visit(a, cur, visit++, acc.value(), nf);
+        if (threadIdx.x == 0) a.vis_count[blockIdx.x] = visit;
+    }
+}
+
+// One CTA per bucket: thread c (and c + 256, ...) finds CTA c's visit of the
+// bucket by binary search in that CTA's visit list (its buckets increase) and
+// adds the visit's warp partials in warp order; the block then combines the
+// threads in a fixed tree.  The order depends only on the launch geometry, so
+// the norms are the same from run to run.
+constexpr int kFinalizeThreads = 256;
+
+__global__ void __launch_bounds__(kFinalizeThreads)
+k_norm_finalize(const double* __restrict__ vis_sq, const int32_t* __restrict__ vis_nf,
+                const int32_t* __restrict__ vis_bucket, const int32_t* __restrict__ vis_count,
+                int32_t n_cta, int32_t vmax, int32_t b0, float* sqnorm, int64_t* nonfinite,
+                double* sqnorm64) {
+    __shared__ double s_sq[kFinalizeThreads];
+    __shared__ long long s_nf[kFinalizeThreads];
+    const int b = b0 + blockIdx.x;
+    double acc = 0.0;
+    long long cnt = 0;
+    for (int c = threadIdx.x; c < n_cta; c += kFinalizeThreads) {
+        const int32_t* vb = vis_bucket + int64_t(c) * vmax;
+        const int n = vis_count[c];
+        int lo = 0, hi = n;
+        while (lo < hi) {
+            const int mid = (lo + hi) >> 1;
+            if (vb[mid] < b) lo = mid + 1;
+            else hi = mid;
+        }
+        if (lo < n && vb[lo] == b) {
+            const int64_t slot = (int64_t(c) * vmax + lo) * kWarps;
+            for (int w = 0; w < kWarps; ++w) {
+                acc += vis_sq[slot + w];
+                cnt += vis_nf[slot + w];
+            }
+        }
+    }
+    s_sq[threadIdx.x] = acc;
+    s_nf[threadIdx.x] = cnt;
+    __syncthreads();
+    for (int w = kFinalizeThreads / 2; w > 0; w >>= 1) {
+        if (threadIdx.x < w) {
+            s_sq[threadIdx.x] += s_sq[threadIdx.x + w];
+            s_nf[threadIdx.x] += s_nf[threadIdx.x + w];
+        }
+        __syncthreads();
+    }
+    if (threadIdx.x == 0) {
+        if (sqnorm) sqnorm[b] = float(s_sq[0]);
+        if (nonfinite) nonfinite[b] = s_nf[0];
+        if (sqnorm64) sqnorm64[b] = s_sq[0];
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Chunked launch of the fused pass: one 128-thread CTA per 1024-element chunk
+// (a quarter tile), one 8-element vector per thread, no grid-stride loop.  The
+// SM keeps several such CTAs resident at different points of their
+// load -> Adam -> store sequence, so DRAM stays busy while some of them do
+// arithmetic; a persistent CTA of 16 warps that load and compute in step
+// leaves it idle meanwhile.  Norms: each CTA writes one (sum of squares,
+// non-finite count) partial per chunk; k_chunk_finalize adds a bucket's
+// chunks in a fixed order.
+// ---------------------------------------------------------------------------
+
+// Adam on one 8-element vector of the chunked pass: s is the rank-ordered
+// sum; adds the vector's squares and non-finite count to sq / nf.
+template <int MODE, int PHASE>
+__device__ __forceinline__ void adam_vector(const RsAdamArgs& a, int64_t i, const float* s,
+                                            float coef, float& sq, int& nf) {
+    F8 w = ld_state_f8(a.master + i);
+    F8 m = ld_state_f8(a.m + i);
+    F8 v = ld_state_f8(a.v + i);
+    float g[8];
+    float tsq = 0.0f;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        g[j] = MODE == kInReduced ? s[j] : __fmul_rn(s[j], a.scale);
+        if constexpr (PHASE == kUpdate) g[j] = __fmul_rn(g[j], coef);
+        float wj = w.v[j];
+        if (a.decay) wj = __fsub_rn(wj, __fmul_rn(a.lr_wd, wj));
+        const float mj = __fadd_rn(__fmul_rn(a.beta1, m.v[j]), __fmul_rn(a.omb1, g[j]));
+        const float vj = __fadd_rn(__fmul_rn(a.beta2, v.v[j]),
+                                   __fmul_rn(a.omb2, __fmul_rn(g[j], g[j])));
+        const float m_hat = __fdiv_rn(mj, a.bias1);
+        const float v_hat = __fdiv_rn(vj, a.bias2);
+        const float u = __fdiv_rn(m_hat, __fadd_rn(__fsqrt_rn(v_hat), a.eps));
+        w.v[j] = __fsub_rn(wj, __fmul_rn(a.lr, u));
+        m.v[j] = mj;
+        v.v[j] = vj;
+        tsq = fmaf(g[j], g[j], tsq);
+        nf += (__float_as_uint(g[j]) & 0x7F800000u) == 0x7F800000u;
+    }
+    sq = tsq;
+    st_f8(a.master + i, w);
+    st_f8(a.m + i, m);
+    st_f8(a.v + i, v);
+    const uint4 p = narrow8(w.v);
+    for (int k = 0; k < a.n_views; ++k) st_u4(static_cast<uint16_t*>(a.views[k]) + i, p);
+    if (PHASE == kFull && a.reduced) {
+        F8 gg;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) gg.v[j] = g[j];
+        st_f8(a.reduced + i, gg);
+    }
+}
+
+template <int RT, int MODE, int PHASE>
+__global__ void __launch_bounds__(kChunkThreads) k_rs_adam_chunk(const __grid_constant__ RsAdamArgs a) {
+    // kNormOnly: reduce and scale only -- g to a.reduced, norm partials, no
+    // Adam (the all-reduce of the DDP schedule)
+    const int64_t c = blockIdx.x;                         // chunk of this launch
+    const int64_t t = a.t0 + c / kChunksPerTile;
+    const int b = __ldg(a.tile_bucket + t);
+    const int64_t i = __ldg(a.bucket_offset + b) + (t - __ldg(a.tile_begin + b)) * kTile +
+                      (c % kChunksPerTile) * kChunk + int64_t(threadIdx.x) * kVec;
+    float sq = 0.0f;
+    int nf = 0;
+    if (i < __ldg(a.bucket_offset + b + 1)) {
+        float coef = 1.0f;
+        if constexpr (PHASE == kUpdate) coef = __ldg(a.clip_coef);
+        float s[8];
+        reduce_vector<RT, MODE>(a, i, s);
+        if constexpr (PHASE == kNormOnly) {
+            F8 gg;
+            float tsq = 0.0f;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                gg.v[j] = __fmul_rn(s[j], a.scale);
+                tsq = fmaf(gg.v[j], gg.v[j], tsq);
+                nf += (__float_as_uint(gg.v[j]) & 0x7F800000u) == 0x7F800000u;
+            }
+            sq = tsq;
+            st_f8(a.reduced + i, gg);
+        } else {
+            adam_vector<MODE, PHASE>(a, i, s, coef, sq, nf);
+        }
+    }
+    if (a.chunk_sq != nullptr) {                          // uniform over the launch
+        // a warp's 256 squares summed in fp32 (relative error ~1e-7), the
+        // CTA's four warps and the bucket's chunks in double
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) sq += __shfl_xor_sync(0xFFFFFFFFu, sq, o);
+        nf = __reduce_add_sync(0xFFFFFFFFu, nf);
+        __shared__ double w_sq[kChunkThreads / 32];
+        __shared__ int w_nf[kChunkThreads / 32];
+        if ((threadIdx.x & 31) == 0) {
+            w_sq[threadIdx.x >> 5] = double(sq);
+            w_nf[threadIdx.x >> 5] = nf;
+        }
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            double tot = 0.0;
+            int cnt = 0;
+#pragma unroll
+            for (int k = 0; k < kChunkThreads / 32; ++k) {
+                tot += w_sq[k];
+                cnt += w_nf[k];
+            }
+            a.chunk_sq[c] = tot;
+            a.chunk_nf[c] = cnt;
+        }
+    }
+}
+
+// Chunked norm pass of the clipped step: reduce, scale, optionally store g,
+// and sum the squares near-exactly (fp32 double-float per thread, see
+// two_sum_square), one double partial per chunk.  The warps combine their
+// double-float pairs with fp32 TwoSum; the rare binary64 term (huge or
+// non-finite values) is combined only when some lane of the warp has one, so
+// the per-element path issues no binary64 instruction.
+template <int RT, int MODE, int NT>
+__global__ void __launch_bounds__(NT) k_norm_chunk(const __grid_constant__ RsAdamArgs a) {
+    constexpr int CH = NT * kVec;                         // elements per chunk
+    constexpr int CPT = int(kTile / CH);
+    static_assert(CPT >= 1 && CPT * CH == kTile, "a tile holds a whole number of chunks");
+    const int64_t c = blockIdx.x;
+    const int64_t t = a.t0 + c / CPT;
+    const int b = __ldg(a.tile_bucket + t);
+    const int64_t i = __ldg(a.bucket_offset + b) + (t - __ldg(a.tile_begin + b)) * kTile +
+                      (c % CPT) * CH + int64_t(threadIdx.x) * kVec;
+    const bool norm = a.chunk_sq != nullptr;
+    NormAcc acc;
+    int nf = 0;
+    if (i < __ldg(a.bucket_offset + b + 1)) {
+        float s[8];
+        reduce_vector<RT, MODE>(a, i, s);
+        norm_vector(a, i, s, acc, nf, norm);
+    }
+    if (!norm) return;                                    // uniform over the launch
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const float ohi = __shfl_xor_sync(0xFFFFFFFFu, acc.hi, o);
+        const float olo = __shfl_xor_sync(0xFFFFFFFFu, acc.lo, o);
+        const float sh = __fadd_rn(acc.hi, ohi);
+        const float bp = __fsub_rn(sh, acc.hi);
+        const float err = __fadd_rn(__fsub_rn(acc.hi, __fsub_rn(sh, bp)), __fsub_rn(ohi, bp));
+        acc.hi = sh;
+        acc.lo = __fadd_rn(__fadd_rn(acc.lo, olo), err);
+    }
+    if (__any_sync(0xFFFFFFFFu, acc.big != 0.0)) {
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) acc.big += __shfl_xor_sync(0xFFFFFFFFu, acc.big, o);
+    }
+    nf = __reduce_add_sync(0xFFFFFFFFu, nf);
+    __shared__ double w_sq[NT / 32];
+    __shared__ int w_nf[NT / 32];
+    if ((threadIdx.x & 31) == 0) {
+        w_sq[threadIdx.x >> 5] = acc.value();
+        w_nf[threadIdx.x >> 5] = nf;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        double tot = 0.0;
+        int cnt = 0;
+#pragma unroll
+        for (int k = 0; k < NT / 32; ++k) {
+            tot += w_sq[k];
+            cnt += w_nf[k];
+        }
+        a.chunk_sq[c] = tot;
+        a.chunk_nf[c] = cnt;
+    }
+}
+
+// One CTA per bucket of a chunked launch starting at tile t0.  A bucket of a
+// large plan has 10^5 chunk partials and there are only tens of buckets, so
+// each thread keeps 8 loads in flight: thread j adds chunks j + 1024 k in
+// increasing k (8 at a time, in order), then a fixed tree combines the
+// threads -- the same order on every run.
+constexpr int kChunkFinalizeThreads = 1024;
+
+__global__ void __launch_bounds__(kChunkFinalizeThreads)
+k_chunk_finalize(const double* __restrict__ chunk_sq, const int32_t* __restrict__ chunk_nf,
+                 const int64_t* __restrict__ tile_begin, int64_t t0, int32_t cpt, int32_t b0,
+                 float* sqnorm, int64_t* nonfinite, double* sqnorm64) {
+    constexpr int T = kChunkFinalizeThreads, U = 8;
+    __shared__ double s_sq[T];
+    __shared__ long long s_nf[T];
+    const int b = b0 + blockIdx.x;
+    const int64_t c0 = (__ldg(tile_begin + b) - t0) * cpt;
+    const int64_t c1 = (__ldg(tile_begin + b + 1) - t0) * cpt;
+    double acc = 0.0;
+    long long cnt = 0;
+    for (int64_t c = c0 + threadIdx.x; c < c1; c += int64_t(T) * U) {
+        double x[U];
+        int y[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int64_t k = c + int64_t(u) * T;
+            x[u] = k < c1 ? chunk_sq[k] : 0.0;
+            y[u] = k < c1 ? chunk_nf[k] : 0;
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            acc += x[u];
+            cnt += y[u];
+        }
+    }
+    s_sq[threadIdx.x] = acc;
+    s_nf[threadIdx.x] = cnt;
+    __syncthreads();
+    for (int w = T / 2; w > 0; w >>= 1) {
+        if (threadIdx.x < w) {
+            s_sq[threadIdx.x] += s_sq[threadIdx.x + w];
+            s_nf[threadIdx.x] += s_nf[threadIdx.x + w];
+        }
+        __syncthreads();
+    }
+    if (threadIdx.x == 0) {
+        if (sqnorm) sqnorm[b] = float(s_sq[0]);
+        if (nonfinite) nonfinite[b] = s_nf[0];
+        if (sqnorm64) sqnorm64[b] = s_sq[0];
+    }
+}
+
+// Global clip coefficient from the per-bucket squared norms (one CTA, fixed
+// order): norm = sqrt(sum), coef = min(1, max_norm / (norm + 1e-6)) in double,
+// stored as fp32; a NaN norm gives a NaN coefficient (it is not clamped away).
+__global__ void __launch_bounds__(256) k_clip_coef(const double* __restrict__ bucket_sq, int32_t nb,
+                                                   double max_norm, float* coef, float* out) {
+    __shared__ double sh[256];
+    double acc = 0.0;
+    for (int b = threadIdx.x; b < nb; b += 256) acc += bucket_sq[b];
+    sh[threadIdx.x] = acc;
+    __syncthreads();
+    for (int w = 128; w > 0; w >>= 1) {
+        if (threadIdx.x < w) sh[threadIdx.x] += sh[threadIdx.x + w];
+        __syncthreads();
+    }
+    if (threadIdx.x == 0) {
+        const double norm = sqrt(sh[0]);
+        double c = max_norm / (norm + 1e-6);
+        if (c > 1.0) c = 1.0;
+        *coef = float(c);
+        if (out) {
+            out[0] = float(norm);
+            out[1] = float(c);
+        }
+    }
+}
+
+using RsKernel = void (*)(RsAdamArgs);
+
+template <int MODE, int PHASE = kFull>
+static RsKernel pick_rs_kernel(int R) {
+    switch (R) {
+        case 1: return k_rs_adam<1, MODE, PHASE>;
+        case 2: return k_rs_adam<2, MODE, PHASE>;
+        case 4: return k_rs_adam<4, MODE, PHASE>;
+        case 8: return k_rs_adam<8, MODE, PHASE>;
+        default: return k_rs_adam<0, MODE, PHASE>;
+    }
+}
+
+template <int MODE>
+static RsKernel pick_norm_kernel_r(int R) {
+    switch (R) {
+        case 1: return k_norm_pass<1, MODE>;
+        case 2: return k_norm_pass<2, MODE>;
+        case 4: return k_norm_pass<4, MODE>;
+        case 8: return k_norm_pass<8, MODE>;
+        default: return k_norm_pass<0, MODE>;
+    }
+}
+
+static RsKernel pick_norm_kernel(int mode, int R) {
+    return mode == kInBf16 ? pick_norm_kernel_r<kInBf16>(R)
+         : mode == kInF32  ? pick_norm_kernel_r<kInF32>(R)
+                           : pick_norm_kernel_r<kInF32PlusBf16>(R);
+}
+
+template <int PHASE>
+static RsKernel pick_rs_kernel_mode(int mode, int R) {
+    return mode == kInBf16 ? pick_rs_kernel<kInBf16, PHASE>(R)
+         : mode == kInF32  ? pick_rs_kernel<kInF32, PHASE>(R)
+                           : pick_rs_kernel<kInF32PlusBf16, PHASE>(R);
+}
+
+// Grid of a fused launch over tiles [t0, t1) and the visit slots per CTA it
+// needs (a CTA visits at most every bucket of the range and at most one
+// bucket per tile it processes).
+static int fused_geometry(RsKernel fn, int dev, int64_t t0, int64_t t1, int32_t b0, int32_t b1,
+                          int* grid, int32_t* vmax) {
+    *grid = 0;
+    *vmax = 0;
+    if (t1 <= t0) return DPG_OK;
+    int st = grid_for(reinterpret_cast<const void*>(fn), kThreads, dev, t1 - t0, grid);
+    if (st != DPG_OK) return st;
+    if (t_fused_max_ctas > 0 && *grid > t_fused_max_ctas) *grid = t_fused_max_ctas;
+    const int64_t per_cta = (t1 - t0 + *grid - 1) / *grid;
+    const int64_t buckets = int64_t(b1) - b0;
+    *vmax = int32_t(per_cta < buckets ? per_cta : buckets);
+    return DPG_OK;
+}
+
+// Launch the fused pass described by `a` (tables and, when a norm output is
+// requested, norm scratch already filled in) on `grid` CTAs, then the norm
+// finalize of buckets [a.b0, a.b1).
+static int launch_fused(RsKernel fn, const RsAdamArgs& a, int grid, float* sqnorm,
+                        int64_t* nonfinite, cudaStream_t s, const char* who,
+                        double* sqnorm64 = nullptr) {
+    int st = DPG_OK;
+    if (a.t1 > a.t0) {
+        cudaEvent_t ev0 = t_fused_start, ev1 = t_fused_stop;
+        t_fused_start = t_fused_stop = nullptr;
+        if (ev0) DPG_CUDA_TRY(cudaEventRecord(ev0, s));
+        fn<<<grid, kThreads, 0, s>>>(a);
+        st = after_launch(who);
+        if (st != DPG_OK) return st;
+        if (ev1) DPG_CUDA_TRY(cudaEventRecord(ev1, s));
+    }
+    if (sqnorm || nonfinite || sqnorm64) {
+        const int32_t n_cta = a.t1 > a.t0 ? grid : 0;
+        k_norm_finalize<<<a.b1 - a.b0, kFinalizeThreads, 0, s>>>(
+            a.vis_sq, a.vis_nf, a.vis_bucket, a.vis_count, n_cta, a.vmax, a.b0, sqnorm, nonfinite,
+            sqnorm64);
+        st = after_launch(who);
+    }
+    return st;
+}
+
+template <int MODE, int PHASE = kFull>
+static RsKernel pick_chunk_kernel(int R) {
+    switch (R) {
+        case 1: return k_rs_adam_chunk<1, MODE, PHASE>;
+        case 2: return k_rs_adam_chunk<2, MODE, PHASE>;
+        case 4: return k_rs_adam_chunk<4, MODE, PHASE>;
+        case 8: return k_rs_adam_chunk<8, MODE, PHASE>;
+        default: return k_rs_adam_chunk<0, MODE, PHASE>;
+    }
+}
+
+// CTA size of the chunked norm pass (128, 256 and 512 threads measured; the
+// smallest is fastest, as for the fused pass).
+constexpr int kNormChunkThreads = 128;
+
+template <int MODE>
+static RsKernel pick_norm_chunk_kernel(int R) {
+    switch (R) {
+        case 1: return k_norm_chunk<1, MODE, kNormChunkThreads>;
+        case 2: return k_norm_chunk<2, MODE, kNormChunkThreads>;
+        case 4: return k_norm_chunk<4, MODE, kNormChunkThreads>;
+        case 8: return k_norm_chunk<8, MODE, kNormChunkThreads>;
+        default: return k_norm_chunk<0, MODE, kNormChunkThreads>;
+    }
+}
+
+// Chunked launch of the fused pass over tiles [a.t0, a.t1) (tables already in
+// `a`), then, when a norm output is requested, the per-bucket finalize.
+static int launch_chunked(RsKernel fn, RsAdamArgs a, const Plan& p, bool want_norm, float* sqnorm,
+                          int64_t* nonfinite, cudaStream_t s, const char* who,
+                          double* sqnorm64 = nullptr, int threads = kChunkThreads) {
+    const int cpt = int(kTile / (int64_t(threads) * kVec));   // chunks per tile
+    a.tile_bucket = p.d_tile_bucket;
+    a.chunk_sq = want_norm ? p.d_chunk_sq : nullptr;
+    a.chunk_nf = want_norm ? p.d_chunk_nf : nullptr;
+    const int64_t n_chunks = (a.t1 - a.t0) * cpt;
+    if (n_chunks > 0x7FFFFFFF) return fail(DPG_ERR_INVALID_ARG, "%s: %lld chunks in one launch", who,
+                                           (long long)n_chunks);
+    int st = DPG_OK;
+    if (n_chunks > 0) {
+        cudaEvent_t ev0 = t_fused_start, ev1 = t_fused_stop;
+        t_fused_start = t_fused_stop = nullptr;
+        if (ev0) DPG_CUDA_TRY(cudaEventRecord(ev0, s));
+        fn<<<unsigned(n_chunks), threads, 0, s>>>(a);
+        st = after_launch(who);
+        if (st != DPG_OK) return st;
+        if (ev1) DPG_CUDA_TRY(cudaEventRecord(ev1, s));
+    }
+    if (want_norm) {
+        k_chunk_finalize<<<a.b1 - a.b0, kChunkFinalizeThreads, 0, s>>>(
+            p.d_chunk_sq, p.d_chunk_nf, p.d_tile_begin, a.t0, cpt, a.b0, sqnorm, nonfinite, sqnorm64);
+        st = after_launch(who);
+    }
+    return st;
+}
+
+static int rs_adam(const dpg_plan_t* plan, const void* const* grads, int32_t grads_dtype,
+                   const void* const* last, const int64_t* tokens, int32_t n_counts,
+                   const dpg_hparams* hp, float* master, float* m, float* v,
+                   void* const* views, int32_t n_views, float* sqnorm, int64_t* nonfinite,
+                   float* reduced, int32_t b0, int32_t b1, void* stream, const char* who,
+                   const void* const* last2 = nullptr) {
+    if (!plan) return fail(DPG_ERR_INVALID_ARG, "%s: plan is NULL", who);
+    Plan& p = const_cast<dpg_plan_t*>(plan)->p;
+    if (b0 < 0 || b1 < b0 || b1 > p.n_buckets)
+        return fail(DPG_ERR_INVALID_ARG, "%s: bucket range [%d, %d) outside [0, %d]", who, b0, b1,
+                    p.n_buckets);
+    if (grads_dtype != DPG_BF16 && grads_dtype != DPG_F32)
+        return fail(DPG_ERR_INVALID_ARG, "%s: grads_dtype %d unknown", who, grads_dtype);
+    if (last && grads_dtype != DPG_F32)
+        return fail(DPG_ERR_INVALID_ARG, "%s: last_micro_bf16 needs fp32 accumulation grads", who);
+    if (last2 && !last)
+        return fail(DPG_ERR_INVALID_ARG, "%s: the final microbatch needs the one before it", who);
+    if (n_views < 0 || n_views > DPG_MAX_VIEWS)
+        return fail(DPG_ERR_INVALID_ARG, "%s: n_views %d outside [0, %d]", who, n_views, DPG_MAX_VIEWS);
+    RsAdamArgs a{};
+    int st = adam_constants(hp, a);
+    if (st != DPG_OK) return st;
+    st = token_scale(tokens, n_counts, &a.scale);
+    if (st != DPG_OK) return st;
+    if (b0 == b1) return DPG_OK;  // nothing to update; buffers are not touched
+    const bool want_norm = sqnorm || nonfinite;
+    const bool has_elems = p.bucket_offset[b1] > p.bucket_offset[b0];
+    if (!has_elems && !want_norm) return DPG_OK;
+    if (!has_elems) n_views = 0;  // only the (zero) norms of empty buckets are written
+    if (has_elems && !grads) return fail(DPG_ERR_INVALID_ARG, "%s: grads is NULL", who);
+    if (has_elems && (!master || !m || !v))
+        return fail(DPG_ERR_INVALID_ARG, "%s: master/m/v must not be NULL", who);
+    if (n_views > 0 && !views) return fail(DPG_ERR_INVALID_ARG, "%s: param_views is NULL", who);
+    const uintptr_t galign = grads_dtype == DPG_BF16 ? 16 : 32;
+    for (int r = 0; has_elems && r < p.R; ++r) {
+        if (!grads[r]) return fail(DPG_ERR_INVALID_ARG, "%s: grads[%d] is NULL", who, r);
+        if (!aligned(grads[r], galign)) return fail(DPG_ERR_MISALIGNED, "%s: grads[%d] misaligned", who, r);
+        a.grads[r] = grads[r];
+        if (last) {
+            if (!last[r]) return fail(DPG_ERR_INVALID_ARG, "%s: last_micro_bf16[%d] is NULL", who, r);
+            if (!aligned(last[r], 16)) return fail(DPG_ERR_MISALIGNED, "%s: last_micro_bf16[%d] misaligned", who, r);
+            a.last[r] = last[r];
+        }
+        if (last2) {
+            if (!last2[r]) return fail(DPG_ERR_INVALID_ARG, "%s: final microbatch[%d] is NULL", who, r);
+            if (!aligned(last2[r], 16)) return fail(DPG_ERR_MISALIGNED, "%s: final microbatch[%d] misaligned", who, r);
+            a.last2[r] = last2[r];
+        }
+    }
+    for (int k = 0; k < n_views; ++k) {
+        if (!views[k]) return fail(DPG_ERR_INVALID_ARG, "%s: param_views[%d] is NULL", who, k);
+        if (!aligned(views[k], 16)) return fail(DPG_ERR_MISALIGNED, "%s: param_views[%d] misaligned", who, k);
+        a.views[k] = views[k];
+    }
+    if (!aligned(master, 32) || !aligned(m, 32) || !aligned(v, 32) || !aligned(reduced, 32))
+        return fail(DPG_ERR_MISALIGNED, "%s: fp32 buffers must be 32-byte aligned", who);
+    st = upload(p);
+    if (st != DPG_OK) return st;
+
+    a.master = master;
+    a.m = m;
+    a.v = v;
+    a.reduced = reduced;
+    a.bucket_offset = p.d_bucket_offset;
+    a.tile_begin = p.d_tile_begin;
+    a.t0 = p.tile_begin[b0];
+    a.t1 = p.tile_begin[b1];
+    a.b0 = b0;
+    a.b1 = b1;
+    a.R = p.R;
+    a.n_views = n_views;
+    const int mode = grads_dtype == DPG_BF16 ? kInBf16
+                   : last2 ? kInF32PlusBf16x2 : (last ? kInF32PlusBf16 : kInF32);
+    if (t_fused_max_ctas == 0) {
+        RsKernel fc = mode == kInBf16 ? pick_chunk_kernel<kInBf16>(p.R)
+                    : mode == kInF32 ? pick_chunk_kernel<kInF32>(p.R)
+                    : mode == kInF32PlusBf16 ? pick_chunk_kernel<kInF32PlusBf16>(p.R)
+                                             : pick_chunk_kernel<kInF32PlusBf16x2>(p.R);
+        return launch_chunked(fc, a, p, want_norm, sqnorm, nonfinite,
+                              static_cast<cudaStream_t>(stream), who);
+    }
+    // a grid cap asks for the persistent kernel, whose CTA count it bounds
+    RsKernel fn = mode == kInBf16 ? pick_rs_kernel<kInBf16>(p.R)
+                : mode == kInF32 ? pick_rs_kernel<kInF32>(p.R)
+                : mode == kInF32PlusBf16 ? pick_rs_kernel<kInF32PlusBf16>(p.R)
+                                         : pick_rs_kernel<kInF32PlusBf16x2>(p.R);
+    int grid = 0;
+    st = fused_geometry(fn, p.device, a.t0, a.t1, b0, b1, &grid, &a.vmax);
+    if (st != DPG_OK) return st;
+    if (want_norm) {
+        if (grid > p.cap_ctas || int64_t(grid) * a.vmax > p.cap_visits)
+            return fail(DPG_ERR_CUDA, "%s: norm scratch too small (%d CTAs x %d visits)", who,
+                        grid, a.vmax);
+        a.vis_sq = p.d_vis_sq;
+        a.vis_nf = p.d_vis_nf;
+        a.vis_bucket = p.d_vis_bucket;
+        a.vis_count = p.d_vis_count;
+    }
+    return launch_fused(fn, a, grid, sqnorm, nonfinite, static_cast<cudaStream_t>(stream), who);
+}
+
+// Validate the per-call buffers of a whole-plan step and copy them into `a`.
+int fill_step_args(const Plan& p, const void* const* grads, int32_t grads_dtype,
+                   const void* const* last, const dpg_hparams* hp, const int64_t* tokens,
+                   int32_t n_counts, float* master, float* m, float* v, void* const* views,
+                   int32_t n_views, RsAdamArgs& a, const char* who) {
+    if (grads_dtype != DPG_BF16 && grads_dtype != DPG_F32)
+        return fail(DPG_ERR_INVALID_ARG, "%s: grads_dtype %d unknown", who, grads_dtype);
+    if (last && grads_dtype != DPG_F32)
+        return fail(DPG_ERR_INVALID_ARG, "%s: last_micro_bf16 needs fp32 accumulation grads", who);
+    if (n_views < 0 || n_views > DPG_MAX_VIEWS)
+        return fail(DPG_ERR_INVALID_ARG, "%s: n_views %d outside [0, %d]", who, n_views, DPG_MAX_VIEWS);
+    int st = adam_constants(hp, a);
+    if (st != DPG_OK) return st;
+    st = token_scale(tokens, n_counts, &a.scale);
+    if (st != DPG_OK) return st;
+    const bool has_elems = p.total_padded > 0;
+    if (!has_elems) n_views = 0;
+    if (has_elems && !grads) return fail(DPG_ERR_INVALID_ARG, "%s: grads is NULL", who);
+    if (has_elems && (!master || !m || !v))
+        return fail(DPG_ERR_INVALID_ARG, "%s: master/m/v must not be NULL", who);
+    if (n_views > 0 && !views) return fail(DPG_ERR_INVALID_ARG, "%s: param_views is NULL", who);
+    const uintptr_t galign = grads_dtype == DPG_BF16 ? 16 : 32;
+    for (int r = 0; has_elems && r < p.R; ++r) {
+        if (!grads[r]) return fail(DPG_ERR_INVALID_ARG, "%s: grads[%d] is NULL", who, r);
+        if (!aligned(grads[r], galign)) return fail(DPG_ERR_MISALIGNED, "%s: grads[%d] misaligned", who, r);
+        a.grads[r] = grads[r];
+        if (last) {
+            if (!last[r]) return fail(DPG_ERR_INVALID_ARG, "%s: last_micro_bf16[%d] is NULL", who, r);
+            if (!aligned(last[r], 16)) return fail(DPG_ERR_MISALIGNED, "%s: last_micro_bf16[%d] misaligned", who, r);
+            a.last[r] = last[r];
+        }
+    }
+    for (int k = 0; k < n_views; ++k) {
+        if (!views[k]) return fail(DPG_ERR_INVALID_ARG, "%s: param_views[%d] is NULL", who, k);
+        if (!aligned(views[k], 16)) return fail(DPG_ERR_MISALIGNED, "%s: param_views[%d] misaligned", who, k);
+        a.views[k] = views[k];
+    }
+    if (!aligned(master, 32) || !aligned(m, 32) || !aligned(v, 32))
+        return fail(DPG_ERR_MISALIGNED, "%s: fp32 buffers must be 32-byte aligned", who);
+    a.master = master;
+    a.m = m;
+    a.v = v;
+    a.n_views = n_views;
+    a.R = p.R;
+    return DPG_OK;
+}
+
+// Whole step with global gradient-norm clipping: norm pass, coefficient on
+// the device, update pass (see dpg_step_clipped in include/dpg.h).
+static int step_clipped(const dpg_plan_t* plan, const void* const* grads, int32_t grads_dtype,
+                        const void* const* last, const int64_t* tokens, int32_t n_counts,
+                        const dpg_hparams* hp, double max_norm, float* master, float* m,
+                        float* v, void* const* views, int32_t n_views, float* sqnorm,
+                        int64_t* nonfinite, float* reduced, float* clip_out, void* stream) {
+    const char* who = "dpg_step_clipped";
+    if (!plan) return fail(DPG_ERR_INVALID_ARG, "%s: plan is NULL", who);
+    Plan& p = const_cast<dpg_plan_t*>(plan)->p;
+    if (!(max_norm > 0.0) || !std::isfinite(max_norm))
+        return fail(DPG_ERR_INVALID_ARG, "%s: max_norm must be finite and > 0", who);
+    RsAdamArgs a{};
+    int st = fill_step_args(p, grads, grads_dtype, last, hp, tokens, n_counts, master, m, v, views,
+                            n_views, a, who);
+    if (st != DPG_OK) return st;
+    if (!aligned(reduced, 32)) return fail(DPG_ERR_MISALIGNED, "%s: reduced_grad misaligned", who);
+    if (p.n_buckets == 0) return DPG_OK;
+    st = upload(p);
+    if (st != DPG_OK) return st;
+    a.bucket_offset = p.d_bucket_offset;
+    a.tile_begin = p.d_tile_begin;
+    a.t0 = 0;
+    a.t1 = p.n_tiles;
+    a.b0 = 0;
+    a.b1 = p.n_buckets;
+    const int mode = grads_dtype == DPG_BF16 ? kInBf16 : (last ? kInF32PlusBf16 : kInF32);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+
+    // pass 1: reduce, scale, exact squares per bucket (and g, when a buffer is given)
+    RsAdamArgs a1 = a;
+    a1.reduced = reduced;
+    // Chunked unless a grid cap is set -- or when the pass only reads the
+    // replicas (no g stored) and R <= 4: then it moves just 2R bytes per
+    // element, and the persistent pass, which keeps up to four tiles' loads
+    // in flight per thread, is faster (4.5B, R = 4: 27.3 against 28.5 ms
+    // for the whole step).
+    if (t_fused_max_ctas == 0 && (reduced != nullptr || p.R >= 8)) {
+        RsKernel fc1 = mode == kInBf16 ? pick_norm_chunk_kernel<kInBf16>(p.R)
+                     : mode == kInF32  ? pick_norm_chunk_kernel<kInF32>(p.R)
+                                       : pick_norm_chunk_kernel<kInF32PlusBf16>(p.R);
+        st = launch_chunked(fc1, a1, p, true, sqnorm, nonfinite, s, who, p.d_bucket_sq64,
+                            kNormChunkThreads);
+    } else {   // the persistent norm pass
+        RsKernel fn1 = pick_norm_kernel(mode, p.R);
+        int grid1 = 0;
+        st = fused_geometry(fn1, p.device, a1.t0, a1.t1, 0, p.n_buckets, &grid1, &a1.vmax);
+        if (st != DPG_OK) return st;
+        if (grid1 > p.cap_ctas || int64_t(grid1) * a1.vmax > p.cap_visits)
+            return fail(DPG_ERR_CUDA, "%s: norm scratch too small", who);
+        a1.vis_sq = p.d_vis_sq;
+        a1.vis_nf = p.d_vis_nf;
+        a1.vis_bucket = p.d_vis_bucket;
+        a1.vis_count = p.d_vis_count;
+        if (a1.t1 > a1.t0) {
+            fn1<<<grid1, kThreads, 0, s>>>(a1);
+            st = after_launch(who);
+            if (st != DPG_OK) return st;
+        }
+        k_norm_finalize<<<p.n_buckets, kFinalizeThreads, 0, s>>>(
+            a1.vis_sq, a1.vis_nf, a1.vis_bucket, a1.vis_count, a1.t1 > a1.t0 ? grid1 : 0, a1.vmax, 0,
+            sqnorm, nonfinite, p.d_bucket_sq64);
+        st = after_launch(who);
+    }
+    if (st != DPG_OK) return st;
+    // the coefficient, on the device: no host synchronisation
+    k_clip_coef<<<1, 256, 0, s>>>(p.d_bucket_sq64, p.n_buckets, max_norm, p.d_clip_coef, clip_out);
+    st = after_launch(who);
+    if (st != DPG_OK) return st;
+    // pass 2: g * coef -> Adam -> bf16 views, from the stored g or the replicas again
+    RsAdamArgs a2 = a;
+    a2.clip_coef = p.d_clip_coef;
+    if (t_fused_max_ctas == 0) {
+        RsKernel fc;
+        if (reduced) {
+            a2.g_in = reduced;
+            fc = k_rs_adam_chunk<1, kInReduced, kUpdate>;
+        } else {
+            fc = mode == kInBf16 ? pick_chunk_kernel<kInBf16, kUpdate>(p.R)
+               : mode == kInF32  ? pick_chunk_kernel<kInF32, kUpdate>(p.R)
+                                 : pick_chunk_kernel<kInF32PlusBf16, kUpdate>(p.R);
+        }
+        return launch_chunked(fc, a2, p, false, nullptr, nullptr, s, who);
+    }
+    RsKernel fn2;
+    if (reduced) {
+        a2.g_in = reduced;
+        fn2 = k_rs_adam<1, kInReduced, kUpdate>;
+    } else {
+        fn2 = pick_rs_kernel_mode<kUpdate>(mode, p.R);
+    }
+    int grid2 = 0;
+    st = fused_geometry(fn2, p.device, a2.t0, a2.t1, 0, p.n_buckets, &grid2, &a2.vmax);
+    if (st != DPG_OK) return st;
+    return launch_fused(fn2, a2, grid2, nullptr, nullptr, s, who);
+}
+
+// All-reduce of the replica gradients (DDP): every element's rank-ordered
+// sum times fp32(1/G), written to `reduced`; optional per-bucket norms.
+static int allreduce_grads(const dpg_plan_t* plan, const void* const* grads, int32_t grads_dtype,
+                           const void* const* last, const int64_t* tokens, int32_t n_counts,
+                           float* reduced, float* sqnorm, int64_t* nonfinite, int32_t b0,
+                           int32_t b1, void* stream) {
+    const char* who = "dpg_allreduce_grads";
+    if (!plan) return fail(DPG_ERR_INVALID_ARG, "%s: plan is NULL", who);
+    Plan& p = const_cast<dpg_plan_t*>(plan)->p;
+    if (b0 < 0 || b1 < b0 || b1 > p.n_buckets)
+        return fail(DPG_ERR_INVALID_ARG, "%s: bucket range [%d, %d) outside [0, %d]", who, b0, b1,
+                    p.n_buckets);
+    if (grads_dtype != DPG_BF16 && grads_dtype != DPG_F32)
+        return fail(DPG_ERR_INVALID_ARG, "%s: grads_dtype %d unknown", who, grads_dtype);
+    if (last && grads_dtype != DPG_F32)
+        return fail(DPG_ERR_INVALID_ARG, "%s: last_micro_bf16 needs fp32 accumulation grads", who);
+    RsAdamArgs a{};
+    int st = token_scale(tokens, n_counts, &a.scale);
+    if (st != DPG_OK) return st;
+    if (b0 == b1) return DPG_OK;
+    const bool want_norm = sqnorm || nonfinite;
+    const bool has_elems = p.bucket_offset[b1] > p.bucket_offset[b0];
+    if (!has_elems && !want_norm) return DPG_OK;
+    if (has_elems) {
+        if (!grads) return fail(DPG_ERR_INVALID_ARG, "%s: grads is NULL", who);
+        if (!reduced) return fail(DPG_ERR_INVALID_ARG, "%s: reduced_grad is NULL", who);
+        if (!aligned(reduced, 32)) return fail(DPG_ERR_MISALIGNED, "%s: reduced_grad misaligned", who);
+        const uintptr_t galign = grads_dtype == DPG_BF16 ? 16 : 32;
+        for (int r = 0; r < p.R; ++r) {
+            if (!grads[r]) return fail(DPG_ERR_INVALID_ARG, "%s: grads[%d] is NULL", who, r);
+            if (!aligned(grads[r], galign)) return fail(DPG_ERR_MISALIGNED, "%s: grads[%d] misaligned", who, r);
+            a.grads[r] = grads[r];
+            if (last) {
+                if (!last[r]) return fail(DPG_ERR_INVALID_ARG, "%s: last_micro_bf16[%d] is NULL", who, r);
+                if (!aligned(last[r], 16)) return fail(DPG_ERR_MISALIGNED, "%s: last_micro_bf16[%d] misaligned", who, r);
+                a.last[r] = last[r];
+            }
+        }
+    }
+    st = upload(p);
+    if (st != DPG_OK) return st;
+    a.reduced = reduced;
+    a.bucket_offset = p.d_bucket_offset;
+    a.tile_begin = p.d_tile_begin;
+    a.t0 = p.tile_begin[b0];
+    a.t1 = p.tile_begin[b1];
+    a.b0 = b0;
+    a.b1 = b1;
+    a.R = p.R;
+    const int mode = grads_dtype == DPG_BF16 ? kInBf16 : (last ? kInF32PlusBf16 : kInF32);
+    if (t_fused_max_ctas == 0 && has_elems) {
+        RsKernel fc = mode == kInBf16 ? pick_chunk_kernel<kInBf16, kNormOnly>(p.R)
+                    : mode == kInF32  ? pick_chunk_kernel<kInF32, kNormOnly>(p.R)
+                                      : pick_chunk_kernel<kInF32PlusBf16, kNormOnly>(p.R);
+        return launch_chunked(fc, a, p, want_norm, sqnorm, nonfinite,
+                              static_cast<cudaStream_t>(stream), who);
+    }
+    RsKernel fn = pick_norm_kernel(mode, p.R);
+    int grid = 0;
+    st = fused_geometry(fn, p.device, a.t0, a.t1, b0, b1, &grid, &a.vmax);
+    if (st != DPG_OK) return st;
+    if (want_norm) {
+        if (grid > p.cap_ctas || int64_t(grid) * a.vmax > p.cap_visits)
+            return fail(DPG_ERR_CUDA, "%s: norm scratch too small", who);
+        a.vis_sq = p.d_vis_sq;
+        a.vis_nf = p.d_vis_nf;
+        a.vis_bucket = p.d_vis_bucket;
+        a.vis_count = p.d_vis_count;
+    }
+    return launch_fused(fn, a, grid, sqnorm, nonfinite, static_cast<cudaStream_t>(stream), who);
+}
+
+// One replica's optimizer step from an already-reduced gradient (DDP /
+// NO_SHARD: every replica updates its own full copy of the state).
+static int adam_from_reduced(const dpg_plan_t* plan, const float* reduced, const dpg_hparams* hp,
+                             float* master, float* m, float* v, void* const* views,
+                             int32_t n_views, float* sqnorm, int64_t* nonfinite, int32_t b0,
+                             int32_t b1, void* stream) {
+    const char* who = "dpg_adam_from_reduced";
+    if (!plan) return fail(DPG_ERR_INVALID_ARG, "%s: plan is NULL", who);
+    Plan& p = const_cast<dpg_plan_t*>(plan)->p;
+    if (b0 < 0 || b1 < b0 || b1 > p.n_buckets)
+        return fail(DPG_ERR_INVALID_ARG, "%s: bucket range [%d, %d) outside [0, %d]", who, b0, b1,
+                    p.n_buckets);
+    if (n_views < 0 || n_views > DPG_MAX_VIEWS)
+        return fail(DPG_ERR_INVALID_ARG, "%s: n_views %d outside [0, %d]", who, n_views, DPG_MAX_VIEWS);
+    RsAdamArgs a{};
+    int st = adam_constants(hp, a);
+    if (st != DPG_OK) return st;
+    if (b0 == b1) return DPG_OK;
+    const bool want_norm = sqnorm || nonfinite;
+    const bool has_elems = p.bucket_offset[b1] > p.bucket_offset[b0];
+    if (!has_elems && !want_norm) return DPG_OK;
+    if (!has_elems) n_views = 0;
+    if (has_elems) {
+        if (!reduced || !master || !m || !v)
+            return fail(DPG_ERR_INVALID_ARG, "%s: reduced_grad/master/m/v must not be NULL", who);
+        if (!aligned(reduced, 32) || !aligned(master, 32) || !aligned(m, 32) || !aligned(v, 32))
+            return fail(DPG_ERR_MISALIGNED, "%s: fp32 buffers must be 32-byte aligned", who);
+    }
+    if (n_views > 0 && !views) return fail(DPG_ERR_INVALID_ARG, "%s: param_views is NULL", who);
+    for (int k = 0; k < n_views; ++k) {
+        if (!views[k]) return fail(DPG_ERR_INVALID_ARG, "%s: param_views[%d] is NULL", who, k);
+        if (!aligned(views[k], 16)) return fail(DPG_ERR_MISALIGNED, "%s: param_views[%d] misaligned", who, k);
+        a.views[k] = views[k];
+    }
+    st = upload(p);
+    if (st != DPG_OK) return st;
+    a.g_in = reduced;
+    a.master = master;
+    a.m = m;
+    a.v = v;
+    a.n_views = n_views;
+    a.bucket_offset = p.d_bucket_offset;
+    a.tile_begin = p.d_tile_begin;
+    a.t0 = p.tile_begin[b0];
+    a.t1 = p.tile_begin[b1];
+    a.b0 = b0;
+    a.b1 = b1;
+    a.R = p.R;
+    if (t_fused_max_ctas == 0)
+        return launch_chunked(k_rs_adam_chunk<1, kInReduced, kFull>, a, p, want_norm, sqnorm,
+                              nonfinite, static_cast<cudaStream_t>(stream), who);
+    RsKernel fn = k_rs_adam<1, kInReduced, kFull>;
+    int grid = 0;
+    st = fused_geometry(fn, p.device, a.t0, a.t1, b0, b1, &grid, &a.vmax);
+    if (st != DPG_OK) return st;
+    if (want_norm) {
+        if (grid > p.cap_ctas || int64_t(grid) * a.vmax > p.cap_visits)
+            return fail(DPG_ERR_CUDA, "%s: norm scratch too small", who);
+        a.vis_sq = p.d_vis_sq;
+        a.vis_nf = p.d_vis_nf;
+        a.vis_bucket = p.d_vis_bucket;
+        a.vis_count = p.d_vis_count;
+    }
+    return launch_fused(fn, a, grid, sqnorm, nonfinite, static_cast<cudaStream_t>(stream), who);
+}
+
+int launch_norm_finalize(const RsAdamArgs& a, int32_t n_cta, int32_t n_buckets, float* sqnorm,
+                         int64_t* nonfinite, cudaStream_t s, const char* who) {
+    k_norm_finalize<<<n_buckets, kFinalizeThreads, 0, s>>>(a.vis_sq, a.vis_nf, a.vis_bucket,
+                                                          a.vis_count, n_cta, a.vmax, 0, sqnorm,
+                                                          nonfinite, nullptr);
+    return after_launch(who);
+}
+
+}  // namespace dpg
+
+using dpg::fail;
+
+extern "C" {
+
+int dpg_reduce_scatter_adam(const dpg_plan_t* plan, const void* const* grads, int32_t grads_dtype,
+                            const void* const* last_micro_bf16, const int64_t* valid_tokens,
+                            int32_t n_counts, const dpg_hparams* hp, float* master,
+                            float* exp_avg, float* exp_avg_sq, void* const* param_views,
+                            int32_t n_views, float* bucket_sqnorm, int64_t* bucket_nonfinite,
+                            float* reduced_grad, int32_t b0, int32_t b1, void* stream) {
+    dpg::clear_error();
+    const dpg::Trace trace("dpg_reduce_scatter_adam");
+    return dpg::rs_adam(plan, grads, grads_dtype, last_micro_bf16, valid_tokens, n_counts, hp,
+                        master, exp_avg, exp_avg_sq, param_views, n_views, bucket_sqnorm,
+                        bucket_nonfinite, reduced_grad, b0, b1, stream, "dpg_reduce_scatter_adam");
+}
+
+int dpg_step(const dpg_plan_t* plan, const void* const* grads, int32_t grads_dtype,
+             const void* const* last_micro_bf16, const int64_t* valid_tokens, int32_t n_counts,
+             const dpg_hparams* hp, float* master, float* exp_avg, float* exp_avg_sq,
+             void* const* param_views, int32_t n_views, float* bucket_sqnorm,
+             int64_t* bucket_nonfinite, void* stream) {
+    dpg::clear_error();
+    const dpg::Trace trace("dpg_step");
+    if (!plan) return fail(DPG_ERR_INVALID_ARG, "dpg_step: plan is NULL");
+    return dpg::rs_adam(plan, grads, grads_dtype, last_micro_bf16, valid_tokens, n_counts, hp,
+                        master, exp_avg, exp_avg_sq, param_views, n_views, bucket_sqnorm,
+                        bucket_nonfinite, nullptr, 0, plan->p.n_buckets, stream, "dpg_step");
+}
+
+int dpg_step_fold2(const dpg_plan_t* plan, const float* const* acc_f32,
+                   const void* const* micro_a_bf16, const void* const* micro_b_bf16,
+                   const int64_t* valid_tokens, int32_t n_counts, const dpg_hparams* hp,
+                   float* master, float* exp_avg, float* exp_avg_sq, void* const* param_views,
+                   int32_t n_views, float* bucket_sqnorm, int64_t* bucket_nonfinite,
+                   void* stream) {
+    dpg::clear_error();
+    const dpg::Trace trace("dpg_step_fold2");
+    if (!plan) return fail(DPG_ERR_INVALID_ARG, "dpg_step_fold2: plan is NULL");
+    if (!micro_a_bf16 || !micro_b_bf16)
+        return fail(DPG_ERR_INVALID_ARG, "dpg_step_fold2: microbatch tables must not be NULL");
+    return dpg::rs_adam(plan, reinterpret_cast<const void* const*>(acc_f32), DPG_F32, micro_a_bf16,
+                        valid_tokens, n_counts, hp, master, exp_avg, exp_avg_sq, param_views,
+                        n_views, bucket_sqnorm, bucket_nonfinite, nullptr, 0, plan->p.n_buckets,
+                        stream, "dpg_step_fold2", micro_b_bf16);
+}
+
+int dpg_step_clipped(const dpg_plan_t* plan, const void* const* grads, int32_t grads_dtype,
+                     const void* const* last_micro_bf16, const int64_t* valid_tokens,
+                     int32_t n_counts, const dpg_hparams* hp, double max_norm, float* master,
+                     float* exp_avg, float* exp_avg_sq, void* const* param_views, int32_t n_views,
+                     float* bucket_sqnorm, int64_t* bucket_nonfinite, float* reduced_grad,
+                     float* clip_out, void* stream) {
+    dpg::clear_error();
+    const dpg::Trace trace("dpg_step_clipped");
+    return dpg::step_clipped(plan, grads, grads_dtype, last_micro_bf16, valid_tokens, n_counts, hp,
+                             max_norm, master, exp_avg, exp_avg_sq, param_views, n_views,
+                             bucket_sqnorm, bucket_nonfinite, reduced_grad, clip_out, stream);
+}
+
+int dpg_allreduce_grads(const dpg_plan_t* plan, const void* const* grads, int32_t grads_dtype,
+                        const void* const* last_micro_bf16, const int64_t* valid_tokens,
+                        int32_t n_counts, float* reduced_grad, float* bucket_sqnorm,
+                        int64_t* bucket_nonfinite, int32_t b0, int32_t b1, void* stream) {
+    dpg::clear_error();
+    const dpg::Trace trace("dpg_allreduce_grads");
+    return dpg::allreduce_grads(plan, grads, grads_dtype, last_micro_bf16, valid_tokens, n_counts,
+                                reduced_grad, bucket_sqnorm, bucket_nonfinite, b0, b1, stream);
+}
+
+int dpg_adam_from_reduced(const dpg_plan_t* plan, const float* reduced_grad, const dpg_hparams* hp,
+                          float* master, float* exp_avg, float* exp_avg_sq,
+                          void* const* param_views, int32_t n_views, float* bucket_sqnorm,
+                          int64_t* bucket_nonfinite, int32_t b0, int32_t b1, void* stream) {
+    dpg::clear_error();
+    const dpg::Trace trace("dpg_adam_from_reduced");
+    return dpg::adam_from_reduced(plan, reduced_grad, hp, master, exp_avg, exp_avg_sq, param_views,
+                                  n_views, bucket_sqnorm, bucket_nonfinite, b0, b1, stream);
+}
+
+}  // extern "C"
+
+// ---------------------------------------------------------------------------
+// dpg_step_noalloc: the same fused pass and finalize, with the bucket tables
+// and the norm partials in one static device array instead of memory the plan
+// allocates.  For callers whose device memory the library must not allocate.
+// ---------------------------------------------------------------------------
+namespace dpg {
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[DPG_NOALLOC_SCRATCH_BYTES];
+
+// Device address of g_noalloc_scratch on device `dev` (current), looked up
+// once per device: in host code the symbol's name is only a host-side stand-in.
+static int noalloc_scratch(int dev, unsigned char** out) {
+    static std::mutex mu;
+    static std::map<int, unsigned char*> addr;
+    std::lock_guard<std::mutex> g(mu);
+    auto it = addr.find(dev);
+    if (it == addr.end()) {
+        void* ptr = nullptr;
+        const cudaError_t e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
+        if (e != cudaSuccess || ptr == nullptr)
+            return fail(DPG_ERR_CUDA, "dpg_step_noalloc: cudaGetSymbolAddress failed on device %d: %s",
+                        dev, cudaGetErrorString(e));
+        it = addr.emplace(dev, static_cast<unsigned char*>(ptr)).first;
+    }
+    *out = it->second;
+    return DPG_OK;
+}
+
+static int step_noalloc(const dpg_plan_t* plan, const void* const* grads, int32_t grads_dtype,
+                        const void* const* last, const int64_t* tokens, int32_t n_counts,
+                        const dpg_hparams* hp, float* master, float* m, float* v,
+                        void* const* views, int32_t n_views, float* sqnorm, int64_t* nonfinite,
+                        void* stream) {
+    const char* who = "dpg_step_noalloc";
+    if (!plan) return fail(DPG_ERR_INVALID_ARG, "%s: plan is NULL", who);
+    const Plan& p = plan->p;
+    if (grads_dtype != DPG_BF16 && grads_dtype != DPG_F32)
+        return fail(DPG_ERR_INVALID_ARG, "%s: grads_dtype %d unknown", who, grads_dtype);
+    if (last && grads_dtype != DPG_F32)
+        return fail(DPG_ERR_INVALID_ARG, "%s: last_micro_bf16 needs fp32 accumulation grads", who);
+    if (n_views < 0 || n_views > DPG_MAX_VIEWS)
+        return fail(DPG_ERR_INVALID_ARG, "%s: n_views %d outside [0, %d]", who, n_views, DPG_MAX_VIEWS);
+    RsAdamArgs a{};
+    int st = adam_constants(hp, a);
+    if (st != DPG_OK) return st;
+    st = token_scale(tokens, n_counts, &a.scale);
+    if (st != DPG_OK) return st;
+    if (p.n_buckets == 0) return DPG_OK;
+    const bool want_norm = sqnorm || nonfinite;
+    const bool has_elems = p.total_padded > 0;
+    if (!has_elems && !want_norm) return DPG_OK;
+    if (!has_elems) n_views = 0;
+
+    // launch geometry, then the bytes of the static array it needs: the two
+    // bucket tables and, for a norm, the visit partials of this launch
+    const int mode = grads_dtype == DPG_BF16 ? kInBf16 : (last ? kInF32PlusBf16 : kInF32);
+    RsKernel fn = mode == kInBf16 ? pick_rs_kernel<kInBf16>(p.R)
+                : mode == kInF32 ? pick_rs_kernel<kInF32>(p.R)
+                                 : pick_rs_kernel<kInF32PlusBf16>(p.R);
+    int dev = 0;
+    DPG_CUDA_TRY(cudaGetDevice(&dev));
+    int grid = 0;
+    st = fused_geometry(fn, dev, 0, p.n_tiles, 0, p.n_buckets, &grid, &a.vmax);
+    if (st != DPG_OK) return st;
+    const size_t nb1 = size_t(p.n_buckets) + 1;
+    const size_t tab_bytes = round256(nb1 * sizeof(int64_t));
+    const VisLayout L = want_norm ? vis_layout(int64_t(grid) * a.vmax, grid) : vis_layout(0, 0);
+    const size_t need = 2 * tab_bytes + L.total;
+    if (need > size_t(DPG_NOALLOC_SCRATCH_BYTES))
+        return fail(DPG_ERR_INVALID_ARG,
+                    "%s: this plan (%d buckets, %lld tiles, %d CTAs x %d bucket visits) needs %zu "
+                    "bytes of scratch; the library's static scratch holds %zu bytes (use dpg_step)",
+                    who, p.n_buckets, (long long)p.n_tiles, grid, a.vmax, need,
+                    size_t(DPG_NOALLOC_SCRATCH_BYTES));
+
+    if (has_elems && !grads) return fail(DPG_ERR_INVALID_ARG, "%s: grads is NULL", who);
+    if (has_elems && (!master || !m || !v))
+        return fail(DPG_ERR_INVALID_ARG, "%s: master/m/v must not be NULL", who);
+    if (n_views > 0 && !views) return fail(DPG_ERR_INVALID_ARG, "%s: param_views is NULL", who);
+    const uintptr_t galign = grads_dtype == DPG_BF16 ? 16 : 32;
+    for (int r = 0; has_elems && r < p.R; ++r) {
+        if (!grads[r]) return fail(DPG_ERR_INVALID_ARG, "%s: grads[%d] is NULL", who, r);
+        if (!aligned(grads[r], galign)) return fail(DPG_ERR_MISALIGNED, "%s: grads[%d] misaligned", who, r);
+        a.grads[r] = grads[r];
+        if (last) {
+            if (!last[r]) return fail(DPG_ERR_INVALID_ARG, "%s: last_micro_bf16[%d] is NULL", who, r);
+            if (!aligned(last[r], 16)) return fail(DPG_ERR_MISALIGNED, "%s: last_micro_bf16[%d] misaligned", who, r);
+            a.last[r] = last[r];
+        }
+    }
+    for (int k = 0; k < n_views; ++k) {
+        if (!views[k]) return fail(DPG_ERR_INVALID_ARG, "%s: param_views[%d] is NULL", who, k);
+        if (!aligned(views[k], 16)) return fail(DPG_ERR_MISALIGNED, "%s: param_views[%d] misaligned", who, k);
+        a.views[k] = views[k];
+    }
+    if (!aligned(master, 32) || !aligned(m, 32) || !aligned(v, 32))
+        return fail(DPG_ERR_MISALIGNED, "%s: fp32 buffers must be 32-byte aligned", who);
+
+    unsigned char* base = nullptr;
+    st = noalloc_scratch(dev, &base);
+    if (st != DPG_OK) return st;
+    int64_t* d_bucket_offset = reinterpret_cast<int64_t*>(base);
+    int64_t* d_tile_begin = reinterpret_cast<int64_t*>(base + tab_bytes);
+    unsigned char* vis = base + 2 * tab_bytes;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    // the tables of this plan, in stream order ahead of the kernels that read them
+    DPG_CUDA_TRY(cudaMemcpyAsync(d_bucket_offset, p.bucket_offset.data(), nb1 * sizeof(int64_t),
+                                 cudaMemcpyHostToDevice, s));
+    DPG_CUDA_TRY(cudaMemcpyAsync(d_tile_begin, p.tile_begin.data(), nb1 * sizeof(int64_t),
+                                 cudaMemcpyHostToDevice, s));
+    a.master = master;
+    a.m = m;
+    a.v = v;
+    a.reduced = nullptr;
+    a.bucket_offset = d_bucket_offset;
+    a.tile_begin = d_tile_begin;
+    a.t0 = 0;
+    a.t1 = p.n_tiles;
+    a.b0 = 0;
+    a.b1 = p.n_buckets;
+    a.R = p.R;
+    a.n_views = n_views;
+    if (want_norm) {
+        a.vis_sq = reinterpret_cast<double*>(vis + L.sq);
+        a.vis_nf = reinterpret_cast<int32_t*>(vis + L.nf);
+        a.vis_bucket = reinterpret_cast<int32_t*>(vis + L.bucket);
+        a.vis_count = reinterpret_cast<int32_t*>(vis + L.count);
+    }
+    return launch_fused(fn, a, grid, sqnorm, nonfinite, s, who);
+}
+
+}  // namespace dpg
+
+extern "C" int dpg_step_noalloc(const dpg_plan_t* plan, const void* const* grads,
+                                int32_t grads_dtype, const void* const* last_micro_bf16,
+                                const int64_t* valid_tokens, int32_t n_counts,
+                                const dpg_hparams* hp, float* master, float* exp_avg,
+                                float* exp_avg_sq, void* const* param_views, int32_t n_views,
+                                float* bucket_sqnorm, int64_t* bucket_nonfinite, void* stream) {
+    dpg::clear_error();
+    return dpg::step_noalloc(plan, grads, grads_dtype, last_micro_bf16, valid_tokens, n_counts, hp,
+                             master, exp_avg, exp_avg_sq, param_views, n_views, bucket_sqnorm,
+                             bucket_nonfinite, stream);
+}
+

@@ -91,7 +91,7 @@ struct Plan {
 int fail(int status, const char* fmt, ...);
 void clear_error();
 
-// device side (dpg_kernels.cu)
+// device side (dpg_runtime.cu)
 int upload(Plan& p);
 void release_device(Plan& p);
 
