@@ -174,13 +174,36 @@ __device__ __forceinline__ void reduce_vector(const RsAdamArgs& a, int64_t i, fl
                 for (int j = 0; j < 8; ++j) s[j] = __fadd_rn(s[j], t[j]);
             }
         } else {
+            // any R: replicas in groups of four whose loads are all issued
+            // before their adds (still added in rank order)
             widen8(ld_grad_u4(static_cast<const uint16_t*>(a.grads[0]) + i), s);
-#pragma unroll 4
-            for (int r = 1; r < R; ++r) {
-                float t[8];
-                widen8(ld_grad_u4(static_cast<const uint16_t*>(a.grads[r]) + i), t);
+            int r = 1;
+            for (; r + 4 <= R; r += 4) {
+                uint4 x[4];
 #pragma unroll
-                for (int j = 0; j < 8; ++j) s[j] = __fadd_rn(s[j], t[j]);
+                for (int u = 0; u < 4; ++u)
+                    x[u] = ld_grad_u4(static_cast<const uint16_t*>(a.grads[r + u]) + i);
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    float t[8];
+                    widen8(x[u], t);
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) s[j] = __fadd_rn(s[j], t[j]);
+                }
+            }
+            uint4 x[3];
+            const int rem = R - r;                            // 0..3
+#pragma unroll
+            for (int u = 0; u < 3; ++u)
+                if (u < rem) x[u] = ld_grad_u4(static_cast<const uint16_t*>(a.grads[r + u]) + i);
+#pragma unroll
+            for (int u = 0; u < 3; ++u) {
+                if (u < rem) {
+                    float t[8];
+                    widen8(x[u], t);
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) s[j] = __fadd_rn(s[j], t[j]);
+                }
             }
         }
     } else {
