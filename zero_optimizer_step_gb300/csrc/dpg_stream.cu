@@ -135,7 +135,8 @@ __device__ __forceinline__ void copy_elems(uint16_t* __restrict__ dst,
     for (int64_t k = done + threadIdx.x; k < n; k += blockDim.x) dst[k] = src[k];
 }
 
-// Persistent: CTA c copies items c, c + grid, ... of the launch's window.
+// CTA c copies item c of the launch's window (launched with one CTA per item;
+// the loop also serves a smaller grid).
 __global__ void __launch_bounds__(256) k_pack(const __grid_constant__ PackArgs a) {
     for (int64_t j = blockIdx.x; j < a.n_items; j += gridDim.x) {
         const PackItem it = a.items[a.item0 + j];
@@ -152,7 +153,7 @@ __global__ void __launch_bounds__(256) k_pack(const __grid_constant__ PackArgs a
 
 // ---------------------------------------------------------------------------
 // checkpoint: fp32 state between the flat bucket layout and the canonical
-// registration-order layout, one CTA per item (persistent)
+// registration-order layout, one CTA per item
 // ---------------------------------------------------------------------------
 struct StateArgs {
     const float* src[DPG_MAX_STATE_ARRAYS];
