@@ -1,0 +1,99 @@
+"""Host logic of bench.py that the reported numbers depend on (no GPU).
+
+* algorithmic bytes per parameter of every schedule: (2R + 26) for the step,
+  the K-microbatch cycle (10K - 8)R + 26, and the paired schedule;
+* the paired accumulation schedule covers microbatches 0..K-3 in order;
+* the ncu launch-list parser behind `roofline.traffic` averages the fused
+  kernel's DRAM bytes over its launches and ignores every other kernel;
+* the stored traffic is used only while the kernel code hashes the same, and
+  the hash ignores comments and whitespace.
+"""
+import json
+import os
+import types
+
+import pytest
+
+import bench
+from workloads import CONFIGS
+
+
+def test_algorithmic_bytes_of_the_workloads():
+    assert bench.algorithmic_bytes_per_param(CONFIGS["llama1b"]) == {"fused": 42, "step": 42}
+    assert bench.algorithmic_bytes_per_param(CONFIGS["gpt2"]) == {"fused": 42, "step": 42}
+    # 4.5B, R = 4, K = 4: 6R+26 fused, (10K - 8)R + 26 per cycle
+    c = CONFIGS["llama8b16l"]
+    assert (c.R, c.K) == (4, 4)
+    assert bench.algorithmic_bytes_per_param(c) == {"fused": 50, "step": 154}
+    # paired: one first pair (8R) + the fused step with two microbatches (8R + 26)
+    assert bench.algorithmic_bytes_per_param(c, fold2=True) == {"fused": 58, "step": 90}
+
+
+def _cfg(R, K):
+    return types.SimpleNamespace(R=R, K=K)
+
+
+@pytest.mark.parametrize("K", range(3, 11))
+def test_fold2_schedule_covers_the_microbatches_in_order(K):
+    seen = []
+    for k, pair in bench.fold2_schedule(K):
+        seen += [k, k + 1] if pair else [k]
+    assert seen == list(range(K - 2))
+    # bytes agree with a by-hand count: first pass 8R / 6R, later 12R / 10R
+    R = 3
+    acc = 0
+    for k, pair in bench.fold2_schedule(K):
+        acc += (8 if pair else 6) * R if k == 0 else (12 if pair else 10) * R
+    assert bench.algorithmic_bytes_per_param(_cfg(R, K), fold2=True)["step"] == 8 * R + 26 + acc
+
+
+def _csv_row(i, name, metric, value):
+    return ",".join(f'"{x}"' for x in [i, "1", "python3", "host", name, "1", "7", "(128, 1, 1)",
+                                       "(10, 1, 1)", "0", "10.3", "sec", metric, "byte", value])
+
+
+def test_traffic_parser_averages_the_fused_kernel_only(tmp_path, monkeypatch):
+    lines = ["==PROF== banner", '"ID","Process ID"']
+    rows = [("0", "void k_rs_adam_chunk<8, 0, 0>(RsAdamArgs)", 100, 40),
+            ("1", "k_chunk_finalize(const double *)", 5, 0),
+            ("2", "void k_rs_adam_chunk<8, 0, 0>(RsAdamArgs)", 300, 60),
+            ("3", "void k_rs_adam_staged<8>(StagedArgs)", 999, 999),
+            ("4", "vectorized_elementwise_kernel", 7, 7)]
+    for i, name, rd, wr in rows:
+        lines.append(_csv_row(i, name, "dram__bytes_read.sum", f"{rd:,}"))
+        lines.append(_csv_row(i, name, "dram__bytes_write.sum", f"{wr:,}"))
+        lines.append(_csv_row(i, name, "gpu__time_duration.sum", "1000"))
+    csv_path = tmp_path / "launches.csv"
+    csv_path.write_text("\n".join(lines) + "\n")
+    out = tmp_path / "traffic.json"
+    monkeypatch.setattr(bench, "TRAFFIC_FILE", str(out))
+    a = types.SimpleNamespace(config="llama1b", traffic_from=str(csv_path), cap_mib=None)
+    bench.write_traffic(a)
+    t = json.loads(out.read_text())["k_rs_adam"]
+    assert t["launches"] == 2
+    assert t["dram_bytes_read"] == 200 and t["dram_bytes_write"] == 50
+    assert t["dram_bytes_per_launch"] == 250
+    assert t["source_sha256"] == bench.kernel_source_sha256()
+    # read back while the code hash matches; scaled by elements for another size
+    cfg = CONFIGS["llama1b"]
+    assert bench.traffic_per_launch(cfg, cfg.cap_bytes, cfg.psi) == pytest.approx(250)
+    t["source_sha256"] = "0" * 64
+    out.write_text(json.dumps({"k_rs_adam": t}))
+    assert bench.traffic_per_launch(cfg, cfg.cap_bytes, cfg.psi) is None
+
+
+def test_code_hash_ignores_comments_and_whitespace(tmp_path, monkeypatch):
+    code = "int f(int x) {\n    return x + 1;   // add one\n}\n/* block */\n"
+    a = tmp_path / "a.cu"
+    a.write_text(code)
+    monkeypatch.setattr(bench, "KERNEL_SRCS", [str(a)])
+    h0 = bench.kernel_source_sha256()
+    a.write_text("// header\nint f(int x) {\n\n  return x + 1;\n}\n")
+    assert bench.kernel_source_sha256() == h0
+    a.write_text("int f(int x) {\n    return x + 2;\n}\n")
+    assert bench.kernel_source_sha256() != h0
+
+
+def test_kernel_sources_exist():
+    for f in bench.KERNEL_SRCS:
+        assert os.path.exists(f), f
