@@ -63,6 +63,8 @@ def parse():
                     help="no GPU: read an ncu launch list (--csv with dram__bytes_read.sum and "
                          "dram__bytes_write.sum) of this bench's --config run and write the "
                          "fused kernel's mean DRAM bytes per launch to profiles/traffic.json")
+    ap.add_argument("--replicas", type=int, default=None,
+                    help="override the workload's R (simulated data-parallel replicas, 1..64)")
     ap.add_argument("--fold2", action="store_true",
                     help="K >= 3: paired accumulation (two bf16 gradient buffers per replica), "
                          "the last two microbatches folded into the fused step")
@@ -333,6 +335,18 @@ def traffic_per_launch(cfg, cap, total_padded):
     return float(t["dram_bytes_per_launch"]) * total_padded / float(t["elements"])
 
 
+def config_of(a):
+    """The named workload, with R overridden by --replicas when given."""
+    import dataclasses
+    cfg = CONFIGS[a.config]
+    r = getattr(a, "replicas", None)
+    if r is None:
+        return cfg
+    if not 1 <= r <= 64:
+        raise SystemExit(f"--replicas {r}: R must be 1..64")
+    return dataclasses.replace(cfg, R=r)
+
+
 def fused_kernel_name(a, R, K) -> str:
     """The fused kernel the timed step launches (for the roofline label)."""
     if getattr(a, "variant", "direct") == "staged":
@@ -343,7 +357,7 @@ def fused_kernel_name(a, R, K) -> str:
 def write_traffic(a):
     """profiles/traffic.json from an ncu launch list of the fused kernel."""
     import csv
-    cfg = CONFIGS[a.config]
+    cfg = config_of(a)
     per = {}
     with open(a.traffic_from, newline="") as fh:
         rows = [r for r in csv.reader(fh) if len(r) > 14 and r[0].isdigit()]
@@ -387,7 +401,7 @@ def run_dpg(a):
         dist.barrier()
     import zero_optimizer_step_gb300 as dpg
 
-    cfg = CONFIGS[a.config]
+    cfg = config_of(a)
     cap = cap_of(cfg, a)
     R, K = cfg.R, cfg.K
     plan = dpg.dpg_plan_buckets(cfg.numels, cap, R)
@@ -680,7 +694,7 @@ def run_reference(a):
     rank, _, world = dist_info()
     if rank != 0:
         return
-    cfg = CONFIGS[a.config]
+    cfg = config_of(a)
     cap = cap_of(cfg, a)
     import oracle
     oracle.build()
@@ -805,7 +819,7 @@ def run_kernel_table(a):
     from zero_optimizer_step_gb300 import build as _build
     _build.build()
     import zero_optimizer_step_gb300 as dpg
-    cfg = CONFIGS[a.config]
+    cfg = config_of(a)
     cap = cap_of(cfg, a)
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
@@ -896,7 +910,7 @@ def run_schedules(a):
     from zero_optimizer_step_gb300 import build as _build
     _build.build()
     import zero_optimizer_step_gb300 as dpg
-    cfg = CONFIGS[a.config]
+    cfg = config_of(a)
     cap = cap_of(cfg, a)
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
@@ -1026,7 +1040,7 @@ def run_overlap(a):
     from zero_optimizer_step_gb300 import build as _build
     _build.build()
     import zero_optimizer_step_gb300 as dpg
-    cfg = CONFIGS[a.config]
+    cfg = config_of(a)
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
     R, psi = cfg.R, cfg.psi

@@ -97,3 +97,13 @@ def test_code_hash_ignores_comments_and_whitespace(tmp_path, monkeypatch):
 def test_kernel_sources_exist():
     for f in bench.KERNEL_SRCS:
         assert os.path.exists(f), f
+
+
+def test_replicas_override():
+    a = types.SimpleNamespace(config="llama1b", replicas=16)
+    c = bench.config_of(a)
+    assert c.R == 16 and c.psi == CONFIGS["llama1b"].psi
+    assert bench.algorithmic_bytes_per_param(c)["fused"] == 2 * 16 + 26
+    assert bench.config_of(types.SimpleNamespace(config="gpt2", replicas=None)) is CONFIGS["gpt2"]
+    with pytest.raises(SystemExit):
+        bench.config_of(types.SimpleNamespace(config="gpt2", replicas=65))
