@@ -121,6 +121,29 @@ def job_throughput(units_per_rank: float, world: int, ms_slowest: float) -> floa
     return units_per_rank * world / (ms_slowest * 1e-3)
 
 
+SPIN_CYCLES = 4_000_000              # about 2 ms of SM clock at 2 GHz
+
+
+def device_times_ms(fn, reps: int, spin_cycles: int = SPIN_CYCLES):
+    """Device time of one call of fn per sample, in ms.
+
+    A GPU spin queued before the start event keeps the device busy while the
+    host checks and marshals fn's arguments and launches its kernels, so the
+    interval holds fn's kernels and the device-side gaps between them, not
+    the Python call overhead (about 80 us for a 147-tensor pack)."""
+    import torch
+    ts = []
+    for _ in range(reps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda._sleep(spin_cycles)
+        e0.record()
+        fn()
+        e1.record()
+        torch.cuda.synchronize()
+        ts.append(e0.elapsed_time(e1))
+    return ts
+
+
 def cap_of(cfg, a) -> int:
     return int(a.cap_mib * (1 << 20)) if a.cap_mib else cfg.cap_bytes
 
@@ -852,6 +875,10 @@ def run_kernel_table(a):
         ("k_pack unpack (dpg_unpack, one replica)", 4, lambda: dpg.dpg_unpack(plan, flat, pgrads)),
         ("k_accumulate<first> (one replica)", 6, lambda: dpg.dpg_accumulate(plan, g[0], acc, True)),
         ("k_accumulate (one replica)", 10, lambda: dpg.dpg_accumulate(plan, g[0], acc, False)),
+        ("k_accumulate_pair<first> (one replica)", 8,
+         lambda: dpg.dpg_accumulate_pair(plan, g[0], g[1 % R], acc, True)),
+        ("k_accumulate_pair (one replica)", 12,
+         lambda: dpg.dpg_accumulate_pair(plan, g[0], g[1 % R], acc, False)),
         ("k_allgather (one view)", 6, lambda: dpg.dpg_allgather_params(plan, w, [p])),
         (f"k_rs_adam_chunk<R={R}> (dpg_reduce_scatter_adam, no norm)", 2 * R + 26,
          lambda: dpg.dpg_reduce_scatter_adam(plan, g, tok, hp(), w, m, v, [p])),
@@ -886,20 +913,16 @@ def run_kernel_table(a):
         for _ in range(3):
             fn()
         torch.cuda.synchronize()
-        ts = []
-        for _ in range(max(5, min(a.steps, 20))):
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            e0.record()
-            fn()
-            e1.record()
-            torch.cuda.synchronize()
-            ts.append(e0.elapsed_time(e1))
-        ms = statistics.median(ts)
+        ms = statistics.median(device_times_ms(fn, max(5, min(a.steps, 20))))
         gbs = bpp * psi / (ms * 1e-3) / 1e9
         rows.append({"kernel": name, "bytes_per_param": bpp, "ms": ms, "achieved_gbs": gbs,
                      "frac": gbs / peak})
     print(json.dumps({"metric": "per-kernel HBM roofline", "config": workload_desc(cfg, cap, plan.n_buckets, N),
-                      "peak_gbs": peak, "peak_kind": peak_kind, "rows": rows}), flush=True)
+                      "peak_gbs": peak, "peak_kind": peak_kind, "rows": rows,
+                      "timing": "median of CUDA-event intervals around one call each, a GPU spin "
+                                "queued before the start event so that the host's call overhead "
+                                "is not in the interval; no L2 flush (every operand > L2)"}),
+          flush=True)
 
 
 # --------------------------------------------------------------------------
@@ -934,15 +957,7 @@ def run_schedules(a):
         for _ in range(2):
             fn()
         torch.cuda.synchronize()
-        ts = []
-        for _ in range(reps):
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            e0.record()
-            fn()
-            e1.record()
-            torch.cuda.synchronize()
-            ts.append(e0.elapsed_time(e1))
-        return statistics.median(ts)
+        return statistics.median(device_times_ms(fn, reps))
 
     rows = []
     z = [w0.clone(), torch.zeros(N, device=dev), torch.zeros(N, device=dev)]
@@ -992,7 +1007,9 @@ def run_schedules(a):
                  "note": "same fused pass writing one sharded bf16 buffer, then two "
                          "layer-by-layer parameter all-gathers (forward, backward)"})
     print(json.dumps({"metric": "DDP vs ZeRO-1/2/3 schedules", "config": workload_desc(cfg, cap, plan.n_buckets, N),
-                      "peak_gbs": peak, "peak_kind": peak_kind, "rows": rows}), flush=True)
+                      "peak_gbs": peak, "peak_kind": peak_kind, "rows": rows,
+                      "timing": "median of CUDA-event intervals around one call each, a GPU spin "
+                                "queued before the start event"}), flush=True)
 
 
 # --------------------------------------------------------------------------
