@@ -790,14 +790,21 @@ def run_hockney(a):
             for _ in range(2):     # warm the occupancy cache and the plan upload
                 dpg.dpg_reduce_scatter_adam(plan, g, tok, hp, w, m, v, [p])
         torch.cuda.current_stream().wait_stream(s)
-        for mode in ("per_bucket", "fused"):
+        # per_bucket: launches with programmatic stream serialization (the
+        # library's default); per_bucket_plain: the same launches without it
+        for mode in ("per_bucket", "per_bucket_plain", "fused"):
             gr = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(gr):
-                if mode == "fused":
-                    dpg.dpg_reduce_scatter_adam(plan, g, tok, hp, w, m, v, [p])
-                else:
-                    for b in range(plan.n_buckets):
-                        dpg.dpg_reduce_scatter_adam(plan, g, tok, hp, w, m, v, [p], b0=b, b1=b + 1)
+            dpg.dpg_set_programmatic_launch(mode != "per_bucket_plain")
+            try:
+                with torch.cuda.graph(gr):
+                    if mode == "fused":
+                        dpg.dpg_reduce_scatter_adam(plan, g, tok, hp, w, m, v, [p])
+                    else:
+                        for b in range(plan.n_buckets):
+                            dpg.dpg_reduce_scatter_adam(plan, g, tok, hp, w, m, v, [p],
+                                                        b0=b, b1=b + 1)
+            finally:
+                dpg.dpg_set_programmatic_launch(True)
             graphs[mode] = gr
         res = {}
         for mode, gr in graphs.items():
@@ -814,19 +821,25 @@ def run_hockney(a):
             res[mode + "_range"] = [min(ts), max(ts)]
         points.append({"cap_bytes": cap, "n_buckets": plan.n_buckets, "total_padded": N,
                        "bytes": (2 * R + 26) * cfg.psi, "per_bucket_ms": res["per_bucket"],
+                       "per_bucket_plain_ms": res["per_bucket_plain"],
                        "fused_ms": res["fused"], "per_bucket_ms_range": res["per_bucket_range"],
+                       "per_bucket_plain_ms_range": res["per_bucket_plain_range"],
                        "fused_ms_range": res["fused_range"]})
         del graphs, g, w, m, v, p
         plan.destroy()
     K = np.array([q["n_buckets"] for q in points], float)
-    T = np.array([q["per_bucket_ms"] for q in points], float) * 1e-3
     Mb = np.array([q["bytes"] for q in points], float)
     A = np.stack([K, Mb], axis=1)
-    (alpha, beta), *_ = np.linalg.lstsq(A, T, rcond=None)
+    fits = {}
+    for key in ("per_bucket", "per_bucket_plain"):
+        T = np.array([q[key + "_ms"] for q in points], float) * 1e-3
+        (alpha, beta), *_ = np.linalg.lstsq(A, T, rcond=None)
+        fits[key] = {"alpha_us": alpha * 1e6, "inv_beta_gbs": 1.0 / beta / 1e9}
     fused = np.array([q["fused_ms"] for q in points]) * 1e-3
     out = {"metric": "hockney alpha-beta fit of the fused reduce-scatter+Adam kernel over bucket caps",
            "workload": f"{cfg.name}: {len(cfg.shapes)} tensors, psi={cfg.psi}, R={R}",
-           "points": points, "fit": {"alpha_us": alpha * 1e6, "inv_beta_gbs": 1.0 / beta / 1e9,
+           "points": points, "fit": {**fits["per_bucket"],
+                                     "plain_launches": fits["per_bucket_plain"],
                                      "model": "T_per_bucket = K*alpha + beta*M (least squares)"},
            "fused_single_launch_ms": {"median": float(np.median(fused)) * 1e3,
                                       "min": float(fused.min()) * 1e3, "max": float(fused.max()) * 1e3},
@@ -870,6 +883,13 @@ def run_kernel_table(a):
         state["t"] += 1
         return dpg.HParams(step=state["t"])
 
+    def plain_launches(fn):
+        dpg.dpg_set_programmatic_launch(False)
+        try:
+            fn()
+        finally:
+            dpg.dpg_set_programmatic_launch(True)
+
     cases = [
         ("k_pack (dpg_pack, one replica)", 4, lambda: dpg.dpg_pack(plan, pgrads, flat)),
         ("k_pack unpack (dpg_unpack, one replica)", 4, lambda: dpg.dpg_unpack(plan, flat, pgrads)),
@@ -899,6 +919,9 @@ def run_kernel_table(a):
         (f"k_gather_bf16 ({R} views, one launch per bucket)", 2 + 2 * R,
          lambda: [dpg.dpg_gather_params_bf16(plan, p, views, b0=b, b1=b + 1)
                   for b in range(plan.n_buckets)]),
+        (f"k_gather_bf16 ({R} views, one launch per bucket, plain launches)", 2 + 2 * R,
+         lambda: plain_launches(lambda: [dpg.dpg_gather_params_bf16(plan, p, views, b0=b, b1=b + 1)
+                                         for b in range(plan.n_buckets)])),
         # calibration (torch's own kernels, not this library): the mix of reads
         # and writes sets the ceiling; the denominator is a 1:1 copy
         ("calibration: torch fill_ (write only, 4 B/param)", 4, lambda: acc.fill_(0.5)),

@@ -411,6 +411,19 @@ int dpg_step_noalloc(const dpg_plan_t* plan, const void* const* grads, int32_t g
  * Negative: DPG_ERR_INVALID_ARG. */
 int dpg_set_fused_max_ctas(int32_t max_ctas);
 
+/* Programmatic dependent launch (a Hopper / Blackwell stream feature).  With
+ * on = 1 (the default) the chunked fused kernels, their norm finalize and
+ * clip coefficient, and the accumulation, all-gather and gather kernels are
+ * launched from the CALLING THREAD with programmatic stream serialization:
+ * the GPU may schedule such a kernel while the previous kernel of the stream
+ * is still draining, which shortens the gap between short back-to-back
+ * launches (per-bucket updates, layer-by-layer gathers).  Each of these
+ * kernels waits on the device, before its first memory access, until the
+ * previous kernel has completed and its writes are visible, so stream order
+ * and results are exactly those of plain launches.  on = 0 launches them
+ * plainly.  Anything other than 0 or 1: DPG_ERR_INVALID_ARG. */
+int dpg_set_programmatic_launch(int32_t on);
+
 /* Diagnostics -------------------------------------------------------------- */
 /* Number of kernels this library has launched since it was loaded. */
 int64_t dpg_launch_count(void);

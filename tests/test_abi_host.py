@@ -182,6 +182,10 @@ def test_other_entry_points_validation():
     assert L.dpg_allgather_params(plan.handle, FAKE, dpg._ptrs([FAKE]), 1, 1, 1, None) == dpg.DPG_OK
     assert L.dpg_set_fused_max_ctas(-1) == dpg.DPG_ERR_INVALID_ARG
     assert L.dpg_set_fused_max_ctas(0) == dpg.DPG_OK
+    assert L.dpg_set_programmatic_launch(2) == dpg.DPG_ERR_INVALID_ARG
+    assert L.dpg_set_programmatic_launch(-1) == dpg.DPG_ERR_INVALID_ARG
+    assert L.dpg_set_programmatic_launch(0) == dpg.DPG_OK
+    assert L.dpg_set_programmatic_launch(1) == dpg.DPG_OK
     A2 = L.dpg_accumulate_pair
     assert A2(None, FAKE, FAKE, FAKE, 1, None) == dpg.DPG_ERR_INVALID_ARG
     assert A2(plan.handle, FAKE, None, FAKE, 1, None) == dpg.DPG_ERR_INVALID_ARG

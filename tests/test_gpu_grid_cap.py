@@ -1,4 +1,4 @@
-"""Launch shape does not change results.
+"""Launch shape and launch mode do not change results.
 
 By default the fused passes launch one small CTA per 1024-element chunk; a
 grid cap (dpg_set_fused_max_ctas) switches every one of them to the
@@ -6,6 +6,11 @@ persistent grid-stride kernels.  For each entry point and input mode, the
 capped run must give the same bits as the default run (the chunked runs are
 checked against the oracle elsewhere), and per-bucket norms within their
 relative 1e-5 bar.
+
+By default the chunked and streaming kernels are launched with programmatic
+stream serialization (each waits on the device for its predecessor before
+touching memory); chains of launches where every kernel reads what the one
+just before it wrote must give the same bits with it switched off.
 """
 import numpy as np
 import pytest
@@ -117,3 +122,63 @@ def test_ddp_pieces_same_bits_under_a_grid_cap(setup, cap):
     a, b = _run_both(run, cap)
     _same(a, b, ("red", "w", "m", "v", "p"))
     _norms_close(a, b)
+
+
+def _run_launch_modes(fn):
+    outs = []
+    for on in (False, True):
+        dpg.dpg_set_programmatic_launch(on)
+        try:
+            outs.append(fn())
+        finally:
+            dpg.dpg_set_programmatic_launch(True)
+        torch.cuda.synchronize()
+    return outs
+
+
+@pytest.mark.parametrize("chain", ["accumulate", "per_bucket", "clipped", "gathers"])
+def test_programmatic_launch_same_bits(setup, chain):
+    plan, bf, bf2, f32, w0, tok = setup
+    N, R = plan.total_padded, len(bf)
+
+    def run():
+        s = _state(plan, w0)
+        if chain == "accumulate":
+            # acc <- g0, += g1, += (g2 + g3), then the fused step reads acc at once
+            accs = [torch.empty(N, device="cuda") for _ in range(R)]
+            for r in range(R):
+                dpg.dpg_accumulate(plan, bf[r], accs[r], True)
+                dpg.dpg_accumulate(plan, bf2[r], accs[r], False)
+                dpg.dpg_accumulate_pair(plan, bf[r], bf2[r], accs[r], False)
+            dpg.dpg_step(plan, accs, tok * 5, dpg.HParams(), s["w"], s["m"], s["v"], [s["p"]],
+                         last_micro=bf2, bucket_sqnorm=s["sq"], bucket_nonfinite=s["nf"])
+            s["red"] = accs[R - 1]
+        elif chain == "per_bucket":
+            # two steps, one launch per bucket; step 2 reads the state step 1 wrote
+            for t in (1, 2):
+                for b in range(plan.n_buckets):
+                    dpg.dpg_reduce_scatter_adam(plan, bf, tok, dpg.HParams(step=t), s["w"], s["m"],
+                                                s["v"], [s["p"]], b0=b, b1=b + 1)
+            dpg.dpg_step(plan, bf2, tok, dpg.HParams(step=3), s["w"], s["m"], s["v"], [s["p"]],
+                         bucket_sqnorm=s["sq"], bucket_nonfinite=s["nf"])
+        elif chain == "clipped":
+            # norm pass -> finalize -> coefficient -> update, twice
+            for t in (1, 2):
+                dpg.dpg_step_clipped(plan, bf, tok, dpg.HParams(step=t), 1e-4, s["w"], s["m"],
+                                     s["v"], [s["p"]], bucket_sqnorm=s["sq"],
+                                     bucket_nonfinite=s["nf"], reduced_grad=s["red"])
+        else:
+            # the step writes the shards; each gather reads them right after
+            views = [torch.zeros(N, dtype=torch.bfloat16, device="cuda") for _ in range(2)]
+            dpg.dpg_step(plan, bf, tok, dpg.HParams(), s["w"], s["m"], s["v"], [s["p"]],
+                         bucket_sqnorm=s["sq"], bucket_nonfinite=s["nf"])
+            for b in range(plan.n_buckets):
+                dpg.dpg_gather_params_bf16(plan, s["p"], views, b0=b, b1=b + 1)
+            dpg.dpg_allgather_params(plan, s["w"], [s["p"]])
+            s["g0"], s["g1"] = views
+        return s
+
+    a, b = _run_launch_modes(run)
+    keys = ("w", "m", "v", "p", "sq", "nf") + (("red",) if chain in ("accumulate", "clipped") else ())
+    keys += ("g0", "g1") if chain == "gathers" else ()
+    _same(a, b, keys)

@@ -41,6 +41,7 @@ EXPORTED = (
     "dpg_step_clipped", "dpg_step_staged", "dpg_check_device_status", "dpg_set_staged_fault",
     "dpg_allreduce_grads", "dpg_adam_from_reduced", "dpg_gather_params_bf16",
     "dpg_accumulate_pair", "dpg_step_fold2", "dpg_set_fused_max_ctas",
+    "dpg_set_programmatic_launch",
 )
 DPG_MAX_STATE_ARRAYS = 8
 DPG_NOALLOC_SCRATCH_BYTES = 8 << 20
@@ -107,6 +108,7 @@ def lib() -> ctypes.CDLL:
         L.dpg_accumulate.argtypes = [P, P, P, i32, P]
         L.dpg_accumulate_pair.argtypes = [P, P, P, P, i32, P]
         L.dpg_set_fused_max_ctas.argtypes = [i32]
+        L.dpg_set_programmatic_launch.argtypes = [i32]
         L.dpg_step_fold2.argtypes = [P, P, P, P, P, i32, P, P, P, P, P, i32, P, P, P]
         L.dpg_reduce_scatter_adam.argtypes = [P, P, i32, P, P, i32, P, P, P, P, P, i32, P, P, P,
                                               i32, i32, P]
@@ -133,7 +135,7 @@ def lib() -> ctypes.CDLL:
                      "dpg_step_clipped", "dpg_step_staged", "dpg_check_device_status",
                      "dpg_set_staged_fault", "dpg_allreduce_grads", "dpg_adam_from_reduced",
                      "dpg_gather_params_bf16", "dpg_accumulate_pair", "dpg_step_fold2",
-                     "dpg_set_fused_max_ctas"):
+                     "dpg_set_fused_max_ctas", "dpg_set_programmatic_launch"):
             getattr(L, name).restype = c_int
         _lib = L
     return _lib
@@ -600,8 +602,17 @@ def dpg_gather_params_bf16(plan: Plan, param_bf16: Ptr, param_views: Sequence[Pt
 
 
 def dpg_set_fused_max_ctas(max_ctas: int = 0):
-    """Cap the CTAs of later fused passes from this thread (0: one per SM)."""
+    """Cap the CTAs of later fused passes from this thread: > 0 selects the
+    persistent grid-stride kernels on at most max_ctas CTAs, 0 restores the
+    default chunked launch (one small CTA per 1024-element chunk)."""
     _check(lib().dpg_set_fused_max_ctas(int(max_ctas)))
+
+
+def dpg_set_programmatic_launch(on: bool = True):
+    """Programmatic dependent launch for later launches from this thread
+    (default on): same stream order and results, shorter gaps between
+    back-to-back kernels."""
+    _check(lib().dpg_set_programmatic_launch(1 if on else 0))
 
 
 def dpg_launch_count() -> int:

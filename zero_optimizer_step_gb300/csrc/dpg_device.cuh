@@ -256,6 +256,18 @@ __device__ __forceinline__ void flush_visit(const RsAdamArgs& a, int bucket, int
     if (threadIdx.x == 0) a.vis_bucket[slot] = bucket;
 }
 
+// Programmatic dependent launch.  A kernel launched with programmatic stream
+// serialization can be scheduled while the kernel before it in the stream is
+// still draining.  griddepcontrol.wait holds every thread until that kernel
+// has completed and its writes are visible (it returns at once for a plain
+// launch), so nothing is read or written before it; the trigger that follows
+// lets the next such kernel be scheduled in turn, to wait behind this one.
+// Every kernel launched through launch_k() starts with this.
+__device__ __forceinline__ void pdl_enter() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // Chunked launches: one 128-thread CTA per 1024-element chunk (a quarter of a
 // bucket-aligned tile), one 8-element vector per thread.
 constexpr int kChunkThreads = 128;

@@ -397,6 +397,7 @@ template <int RT, int MODE, int PHASE>
 __global__ void __launch_bounds__(kChunkThreads) k_rs_adam_chunk(const __grid_constant__ RsAdamArgs a) {
     // kNormOnly: reduce and scale only -- g to a.reduced, norm partials, no
     // Adam (the all-reduce of the DDP schedule)
+    pdl_enter();
     const int64_t c = blockIdx.x;                         // chunk of this launch
     const int64_t t = a.t0 + c / kChunksPerTile;
     const int b = __ldg(a.tile_bucket + t);
@@ -462,6 +463,7 @@ __global__ void __launch_bounds__(NT) k_norm_chunk(const __grid_constant__ RsAda
     constexpr int CH = NT * kVec;                         // elements per chunk
     constexpr int CPT = int(kTile / CH);
     static_assert(CPT >= 1 && CPT * CH == kTile, "a tile holds a whole number of chunks");
+    pdl_enter();
     const int64_t c = blockIdx.x;
     const int64_t t = a.t0 + c / CPT;
     const int b = __ldg(a.tile_bucket + t);
@@ -525,6 +527,7 @@ k_chunk_finalize(const double* __restrict__ chunk_sq, const int32_t* __restrict_
     constexpr int T = kChunkFinalizeThreads, U = 8;
     __shared__ double s_sq[T];
     __shared__ long long s_nf[T];
+    pdl_enter();
     const int b = b0 + blockIdx.x;
     const int64_t c0 = (__ldg(tile_begin + b) - t0) * cpt;
     const int64_t c1 = (__ldg(tile_begin + b + 1) - t0) * cpt;
@@ -568,6 +571,7 @@ k_chunk_finalize(const double* __restrict__ chunk_sq, const int32_t* __restrict_
 __global__ void __launch_bounds__(256) k_clip_coef(const double* __restrict__ bucket_sq, int32_t nb,
                                                    double max_norm, float* coef, float* out) {
     __shared__ double sh[256];
+    pdl_enter();
     double acc = 0.0;
     for (int b = threadIdx.x; b < nb; b += 256) acc += bucket_sq[b];
     sh[threadIdx.x] = acc;
@@ -711,15 +715,16 @@ static int launch_chunked(RsKernel fn, RsAdamArgs a, const Plan& p, bool want_no
         cudaEvent_t ev0 = t_fused_start, ev1 = t_fused_stop;
         t_fused_start = t_fused_stop = nullptr;
         if (ev0) DPG_CUDA_TRY(cudaEventRecord(ev0, s));
-        fn<<<unsigned(n_chunks), threads, 0, s>>>(a);
-        st = after_launch(who);
+        st = launch_k(fn, unsigned(n_chunks), threads, s, who, a);
         if (st != DPG_OK) return st;
         if (ev1) DPG_CUDA_TRY(cudaEventRecord(ev1, s));
     }
     if (want_norm) {
-        k_chunk_finalize<<<a.b1 - a.b0, kChunkFinalizeThreads, 0, s>>>(
-            p.d_chunk_sq, p.d_chunk_nf, p.d_tile_begin, a.t0, cpt, a.b0, sqnorm, nonfinite, sqnorm64);
-        st = after_launch(who);
+        st = launch_k(k_chunk_finalize, unsigned(a.b1 - a.b0), kChunkFinalizeThreads, s, who,
+                      static_cast<const double*>(p.d_chunk_sq),
+                      static_cast<const int32_t*>(p.d_chunk_nf),
+                      static_cast<const int64_t*>(p.d_tile_begin), a.t0, cpt, a.b0, sqnorm,
+                      nonfinite, sqnorm64);
     }
     return st;
 }
@@ -938,8 +943,8 @@ static int step_clipped(const dpg_plan_t* plan, const void* const* grads, int32_
     }
     if (st != DPG_OK) return st;
     // the coefficient, on the device: no host synchronisation
-    k_clip_coef<<<1, 256, 0, s>>>(p.d_bucket_sq64, p.n_buckets, max_norm, p.d_clip_coef, clip_out);
-    st = after_launch(who);
+    st = launch_k(k_clip_coef, 1, 256, s, who, static_cast<const double*>(p.d_bucket_sq64),
+                  p.n_buckets, max_norm, p.d_clip_coef, clip_out);
     if (st != DPG_OK) return st;
     // pass 2: g * coef -> Adam -> bf16 views, from the stored g or the replicas again
     RsAdamArgs a2 = a;

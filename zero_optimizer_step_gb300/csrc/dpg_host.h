@@ -6,6 +6,7 @@
 #include <atomic>
 #include <cstddef>
 #include <cstdint>
+#include <utility>
 
 #include "dpg_device.cuh"
 
@@ -29,6 +30,9 @@ extern thread_local int64_t t_staged_timeout_ns;
 // Upper bound on the CTAs of the fused passes launched from this thread (0:
 // the default chunked launch; > 0 selects the persistent grid-stride kernels).
 extern thread_local int32_t t_fused_max_ctas;
+// 1: the streaming and chunked kernels are launched with programmatic stream
+// serialization (the default); 0: plain stream-ordered launches.
+extern thread_local int32_t t_programmatic;
 
 int sm_count(int dev, int* out);
 // one CTA per unit of work (the streaming kernels)
@@ -39,6 +43,31 @@ bool aligned(const void* p, uintptr_t a);
 // checks the launch just issued and counts it
 int after_launch(const char* what);
 size_t round256(size_t x);
+
+// Launches kernel k (which must begin with pdl_enter()) on `grid` CTAs of
+// `block` threads, with programmatic stream serialization unless the calling
+// thread switched it off, then checks and counts the launch like
+// after_launch().
+template <typename... P, typename... A>
+int launch_k(void (*k)(P...), unsigned grid, unsigned block, cudaStream_t s, const char* who,
+             A&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(block);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = t_programmatic ? 1 : 0;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, k, std::forward<A>(args)...);
+    if (e != cudaSuccess) {
+        (void)cudaGetLastError();
+        return fail(DPG_ERR_CUDA, "%s: launch failed: %s", who, cudaGetErrorString(e));
+    }
+    return after_launch(who);
+}
 
 // Byte layout of a norm scratch with `visits` (CTA, bucket visit) slots for up
 // to `ctas` CTAs; every section starts on a 256-byte boundary.

@@ -20,6 +20,7 @@ thread_local cudaEvent_t t_fused_start = nullptr, t_fused_stop = nullptr;
 thread_local int64_t t_staged_skip = -1;
 thread_local int64_t t_staged_timeout_ns = 0;
 thread_local int32_t t_fused_max_ctas = 0;
+thread_local int32_t t_programmatic = 1;
 
 // ---------------------------------------------------------------------------
 // host helpers
@@ -238,6 +239,14 @@ int dpg_set_fused_max_ctas(int32_t max_ctas) {
     dpg::clear_error();
     if (max_ctas < 0) return fail(DPG_ERR_INVALID_ARG, "dpg_set_fused_max_ctas: %d < 0", max_ctas);
     dpg::t_fused_max_ctas = max_ctas;
+    return DPG_OK;
+}
+
+int dpg_set_programmatic_launch(int32_t on) {
+    dpg::clear_error();
+    if (on != 0 && on != 1)
+        return fail(DPG_ERR_INVALID_ARG, "dpg_set_programmatic_launch: %d is not 0 or 1", on);
+    dpg::t_programmatic = on;
     return DPG_OK;
 }
 

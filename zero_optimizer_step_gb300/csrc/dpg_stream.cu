@@ -18,6 +18,7 @@ namespace dpg {
 template <bool FIRST>
 __global__ void __launch_bounds__(256) k_accumulate(const uint16_t* __restrict__ g,
                                                     float* __restrict__ acc, int64_t n_vec) {
+    pdl_enter();
     for (int64_t k = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; k < n_vec;
          k += int64_t(gridDim.x) * blockDim.x) {
         const int64_t i = k * kVec;
@@ -44,6 +45,7 @@ template <bool FIRST>
 __global__ void __launch_bounds__(256) k_accumulate_pair(const uint16_t* __restrict__ ga,
                                                          const uint16_t* __restrict__ gb,
                                                          float* __restrict__ acc, int64_t n_vec) {
+    pdl_enter();
     for (int64_t k = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; k < n_vec;
          k += int64_t(gridDim.x) * blockDim.x) {
         const int64_t i = k * kVec;
@@ -71,6 +73,7 @@ struct ViewArgs {
 __global__ void __launch_bounds__(256) k_allgather(const float* __restrict__ master,
                                                    const __grid_constant__ ViewArgs va,
                                                    int64_t lo_vec, int64_t hi_vec) {
+    pdl_enter();
     for (int64_t k = lo_vec + int64_t(blockIdx.x) * blockDim.x + threadIdx.x; k < hi_vec;
          k += int64_t(gridDim.x) * blockDim.x) {
         const int64_t i = k * kVec;
@@ -86,6 +89,7 @@ __global__ void __launch_bounds__(256) k_allgather(const float* __restrict__ mas
 __global__ void __launch_bounds__(256) k_gather_bf16(const uint16_t* __restrict__ param,
                                                      const __grid_constant__ ViewArgs va,
                                                      int64_t lo_vec, int64_t hi_vec) {
+    pdl_enter();
     for (int64_t k = lo_vec + int64_t(blockIdx.x) * blockDim.x + threadIdx.x; k < hi_vec;
          k += int64_t(gridDim.x) * blockDim.x) {
         const uint4 x = ld_grad_u4(param + k * kVec);
@@ -216,9 +220,8 @@ int dpg_accumulate(const dpg_plan_t* plan, const void* flat_bf16, float* acc_f32
     if (st != DPG_OK) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const uint16_t* g = static_cast<const uint16_t*>(flat_bf16);
-    if (first) dpg::k_accumulate<true><<<grid, 256, 0, s>>>(g, acc_f32, n_vec);
-    else dpg::k_accumulate<false><<<grid, 256, 0, s>>>(g, acc_f32, n_vec);
-    return dpg::after_launch("dpg_accumulate");
+    return dpg::launch_k(first ? dpg::k_accumulate<true> : dpg::k_accumulate<false>, grid, 256, s,
+                         "dpg_accumulate", g, acc_f32, n_vec);
 }
 
 int dpg_accumulate_pair(const dpg_plan_t* plan, const void* micro_a_bf16, const void* micro_b_bf16,
@@ -239,9 +242,8 @@ int dpg_accumulate_pair(const dpg_plan_t* plan, const void* micro_a_bf16, const 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const uint16_t* ga = static_cast<const uint16_t*>(micro_a_bf16);
     const uint16_t* gb = static_cast<const uint16_t*>(micro_b_bf16);
-    if (first) dpg::k_accumulate_pair<true><<<grid, 256, 0, s>>>(ga, gb, acc_f32, n_vec);
-    else dpg::k_accumulate_pair<false><<<grid, 256, 0, s>>>(ga, gb, acc_f32, n_vec);
-    return dpg::after_launch("dpg_accumulate_pair");
+    return dpg::launch_k(first ? dpg::k_accumulate_pair<true> : dpg::k_accumulate_pair<false>, grid,
+                         256, s, "dpg_accumulate_pair", ga, gb, acc_f32, n_vec);
 }
 
 int dpg_allgather_params(const dpg_plan_t* plan, const float* master, void* const* views,
@@ -273,8 +275,8 @@ int dpg_allgather_params(const dpg_plan_t* plan, const float* master, void* cons
     int grid = 0;
     int st = dpg::grid_cover((hi - lo + 255) / 256, &grid, "dpg_allgather_params");
     if (st != DPG_OK) return st;
-    dpg::k_allgather<<<grid, 256, 0, static_cast<cudaStream_t>(stream)>>>(master, va, lo, hi);
-    return dpg::after_launch("dpg_allgather_params");
+    return dpg::launch_k(dpg::k_allgather, grid, 256, static_cast<cudaStream_t>(stream),
+                         "dpg_allgather_params", master, va, lo, hi);
 }
 
 int dpg_gather_params_bf16(const dpg_plan_t* plan, const void* param_bf16, void* const* views,
@@ -306,9 +308,9 @@ int dpg_gather_params_bf16(const dpg_plan_t* plan, const void* param_bf16, void*
     int grid = 0;
     int st = dpg::grid_cover((hi - lo + 255) / 256, &grid, "dpg_gather_params_bf16");
     if (st != DPG_OK) return st;
-    dpg::k_gather_bf16<<<grid, 256, 0, static_cast<cudaStream_t>(stream)>>>(
-        static_cast<const uint16_t*>(param_bf16), va, lo, hi);
-    return dpg::after_launch("dpg_gather_params_bf16");
+    return dpg::launch_k(dpg::k_gather_bf16, grid, 256, static_cast<cudaStream_t>(stream),
+                         "dpg_gather_params_bf16", static_cast<const uint16_t*>(param_bf16), va, lo,
+                         hi);
 }
 
 static int pack_common(const dpg_plan_t* plan, const void* const* ptrs, void* flat, int unpack,
