@@ -431,23 +431,33 @@ __global__ void __launch_bounds__(kChunkThreads) k_rs_adam_chunk(const __grid_co
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) sq += __shfl_xor_sync(0xFFFFFFFFu, sq, o);
         nf = __reduce_add_sync(0xFFFFFFFFu, nf);
-        __shared__ double w_sq[kChunkThreads / 32];
-        __shared__ int w_nf[kChunkThreads / 32];
+        constexpr int W = kChunkThreads / 32;
+        __shared__ double w_sq[W];
+        __shared__ int w_nf[W];
+        const int warp = threadIdx.x >> 5;
         if ((threadIdx.x & 31) == 0) {
-            w_sq[threadIdx.x >> 5] = double(sq);
-            w_nf[threadIdx.x >> 5] = nf;
+            w_sq[warp] = double(sq);
+            w_nf[warp] = nf;
         }
-        __syncthreads();
-        if (threadIdx.x == 0) {
-            double tot = 0.0;
-            int cnt = 0;
+        // Warps 1..W-1 only signal named barrier 1 (its arrive orders their
+        // slot writes before warp 0's reads) and retire; warp 0 waits for all
+        // kChunkThreads arrivals and sums the slots in warp order.  Every
+        // thread of the CTA reaches exactly one of the two instructions.
+        if (warp != 0) {
+            asm volatile("bar.arrive 1, %0;" ::"n"(kChunkThreads) : "memory");
+        } else {
+            asm volatile("bar.sync 1, %0;" ::"n"(kChunkThreads) : "memory");
+            if (threadIdx.x == 0) {
+                double tot = 0.0;
+                int cnt = 0;
 #pragma unroll
-            for (int k = 0; k < kChunkThreads / 32; ++k) {
-                tot += w_sq[k];
-                cnt += w_nf[k];
+                for (int k = 0; k < W; ++k) {
+                    tot += w_sq[k];
+                    cnt += w_nf[k];
+                }
+                a.chunk_sq[c] = tot;
+                a.chunk_nf[c] = cnt;
             }
-            a.chunk_sq[c] = tot;
-            a.chunk_nf[c] = cnt;
         }
     }
 }
