@@ -37,8 +37,9 @@
  *   - A plan uploads its tables to the current device on its first device
  *     call (a synchronous copy), or explicitly with dpg_plan_upload(); call
  *     that before capturing a stream into a CUDA graph.  A plan serves one
- *     device.  Calls that use the norm scratch of the same plan must not
- *     overlap on the GPU (issue them on one stream).
+ *     device.  Calls that use the norm scratch of the same plan (its
+ *     partials and per-bucket arrival counters, which every call leaves at
+ *     zero) must not overlap on the GPU (issue them on one stream).
  *   - Gradient INPUTS (grads, last_micro, the accumulate sources) of
  *     dpg_accumulate, dpg_accumulate_pair, dpg_reduce_scatter_adam, dpg_step,
  *     dpg_step_fold2, dpg_step_clipped and dpg_allreduce_grads may instead be

@@ -259,6 +259,43 @@ def test_norm_is_deterministic_across_runs():
     np.testing.assert_array_equal(res[0].gpu["sq"], res[1].gpu["sq"])
 
 
+def test_multi_segment_bucket_norms_and_counter_reset():
+    """A 20M-element parameter alone in its bucket (4883 tiles: three norm
+    segments of at most 2048 tiles) next to a small bucket, launched whole and
+    bucket by bucket; then one plan reused on other inputs: the per-bucket
+    arrival counters reset themselves, so its norms equal a fresh plan's."""
+    numels = [20_000_000, 3000, 777, 1_000_000]
+    for b_split in (None, 1):
+        res = run_case(StepCase(numels=numels, cap_bytes=16 << 20, R=2, seed=41, b_split=b_split))
+        assert res.plan.n_buckets == 2
+        assert_parity(res)
+
+    plan = dpg.dpg_plan_buckets(numels, 16 << 20, 2)
+    N = plan.total_padded
+    segs = segments(plan.param_offset, numels)
+
+    def norms(pl, seed):
+        g = [flat_grads_bf16(segs, N, 1e-3, stream_seed(seed, KIND_GRAD, r), device="cuda")
+             for r in range(2)]
+        w, m, v = (torch.zeros(N, device="cuda") for _ in range(3))
+        p = torch.empty(N, dtype=torch.bfloat16, device="cuda")
+        sq = torch.full((pl.n_buckets,), float("nan"), device="cuda")
+        nf = torch.full((pl.n_buckets,), -1, dtype=torch.int64, device="cuda")
+        dpg.dpg_step(pl, g, [100, 200], dpg.HParams(), w, m, v, [p], bucket_sqnorm=sq,
+                     bucket_nonfinite=nf)
+        torch.cuda.synchronize()
+        return sq, nf
+
+    a, _ = norms(plan, 41)
+    b, nfb = norms(plan, 42)
+    b2, _ = norms(plan, 42)
+    fresh = dpg.dpg_plan_buckets(numels, 16 << 20, 2)
+    bf, _ = norms(fresh, 42)
+    assert torch.isfinite(b).all() and not torch.equal(a, b)
+    assert torch.equal(b, bf) and torch.equal(b2, bf)
+    assert (nfb == 0).all()
+
+
 def test_launch_count_and_kernels():
     cfg = CONFIGS["tiny"]
     before = dpg.dpg_launch_count()

@@ -523,24 +523,47 @@ __global__ void __launch_bounds__(NT) k_norm_chunk(const __grid_constant__ RsAda
     }
 }
 
-// One CTA per bucket of a chunked launch starting at tile t0.  A bucket of a
-// large plan has 10^5 chunk partials and there are only tens of buckets, so
-// each thread keeps 8 loads in flight: thread j adds chunks j + 1024 k in
-// increasing k (8 at a time, in order), then a fixed tree combines the
-// threads -- the same order on every run.
+// Per-bucket norms of a chunked launch from its per-chunk partials.  One CTA
+// per segment (at most kSegTiles tiles of one bucket): thread j adds the
+// segment's chunks j + 1024 k in increasing k, 8 loads in flight, then a fixed
+// butterfly tree (within each warp, then over the 32 warp sums) gives the
+// segment's sum.  The CTA that completes a bucket's last segment (a per-bucket
+// arrival counter, which it resets to zero for the next launch) adds the
+// bucket's segment sums in segment order.  Every grouping is fixed by the
+// plan, so the result is the same on every run and for any bucket range.
 constexpr int kChunkFinalizeThreads = 1024;
 
+struct FinalizeArgs {
+    const double* chunk_sq;     // per-chunk partials of the launch (chunk 0 = tile t0)
+    const int32_t* chunk_nf;
+    const int64_t* tile_begin;  // plan tables
+    const int32_t* seg_first;
+    const int32_t* seg_bucket;
+    double* seg_sq;             // per-segment sums
+    long long* seg_nf;
+    int32_t* done;              // per-bucket arrival counters
+    int64_t t0;                 // first tile of the launch
+    int32_t cpt;                // chunks per tile
+    int32_t s0;                 // first segment of the launch
+    float* sqnorm;              // outputs, indexed by bucket (nullable)
+    int64_t* nonfinite;
+    double* sqnorm64;
+};
+
 __global__ void __launch_bounds__(kChunkFinalizeThreads)
-k_chunk_finalize(const double* __restrict__ chunk_sq, const int32_t* __restrict__ chunk_nf,
-                 const int64_t* __restrict__ tile_begin, int64_t t0, int32_t cpt, int32_t b0,
-                 float* sqnorm, int64_t* nonfinite, double* sqnorm64) {
-    constexpr int T = kChunkFinalizeThreads, U = 8;
-    __shared__ double s_sq[T];
-    __shared__ long long s_nf[T];
+k_chunk_finalize(const __grid_constant__ FinalizeArgs f) {
+    constexpr int T = kChunkFinalizeThreads, U = 8, NW = T / 32;
+    static_assert(NW == 32, "warp 0 combines one sum per warp, one per lane");
+    __shared__ double w_sq[NW];
+    __shared__ long long w_nf[NW];
     pdl_enter();
-    const int b = b0 + blockIdx.x;
-    const int64_t c0 = (__ldg(tile_begin + b) - t0) * cpt;
-    const int64_t c1 = (__ldg(tile_begin + b + 1) - t0) * cpt;
+    const int32_t s = f.s0 + int32_t(blockIdx.x);
+    const int b = __ldg(f.seg_bucket + s);
+    const int64_t span = kSegTiles * f.cpt;
+    const int64_t cb = (__ldg(f.tile_begin + b) - f.t0) * f.cpt;
+    const int64_t ce = (__ldg(f.tile_begin + b + 1) - f.t0) * f.cpt;
+    const int64_t c0 = cb + int64_t(s - __ldg(f.seg_first + b)) * span;
+    const int64_t c1 = c0 + span < ce ? c0 + span : ce;
     double acc = 0.0;
     long long cnt = 0;
     for (int64_t c = c0 + threadIdx.x; c < c1; c += int64_t(T) * U) {
@@ -549,8 +572,8 @@ k_chunk_finalize(const double* __restrict__ chunk_sq, const int32_t* __restrict_
 #pragma unroll
         for (int u = 0; u < U; ++u) {
             const int64_t k = c + int64_t(u) * T;
-            x[u] = k < c1 ? chunk_sq[k] : 0.0;
-            y[u] = k < c1 ? chunk_nf[k] : 0;
+            x[u] = k < c1 ? f.chunk_sq[k] : 0.0;
+            y[u] = k < c1 ? f.chunk_nf[k] : 0;
         }
 #pragma unroll
         for (int u = 0; u < U; ++u) {
@@ -558,21 +581,42 @@ k_chunk_finalize(const double* __restrict__ chunk_sq, const int32_t* __restrict_
             cnt += y[u];
         }
     }
-    s_sq[threadIdx.x] = acc;
-    s_nf[threadIdx.x] = cnt;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        acc += __shfl_xor_sync(0xFFFFFFFFu, acc, o);
+        cnt += __shfl_xor_sync(0xFFFFFFFFu, cnt, o);
+    }
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (lane == 0) {
+        w_sq[warp] = acc;
+        w_nf[warp] = cnt;
+    }
     __syncthreads();
-    for (int w = T / 2; w > 0; w >>= 1) {
-        if (threadIdx.x < w) {
-            s_sq[threadIdx.x] += s_sq[threadIdx.x + w];
-            s_nf[threadIdx.x] += s_nf[threadIdx.x + w];
-        }
-        __syncthreads();
+    if (warp != 0) return;
+    acc = w_sq[lane];
+    cnt = w_nf[lane];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        acc += __shfl_xor_sync(0xFFFFFFFFu, acc, o);
+        cnt += __shfl_xor_sync(0xFFFFFFFFu, cnt, o);
     }
-    if (threadIdx.x == 0) {
-        if (sqnorm) sqnorm[b] = float(s_sq[0]);
-        if (nonfinite) nonfinite[b] = s_nf[0];
-        if (sqnorm64) sqnorm64[b] = s_sq[0];
+    if (lane != 0) return;
+    f.seg_sq[s] = acc;
+    f.seg_nf[s] = cnt;
+    __threadfence();                      // the sums before the arrival
+    const int32_t first = __ldg(f.seg_first + b), end = __ldg(f.seg_first + b + 1);
+    if (atomicAdd(f.done + b, 1) != end - first - 1) return;
+    __threadfence();                      // every arrival before the reads
+    double tot = 0.0;
+    long long n = 0;
+    for (int32_t k = first; k < end; ++k) {
+        tot += __ldcg(f.seg_sq + k);
+        n += __ldcg(f.seg_nf + k);
     }
+    if (f.sqnorm) f.sqnorm[b] = float(tot);
+    if (f.nonfinite) f.nonfinite[b] = n;
+    if (f.sqnorm64) f.sqnorm64[b] = tot;
+    f.done[b] = 0;                        // ready for the next launch
 }
 
 // Global clip coefficient from the per-bucket squared norms (one CTA, fixed
@@ -730,11 +774,23 @@ static int launch_chunked(RsKernel fn, RsAdamArgs a, const Plan& p, bool want_no
         if (ev1) DPG_CUDA_TRY(cudaEventRecord(ev1, s));
     }
     if (want_norm) {
-        st = launch_k(k_chunk_finalize, unsigned(a.b1 - a.b0), kChunkFinalizeThreads, s, who,
-                      static_cast<const double*>(p.d_chunk_sq),
-                      static_cast<const int32_t*>(p.d_chunk_nf),
-                      static_cast<const int64_t*>(p.d_tile_begin), a.t0, cpt, a.b0, sqnorm,
-                      nonfinite, sqnorm64);
+        FinalizeArgs f{};
+        f.chunk_sq = p.d_chunk_sq;
+        f.chunk_nf = p.d_chunk_nf;
+        f.tile_begin = p.d_tile_begin;
+        f.seg_first = p.d_seg_first;
+        f.seg_bucket = p.d_seg_bucket;
+        f.seg_sq = p.d_seg_sq;
+        f.seg_nf = p.d_seg_nf;
+        f.done = p.d_bucket_done;
+        f.t0 = a.t0;
+        f.cpt = cpt;
+        f.s0 = p.seg_first[size_t(a.b0)];
+        f.sqnorm = sqnorm;
+        f.nonfinite = nonfinite;
+        f.sqnorm64 = sqnorm64;
+        const int32_t n_seg = p.seg_first[size_t(a.b1)] - f.s0;
+        if (n_seg > 0) st = launch_k(k_chunk_finalize, unsigned(n_seg), kChunkFinalizeThreads, s, who, f);
     }
     return st;
 }

@@ -40,6 +40,12 @@ constexpr int64_t kTile = int64_t(kThreads) * kVec;
 constexpr int64_t kPackChunk = 65536;
 constexpr int kPackPtrs = 1024;
 
+// The per-bucket norm of a chunked launch is summed by one finalize CTA per
+// segment of at most kSegTiles tiles of one bucket (8192 chunk partials: one
+// round of 8 loads for each of its 1024 threads); the last CTA of a bucket
+// adds its segments' sums.
+constexpr int64_t kSegTiles = 2048;
+
 struct PackItem {
     int32_t param;     // registration index of the parameter
     int32_t reserved;
@@ -80,6 +86,17 @@ struct Plan {
     int32_t* d_tile_bucket = nullptr;
     double* d_chunk_sq = nullptr;
     int32_t* d_chunk_nf = nullptr;
+    // chunk-norm finalize: segments of <= kSegTiles tiles, bucket b owning
+    // segments [seg_first[b], seg_first[b + 1]); per-segment sums; per-bucket
+    // arrival counters (zero between launches: the last CTA resets its own)
+    std::vector<int32_t> seg_first;   // n_buckets + 1 (host copy)
+    int32_t n_seg = 0;
+    void* d_seg = nullptr;            // one allocation, sections below
+    int32_t* d_seg_first = nullptr;   // n_buckets + 1
+    int32_t* d_seg_bucket = nullptr;  // n_seg
+    double* d_seg_sq = nullptr;       // n_seg
+    long long* d_seg_nf = nullptr;    // n_seg
+    int32_t* d_bucket_done = nullptr; // n_buckets
     // global-norm clipping: per-bucket fp64 squared norms and the coefficient
     void* d_clip = nullptr;
     double* d_bucket_sq64 = nullptr;  // n_buckets + 1

@@ -137,6 +137,30 @@ int upload(Plan& p) {
     const size_t csq_bytes = round256(n_chunks1 * sizeof(double));
     void* chunk = nullptr;
     if (e == cudaSuccess) e = cudaMalloc(&chunk, tb_bytes + csq_bytes + n_chunks1 * sizeof(int32_t));
+    // finalize segments: ceil(tiles / kSegTiles) per bucket, at least one
+    std::vector<int32_t> seg_first(nb1, 0), seg_bucket;
+    for (int32_t b = 0; b < p.n_buckets; ++b) {
+        const int64_t nt = p.tile_begin[b + 1] - p.tile_begin[b];
+        const int64_t ns = nt > 0 ? (nt + kSegTiles - 1) / kSegTiles : 1;
+        for (int64_t k = 0; k < ns; ++k) seg_bucket.push_back(b);
+        seg_first[size_t(b) + 1] = int32_t(seg_bucket.size());
+    }
+    const size_t n_seg1 = seg_bucket.empty() ? 1 : seg_bucket.size();
+    const size_t sf_bytes = round256(nb1 * sizeof(int32_t));
+    const size_t sb_bytes = round256(n_seg1 * sizeof(int32_t));
+    const size_t ss_bytes = round256(n_seg1 * sizeof(double));
+    const size_t sn_bytes = round256(n_seg1 * sizeof(long long));
+    const size_t done_bytes = round256(nb1 * sizeof(int32_t));
+    void* seg = nullptr;
+    if (e == cudaSuccess) e = cudaMalloc(&seg, sf_bytes + sb_bytes + ss_bytes + sn_bytes + done_bytes);
+    unsigned char* sbase = static_cast<unsigned char*>(seg);
+    if (e == cudaSuccess)
+        e = cudaMemcpy(sbase, seg_first.data(), nb1 * sizeof(int32_t), cudaMemcpyHostToDevice);
+    if (e == cudaSuccess && !seg_bucket.empty())
+        e = cudaMemcpy(sbase + sf_bytes, seg_bucket.data(), seg_bucket.size() * sizeof(int32_t),
+                       cudaMemcpyHostToDevice);
+    if (e == cudaSuccess)
+        e = cudaMemset(sbase + sf_bytes + sb_bytes + ss_bytes + sn_bytes, 0, done_bytes);
     std::vector<int32_t> tile_bucket(n_tiles1, 0);
     for (int32_t b = 0; b < p.n_buckets; ++b)
         for (int64_t t = p.tile_begin[b]; t < p.tile_begin[b + 1]; ++t) tile_bucket[size_t(t)] = b;
@@ -148,6 +172,7 @@ int upload(Plan& p) {
         e = cudaMemcpy(it, p.items.data(), p.items.size() * sizeof(PackItem), cudaMemcpyHostToDevice);
     if (e != cudaSuccess) {
         cudaFree(bo); cudaFree(tb); cudaFree(it); cudaFree(vis); cudaFree(clip); cudaFree(chunk);
+        cudaFree(seg);
         cudaGetLastError();
         return fail(e == cudaErrorMemoryAllocation ? DPG_ERR_OOM : DPG_ERR_CUDA,
                     "plan upload: %s", cudaGetErrorString(e));
@@ -169,6 +194,14 @@ int upload(Plan& p) {
     p.d_tile_bucket = static_cast<int32_t*>(chunk);
     p.d_chunk_sq = reinterpret_cast<double*>(static_cast<unsigned char*>(chunk) + tb_bytes);
     p.d_chunk_nf = reinterpret_cast<int32_t*>(static_cast<unsigned char*>(chunk) + tb_bytes + csq_bytes);
+    p.seg_first = std::move(seg_first);
+    p.n_seg = int32_t(seg_bucket.size());
+    p.d_seg = seg;
+    p.d_seg_first = reinterpret_cast<int32_t*>(sbase);
+    p.d_seg_bucket = reinterpret_cast<int32_t*>(sbase + sf_bytes);
+    p.d_seg_sq = reinterpret_cast<double*>(sbase + sf_bytes + sb_bytes);
+    p.d_seg_nf = reinterpret_cast<long long*>(sbase + sf_bytes + sb_bytes + ss_bytes);
+    p.d_bucket_done = reinterpret_cast<int32_t*>(sbase + sf_bytes + sb_bytes + ss_bytes + sn_bytes);
     p.cap_visits = cap_visits;
     p.cap_ctas = int32_t(cap_ctas);
     p.device = dev;
@@ -187,6 +220,7 @@ void release_device(Plan& p) {
         cudaFree(p.d_vis);
         cudaFree(p.d_clip);
         cudaFree(p.d_chunk);
+        cudaFree(p.d_seg);
     }
     if (have_cur) cudaSetDevice(cur);
     cudaGetLastError();
