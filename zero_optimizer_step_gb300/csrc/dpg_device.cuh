@@ -129,9 +129,9 @@ struct RsAdamArgs {
     int32_t decay;
     const float* g_in;      // kInReduced: the normalised reduced gradient
     const float* clip_coef; // kUpdate: device scalar, g <- g * coef
-    // chunked launches (one CTA per chunk): tile -> bucket map and the
-    // per-chunk norm partials (NULL: no norm)
-    const int32_t* tile_bucket;
+    // chunked launches (one CTA per chunk): per tile {first element, end of
+    // its bucket} and the per-chunk norm partials (NULL: no norm)
+    const longlong2* tile_span;
     double* chunk_sq;
     int32_t* chunk_nf;
 };

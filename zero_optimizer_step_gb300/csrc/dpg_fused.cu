@@ -399,13 +399,11 @@ __global__ void __launch_bounds__(kChunkThreads) k_rs_adam_chunk(const __grid_co
     // Adam (the all-reduce of the DDP schedule)
     pdl_enter();
     const int64_t c = blockIdx.x;                         // chunk of this launch
-    const int64_t t = a.t0 + c / kChunksPerTile;
-    const int b = __ldg(a.tile_bucket + t);
-    const int64_t i = __ldg(a.bucket_offset + b) + (t - __ldg(a.tile_begin + b)) * kTile +
-                      (c % kChunksPerTile) * kChunk + int64_t(threadIdx.x) * kVec;
+    const longlong2 span = __ldg(a.tile_span + a.t0 + c / kChunksPerTile);
+    const int64_t i = span.x + (c % kChunksPerTile) * kChunk + int64_t(threadIdx.x) * kVec;
     float sq = 0.0f;
     int nf = 0;
-    if (i < __ldg(a.bucket_offset + b + 1)) {
+    if (i < span.y) {
         float coef = 1.0f;
         if constexpr (PHASE == kUpdate) coef = __ldg(a.clip_coef);
         float s[8];
@@ -475,14 +473,12 @@ __global__ void __launch_bounds__(NT) k_norm_chunk(const __grid_constant__ RsAda
     static_assert(CPT >= 1 && CPT * CH == kTile, "a tile holds a whole number of chunks");
     pdl_enter();
     const int64_t c = blockIdx.x;
-    const int64_t t = a.t0 + c / CPT;
-    const int b = __ldg(a.tile_bucket + t);
-    const int64_t i = __ldg(a.bucket_offset + b) + (t - __ldg(a.tile_begin + b)) * kTile +
-                      (c % CPT) * CH + int64_t(threadIdx.x) * kVec;
+    const longlong2 span = __ldg(a.tile_span + a.t0 + c / CPT);
+    const int64_t i = span.x + (c % CPT) * CH + int64_t(threadIdx.x) * kVec;
     const bool norm = a.chunk_sq != nullptr;
     NormAcc acc;
     int nf = 0;
-    if (i < __ldg(a.bucket_offset + b + 1)) {
+    if (i < span.y) {
         float s[8];
         reduce_vector<RT, MODE>(a, i, s);
         norm_vector(a, i, s, acc, nf, norm);
@@ -758,7 +754,7 @@ static int launch_chunked(RsKernel fn, RsAdamArgs a, const Plan& p, bool want_no
                           int64_t* nonfinite, cudaStream_t s, const char* who,
                           double* sqnorm64 = nullptr, int threads = kChunkThreads) {
     const int cpt = int(kTile / (int64_t(threads) * kVec));   // chunks per tile
-    a.tile_bucket = p.d_tile_bucket;
+    a.tile_span = reinterpret_cast<const longlong2*>(p.d_tile_span);
     a.chunk_sq = want_norm ? p.d_chunk_sq : nullptr;
     a.chunk_nf = want_norm ? p.d_chunk_nf : nullptr;
     const int64_t n_chunks = (a.t1 - a.t0) * cpt;

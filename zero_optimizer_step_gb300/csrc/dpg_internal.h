@@ -80,10 +80,10 @@ struct Plan {
     int32_t* d_vis_count = nullptr; // cap_ctas
     int64_t cap_visits = 0;
     int32_t cap_ctas = 0;
-    // chunked launches: tile -> bucket map (n_tiles) and per-chunk norm
-    // partials (chunks_per_tile * n_tiles each), one allocation
+    // chunked launches: tile spans (n_tiles) and per-chunk norm partials
+    // (chunks_per_tile * n_tiles each), one allocation
     void* d_chunk = nullptr;
-    int32_t* d_tile_bucket = nullptr;
+    int64_t* d_tile_span = nullptr;     // 2 per tile: first element, end of its bucket
     double* d_chunk_sq = nullptr;
     int32_t* d_chunk_nf = nullptr;
     // chunk-norm finalize: segments of <= kSegTiles tiles, bucket b owning

@@ -130,10 +130,10 @@ int upload(Plan& p) {
     const size_t clip_sq_bytes = round256(nb1 * sizeof(double));
     void* clip = nullptr;
     if (e == cudaSuccess) e = cudaMalloc(&clip, clip_sq_bytes + 256);
-    // chunked launches: tile -> bucket map, then the per-chunk norm partials
+    // chunked launches: tile spans, then the per-chunk norm partials
     const size_t n_tiles1 = size_t(p.n_tiles > 0 ? p.n_tiles : 1);
     const size_t n_chunks1 = n_tiles1 * kChunksPerTile;
-    const size_t tb_bytes = round256(n_tiles1 * sizeof(int32_t));
+    const size_t tb_bytes = round256(n_tiles1 * 2 * sizeof(int64_t));
     const size_t csq_bytes = round256(n_chunks1 * sizeof(double));
     void* chunk = nullptr;
     if (e == cudaSuccess) e = cudaMalloc(&chunk, tb_bytes + csq_bytes + n_chunks1 * sizeof(int32_t));
@@ -161,11 +161,14 @@ int upload(Plan& p) {
                        cudaMemcpyHostToDevice);
     if (e == cudaSuccess)
         e = cudaMemset(sbase + sf_bytes + sb_bytes + ss_bytes + sn_bytes, 0, done_bytes);
-    std::vector<int32_t> tile_bucket(n_tiles1, 0);
+    std::vector<int64_t> tile_span(2 * n_tiles1, 0);
     for (int32_t b = 0; b < p.n_buckets; ++b)
-        for (int64_t t = p.tile_begin[b]; t < p.tile_begin[b + 1]; ++t) tile_bucket[size_t(t)] = b;
+        for (int64_t t = p.tile_begin[b]; t < p.tile_begin[b + 1]; ++t) {
+            tile_span[2 * size_t(t)] = p.bucket_offset[b] + (t - p.tile_begin[b]) * kTile;
+            tile_span[2 * size_t(t) + 1] = p.bucket_offset[b + 1];
+        }
     if (e == cudaSuccess)
-        e = cudaMemcpy(chunk, tile_bucket.data(), n_tiles1 * sizeof(int32_t), cudaMemcpyHostToDevice);
+        e = cudaMemcpy(chunk, tile_span.data(), tile_span.size() * sizeof(int64_t), cudaMemcpyHostToDevice);
     if (e == cudaSuccess) e = cudaMemcpy(bo, p.bucket_offset.data(), nb1 * sizeof(int64_t), cudaMemcpyHostToDevice);
     if (e == cudaSuccess) e = cudaMemcpy(tb, p.tile_begin.data(), nb1 * sizeof(int64_t), cudaMemcpyHostToDevice);
     if (e == cudaSuccess && !p.items.empty())
@@ -191,7 +194,7 @@ int upload(Plan& p) {
     p.d_clip_coef = reinterpret_cast<float*>(static_cast<unsigned char*>(clip) + clip_sq_bytes);
     p.d_status = reinterpret_cast<int32_t*>(static_cast<unsigned char*>(clip) + clip_sq_bytes + 128);
     p.d_chunk = chunk;
-    p.d_tile_bucket = static_cast<int32_t*>(chunk);
+    p.d_tile_span = static_cast<int64_t*>(chunk);
     p.d_chunk_sq = reinterpret_cast<double*>(static_cast<unsigned char*>(chunk) + tb_bytes);
     p.d_chunk_nf = reinterpret_cast<int32_t*>(static_cast<unsigned char*>(chunk) + tb_bytes + csq_bytes);
     p.seg_first = std::move(seg_first);
