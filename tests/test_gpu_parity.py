@@ -58,6 +58,7 @@ CASES = {
     "R64_max_replicas": dict(numels=_ragged(8, 10, 5_000), cap_bytes=1 << 14, R=64),
     "R8_split_launch": dict(numels=_ragged(9, 40, 100_000), cap_bytes=1 << 18, R=8, b_split=3),
     "R8_views_distinct": dict(numels=_ragged(10, 15, 40_000), cap_bytes=1 << 18, R=8, n_views=8),
+    "R2_views_max": dict(numels=_ragged(19, 8, 6_000), cap_bytes=1 << 14, R=2, n_views=64),
     "R8_tiny_buckets": dict(numels=_ragged(11, 500, 64), cap_bytes=256, R=8),
     "R4_oversize_param": dict(numels=[5, 300_001, 7, 0, 12], cap_bytes=4096, R=4),
     "R8_nan": dict(numels=_ragged(12, 10, 10_000), cap_bytes=1 << 15, R=8, inject="nan"),
