@@ -1128,11 +1128,9 @@ def run_overlap(a):
             eb.record(bwd_stream)
             if not overlap:
                 upd_stream.wait_event(eb)
-            with torch.cuda.stream(upd_stream):
-                for b in range(plan.n_buckets):
-                    upd_stream.wait_event(evs[b])
-                    dpg.dpg_reduce_scatter_adam(plan, g, tok, dpg.HParams(step=1), w, m, v, [p],
-                                                b0=b, b1=b + 1, stream=upd_stream)
+            # bucket b's update waits on its ready event, issued by the library
+            dpg.dpg_reduce_scatter_adam_when_ready(plan, g, tok, dpg.HParams(step=1), w, m, v, [p],
+                                                   ready_events=evs, stream=upd_stream)
             eu.record(upd_stream)
             torch.cuda.synchronize()
             return e0.elapsed_time(eb), e0.elapsed_time(eu)

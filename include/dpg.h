@@ -249,6 +249,30 @@ int dpg_reduce_scatter_adam(const dpg_plan_t* plan, const void* const* grads,
                             float* reduced_grad, int32_t b0, int32_t b1, void* stream);
 
 /* ---------------------------------------------------------------------------
+ * The same update issued bucket by bucket as the backward pass finishes each
+ *      ["Parallelisms" -- Gradient bucketing, Critical path: a bucket is
+ *       reduced as soon as its gradients are ready, overlapping the rest of
+ *       the backward]
+ * For b = b0 .. b1-1 in order: `stream` waits on ready_events[b - b0] (a
+ * cudaEvent_t the producer records once bucket b's gradients are complete in
+ * every replica; HOST array of b1 - b0 handles), then bucket b's update is
+ * launched on `stream` -- one fused launch (and, with a norm output, one
+ * finalize) per bucket, issued from C++ without returning to the caller.
+ * Arguments and results otherwise as dpg_reduce_scatter_adam over [b0, b1),
+ * to the bit.  All arguments are checked before the stream is given any
+ * wait or launch; a NULL ready_events (b1 > b0) or a NULL handle is
+ * DPG_ERR_INVALID_ARG.
+ * ------------------------------------------------------------------------- */
+int dpg_reduce_scatter_adam_when_ready(const dpg_plan_t* plan, const void* const* grads,
+                                       int32_t grads_dtype, const void* const* last_micro_bf16,
+                                       const int64_t* valid_tokens, int32_t n_counts,
+                                       const dpg_hparams* hp, float* master, float* exp_avg,
+                                       float* exp_avg_sq, void* const* param_views,
+                                       int32_t n_views, float* bucket_sqnorm,
+                                       int64_t* bucket_nonfinite, float* reduced_grad, int32_t b0,
+                                       int32_t b1, void* const* ready_events, void* stream);
+
+/* ---------------------------------------------------------------------------
  * All-gather / cast on its own, buckets [b0, b1)
  *      ["Parallelisms" -- ZeRO-1: workers all-gather the updated shards]
  * param_views[k][i] = bf16_rne(master[i]) for every element of the buckets.

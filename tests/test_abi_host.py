@@ -170,6 +170,39 @@ def test_reduce_scatter_adam_validation():
     assert dpg.lib().dpg_last_error() == b""
 
 
+def _rs_ready(plan, events, **over):
+    L = dpg.lib()
+    args = dict(grads=[FAKE] * plan.R, tokens=[10] * plan.R, hp=dpg.HParams(), master=FAKE,
+                b0=0, b1=plan.n_buckets)
+    args.update(over)
+    tok = np.asarray(args["tokens"], np.int64)
+    hp = args["hp"].c()
+    evs = None if events is None else (ctypes.c_void_p * max(1, len(events)))(*events)
+    return L.dpg_reduce_scatter_adam_when_ready(
+        plan.handle, dpg._ptrs(args["grads"]), dpg.DPG_BF16, None, tok.ctypes.data, tok.size,
+        ctypes.byref(hp), args["master"], FAKE, FAKE, dpg._ptrs([FAKE]), 1, None, None, None,
+        args["b0"], args["b1"], evs, None)
+
+
+def test_when_ready_validation():
+    """The event-gated per-bucket update checks its events, then every other
+    argument over the whole range, before it gives the stream any work."""
+    plan = dpg.dpg_plan_buckets([64, 32, 320], 2048, 4)
+    nb = plan.n_buckets
+    E = dpg
+    assert _rs_ready(plan, None) == E.DPG_ERR_INVALID_ARG
+    assert _rs_ready(plan, [FAKE] * (nb - 1) + [0]) == E.DPG_ERR_INVALID_ARG
+    assert _rs_ready(plan, [FAKE] * nb, tokens=[0] * 4) == E.DPG_ERR_ZERO_TOKENS
+    assert _rs_ready(plan, [FAKE] * nb, master=FAKE + 16) == E.DPG_ERR_MISALIGNED
+    assert _rs_ready(plan, [FAKE] * nb, grads=[FAKE, 0, FAKE, FAKE]) == E.DPG_ERR_INVALID_ARG
+    assert _rs_ready(plan, [FAKE] * nb, b0=2, b1=1) == E.DPG_ERR_INVALID_ARG
+    # an empty range needs no events and issues nothing
+    assert _rs_ready(plan, None, b0=1, b1=1) == E.DPG_OK
+    assert dpg.lib().dpg_reduce_scatter_adam_when_ready(
+        None, None, 0, None, None, 0, None, None, None, None, None, 0, None, None, None, 0, 0,
+        None, None) == E.DPG_ERR_INVALID_ARG
+
+
 def test_other_entry_points_validation():
     L = dpg.lib()
     plan = dpg.dpg_plan_buckets([64, 32, 320], 2048, 4)

@@ -5,7 +5,9 @@ its gradients are ready).
 A producer stream writes each bucket's replica gradients in backward-ready
 order (bucket 0 first), each after a GPU spin, and records an event; an
 update stream waits on each event and launches that bucket's fused update
-(programmatic launches on, the default).  The result -- master, moments,
+(programmatic launches on, the default), either through the library's
+event-gated entry (dpg_reduce_scatter_adam_when_ready) or bucket by bucket
+from Python.  The result -- master, moments,
 parameters, reduced gradient and per-bucket norms -- must be the bits of one
 whole-plan launch on the finished gradients: a kernel of the update stream
 never reads a bucket before its event, whatever the launch mode.
@@ -35,8 +37,9 @@ def _state(N, w0, nb):
                 nf=torch.full((nb,), -1, dtype=torch.int64, device="cuda"))
 
 
+@pytest.mark.parametrize("native", [True, False])
 @pytest.mark.parametrize("programmatic", [True, False])
-def test_event_gated_bucket_updates_equal_one_step(programmatic):
+def test_event_gated_bucket_updates_equal_one_step(programmatic, native):
     R = 4
     numels = random_param_list(np.random.Generator(np.random.Philox(77)), 60, 400_000)
     plan = dpg.dpg_plan_buckets(numels, 1 << 20, R)
@@ -69,13 +72,20 @@ def test_event_gated_bucket_updates_equal_one_step(programmatic):
                 for r in range(R):
                     grads[r][off[b]:off[b + 1]].copy_(src[r][off[b]:off[b + 1]])
                 events[b].record(producer)
-        with torch.cuda.stream(updater):
-            for b in range(nb):
-                updater.wait_event(events[b])
-                dpg.dpg_reduce_scatter_adam(plan, grads, tok, hp, got["w"], got["m"], got["v"],
-                                            [got["p"]], bucket_sqnorm=got["sq"],
-                                            bucket_nonfinite=got["nf"], reduced_grad=got["red"],
-                                            b0=b, b1=b + 1, stream=updater)
+        if native:                                # the library's event-gated entry
+            dpg.dpg_reduce_scatter_adam_when_ready(
+                plan, grads, tok, hp, got["w"], got["m"], got["v"], [got["p"]],
+                ready_events=events, bucket_sqnorm=got["sq"], bucket_nonfinite=got["nf"],
+                reduced_grad=got["red"], stream=updater)
+        else:                                     # the same schedule from Python
+            with torch.cuda.stream(updater):
+                for b in range(nb):
+                    updater.wait_event(events[b])
+                    dpg.dpg_reduce_scatter_adam(plan, grads, tok, hp, got["w"], got["m"],
+                                                got["v"], [got["p"]], bucket_sqnorm=got["sq"],
+                                                bucket_nonfinite=got["nf"],
+                                                reduced_grad=got["red"], b0=b, b1=b + 1,
+                                                stream=updater)
         torch.cuda.synchronize()
     finally:
         dpg.dpg_set_programmatic_launch(True)

@@ -41,7 +41,7 @@ EXPORTED = (
     "dpg_step_clipped", "dpg_step_staged", "dpg_check_device_status", "dpg_set_staged_fault",
     "dpg_allreduce_grads", "dpg_adam_from_reduced", "dpg_gather_params_bf16",
     "dpg_accumulate_pair", "dpg_step_fold2", "dpg_set_fused_max_ctas",
-    "dpg_set_programmatic_launch",
+    "dpg_set_programmatic_launch", "dpg_reduce_scatter_adam_when_ready",
 )
 DPG_MAX_STATE_ARRAYS = 8
 DPG_NOALLOC_SCRATCH_BYTES = 8 << 20
@@ -109,6 +109,8 @@ def lib() -> ctypes.CDLL:
         L.dpg_accumulate_pair.argtypes = [P, P, P, P, i32, P]
         L.dpg_set_fused_max_ctas.argtypes = [i32]
         L.dpg_set_programmatic_launch.argtypes = [i32]
+        L.dpg_reduce_scatter_adam_when_ready.argtypes = [P, P, i32, P, P, i32, P, P, P, P, P, i32,
+                                                         P, P, P, i32, i32, P, P]
         L.dpg_step_fold2.argtypes = [P, P, P, P, P, i32, P, P, P, P, P, i32, P, P, P]
         L.dpg_reduce_scatter_adam.argtypes = [P, P, i32, P, P, i32, P, P, P, P, P, i32, P, P, P,
                                               i32, i32, P]
@@ -135,7 +137,8 @@ def lib() -> ctypes.CDLL:
                      "dpg_step_clipped", "dpg_step_staged", "dpg_check_device_status",
                      "dpg_set_staged_fault", "dpg_allreduce_grads", "dpg_adam_from_reduced",
                      "dpg_gather_params_bf16", "dpg_accumulate_pair", "dpg_step_fold2",
-                     "dpg_set_fused_max_ctas", "dpg_set_programmatic_launch"):
+                     "dpg_set_fused_max_ctas", "dpg_set_programmatic_launch",
+                     "dpg_reduce_scatter_adam_when_ready"):
             getattr(L, name).restype = c_int
         _lib = L
     return _lib
@@ -418,6 +421,49 @@ def dpg_reduce_scatter_adam(plan: Plan, grads: Sequence[Ptr], valid_tokens, hp: 
         tok.ctypes.data, n_tok, ctypes.byref(hpc), _ptr(master), _ptr(exp_avg), _ptr(exp_avg_sq),
         _ptrs(param_views), len(param_views), _ptr(bucket_sqnorm), _ptr(bucket_nonfinite),
         _ptr(reduced_grad), b0, plan.n_buckets if b1 is None else b1, _stream(stream)))
+
+
+def _event_handle(e) -> Optional[int]:
+    if e is None or isinstance(e, int):
+        return e
+    return e.cuda_event          # torch.cuda.Event: its cudaEvent_t, once recorded
+
+
+def dpg_reduce_scatter_adam_when_ready(plan: Plan, grads: Sequence[Ptr], valid_tokens,
+                                       hp: HParams, master: Ptr, exp_avg: Ptr, exp_avg_sq: Ptr,
+                                       param_views: Sequence[Ptr] = (), *, ready_events,
+                                       last_micro: Sequence[Ptr] = None,
+                                       bucket_sqnorm: Ptr = None, bucket_nonfinite: Ptr = None,
+                                       reduced_grad: Ptr = None, b0: int = 0,
+                                       b1: Optional[int] = None,
+                                       grads_dtype: Optional[int] = None, stream=None):
+    """dpg_reduce_scatter_adam over [b0, b1), bucket b launched on `stream` only
+    after ready_events[b - b0] (recorded by the producer of its gradients)."""
+    if len(grads) != plan.R:
+        raise ValueError(f"need R={plan.R} gradient buffers, got {len(grads)}")
+    b1 = plan.n_buckets if b1 is None else b1
+    if len(ready_events) != max(0, b1 - b0):
+        raise ValueError(f"need {max(0, b1 - b0)} ready events, got {len(ready_events)}")
+    gd = _grad_dtype(grads) if grads_dtype is None else grads_dtype
+    N = plan.total_padded
+    for k, g in enumerate(grads):
+        _need_in(g, "bf16" if gd == DPG_BF16 else "f32", N, f"grads[{k}]")
+    for k, g in enumerate(last_micro or ()):
+        _need_in(g, "bf16", N, f"last_micro[{k}]")
+    for name, t in (("master", master), ("exp_avg", exp_avg), ("exp_avg_sq", exp_avg_sq),
+                    ("reduced_grad", reduced_grad)):
+        _need(t, "f32", N, name)
+    for k, t in enumerate(param_views):
+        _need(t, "bf16", N, f"param_views[{k}]")
+    _need(bucket_sqnorm, "f32", plan.n_buckets, "bucket_sqnorm")
+    tok, n_tok = _tokens(valid_tokens)
+    hpc = hp.c()
+    evs = (ctypes.c_void_p * max(1, len(ready_events)))(*[_event_handle(e) for e in ready_events])
+    _check(lib().dpg_reduce_scatter_adam_when_ready(
+        plan.handle, _ptrs(grads), gd, None if last_micro is None else _ptrs(last_micro),
+        tok.ctypes.data, n_tok, ctypes.byref(hpc), _ptr(master), _ptr(exp_avg), _ptr(exp_avg_sq),
+        _ptrs(param_views), len(param_views), _ptr(bucket_sqnorm), _ptr(bucket_nonfinite),
+        _ptr(reduced_grad), b0, b1, evs, _stream(stream)))
 
 
 def dpg_step(plan: Plan, grads: Sequence[Ptr], valid_tokens, hp: HParams, master: Ptr,

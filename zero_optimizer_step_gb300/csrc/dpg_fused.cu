@@ -796,7 +796,7 @@ static int rs_adam(const dpg_plan_t* plan, const void* const* grads, int32_t gra
                    const dpg_hparams* hp, float* master, float* m, float* v,
                    void* const* views, int32_t n_views, float* sqnorm, int64_t* nonfinite,
                    float* reduced, int32_t b0, int32_t b1, void* stream, const char* who,
-                   const void* const* last2 = nullptr) {
+                   const void* const* last2 = nullptr, bool check_only = false) {
     if (!plan) return fail(DPG_ERR_INVALID_ARG, "%s: plan is NULL", who);
     Plan& p = const_cast<dpg_plan_t*>(plan)->p;
     if (b0 < 0 || b1 < b0 || b1 > p.n_buckets)
@@ -848,7 +848,7 @@ static int rs_adam(const dpg_plan_t* plan, const void* const* grads, int32_t gra
     if (!aligned(master, 32) || !aligned(m, 32) || !aligned(v, 32) || !aligned(reduced, 32))
         return fail(DPG_ERR_MISALIGNED, "%s: fp32 buffers must be 32-byte aligned", who);
     st = upload(p);
-    if (st != DPG_OK) return st;
+    if (st != DPG_OK || check_only) return st;
 
     a.master = master;
     a.m = m;
@@ -1199,6 +1199,41 @@ int dpg_reduce_scatter_adam(const dpg_plan_t* plan, const void* const* grads, in
     return dpg::rs_adam(plan, grads, grads_dtype, last_micro_bf16, valid_tokens, n_counts, hp,
                         master, exp_avg, exp_avg_sq, param_views, n_views, bucket_sqnorm,
                         bucket_nonfinite, reduced_grad, b0, b1, stream, "dpg_reduce_scatter_adam");
+}
+
+int dpg_reduce_scatter_adam_when_ready(const dpg_plan_t* plan, const void* const* grads,
+                                       int32_t grads_dtype, const void* const* last_micro_bf16,
+                                       const int64_t* valid_tokens, int32_t n_counts,
+                                       const dpg_hparams* hp, float* master, float* exp_avg,
+                                       float* exp_avg_sq, void* const* param_views,
+                                       int32_t n_views, float* bucket_sqnorm,
+                                       int64_t* bucket_nonfinite, float* reduced_grad, int32_t b0,
+                                       int32_t b1, void* const* ready_events, void* stream) {
+    dpg::clear_error();
+    const char* who = "dpg_reduce_scatter_adam_when_ready";
+    const dpg::Trace trace(who);
+    // every argument is checked once, over the whole range, before the stream
+    // is given any wait or launch
+    if (!plan) return fail(DPG_ERR_INVALID_ARG, "%s: plan is NULL", who);
+    if (b0 >= 0 && b1 > b0 && b1 <= plan->p.n_buckets) {
+        if (!ready_events) return fail(DPG_ERR_INVALID_ARG, "%s: ready_events is NULL", who);
+        for (int32_t b = b0; b < b1; ++b)
+            if (!ready_events[b - b0])
+                return fail(DPG_ERR_INVALID_ARG, "%s: ready_events[%d] is NULL", who, b - b0);
+    }
+    int st = dpg::rs_adam(plan, grads, grads_dtype, last_micro_bf16, valid_tokens, n_counts, hp,
+                          master, exp_avg, exp_avg_sq, param_views, n_views, bucket_sqnorm,
+                          bucket_nonfinite, reduced_grad, b0, b1, stream, who, nullptr, true);
+    if (st != DPG_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    for (int32_t b = b0; b < b1; ++b) {
+        DPG_CUDA_TRY(cudaStreamWaitEvent(s, static_cast<cudaEvent_t>(ready_events[b - b0]), 0));
+        st = dpg::rs_adam(plan, grads, grads_dtype, last_micro_bf16, valid_tokens, n_counts, hp,
+                          master, exp_avg, exp_avg_sq, param_views, n_views, bucket_sqnorm,
+                          bucket_nonfinite, reduced_grad, b, b + 1, stream, who);
+        if (st != DPG_OK) return st;
+    }
+    return DPG_OK;
 }
 
 int dpg_step(const dpg_plan_t* plan, const void* const* grads, int32_t grads_dtype,
