@@ -1,9 +1,11 @@
 /*
  * A C client of the library: no Python, no PyTorch.  It plans the tiny
  * three-parameter case ([64,32], [32], [32,10], R = 4, 2048-byte buckets),
- * allocates every buffer with the CUDA runtime, runs two dpg_step calls and
- * one dpg_allgather_params, and compares every output bit for bit with the
- * oracle (a test-only C library) run on the same inputs.
+ * allocates every buffer with the CUDA runtime, runs one dpg_step, a second
+ * step through dpg_reduce_scatter_adam_when_ready gated on per-bucket events
+ * recorded on another stream, and one dpg_allgather_params, and compares
+ * every output bit for bit with the oracle (a test-only C library) run on the
+ * same inputs.
  * Exit status 0 on a match; prints the first mismatch otherwise.
  * Inputs: a fixed xorshift stream of normals (Box-Muller), plain and
  * reproducible; nothing here computes the method's arithmetic.
@@ -142,10 +144,27 @@ int main(void) {
     const void* gptr[R];
     for (int r = 0; r < R; ++r) gptr[r] = hg[r];
     void* views[1] = {dview};
+    /* the second step waits, bucket by bucket, on events a producer stream records */
+    cudaStream_t producer;
+    CHECK_CUDA(cudaStreamCreateWithFlags(&producer, cudaStreamNonBlocking));
+    cudaEvent_t ready[8];
+    if (n_buckets > 8) {
+        fprintf(stderr, "unexpected bucket count %d\n", n_buckets);
+        return 7;
+    }
+    for (int32_t b = 0; b < n_buckets; ++b) {
+        CHECK_CUDA(cudaEventCreateWithFlags(&ready[b], cudaEventDisableTiming));
+        CHECK_CUDA(cudaEventRecord(ready[b], producer));
+    }
     for (int64_t t = 1; t <= 2; ++t) {
         dpg_hparams hp = {1e-3, 0.9, 0.999, 1e-8, 0.0, t};
-        CHECK_DPG(dpg_step(plan, (const void* const*)dg, DPG_BF16, NULL, tokens, R, &hp, dw, dm,
-                           dv, views, 1, dsq, dnf, s));
+        if (t == 1)
+            CHECK_DPG(dpg_step(plan, (const void* const*)dg, DPG_BF16, NULL, tokens, R, &hp, dw,
+                               dm, dv, views, 1, dsq, dnf, s));
+        else
+            CHECK_DPG(dpg_reduce_scatter_adam_when_ready(
+                plan, (const void* const*)dg, DPG_BF16, NULL, tokens, R, &hp, dw, dm, dv, views,
+                1, dsq, dnf, NULL, 0, n_buckets, (void* const*)ready, s));
         uint16_t* ov_ptr[1] = {oview};
         if (oracle_step(n_buckets, bo, bp, R, gptr, 0, NULL, tokens, R, 1e-3, 0.9, 0.999, 1e-8,
                         0.0, t, ow, om, ov, ov_ptr, 1, NULL, osq) != 0) {
@@ -198,12 +217,15 @@ int main(void) {
     cudaFree(dview2);
     cudaFree(dsq);
     cudaFree(dnf);
+    for (int32_t b = 0; b < n_buckets; ++b) cudaEventDestroy(ready[b]);
+    cudaStreamDestroy(producer);
     cudaStreamDestroy(s);
     dpg_plan_destroy(plan);
     free(hw); free(ow); free(om); free(ov); free(oview);
     free(gw); free(gm); free(gv); free(gview); free(gview2);
     if (!ok) return 1;
-    printf("C client: %lld elements, %d buckets, two steps and an all-gather bit-exact\n",
+    printf("C client: %lld elements, %d buckets, two steps (one event-gated) and an "
+           "all-gather bit-exact\n",
            (long long)n, n_buckets);
     return 0;
 }
