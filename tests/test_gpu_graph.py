@@ -99,7 +99,14 @@ def test_captured_accumulation_cycle_replays():
     with torch.cuda.graph(gr, stream=s):
         cycle(graph, acc_g)
     for _ in range(2):
+        # poison the norm outputs: each replay must write them again (the
+        # finalize's per-bucket arrival counters are back at zero after every
+        # launch, replayed or not)
+        for buf in (graph, eager):
+            buf["sq"].fill_(float("nan"))
+            buf["nf"].fill_(-1)
         gr.replay()
         cycle(eager, acc_e)
-    torch.cuda.synchronize()
+        torch.cuda.synchronize()
+        assert torch.isfinite(graph["sq"]).all() and (graph["nf"] >= 0).all()
     _same(eager, graph)
