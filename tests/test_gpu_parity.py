@@ -88,6 +88,19 @@ def test_step_parity(name):
         assert res.gpu["nf"].sum() > 0
 
 
+@pytest.mark.parametrize("cap_bytes", [4096, 1 << 20, 256 << 20])
+def test_sweep_list_parity(cap_bytes):
+    """The 10,000-tensor sweep list at its real size (about 4.9M parameters,
+    1 to 4096 elements each): at 4 KiB caps 2595 buckets, most of them a
+    single tile or less, up to one bucket holding everything."""
+    cfg = CONFIGS["sweep"]
+    res = run_case(StepCase(numels=cfg.numels, cap_bytes=cap_bytes, R=cfg.R, seed=cfg.seed,
+                            grad_std=1e-3))
+    assert res.plan.n_buckets == {4096: 2595, 1 << 20: 10, 256 << 20: 1}[cap_bytes]
+    assert_parity(res)
+    assert exact_everywhere(res)
+
+
 def test_empty_plan_is_a_no_op():
     res = run_case(StepCase(numels=[], cap_bytes=1024, R=4))
     assert res.plan.n_buckets == 0 and res.plan.total_padded == 0
