@@ -65,6 +65,9 @@ def parse():
                          "fused kernel's mean DRAM bytes per launch to profiles/traffic.json")
     ap.add_argument("--replicas", type=int, default=None,
                     help="override the workload's R (simulated data-parallel replicas, 1..64)")
+    ap.add_argument("--deferred", action="store_true",
+                    help="K >= 2: deferred accumulation (K bf16 gradient buffers per replica, all "
+                         "summed inside the fused step; no accumulation pass)")
     ap.add_argument("--fold2", action="store_true",
                     help="K >= 3: paired accumulation (two bf16 gradient buffers per replica), "
                          "the last two microbatches folded into the fused step")
@@ -95,6 +98,8 @@ def parse():
     a = ap.parse_args()
     if a.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if a.deferred and a.fold2:
+        ap.error("--deferred and --fold2 are two different accumulation schedules")
     return a
 
 
@@ -148,7 +153,7 @@ def cap_of(cfg, a) -> int:
     return int(a.cap_mib * (1 << 20)) if a.cap_mib else cfg.cap_bytes
 
 
-def workload_desc(cfg, cap, plan_nb, total, fold2=False) -> dict:
+def workload_desc(cfg, cap, plan_nb, total, fold2=False, deferred=False) -> dict:
     d = {"workload": f"{cfg.name}: {len(cfg.shapes)} tensors, psi={cfg.psi}, R={cfg.R} simulated "
                      f"replicas, {cap / (1 << 20):g} MiB buckets, K={cfg.K} microbatch(es), ZeRO-2 "
                      f"fused reduce-scatter+Adam+all-gather",
@@ -156,7 +161,9 @@ def workload_desc(cfg, cap, plan_nb, total, fold2=False) -> dict:
          "total_padded": total, "grad_dtype": "bf16", "state_dtype": "f32",
          "param_views": 1, "l2": "inputs larger than L2 (no flush)"}
     if cfg.K > 1:
-        d["accumulation"] = ("paired: two bf16 gradient buffers per replica; microbatches folded "
+        d["accumulation"] = ("deferred: K bf16 gradient buffers per replica, every microbatch "
+                             "summed inside the fused step (no accumulation pass)" if deferred else
+                             "paired: two bf16 gradient buffers per replica; microbatches folded "
                              "into the fp32 buffers two at a time, the last two into the fused "
                              "step" if fold2 else
                              "one fp32 pass per microbatch, the last folded into the fused step")
@@ -175,8 +182,10 @@ def fold2_schedule(K: int):
     return out
 
 
-def algorithmic_bytes_per_param(cfg, fold2=False) -> dict:
+def algorithmic_bytes_per_param(cfg, fold2=False, deferred=False) -> dict:
     R, K = cfg.R, cfg.K
+    if K > 1 and deferred:
+        return {"fused": 2 * K * R + 26, "step": 2 * K * R + 26}
     if K > 1 and fold2:
         fused = 8 * R + 26
         acc = sum((8 if k == 0 else 12) * R if pair else (6 if k == 0 else 10) * R
@@ -433,10 +442,16 @@ def run_dpg(a):
     segs = segments(plan.param_offset, cfg.numels)
     dev = torch.device("cuda", local)
     tokens = token_counts(cfg)
-    g = [flat_grads_bf16(segs, N, cfg.grad_std, stream_seed(cfg.seed, KIND_GRAD, r, 0), device=dev)
-         for r in range(R)]
-    acc = [torch.empty(N, device=dev) for _ in range(R)] if K > 1 else None
+    deferred = bool(a.deferred) and K >= 2
     fold2 = bool(a.fold2) and K >= 3
+    # deferred accumulation keeps every microbatch: R x K distinct bf16 buffers
+    gd = ([[flat_grads_bf16(segs, N, cfg.grad_std, stream_seed(cfg.seed, KIND_GRAD, r, k),
+                            device=dev) for k in range(K)] for r in range(R)]
+          if deferred else None)
+    g = (None if deferred else
+         [flat_grads_bf16(segs, N, cfg.grad_std, stream_seed(cfg.seed, KIND_GRAD, r, 0), device=dev)
+          for r in range(R)])
+    acc = [torch.empty(N, device=dev) for _ in range(R)] if K > 1 and not deferred else None
     # paired accumulation keeps a second bf16 gradient buffer per replica
     g2 = ([flat_grads_bf16(segs, N, cfg.grad_std, stream_seed(cfg.seed, KIND_GRAD, r, 1), device=dev)
            for r in range(R)] if fold2 else None)
@@ -452,6 +467,12 @@ def run_dpg(a):
     def step(ev_pair=None):
         state["t"] += 1
         hp = dpg.HParams(step=state["t"])
+        if deferred:
+            if ev_pair is not None:
+                dpg.dpg_time_next_fused_launch(*ev_pair)
+            dpg.dpg_step_deferred(plan, gd, tokens, hp, w, m, v, [param], bucket_sqnorm=sq,
+                                  bucket_nonfinite=nf, stream=stream)
+            return
         if fold2:
             for k, pair in fold2_schedule(K):
                 for r in range(R):
@@ -517,11 +538,11 @@ def run_dpg(a):
 
     # end to end: host (pinned) gradients copied in, norms copied out, every step
     e2e = None
-    if not a.no_e2e:
+    if not a.no_e2e and not deferred:
         e2e = run_e2e(a, dpg, plan, g, acc, w, m, v, param, sq, nf, tokens, cfg, dev, stream,
                       state, world, fold2)
 
-    bpp = algorithmic_bytes_per_param(cfg, fold2)
+    bpp = algorithmic_bytes_per_param(cfg, fold2, deferred)
     peak, peak_kind = load_peak()
     achieved = bpp["fused"] * cfg.psi / (k_ms * 1e-3) / 1e9
     traffic = traffic_per_launch(cfg, cap, N)
@@ -532,7 +553,7 @@ def run_dpg(a):
         "value": value, "unit": "params/s", "n_gpus": world, "steps": a.steps,
         "warmup": a.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": workload_desc(cfg, cap, plan.n_buckets, N, fold2),
+        "config": workload_desc(cfg, cap, plan.n_buckets, N, fold2, deferred),
         "hbm_gbs_step": bpp["step"] * cfg.psi / (ms * 1e-3) / 1e9,
         "roofline": {"bound": "hbm", "kernel": fused_kernel_name(a, R, K), "achieved": achieved,
                      "peak": peak, "peak_kind": f"{peak_kind} (copy bandwidth)", "unit": "GB/s",

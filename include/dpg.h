@@ -205,6 +205,34 @@ int dpg_accumulate_pair(const dpg_plan_t* plan, const void* micro_a_bf16,
  * acc_f32: R fp32 flat buffers, 32-byte aligned.  valid_tokens counts every
  * microbatch of the cycle (R*K counts).  Norm outputs as dpg_step.
  * ------------------------------------------------------------------------- */
+/* ---------------------------------------------------------------------------
+ * Deferred accumulation: the step of a K-microbatch cycle with no
+ * accumulation pass before it
+ *      ["Distributed Training and Parallelism" -- Data parallelism and the
+ *       global gradient (no_sync: no intermediate reductions; the global
+ *       count covers every microbatch)]
+ * A caller that keeps each replica's K microbatch gradients in K bf16 flat
+ * buffers (2K bytes per parameter per replica, against 4 + 2 for one fp32
+ * accumulator and one bf16 buffer) hands them all to the fused pass, which
+ * computes for every element
+ *   x_r = ((f32(g[r][0]) + f32(g[r][1])) + ...) + f32(g[r][K-1])   (binary32)
+ *   s   = x_0 + x_1 + ... + x_{R-1}                               (rank order)
+ * -- exactly the sums of K-1 dpg_accumulate passes followed by dpg_step with
+ * the last microbatch fused -- then scales, runs Adam and casts as dpg_step.
+ * One pass moves 2KR + 26 bytes per parameter for the whole cycle.
+ * micro_bf16: HOST array of R*K DEVICE (or page-locked host) pointers,
+ *   replica-major (micro_bf16[r*K + k] = microbatch k of replica r), 16-byte
+ *   aligned; 1 <= K and R*K <= DPG_MAX_REPLICAS (else DPG_ERR_INVALID_ARG).
+ * valid_tokens counts every microbatch of the cycle (R*K counts).  Norm
+ * outputs as dpg_step.  Always the chunked launch (a grid cap set with
+ * dpg_set_fused_max_ctas does not apply).
+ * ------------------------------------------------------------------------- */
+int dpg_step_deferred(const dpg_plan_t* plan, const void* const* micro_bf16, int32_t K,
+                      const int64_t* valid_tokens, int32_t n_counts, const dpg_hparams* hp,
+                      float* master, float* exp_avg, float* exp_avg_sq, void* const* param_views,
+                      int32_t n_views, float* bucket_sqnorm, int64_t* bucket_nonfinite,
+                      void* stream);
+
 int dpg_step_fold2(const dpg_plan_t* plan, const float* const* acc_f32,
                    const void* const* micro_a_bf16, const void* const* micro_b_bf16,
                    const int64_t* valid_tokens, int32_t n_counts, const dpg_hparams* hp,

@@ -203,6 +203,30 @@ def test_when_ready_validation():
         None, None) == E.DPG_ERR_INVALID_ARG
 
 
+def test_step_deferred_validation():
+    """Deferred accumulation checks K, R*K and every microbatch pointer before
+    any device work."""
+    plan = dpg.dpg_plan_buckets([64, 32, 320], 2048, 4)
+    L = dpg.lib()
+    hp = dpg.HParams().c()
+
+    def call(micro, K, tokens=None):
+        tok = np.asarray(tokens if tokens is not None else [10] * (4 * max(K, 1)), np.int64)
+        return L.dpg_step_deferred(plan.handle, None if micro is None else dpg._ptrs(micro), K,
+                                   tok.ctypes.data, tok.size, ctypes.byref(hp), FAKE, FAKE, FAKE,
+                                   dpg._ptrs([FAKE]), 1, None, None, None)
+
+    E = dpg
+    assert call([FAKE] * 4, 0) == E.DPG_ERR_INVALID_ARG
+    assert call([FAKE] * 68, 17) == E.DPG_ERR_INVALID_ARG          # R*K > 64
+    assert call(None, 2) == E.DPG_ERR_INVALID_ARG
+    assert call([FAKE] * 7 + [0], 2) == E.DPG_ERR_INVALID_ARG       # a later microbatch NULL
+    assert call([FAKE] * 7 + [FAKE + 2], 2) == E.DPG_ERR_MISALIGNED
+    assert call([FAKE] * 8, 2, tokens=[0] * 8) == E.DPG_ERR_ZERO_TOKENS
+    assert L.dpg_step_deferred(None, None, 1, None, 0, None, None, None, None, None, 0, None,
+                               None, None) == E.DPG_ERR_INVALID_ARG
+
+
 def test_other_entry_points_validation():
     L = dpg.lib()
     plan = dpg.dpg_plan_buckets([64, 32, 320], 2048, 4)

@@ -1,7 +1,8 @@
 """Host logic of bench.py that the reported numbers depend on (no GPU).
 
 * algorithmic bytes per parameter of every schedule: (2R + 26) for the step,
-  the K-microbatch cycle (10K - 8)R + 26, and the paired schedule;
+  the K-microbatch cycle (10K - 8)R + 26, the paired schedule, and the
+  deferred one (2KR + 26);
 * the paired accumulation schedule covers microbatches 0..K-3 in order;
 * the ncu launch-list parser behind `roofline.traffic` averages the fused
   kernel's DRAM bytes over its launches and ignores every other kernel;
@@ -27,6 +28,9 @@ def test_algorithmic_bytes_of_the_workloads():
     assert bench.algorithmic_bytes_per_param(c) == {"fused": 50, "step": 154}
     # paired: one first pair (8R) + the fused step with two microbatches (8R + 26)
     assert bench.algorithmic_bytes_per_param(c, fold2=True) == {"fused": 58, "step": 90}
+    # deferred: one pass reading all K bf16 microbatches of every replica
+    assert bench.algorithmic_bytes_per_param(c, deferred=True) == {"fused": 58, "step": 58}
+    assert bench.algorithmic_bytes_per_param(_cfg(8, 3), deferred=True)["step"] == 2 * 3 * 8 + 26
 
 
 def _cfg(R, K):

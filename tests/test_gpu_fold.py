@@ -165,3 +165,85 @@ def test_fold2_reads_pinned_host_microbatches():
         outs.append((*d, p))
     for a, b in zip(*outs):
         assert torch.equal(a.view(torch.uint8), b.view(torch.uint8))
+
+
+# ---------------------------------------------------------------------------
+# deferred accumulation: every microbatch kept in bf16, summed in the step
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("R,K,warm", [(4, 4, False), (8, 4, True), (3, 6, False), (1, 1, False),
+                                      (2, 3, True), (4, 2, False), (16, 4, False)])
+def test_deferred_cycle_matches_oracle(R, K, warm):
+    """dpg_step_deferred on R x K bf16 microbatch buffers equals the oracle's
+    K - 1 accumulations (one microbatch at a time) followed by its step with
+    the last microbatch, bit for bit.  K = 4 runs the kernel with K fixed at
+    compile time, the others the run-time K; R = 3 and 16 the generic
+    replica loop."""
+    plan, op, micro, tok = _micro(R, K, seed=70 + R * 10 + K, n=30, mx=60_000, cap=1 << 18)
+    N = op.total_padded
+    w0 = master_f32(N, stream_seed(71, KIND_MASTER))
+    if warm:
+        m0, v0 = warm_moments(N, 1e-3, stream_seed(71, KIND_M), stream_seed(71, KIND_V))
+    else:
+        m0, v0 = torch.zeros(N), torch.zeros(N)
+    t = 5 if warm else 1
+    dm = [[x.cuda() for x in row] for row in micro]
+    d = [w0.cuda(), m0.cuda(), v0.cuda()]
+    view = torch.empty(N, dtype=torch.bfloat16, device="cuda")
+    sq = torch.empty(op.n_buckets, device="cuda")
+    nf = torch.empty(op.n_buckets, dtype=torch.int64, device="cuda")
+    dpg.dpg_step_deferred(plan, dm, tok, dpg.HParams(step=t), *d, [view], bucket_sqnorm=sq,
+                          bucket_nonfinite=nf)
+    torch.cuda.synchronize()
+
+    hm = [[np_bf16(x) for x in row] for row in micro]
+    w, m, v = np_f32(w0).copy(), np_f32(m0).copy(), np_f32(v0).copy()
+    if K == 1:
+        views, red, rsq = oracle.step(op.bucket_offset, op.bucket_padded, [hm[r][0] for r in range(R)],
+                                      tok, w, m, v, n_views=1, t=t, want_reduced=True)
+    else:
+        accs = [np.empty(N, np.float32) for _ in range(R)]
+        for r in range(R):
+            for k in range(K - 1):
+                oracle.accumulate(hm[r][k], accs[r], first=(k == 0))
+        views, red, rsq = oracle.step(op.bucket_offset, op.bucket_padded, accs, tok, w, m, v,
+                                      last=[hm[r][K - 1] for r in range(R)], n_views=1, t=t,
+                                      want_reduced=True)
+    for got, ref in zip(d, (w, m, v)):
+        assert ulp_f32(np_f32(got), ref) == 0
+    assert ulp_bf16(np_bf16(view), views[0]) == 0
+    check_norms(np_f32(sq), rsq)
+    nfr = [int(np.sum(~np.isfinite(red[o:o + p]))) for o, p in zip(op.bucket_offset, op.bucket_padded)]
+    np.testing.assert_array_equal(nf.cpu().numpy(), nfr)
+
+
+def test_deferred_equals_accumulate_then_step_on_device():
+    """The same bits as the library's own accumulation path, and with the
+    microbatches in page-locked host memory."""
+    R, K = 4, 4
+    plan, op, micro, tok = _micro(R, K, seed=77)
+    N = op.total_padded
+    w0 = master_f32(N, stream_seed(77, KIND_MASTER), device="cuda")
+    dm = [[x.cuda() for x in row] for row in micro]
+    outs = []
+    for how in ("accumulate", "deferred", "deferred_pinned"):
+        d = [w0.clone(), torch.zeros(N, device="cuda"), torch.zeros(N, device="cuda")]
+        p = torch.empty(N, dtype=torch.bfloat16, device="cuda")
+        sq = torch.empty(op.n_buckets, device="cuda")
+        if how == "accumulate":
+            acc = [torch.empty(N, device="cuda") for _ in range(R)]
+            for r in range(R):
+                for k in range(K - 1):
+                    dpg.dpg_accumulate(plan, dm[r][k], acc[r], first=(k == 0))
+            dpg.dpg_step(plan, acc, tok, dpg.HParams(), *d, [p],
+                         last_micro=[dm[r][K - 1] for r in range(R)], bucket_sqnorm=sq)
+        elif how == "deferred":
+            dpg.dpg_step_deferred(plan, dm, tok, dpg.HParams(), *d, [p], bucket_sqnorm=sq)
+        else:
+            pinned = [[x.pin_memory() for x in row] for row in micro]
+            dpg.dpg_step_deferred(plan, pinned, tok, dpg.HParams(), *d, [p], bucket_sqnorm=sq)
+        torch.cuda.synchronize()
+        outs.append((*d, p, sq))
+    for other in outs[1:]:
+        for a, b in zip(outs[0][:4], other[:4]):
+            assert torch.equal(a.view(torch.uint8), b.view(torch.uint8))
+        np.testing.assert_allclose(np_f32(other[4]), np_f32(outs[0][4]), rtol=1e-5)

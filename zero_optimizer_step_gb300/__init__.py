@@ -41,7 +41,7 @@ EXPORTED = (
     "dpg_step_clipped", "dpg_step_staged", "dpg_check_device_status", "dpg_set_staged_fault",
     "dpg_allreduce_grads", "dpg_adam_from_reduced", "dpg_gather_params_bf16",
     "dpg_accumulate_pair", "dpg_step_fold2", "dpg_set_fused_max_ctas",
-    "dpg_set_programmatic_launch", "dpg_reduce_scatter_adam_when_ready",
+    "dpg_set_programmatic_launch", "dpg_reduce_scatter_adam_when_ready", "dpg_step_deferred",
 )
 DPG_MAX_STATE_ARRAYS = 8
 DPG_NOALLOC_SCRATCH_BYTES = 8 << 20
@@ -109,6 +109,7 @@ def lib() -> ctypes.CDLL:
         L.dpg_accumulate_pair.argtypes = [P, P, P, P, i32, P]
         L.dpg_set_fused_max_ctas.argtypes = [i32]
         L.dpg_set_programmatic_launch.argtypes = [i32]
+        L.dpg_step_deferred.argtypes = [P, P, i32, P, i32, P, P, P, P, P, i32, P, P, P]
         L.dpg_reduce_scatter_adam_when_ready.argtypes = [P, P, i32, P, P, i32, P, P, P, P, P, i32,
                                                          P, P, P, i32, i32, P, P]
         L.dpg_step_fold2.argtypes = [P, P, P, P, P, i32, P, P, P, P, P, i32, P, P, P]
@@ -138,7 +139,7 @@ def lib() -> ctypes.CDLL:
                      "dpg_set_staged_fault", "dpg_allreduce_grads", "dpg_adam_from_reduced",
                      "dpg_gather_params_bf16", "dpg_accumulate_pair", "dpg_step_fold2",
                      "dpg_set_fused_max_ctas", "dpg_set_programmatic_launch",
-                     "dpg_reduce_scatter_adam_when_ready"):
+                     "dpg_reduce_scatter_adam_when_ready", "dpg_step_deferred"):
             getattr(L, name).restype = c_int
         _lib = L
     return _lib
@@ -421,6 +422,34 @@ def dpg_reduce_scatter_adam(plan: Plan, grads: Sequence[Ptr], valid_tokens, hp: 
         tok.ctypes.data, n_tok, ctypes.byref(hpc), _ptr(master), _ptr(exp_avg), _ptr(exp_avg_sq),
         _ptrs(param_views), len(param_views), _ptr(bucket_sqnorm), _ptr(bucket_nonfinite),
         _ptr(reduced_grad), b0, plan.n_buckets if b1 is None else b1, _stream(stream)))
+
+
+def dpg_step_deferred(plan: Plan, micro: Sequence[Sequence[Ptr]], valid_tokens, hp: HParams,
+                      master: Ptr, exp_avg: Ptr, exp_avg_sq: Ptr, param_views: Sequence[Ptr] = (),
+                      *, bucket_sqnorm: Ptr = None, bucket_nonfinite: Ptr = None, stream=None):
+    """Step of a K-microbatch cycle from every replica's K bf16 microbatch
+    buffers (micro[r][k]), summed inside the fused pass in microbatch order:
+    the bits of K-1 dpg_accumulate passes plus dpg_step."""
+    if len(micro) != plan.R:
+        raise ValueError(f"need R={plan.R} replicas of microbatch buffers, got {len(micro)}")
+    K = len(micro[0]) if micro else 0
+    if any(len(mr) != K for mr in micro):
+        raise ValueError("every replica needs the same number of microbatches")
+    N = plan.total_padded
+    flat = [t for mr in micro for t in mr]
+    for k, t in enumerate(flat):
+        _need_in(t, "bf16", N, f"micro[{k // max(1, K)}][{k % max(1, K)}]")
+    for name, t in (("master", master), ("exp_avg", exp_avg), ("exp_avg_sq", exp_avg_sq)):
+        _need(t, "f32", N, name)
+    for k, t in enumerate(param_views):
+        _need(t, "bf16", N, f"param_views[{k}]")
+    _need(bucket_sqnorm, "f32", plan.n_buckets, "bucket_sqnorm")
+    tok, n_tok = _tokens(valid_tokens)
+    hpc = hp.c()
+    _check(lib().dpg_step_deferred(
+        plan.handle, _ptrs(flat), K, tok.ctypes.data, n_tok, ctypes.byref(hpc), _ptr(master),
+        _ptr(exp_avg), _ptr(exp_avg_sq), _ptrs(param_views), len(param_views),
+        _ptr(bucket_sqnorm), _ptr(bucket_nonfinite), _stream(stream)))
 
 
 def _event_handle(e) -> Optional[int]:

@@ -98,6 +98,10 @@ __device__ __forceinline__ uint4 narrow8(const float* f) {
 // kInF32PlusBf16x2: fp32 accumulation buffers plus the last TWO bf16
 // microbatches, folded in microbatch order.
 enum : int { kInBf16 = 0, kInF32 = 1, kInF32PlusBf16 = 2, kInReduced = 3, kInF32PlusBf16x2 = 4 };
+// Deferred accumulation: K bf16 microbatch buffers per replica, replica-major
+// (grads[r * K + k]); MODE = kInBf16Deferred + KT, KT = K fixed at compile
+// time, or 0 for K read from the arguments.
+constexpr int kInBf16Deferred = 16;
 
 // Passes of the fused kernel.  kFull: reduce, scale, Adam, cast (the step).
 // With global norm clipping the step takes two passes: the norm pass
@@ -124,6 +128,7 @@ struct RsAdamArgs {
     int64_t t0, t1;      // tile range of buckets [b0, b1)
     int32_t b0, b1;
     int32_t R, n_views;
+    int32_t K;           // deferred accumulation: microbatches per replica
     float scale;         // fp32(1/G)
     float beta1, beta2, omb1, omb2, bias1, bias2, lr, eps, lr_wd;
     int32_t decay;
@@ -204,6 +209,45 @@ __device__ __forceinline__ void reduce_vector(const RsAdamArgs& a, int64_t i, fl
 #pragma unroll
                     for (int j = 0; j < 8; ++j) s[j] = __fadd_rn(s[j], t[j]);
                 }
+            }
+        }
+    } else if constexpr (MODE >= kInBf16Deferred) {
+        // each replica's K microbatches summed in microbatch order -- the
+        // binary32 additions of the no_sync accumulation path -- then the
+        // replicas in rank order
+        constexpr int KT = MODE - kInBf16Deferred;
+        const int K = KT > 0 ? KT : a.K;
+#pragma unroll(RT > 0 ? RT : 1)
+        for (int r = 0; r < R; ++r) {
+            const void* const* g = a.grads + r * K;
+            float x[8];
+            if constexpr (KT > 0) {
+                uint4 q[KT];
+#pragma unroll
+                for (int k = 0; k < KT; ++k) q[k] = ld_grad_u4(static_cast<const uint16_t*>(g[k]) + i);
+                widen8(q[0], x);
+#pragma unroll
+                for (int k = 1; k < KT; ++k) {
+                    float t[8];
+                    widen8(q[k], t);
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) x[j] = __fadd_rn(x[j], t[j]);
+                }
+            } else {
+                widen8(ld_grad_u4(static_cast<const uint16_t*>(g[0]) + i), x);
+                for (int k = 1; k < K; ++k) {
+                    float t[8];
+                    widen8(ld_grad_u4(static_cast<const uint16_t*>(g[k]) + i), t);
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) x[j] = __fadd_rn(x[j], t[j]);
+                }
+            }
+            if (r == 0) {
+#pragma unroll
+                for (int j = 0; j < 8; ++j) s[j] = x[j];
+            } else {
+#pragma unroll
+                for (int j = 0; j < 8; ++j) s[j] = __fadd_rn(s[j], x[j]);
             }
         }
     } else {

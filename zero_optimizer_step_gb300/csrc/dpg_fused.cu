@@ -939,6 +939,55 @@ int fill_step_args(const Plan& p, const void* const* grads, int32_t grads_dtype,
     return DPG_OK;
 }
 
+// Whole step with deferred accumulation: every replica's K bf16 microbatch
+// buffers summed inside the fused pass (see dpg_step_deferred in
+// include/dpg.h).  Always the chunked launch.
+static int step_deferred(const dpg_plan_t* plan, const void* const* micro, int32_t K,
+                         const int64_t* tokens, int32_t n_counts, const dpg_hparams* hp,
+                         float* master, float* m, float* v, void* const* views, int32_t n_views,
+                         float* sqnorm, int64_t* nonfinite, void* stream) {
+    const char* who = "dpg_step_deferred";
+    if (!plan) return fail(DPG_ERR_INVALID_ARG, "%s: plan is NULL", who);
+    Plan& p = const_cast<dpg_plan_t*>(plan)->p;
+    if (K < 1 || int64_t(K) * p.R > DPG_MAX_REPLICAS)
+        return fail(DPG_ERR_INVALID_ARG, "%s: K = %d microbatches with R = %d needs 1 <= K and "
+                    "R * K <= %d", who, K, p.R, DPG_MAX_REPLICAS);
+    RsAdamArgs a{};
+    int st = fill_step_args(p, micro, DPG_BF16, nullptr, hp, tokens, n_counts, master, m, v, views,
+                            n_views, a, who);
+    if (st != DPG_OK) return st;
+    const bool want_norm = sqnorm || nonfinite;
+    if (p.n_buckets == 0 || (p.total_padded == 0 && !want_norm)) return DPG_OK;
+    for (int q = 0; p.total_padded > 0 && q < p.R * K; ++q) {
+        if (!micro[q]) return fail(DPG_ERR_INVALID_ARG, "%s: microbatch buffer %d is NULL", who, q);
+        if (!aligned(micro[q], 16)) return fail(DPG_ERR_MISALIGNED, "%s: microbatch buffer %d misaligned", who, q);
+        a.grads[q] = micro[q];
+    }
+    st = upload(p);
+    if (st != DPG_OK) return st;
+    a.K = K;
+    a.bucket_offset = p.d_bucket_offset;
+    a.tile_begin = p.d_tile_begin;
+    a.t0 = 0;
+    a.t1 = p.n_tiles;
+    a.b0 = 0;
+    a.b1 = p.n_buckets;
+    RsKernel fc;
+    if (K == 4) {
+        switch (p.R) {
+            case 1: fc = k_rs_adam_chunk<1, kInBf16Deferred + 4, kFull>; break;
+            case 2: fc = k_rs_adam_chunk<2, kInBf16Deferred + 4, kFull>; break;
+            case 4: fc = k_rs_adam_chunk<4, kInBf16Deferred + 4, kFull>; break;
+            case 8: fc = k_rs_adam_chunk<8, kInBf16Deferred + 4, kFull>; break;
+            default: fc = k_rs_adam_chunk<0, kInBf16Deferred + 4, kFull>; break;
+        }
+    } else {
+        fc = pick_chunk_kernel<kInBf16Deferred>(p.R);
+    }
+    return launch_chunked(fc, a, p, want_norm, sqnorm, nonfinite, static_cast<cudaStream_t>(stream),
+                          who);
+}
+
 // Whole step with global gradient-norm clipping: norm pass, coefficient on
 // the device, update pass (see dpg_step_clipped in include/dpg.h).
 static int step_clipped(const dpg_plan_t* plan, const void* const* grads, int32_t grads_dtype,
@@ -1264,6 +1313,18 @@ int dpg_step_fold2(const dpg_plan_t* plan, const float* const* acc_f32,
                         valid_tokens, n_counts, hp, master, exp_avg, exp_avg_sq, param_views,
                         n_views, bucket_sqnorm, bucket_nonfinite, nullptr, 0, plan->p.n_buckets,
                         stream, "dpg_step_fold2", micro_b_bf16);
+}
+
+int dpg_step_deferred(const dpg_plan_t* plan, const void* const* micro_bf16, int32_t K,
+                      const int64_t* valid_tokens, int32_t n_counts, const dpg_hparams* hp,
+                      float* master, float* exp_avg, float* exp_avg_sq, void* const* param_views,
+                      int32_t n_views, float* bucket_sqnorm, int64_t* bucket_nonfinite,
+                      void* stream) {
+    dpg::clear_error();
+    const dpg::Trace trace("dpg_step_deferred");
+    return dpg::step_deferred(plan, micro_bf16, K, valid_tokens, n_counts, hp, master, exp_avg,
+                              exp_avg_sq, param_views, n_views, bucket_sqnorm, bucket_nonfinite,
+                              stream);
 }
 
 int dpg_step_clipped(const dpg_plan_t* plan, const void* const* grads, int32_t grads_dtype,
