@@ -489,7 +489,10 @@ int dpg_time_next_fused_launch(void* start_event, void* stop_event);
 /* Test-only fault injection for the staged step: its next launch by the
  * calling thread never fetches unit `skip_unit` (-1: none), so the CTA
  * that owns it must run out its wait, and every wait is bounded by
- * `timeout_ns` (<= 0: the default 1 s).  Used to test the timeout path. */
+ * `timeout_ns` (<= 0: the default 1 s).  Used to test the timeout path.
+ * Honoured only when the environment variable DPG_TEST_HOOKS is "1" at the
+ * time of the call; otherwise it changes nothing and returns
+ * DPG_ERR_INVALID_ARG. */
 int dpg_set_staged_fault(int64_t skip_unit, int64_t timeout_ns);
 
 #ifdef __cplusplus

@@ -297,3 +297,19 @@ def test_state_export_import_validation():
     # an empty plan has nothing to copy
     empty = dpg.dpg_plan_buckets([], 1024, 2)
     assert L.dpg_import_state(empty.handle, dpg._ptrs([0]), dpg._ptrs([0]), 1, None) == dpg.DPG_OK
+
+
+def test_staged_fault_hook_needs_opt_in(monkeypatch):
+    # a production process (no DPG_TEST_HOOKS=1) cannot arm the test hook
+    for val in (None, "0", "yes"):
+        if val is None:
+            monkeypatch.delenv("DPG_TEST_HOOKS", raising=False)
+        else:
+            monkeypatch.setenv("DPG_TEST_HOOKS", val)
+        with pytest.raises(dpg.DpgError) as e:
+            dpg.dpg_set_staged_fault(skip_unit=3, timeout_ns=1)
+        assert e.value.status == dpg.DPG_ERR_INVALID_ARG
+        assert "DPG_TEST_HOOKS" in str(e.value)
+    monkeypatch.setenv("DPG_TEST_HOOKS", "1")
+    dpg.dpg_set_staged_fault(skip_unit=3, timeout_ns=1)
+    dpg.dpg_set_staged_fault(skip_unit=-1, timeout_ns=0)   # disarm again

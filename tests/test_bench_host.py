@@ -111,3 +111,25 @@ def test_replicas_override():
     assert bench.config_of(types.SimpleNamespace(config="gpt2", replicas=None)) is CONFIGS["gpt2"]
     with pytest.raises(SystemExit):
         bench.config_of(types.SimpleNamespace(config="gpt2", replicas=65))
+
+
+def test_reference_line_states_what_it_timed():
+    # the reference arm times a sample per step; its line must say so, and
+    # its full-workload step time must agree with its rate
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    out = subprocess.run([sys.executable, os.path.join(root, "bench.py"), "--impl", "reference",
+                          "--config", "gpt2", "--steps", "3", "--warmup", "3",
+                          "--cpu-sample-elems", "32768"],
+                         capture_output=True, text=True, timeout=600, check=True).stdout
+    line = json.loads(out.strip().splitlines()[-1])
+    c = line["config"]
+    assert line["impl"] == "reference"
+    assert c["psi"] == CONFIGS["gpt2"].psi
+    assert c["sample_elems_per_step"] == 32768
+    assert c["sample_share_of_psi"] == pytest.approx(32768 / c["psi"])
+    assert c["psi"] / (line["ms_per_step"] * 1e-3) == pytest.approx(line["value"], rel=1e-9)
+    assert 32768 / (line["sample_ms_per_step"] * 1e-3) == pytest.approx(line["value"], rel=1e-9)
+    assert line["cpu_baseline"]["value"] == line["value"]
+    assert line["e2e"]["h2d_bytes_per_step"] == 0

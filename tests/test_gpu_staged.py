@@ -116,10 +116,16 @@ def test_staged_matches_direct_path_on_gpt2_sized_list():
     assert torch.equal(outs[0][1].view(torch.int16), outs[1][1].view(torch.int16))
 
 
-def test_staged_wait_times_out_and_context_survives():
+def test_staged_wait_times_out_and_context_survives(monkeypatch):
     numels = [40_000, 123_456, 7_777]
     plan, op, grads, w0, tok = _case(numels, 1 << 20, 4)
     before = dpg.dpg_launch_count()
+    # the hook is refused unless the process opted in through the environment
+    monkeypatch.delenv("DPG_TEST_HOOKS", raising=False)
+    with pytest.raises(dpg.DpgError) as e:
+        dpg.dpg_set_staged_fault(skip_unit=3, timeout_ns=50_000_000)
+    assert e.value.status == dpg.DPG_ERR_INVALID_ARG
+    monkeypatch.setenv("DPG_TEST_HOOKS", "1")
     dpg.dpg_set_staged_fault(skip_unit=3, timeout_ns=50_000_000)
     _device(plan, grads, w0, tok, dpg.dpg_step_staged)
     with pytest.raises(dpg.DpgError) as e:

@@ -6,6 +6,8 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <cstdlib>
+#include <cstring>
 #include <mutex>
 
 #include "dpg_host.h"
@@ -422,6 +424,12 @@ int dpg_check_device_status(const dpg_plan_t* plan, void* stream) {
 
 int dpg_set_staged_fault(int64_t skip_unit, int64_t timeout_ns) {
     dpg::clear_error();
+    // a test hook: honoured only in a process that opted in through the
+    // environment, so a production caller cannot arm it by accident
+    const char* on = std::getenv("DPG_TEST_HOOKS");
+    if (!on || std::strcmp(on, "1") != 0)
+        return fail(DPG_ERR_INVALID_ARG, "dpg_set_staged_fault: test hooks are disabled "
+                                         "(set DPG_TEST_HOOKS=1 in the environment)");
     dpg::t_staged_skip = skip_unit;
     dpg::t_staged_timeout_ns = timeout_ns;
     return DPG_OK;
