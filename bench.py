@@ -73,6 +73,8 @@ def parse():
                          "the last two microbatches folded into the fused step")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-secondary", action="store_true",
+                    help="default line only: skip the Hockney record and the 4.5B workload")
     ap.add_argument("--cpu-sample-elems", type=int, default=CPU_SAMPLE_ELEMS,
                     help="elements of each oracle sample (CPU baseline and reference arm)")
     ap.add_argument("--kernels", action="store_true",
@@ -419,6 +421,134 @@ def write_traffic(a):
     print(json.dumps(out), flush=True)
 
 
+def timed_cycles(fn, steps, warm, world, dev, stream):
+    """Run fn() warm times, then steps times between two events; returns the
+    mean ms per call (max over ranks) and the sorted fused-launch intervals
+    that fn recorded into the event pairs it was given."""
+    import torch
+    for _ in range(warm):
+        fn(None)
+    torch.cuda.synchronize()
+    ev_k = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+            for _ in range(steps)]
+    for e0, e1 in ev_k:
+        e0.record(stream)
+        e1.record(stream)
+    e_start, e_stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    torch.cuda.synchronize()
+    e_start.record(stream)
+    for i in range(steps):
+        fn(ev_k[i])
+    e_stop.record(stream)
+    torch.cuda.synchronize()
+    ms = max_over_ranks(e_start.elapsed_time(e_stop) / steps, world, dev)
+    return ms, sorted(e0.elapsed_time(e1) for e0, e1 in ev_k)
+
+
+def fused_roofline(kernel, bpp, psi, k_all, peak, peak_kind, traffic):
+    k_ms = statistics.mean(k_all)
+    achieved = bpp * psi / (k_ms * 1e-3) / 1e9
+    return {"bound": "hbm", "kernel": kernel, "achieved": achieved, "peak": peak,
+            "peak_kind": f"{peak_kind} (copy bandwidth)", "unit": "GB/s", "frac": achieved / peak,
+            "traffic": traffic, "algorithmic_bytes_per_param": bpp,
+            "algorithmic_bytes_per_launch": bpp * psi, "kernel_ms": k_ms,
+            "kernel_ms_p10_p50_p90": [k_all[int(round(q * (len(k_all) - 1)))]
+                                      for q in (0.1, 0.5, 0.9)]}
+
+
+def run_secondary(a, dpg, dev, world):
+    """The 4.5B accumulation workload (Llama-3-8B shapes cut to 16 layers,
+    R = 4, K = 4 microbatches, 100 MiB buckets) measured in the default line:
+    the whole K-microbatch cycle with one fp32 pass per microbatch (the pages'
+    no_sync schedule: K - 1 accumulations, the last microbatch folded into the
+    fused step), the fused step alone, and the same cycle as one deferred
+    pass over K bf16 buffers per replica.  Microbatch gradients are drawn on
+    the device."""
+    import torch
+    cfg = CONFIGS["llama8b16l"]
+    R, K = cfg.R, cfg.K
+    plan = dpg.dpg_plan_buckets(cfg.numels, cfg.cap_bytes, R)
+    dpg.dpg_plan_upload(plan)
+    N = plan.total_padded
+    segs = segments(plan.param_offset, cfg.numels)
+    tokens = token_counts(cfg)
+    stream = torch.cuda.current_stream()
+    peak, peak_kind = load_peak()
+    grad = lambda r, k: flat_grads_bf16(segs, N, cfg.grad_std,
+                                        stream_seed(cfg.seed, KIND_GRAD, r, k), device=dev)
+    gd = [[grad(r, 0)] for r in range(R)]
+    acc = [torch.empty(N, device=dev) for _ in range(R)]
+    w = master_f32(N, stream_seed(cfg.seed, KIND_MASTER), device=dev)
+    m, v = torch.zeros(N, device=dev), torch.zeros(N, device=dev)
+    param = torch.empty(N, dtype=torch.bfloat16, device=dev)
+    sq = torch.empty(plan.n_buckets, device=dev)
+    nf = torch.empty(plan.n_buckets, dtype=torch.int64, device=dev)
+    state = {"t": 0}
+    steps, warm = max(3, min(a.steps, 6)), 3
+
+    def cycle(ev):
+        # one fp32 pass per microbatch; the backward of every microbatch
+        # writes the same bf16 gradient buffer of its replica
+        state["t"] += 1
+        hp = dpg.HParams(step=state["t"])
+        for k in range(K - 1):
+            for r in range(R):
+                dpg.dpg_accumulate(plan, gd[r][0], acc[r], first=(k == 0), stream=stream)
+        if ev is not None:
+            dpg.dpg_time_next_fused_launch(*ev)
+        dpg.dpg_step(plan, acc, tokens, hp, w, m, v, [param], last_micro=[gd[r][0] for r in range(R)],
+                     bucket_sqnorm=sq, bucket_nonfinite=nf, stream=stream)
+
+    clocks = ClockSampler(torch.cuda.current_device())
+    clocks.start()
+    l0 = dpg.dpg_launch_count()
+    cyc_ms, k_acc = timed_cycles(cycle, steps, warm, world, dev, stream)
+    n_cycle = (dpg.dpg_launch_count() - l0) // (steps + warm)
+    bpp = algorithmic_bytes_per_param(cfg)
+    out = {"config": workload_desc(cfg, cfg.cap_bytes, plan.n_buckets, N),
+           "steps": steps, "warmup": warm, "ms_per_step": cyc_ms,
+           "value": job_throughput(cfg.psi, world, cyc_ms), "unit": "params/s",
+           "hbm_gbs_step": bpp["step"] * cfg.psi / (cyc_ms * 1e-3) / 1e9,
+           "cycle_bytes_per_param": bpp["step"],
+           "cycle_frac": bpp["step"] * cfg.psi / (cyc_ms * 1e-3) / 1e9 / peak,
+           "gpu_launches_per_cycle": int(n_cycle),
+           "roofline": fused_roofline(fused_kernel_name(a, R, K), bpp["fused"], cfg.psi, k_acc,
+                                      peak, peak_kind, traffic_per_launch(cfg, cfg.cap_bytes, N))}
+    # deferred: every replica's K microbatches held in bf16, summed in the step
+    del acc
+    torch.cuda.empty_cache()
+    for r in range(R):
+        gd[r] += [grad(r, k) for k in range(1, K)]
+
+    def deferred(ev):
+        state["t"] += 1
+        hp = dpg.HParams(step=state["t"])
+        if ev is not None:
+            dpg.dpg_time_next_fused_launch(*ev)
+        dpg.dpg_step_deferred(plan, gd, tokens, hp, w, m, v, [param], bucket_sqnorm=sq,
+                              bucket_nonfinite=nf, stream=stream)
+
+    d_ms, k_def = timed_cycles(deferred, steps, warm, world, dev, stream)
+    bpd = algorithmic_bytes_per_param(cfg, deferred=True)
+    out["deferred"] = {
+        "accumulation": workload_desc(cfg, cfg.cap_bytes, plan.n_buckets, N,
+                                      deferred=True)["accumulation"],
+        "ms_per_step": d_ms, "value": job_throughput(cfg.psi, world, d_ms), "unit": "params/s",
+        "cycle_bytes_per_param": bpd["step"],
+        "cycle_frac": bpd["step"] * cfg.psi / (d_ms * 1e-3) / 1e9 / peak,
+        "roofline": fused_roofline(f"k_rs_adam_chunk<R={R}> (K={K} bf16 microbatches per "
+                                   f"replica)", bpd["fused"], cfg.psi, k_def, peak, peak_kind,
+                                   None)}
+    out["clocks"] = clocks.stop()
+    del gd, w, m, v, param, sq, nf
+    plan.destroy()
+    torch.cuda.empty_cache()
+    return out
+
+
 def run_dpg(a):
     import torch
     import torch.distributed as dist
@@ -542,6 +672,16 @@ def run_dpg(a):
         e2e = run_e2e(a, dpg, plan, g, acc, w, m, v, param, sq, nf, tokens, cfg, dev, stream,
                       state, world, fold2)
 
+    # the 1B default line also carries the alpha-beta record and the 4.5B
+    # accumulation workload, each measured after the 1B buffers are freed
+    extra = {}
+    if (a.config == "llama1b" and a.cap_mib is None and getattr(a, "replicas", None) is None
+            and a.variant == "direct" and not a.no_secondary):
+        del g, gd, acc, g2, w, m, v, param, sq, nf
+        torch.cuda.empty_cache()
+        extra["hockney"] = hockney_compact(dpg)
+        extra["secondary"] = run_secondary(a, dpg, dev, world)
+
     bpp = algorithmic_bytes_per_param(cfg, fold2, deferred)
     peak, peak_kind = load_peak()
     achieved = bpp["fused"] * cfg.psi / (k_ms * 1e-3) / 1e9
@@ -563,6 +703,7 @@ def run_dpg(a):
         "gpu_launches": int(launches),
         "clocks": clk,
         "e2e": e2e,
+        **extra,
     }
     if rank == 0 and world == 1 and not a.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(cfg, dev)
@@ -795,18 +936,16 @@ def run_reference(a):
 # T(m) = alpha + beta m; K small operations cost K alpha + beta M, one fused
 # operation alpha + beta M)
 # --------------------------------------------------------------------------
-def run_hockney(a):
+def hockney_points(dpg, cfg, caps, reps, modes=("per_bucket", "per_bucket_plain", "fused")):
+    """For each bucket cap: the step's fused update over the whole plan as one
+    launch per bucket and as one launch over all buckets, each replayed from a
+    CUDA graph with L2 flushed before every replay (median ms)."""
     import torch
-    from zero_optimizer_step_gb300 import build as _build
-    _build.build()
-    import zero_optimizer_step_gb300 as dpg
-    cfg = CONFIGS[a.hockney_config]
-    dev = torch.device("cuda", 0)
-    torch.cuda.set_device(dev)
+    dev = torch.device("cuda", torch.cuda.current_device())
     R = cfg.R
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)   # > L2 (129 MB)
     points = []
-    for cap in cfg.cap_sweep:
+    for cap in caps:
         plan = dpg.dpg_plan_buckets(cfg.numels, cap, R)
         dpg.dpg_plan_upload(plan)
         N = plan.total_padded
@@ -827,7 +966,7 @@ def run_hockney(a):
         torch.cuda.current_stream().wait_stream(s)
         # per_bucket: launches with programmatic stream serialization (the
         # library's default); per_bucket_plain: the same launches without it
-        for mode in ("per_bucket", "per_bucket_plain", "fused"):
+        for mode in modes:
             gr = torch.cuda.CUDAGraph()
             dpg.dpg_set_programmatic_launch(mode != "per_bucket_plain")
             try:
@@ -841,10 +980,11 @@ def run_hockney(a):
             finally:
                 dpg.dpg_set_programmatic_launch(True)
             graphs[mode] = gr
-        res = {}
+        pt = {"cap_bytes": cap, "n_buckets": plan.n_buckets, "total_padded": N,
+              "bytes": (2 * R + 26) * cfg.psi}
         for mode, gr in graphs.items():
             ts = []
-            for _ in range(max(3, a.steps)):
+            for _ in range(max(3, reps)):
                 flush.zero_()
                 e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
                 e0.record()
@@ -852,34 +992,59 @@ def run_hockney(a):
                 e1.record()
                 torch.cuda.synchronize()
                 ts.append(e0.elapsed_time(e1))
-            res[mode] = statistics.median(ts)
-            res[mode + "_range"] = [min(ts), max(ts)]
-        points.append({"cap_bytes": cap, "n_buckets": plan.n_buckets, "total_padded": N,
-                       "bytes": (2 * R + 26) * cfg.psi, "per_bucket_ms": res["per_bucket"],
-                       "per_bucket_plain_ms": res["per_bucket_plain"],
-                       "fused_ms": res["fused"], "per_bucket_ms_range": res["per_bucket_range"],
-                       "per_bucket_plain_ms_range": res["per_bucket_plain_range"],
-                       "fused_ms_range": res["fused_range"]})
+            pt[mode + "_ms"] = statistics.median(ts)
+            pt[mode + "_ms_range"] = [min(ts), max(ts)]
+        points.append(pt)
         del graphs, g, w, m, v, p
         plan.destroy()
+    torch.cuda.empty_cache()
+    return points
+
+
+def hockney_fit(points, key="per_bucket"):
+    """Least squares T = K*alpha + beta*M over the points (K launches moving M
+    bytes in all): alpha in us, 1/beta in GB/s."""
     K = np.array([q["n_buckets"] for q in points], float)
     Mb = np.array([q["bytes"] for q in points], float)
-    A = np.stack([K, Mb], axis=1)
-    fits = {}
-    for key in ("per_bucket", "per_bucket_plain"):
-        T = np.array([q[key + "_ms"] for q in points], float) * 1e-3
-        (alpha, beta), *_ = np.linalg.lstsq(A, T, rcond=None)
-        fits[key] = {"alpha_us": alpha * 1e6, "inv_beta_gbs": 1.0 / beta / 1e9}
+    T = np.array([q[key + "_ms"] for q in points], float) * 1e-3
+    (alpha, beta), *_ = np.linalg.lstsq(np.stack([K, Mb], axis=1), T, rcond=None)
+    return {"alpha_us": alpha * 1e6, "inv_beta_gbs": 1.0 / beta / 1e9}
+
+
+def run_hockney(a):
+    import torch
+    from zero_optimizer_step_gb300 import build as _build
+    _build.build()
+    import zero_optimizer_step_gb300 as dpg
+    cfg = CONFIGS[a.hockney_config]
+    torch.cuda.set_device(torch.device("cuda", 0))
+    points = hockney_points(dpg, cfg, cfg.cap_sweep, a.steps)
     fused = np.array([q["fused_ms"] for q in points]) * 1e-3
     out = {"metric": "hockney alpha-beta fit of the fused reduce-scatter+Adam kernel over bucket caps",
-           "workload": f"{cfg.name}: {len(cfg.shapes)} tensors, psi={cfg.psi}, R={R}",
-           "points": points, "fit": {**fits["per_bucket"],
-                                     "plain_launches": fits["per_bucket_plain"],
+           "workload": f"{cfg.name}: {len(cfg.shapes)} tensors, psi={cfg.psi}, R={cfg.R}",
+           "points": points, "fit": {**hockney_fit(points, "per_bucket"),
+                                     "plain_launches": hockney_fit(points, "per_bucket_plain"),
                                      "model": "T_per_bucket = K*alpha + beta*M (least squares)"},
            "fused_single_launch_ms": {"median": float(np.median(fused)) * 1e3,
                                       "min": float(fused.min()) * 1e3, "max": float(fused.max()) * 1e3},
            "timing": "CUDA graph replay, L2 flushed (256 MB write) before every replay"}
     print(json.dumps(out), flush=True)
+
+
+def hockney_compact(dpg, reps=5):
+    """The alpha-beta record of the default line: the 1B list at its three caps
+    (1 / 25 / 100 MiB), one launch per bucket against one launch in all."""
+    cfg = CONFIGS["llama1b"]
+    points = hockney_points(dpg, cfg, cfg.cap_sweep, reps, modes=("per_bucket", "fused"))
+    return {"workload": f"{cfg.name}: psi={cfg.psi}, R={cfg.R}, caps "
+                        + "/".join(f"{c / (1 << 20):g}" for c in cfg.cap_sweep) + " MiB",
+            "model": "T_per_bucket = K*alpha + beta*M (least squares; K launches, M bytes)",
+            "fit": hockney_fit(points, "per_bucket"),
+            "points": [{"cap_mib": q["cap_bytes"] / (1 << 20), "n_buckets": q["n_buckets"],
+                        "per_bucket_ms": q["per_bucket_ms"], "fused_ms": q["fused_ms"]}
+                       for q in points],
+            "timing": f"median of {max(3, reps)} CUDA graph replays per point, programmatic "
+                      f"launches, L2 flushed before each"}
 
 
 # --------------------------------------------------------------------------

@@ -224,3 +224,36 @@ def test_pack_unpack_and_state_copies_stay_inside():
     back = [Buf(N, torch.float32) for _ in range(2)]
     dpg.dpg_import_state(plan, [c.t for c in canon], [b.t for b in back])
     _check(back, csn)
+
+
+@pytest.mark.parametrize("K", [4, 3])
+def test_deferred_step_stays_inside(K):
+    # K = 4 runs the kernel compiled for four microbatches, K = 3 the
+    # run-time-K loop; both read R*K microbatch buffers per element
+    numels, plan, _, tok = _case(R=2, seed=26)
+    N, nb = plan.total_padded, plan.n_buckets
+    segs = segments(plan.param_offset, numels)
+    micro = [[Buf(N, torch.bfloat16,
+                  flat_grads_bf16(segs, N, 1e-3, stream_seed(26, KIND_GRAD, r, k)))
+              for k in range(K)] for r in range(2)]
+    snaps = [(b, b.snapshot()) for mr in micro for b in mr]
+    w, m, v = _state(plan, seed=26)
+    views = [Buf(N, torch.bfloat16) for _ in range(2)]
+    sq, nf = Buf(nb, torch.float32), Buf(nb, torch.int64)
+    dpg.dpg_step_deferred(plan, [[b.t for b in mr] for mr in micro], [3000 + k for k in range(2 * K)],
+                          dpg.HParams(), w.t, m.t, v.t, [x.t for x in views],
+                          bucket_sqnorm=sq.t, bucket_nonfinite=nf.t)
+    _check([w, m, v, sq, nf, *views], snaps)
+
+
+def test_noalloc_step_stays_inside():
+    _, plan, grads, tok = _case(seed=27)
+    N, nb = plan.total_padded, plan.n_buckets
+    snaps = [(g, g.snapshot()) for g in grads]
+    for _ in range(2):
+        w, m, v = _state(plan, seed=27)
+        view = Buf(N, torch.bfloat16)
+        sq, nf = Buf(nb, torch.float32), Buf(nb, torch.int64)
+        dpg.dpg_step_noalloc(plan, [g.t for g in grads], tok, dpg.HParams(), w.t, m.t, v.t,
+                             [view.t], bucket_sqnorm=sq.t, bucket_nonfinite=nf.t)
+        _check([w, m, v, view, sq, nf], snaps)
