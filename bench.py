@@ -65,6 +65,8 @@ def parse():
                          "fused kernel's mean DRAM bytes per launch to profiles/traffic.json")
     ap.add_argument("--replicas", type=int, default=None,
                     help="override the workload's R (simulated data-parallel replicas, 1..64)")
+    ap.add_argument("--microbatches", type=int, default=None,
+                    help="override the workload's K (microbatches accumulated per step, 1..16)")
     ap.add_argument("--deferred", action="store_true",
                     help="K >= 2: deferred accumulation (K bf16 gradient buffers per replica, all "
                          "summed inside the fused step; no accumulation pass)")
@@ -73,6 +75,10 @@ def parse():
                          "the last two microbatches folded into the fused step")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--sharded", action="store_true",
+                    help="ZeRO-2 split across the torchrun ranks (R = number of GPUs): each "
+                         "rank exchanges gradient slices (NCCL point-to-point), updates its "
+                         "shard with the library's fused pass and all-gathers the bf16 shards")
     ap.add_argument("--no-secondary", action="store_true",
                     help="default line only: skip the Hockney record and the 4.5B workload")
     ap.add_argument("--cpu-sample-elems", type=int, default=CPU_SAMPLE_ELEMS,
@@ -355,70 +361,113 @@ def kernel_source_sha256() -> str:
     return h.hexdigest()
 
 
-def traffic_per_launch(cfg, cap, total_padded):
+def traffic_key(cfg, fold2=False, deferred=False) -> str:
+    """Entry of profiles/traffic.json for the fused kernel a workload launches:
+    the kernel's input mode depends on R, K and the accumulation schedule."""
+    sched = ("bf16" if cfg.K == 1 else "deferred" if deferred else "fold2" if fold2
+             else "acc_fp32_last_bf16")
+    return f"k_rs_adam_chunk R={cfg.R} K={cfg.K} {sched}"
+
+
+def traffic_per_launch(cfg, cap, total_padded, fold2=False, deferred=False):
     """DRAM bytes per fused launch from the committed ncu summary, if it was
-    taken on the current kernel source; scaled by elements if the capture ran
-    a smaller case of the same kernel.  None otherwise."""
+    taken on the current kernel code for the same kernel variant; scaled by
+    elements when the capture ran a smaller case (the pass streams every
+    element once, so its traffic grows in proportion).  None otherwise."""
     try:
-        t = json.load(open(TRAFFIC_FILE))["k_rs_adam"]
-    except (OSError, KeyError, ValueError):
+        t = json.load(open(TRAFFIC_FILE))["entries"][traffic_key(cfg, fold2, deferred)]
+    except (OSError, KeyError, ValueError, TypeError):
         return None
-    src = kernel_source_sha256()
-    if t.get("source_sha256") != src or t.get("R") != cfg.R or t.get("K", 1) != cfg.K:
+    if t.get("source_sha256") != kernel_source_sha256():
         return None
     return float(t["dram_bytes_per_launch"]) * total_padded / float(t["elements"])
 
 
 def config_of(a):
-    """The named workload, with R overridden by --replicas when given."""
+    """The named workload, with R and K overridden by --replicas and
+    --microbatches when given."""
     import dataclasses
     cfg = CONFIGS[a.config]
     r = getattr(a, "replicas", None)
-    if r is None:
-        return cfg
-    if not 1 <= r <= 64:
-        raise SystemExit(f"--replicas {r}: R must be 1..64")
-    return dataclasses.replace(cfg, R=r)
+    if r is not None:
+        if not 1 <= r <= 64:
+            raise SystemExit(f"--replicas {r}: R must be 1..64")
+        cfg = dataclasses.replace(cfg, R=r)
+    k = getattr(a, "microbatches", None)
+    if k is not None:
+        if not 1 <= k <= 16:
+            raise SystemExit(f"--microbatches {k}: K must be 1..16")
+        cfg = dataclasses.replace(cfg, K=k)
+    return cfg
 
 
-def fused_kernel_name(a, R, K) -> str:
+def fused_kernel_name(a, R, K, fold2=False, deferred=False) -> str:
     """The fused kernel the timed step launches (for the roofline label)."""
     if getattr(a, "variant", "direct") == "staged":
         return f"k_rs_adam_staged<R={R}>"
-    return f"k_rs_adam_chunk<R={R}>" + ("" if K == 1 else " (fp32 accumulators + last microbatch)")
+    mode = ("" if K == 1 else f" (K={K} bf16 microbatches per replica)" if deferred else
+            " (fp32 accumulators + two last microbatches)" if fold2 else
+            " (fp32 accumulators + last microbatch)")
+    return f"k_rs_adam_chunk<R={R}>" + mode
 
 
 def write_traffic(a):
-    """profiles/traffic.json from an ncu launch list of the fused kernel."""
+    """Add the fused kernel's DRAM bytes per launch, from an ncu launch list of
+    this bench's run (same arguments), to profiles/traffic.json."""
     import csv
+    import re
     cfg = config_of(a)
+    cap = cap_of(cfg, a)
+    fold2 = bool(a.fold2) and cfg.K >= 3
+    deferred = bool(a.deferred) and cfg.K >= 2
     per = {}
     with open(a.traffic_from, newline="") as fh:
         rows = [r for r in csv.reader(fh) if len(r) > 14 and r[0].isdigit()]
     for r in rows:
         name, metric, value = r[4], r[12], float(r[14].replace(",", ""))
-        if not name.startswith(("void k_rs_adam<", "void k_rs_adam_chunk<")) or "staged" in name:
+        if not re.match(r"(void )?(dpg::)?k_rs_adam_chunk<", name):
             continue
         per.setdefault(r[0], {})[metric] = value
     launches = [d for d in per.values()
                 if "dram__bytes_read.sum" in d and "dram__bytes_write.sum" in d]
     if not launches:
-        raise SystemExit(f"{a.traffic_from}: no k_rs_adam launch with DRAM byte counts")
+        raise SystemExit(f"{a.traffic_from}: no k_rs_adam_chunk launch with DRAM byte counts")
     rd = statistics.mean(d["dram__bytes_read.sum"] for d in launches)
     wr = statistics.mean(d["dram__bytes_write.sum"] for d in launches)
-    out = {"k_rs_adam": {
-        "workload": f"{cfg.name} ({cfg.psi:,} params, R={cfg.R}, "
-                    f"{cap_of(cfg, a) / (1 << 20):g} MiB buckets), full size",
-        "R": cfg.R, "K": cfg.K, "elements": cfg.psi,
+    import zero_optimizer_step_gb300 as dpg
+    plan = dpg.dpg_plan_buckets(cfg.numels, cap, cfg.R)
+    elements = plan.total_padded
+    plan.destroy()
+    bpp = algorithmic_bytes_per_param(cfg, fold2, deferred)["fused"]
+    args = " ".join(f"--{k.replace('_', '-')} {v}" for k, v in
+                    (("config", a.config), ("replicas", a.replicas),
+                     ("microbatches", a.microbatches), ("cap_mib", a.cap_mib)) if v is not None)
+    args += " --deferred" if deferred else " --fold2" if fold2 else ""
+    entry = {
+        "workload": f"{cfg.name} ({cfg.psi:,} params, {elements:,} padded elements, R={cfg.R}, "
+                    f"K={cfg.K}, {cap / (1 << 20):g} MiB buckets)",
+        "R": cfg.R, "K": cfg.K, "elements": elements,
         "dram_bytes_read": rd, "dram_bytes_write": wr, "dram_bytes_per_launch": rd + wr,
+        "algorithmic_bytes_per_launch": bpp * cfg.psi,
+        "traffic_over_algorithmic": (rd + wr) / (bpp * cfg.psi),
         "launches": len(launches), "source_sha256": kernel_source_sha256(),
-        "hash": "sha256 of the library's CUDA sources and headers with comments and whitespace removed",
         "how": "ncu --metrics gpu__time_duration.sum,dram__bytes_read.sum,dram__bytes_write.sum "
-               "--clock-control none -k regex:\"k_rs_adam|finalize\" on python bench.py "
-               "--no-e2e --no-cpu-baseline (one pass, full-size workload); mean per launch"}}
+               "--clock-control none -k regex:k_rs_adam_chunk -c 3 --csv on python bench.py "
+               f"{args} --no-e2e --no-cpu-baseline --steps 3 --warmup 3; mean per launch"}
+    try:
+        out = json.load(open(TRAFFIC_FILE))
+        if "entries" not in out:
+            raise ValueError
+    except (OSError, ValueError):
+        out = {"entries": {}}
+    out["hash"] = ("sha256 of the library's CUDA sources and headers with comments and "
+                   "whitespace removed")
+    out["scaling"] = ("bench.py scales an entry to another workload of the same kernel variant "
+                      "by padded elements (the pass streams every element once)")
+    out["entries"][traffic_key(cfg, fold2, deferred)] = entry
     with open(TRAFFIC_FILE, "w") as fh:
         json.dump(out, fh, indent=1)
-    print(json.dumps(out), flush=True)
+    print(json.dumps(entry), flush=True)
 
 
 def timed_cycles(fn, steps, warm, world, dev, stream):
@@ -541,7 +590,7 @@ def run_secondary(a, dpg, dev, world):
         "cycle_frac": bpd["step"] * cfg.psi / (d_ms * 1e-3) / 1e9 / peak,
         "roofline": fused_roofline(f"k_rs_adam_chunk<R={R}> (K={K} bf16 microbatches per "
                                    f"replica)", bpd["fused"], cfg.psi, k_def, peak, peak_kind,
-                                   None)}
+                                   traffic_per_launch(cfg, cfg.cap_bytes, N, deferred=True))}
     out["clocks"] = clocks.stop()
     del gd, w, m, v, param, sq, nf
     plan.destroy()
@@ -676,6 +725,7 @@ def run_dpg(a):
     # accumulation workload, each measured after the 1B buffers are freed
     extra = {}
     if (a.config == "llama1b" and a.cap_mib is None and getattr(a, "replicas", None) is None
+            and getattr(a, "microbatches", None) is None
             and a.variant == "direct" and not a.no_secondary):
         del g, gd, acc, g2, w, m, v, param, sq, nf
         torch.cuda.empty_cache()
@@ -685,7 +735,7 @@ def run_dpg(a):
     bpp = algorithmic_bytes_per_param(cfg, fold2, deferred)
     peak, peak_kind = load_peak()
     achieved = bpp["fused"] * cfg.psi / (k_ms * 1e-3) / 1e9
-    traffic = traffic_per_launch(cfg, cap, N)
+    traffic = traffic_per_launch(cfg, cap, N, fold2, deferred)
     value = job_throughput(cfg.psi, world, ms)
     line = {
         "metric": "params/s of the fused bucket reduce-scatter + Adam + all-gather step "
@@ -695,7 +745,8 @@ def run_dpg(a):
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": workload_desc(cfg, cap, plan.n_buckets, N, fold2, deferred),
         "hbm_gbs_step": bpp["step"] * cfg.psi / (ms * 1e-3) / 1e9,
-        "roofline": {"bound": "hbm", "kernel": fused_kernel_name(a, R, K), "achieved": achieved,
+        "roofline": {"bound": "hbm", "kernel": fused_kernel_name(a, R, K, fold2, deferred),
+                     "achieved": achieved,
                      "peak": peak, "peak_kind": f"{peak_kind} (copy bandwidth)", "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic,
                      "algorithmic_bytes_per_launch": bpp["fused"] * cfg.psi,
@@ -712,6 +763,83 @@ def run_dpg(a):
     if world > 1:
         dist.barrier()
         dist.destroy_process_group()
+
+
+def run_sharded(a):
+    """The ZeRO-2 split across ranks, one GPU each: rank r holds replica r's
+    gradient; per step the ranks exchange gradient slices, each updates its
+    own shard of every bucket, and the bf16 shards are all-gathered
+    (zero_optimizer_step_gb300.sharded).  value = parameters of the model
+    updated per second by the whole job."""
+    import torch
+    import torch.distributed as dist
+    rank, local, world = dist_info()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+    else:
+        import socket
+        with socket.socket() as sk:
+            sk.bind(("127.0.0.1", 0))
+            port = sk.getsockname()[1]
+        dist.init_process_group("nccl", init_method=f"tcp://127.0.0.1:{port}", rank=0,
+                                world_size=1, device_id=dev)
+    from zero_optimizer_step_gb300 import build as _build
+    if rank == 0:
+        _build.build()
+    dist.barrier()
+    import dataclasses
+
+    import zero_optimizer_step_gb300 as dpg
+    from zero_optimizer_step_gb300.sharded import ShardedStep
+    cfg = dataclasses.replace(CONFIGS[a.config], R=world, K=1)
+    cap = cap_of(cfg, a)
+    plan = dpg.dpg_plan_buckets(cfg.numels, cap, world)
+    N = plan.total_padded
+    segs = segments(plan.param_offset, cfg.numels)
+    grad = flat_grads_bf16(segs, N, cfg.grad_std, stream_seed(cfg.seed, KIND_GRAD, rank), device=dev)
+    st = ShardedStep(plan, rank, world, dev)
+    dpg.dpg_plan_upload(st.shard)
+    S = st.shard.total_padded
+    master = st.state_from_global(master_f32(N, stream_seed(cfg.seed, KIND_MASTER), device=dev))
+    m, v = torch.zeros(S, device=dev), torch.zeros(S, device=dev)
+    param = torch.empty(N, dtype=torch.bfloat16, device=dev)
+    sq = torch.empty(plan.n_buckets, device=dev)
+    local_tokens = token_counts(cfg)[rank:rank + 1]
+    stream = torch.cuda.current_stream()
+    state = {"t": 0}
+
+    def step(ev=None):
+        state["t"] += 1
+        tokens = st.all_tokens(local_tokens)
+        st.exchange(grad)
+        if ev is not None:
+            dpg.dpg_time_next_fused_launch(*ev)
+        st.update(tokens, dpg.HParams(step=state["t"]), master, m, v, bucket_sqnorm=sq,
+                  stream=stream)
+        st.allgather(param)
+
+    ms, k_all = timed_cycles(step, a.steps, a.warmup, world, dev, stream)
+    k_all = [max_over_ranks(x, world, dev) for x in k_all]
+    peak, peak_kind = load_peak()
+    bpp = 2 * world + 26
+    line = {"metric": "params/s of the fused bucket reduce-scatter + Adam + all-gather step "
+                      "(achieved HBM GB/s vs GB300 peak in roofline)",
+            "value": cfg.psi / (ms * 1e-3), "unit": "params/s", "n_gpus": world,
+            "steps": a.steps, "warmup": a.warmup, "ms_per_step": ms, "higher_is_better": True,
+            "scaling": "strong", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {**workload_desc(cfg, cap, plan.n_buckets, N),
+                       "sharded": "ZeRO-2 split: rank r owns shard r of every bucket; NCCL "
+                                  "point-to-point exchange of bf16 gradient slices, the fused "
+                                  "update of the rank's shard, NCCL all-gather of bf16 shards",
+                       "shard_elements_per_rank": S},
+            "roofline": fused_roofline(f"k_rs_adam_chunk<R={world}> on the rank's shard", bpp,
+                                       S, k_all, peak, peak_kind, None)}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    dist.barrier()
+    dist.destroy_process_group()
 
 
 def host_mem_available() -> int:
@@ -1386,6 +1514,8 @@ def main():
         return
     if a.impl == "reference":
         run_reference(a)
+    elif a.sharded:
+        run_sharded(a)
     else:
         run_dpg(a)
 

@@ -118,6 +118,24 @@ int dpg_abi_version(void);
  * ------------------------------------------------------------------------- */
 int dpg_plan_buckets(const int64_t* numels, int32_t n_params, int64_t cap_bytes,
                      int32_t R, dpg_plan_t** out);
+
+/* Shard plan of the ZeRO-2 split across R data-parallel ranks, one GPU each
+ * ["Parallelisms" -- ZeRO-2; "Parallelism Starts With the Bottleneck" --
+ *  Allreduce equals reducescatter plus allgather].  Rank r owns shard r of
+ * every bucket of `plan`.  *out receives a plan with the same R and one
+ * bucket per bucket of `plan`: its bucket b holds one slice of
+ * shard_numel_b = padded_b / R elements (the shard), zero-padded to a
+ * multiple of 8*R.  It is the same for every rank.  A rank lays out by it
+ * the slices of its shard that it receives from the R ranks (one flat buffer
+ * per source rank, padding zero), its fp32 master/m/v shard and its bf16
+ * parameter shard; dpg_reduce_scatter_adam on the shard plan, with the R
+ * received buffers in rank order as `grads`, then computes exactly the
+ * values of shard r of the single-device step (the same rank-ordered fp32
+ * sums, scale and Adam), and per-bucket norms of that shard alone.  The
+ * exchange itself (slice q of a rank's bucket to rank q before, the bf16
+ * shards to every rank after) is the caller's collective.  Host only.
+ * Free with dpg_plan_destroy. */
+int dpg_plan_shards(const dpg_plan_t* plan, dpg_plan_t** out);
 void dpg_plan_destroy(dpg_plan_t* plan);
 /* Sizes of a plan; any output pointer may be NULL. */
 int dpg_plan_info(const dpg_plan_t* plan, int32_t* n_params, int32_t* n_buckets,

@@ -313,3 +313,39 @@ def test_staged_fault_hook_needs_opt_in(monkeypatch):
     monkeypatch.setenv("DPG_TEST_HOOKS", "1")
     dpg.dpg_set_staged_fault(skip_unit=3, timeout_ns=1)
     dpg.dpg_set_staged_fault(skip_unit=-1, timeout_ns=0)   # disarm again
+
+
+def test_shard_plan_layout():
+    # one bucket per bucket of the global plan, holding its shard, padded to 8R
+    for name in ("tiny", "gpt2", "sweep"):
+        c = CONFIGS[name]
+        g = dpg.dpg_plan_buckets(c.numels, c.cap_bytes, c.R)
+        s = dpg.dpg_plan_shards(g)
+        assert (s.n_buckets, s.R, s.n_params) == (g.n_buckets, g.R, g.n_buckets)
+        np.testing.assert_array_equal(s.numels[::-1], g.shard_numel)
+        np.testing.assert_array_equal(s.param_bucket, np.arange(g.n_buckets)[::-1])
+        np.testing.assert_array_equal(s.param_offset[::-1], s.bucket_offset)
+        assert np.all(s.bucket_padded % (8 * g.R) == 0)
+        assert np.all((s.bucket_padded >= g.shard_numel) & (s.bucket_padded - g.shard_numel < 8 * g.R))
+        assert s.total_padded == int(s.bucket_padded.sum())
+    # the tiny case worked by hand: shards of 88 and 512 elements, R = 4
+    t = CONFIGS["tiny"]
+    s = dpg.dpg_plan_shards(dpg.dpg_plan_buckets(t.numels, t.cap_bytes, t.R))
+    np.testing.assert_array_equal(s.bucket_offset, [0, 96])
+    np.testing.assert_array_equal(s.bucket_padded, [96, 512])
+    # an empty plan has an empty shard plan
+    e = dpg.dpg_plan_shards(dpg.dpg_plan_buckets([], 1024, 2))
+    assert e.n_buckets == 0 and e.total_padded == 0
+
+
+def test_shard_plan_validation():
+    L = dpg.lib()
+    out = ctypes.c_void_p()
+    assert L.dpg_plan_shards(None, ctypes.byref(out)) == dpg.DPG_ERR_INVALID_ARG
+    g = dpg.dpg_plan_buckets([100], 1024, 2)
+    assert L.dpg_plan_shards(g.handle, None) == dpg.DPG_ERR_INVALID_ARG
+    # zero-size parameters only: one empty bucket, and one empty shard
+    z = dpg.dpg_plan_buckets([0, 0], 1024, 2)
+    assert z.n_buckets == 1 and z.total_padded == 0
+    zs = dpg.dpg_plan_shards(z)
+    assert zs.n_buckets == 1 and zs.total_padded == 0

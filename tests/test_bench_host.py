@@ -58,10 +58,10 @@ def _csv_row(i, name, metric, value):
 
 def test_traffic_parser_averages_the_fused_kernel_only(tmp_path, monkeypatch):
     lines = ["==PROF== banner", '"ID","Process ID"']
-    rows = [("0", "void k_rs_adam_chunk<8, 0, 0>(RsAdamArgs)", 100, 40),
-            ("1", "k_chunk_finalize(const double *)", 5, 0),
-            ("2", "void k_rs_adam_chunk<8, 0, 0>(RsAdamArgs)", 300, 60),
-            ("3", "void k_rs_adam_staged<8>(StagedArgs)", 999, 999),
+    rows = [("0", "void dpg::k_rs_adam_chunk<8, 0, 0>(dpg::RsAdamArgs)", 100, 40),
+            ("1", "dpg::k_chunk_finalize(dpg::FinalizeArgs)", 5, 0),
+            ("2", "void dpg::k_rs_adam_chunk<8, 0, 0>(dpg::RsAdamArgs)", 300, 60),
+            ("3", "void dpg::k_rs_adam_staged<8>(dpg::StagedArgs)", 999, 999),
             ("4", "vectorized_elementwise_kernel", 7, 7)]
     for i, name, rd, wr in rows:
         lines.append(_csv_row(i, name, "dram__bytes_read.sum", f"{rd:,}"))
@@ -71,19 +71,33 @@ def test_traffic_parser_averages_the_fused_kernel_only(tmp_path, monkeypatch):
     csv_path.write_text("\n".join(lines) + "\n")
     out = tmp_path / "traffic.json"
     monkeypatch.setattr(bench, "TRAFFIC_FILE", str(out))
-    a = types.SimpleNamespace(config="llama1b", traffic_from=str(csv_path), cap_mib=None)
+    a = types.SimpleNamespace(config="gpt2", traffic_from=str(csv_path), cap_mib=None,
+                              replicas=None, microbatches=None, fold2=False, deferred=False)
     bench.write_traffic(a)
-    t = json.loads(out.read_text())["k_rs_adam"]
+    small = CONFIGS["gpt2"]
+    t = json.loads(out.read_text())["entries"][bench.traffic_key(small)]
     assert t["launches"] == 2
     assert t["dram_bytes_read"] == 200 and t["dram_bytes_write"] == 50
     assert t["dram_bytes_per_launch"] == 250
     assert t["source_sha256"] == bench.kernel_source_sha256()
-    # read back while the code hash matches; scaled by elements for another size
-    cfg = CONFIGS["llama1b"]
-    assert bench.traffic_per_launch(cfg, cfg.cap_bytes, cfg.psi) == pytest.approx(250)
-    t["source_sha256"] = "0" * 64
-    out.write_text(json.dumps({"k_rs_adam": t}))
-    assert bench.traffic_per_launch(cfg, cfg.cap_bytes, cfg.psi) is None
+    # a second variant lands in its own entry, the first one stays
+    a2 = types.SimpleNamespace(**{**vars(a), "replicas": 4, "microbatches": 4})
+    bench.write_traffic(a2)
+    entries = json.loads(out.read_text())["entries"]
+    assert set(entries) == {"k_rs_adam_chunk R=8 K=1 bf16", "k_rs_adam_chunk R=4 K=4 acc_fp32_last_bf16"}
+    # read back while the code hash matches, scaled by elements to a larger
+    # workload of the same variant; another variant has no entry
+    big = CONFIGS["llama1b"]
+    n_small = t["elements"]
+    assert bench.traffic_per_launch(big, big.cap_bytes, 10 * n_small) == pytest.approx(2500)
+    acc = types.SimpleNamespace(R=4, K=4)
+    assert bench.traffic_per_launch(acc, 0, n_small) == pytest.approx(250)
+    assert bench.traffic_per_launch(acc, 0, n_small, deferred=True) is None
+    assert bench.traffic_per_launch(types.SimpleNamespace(R=2, K=1), 0, n_small) is None
+    whole = json.loads(out.read_text())
+    whole["entries"]["k_rs_adam_chunk R=8 K=1 bf16"]["source_sha256"] = "0" * 64
+    out.write_text(json.dumps(whole))
+    assert bench.traffic_per_launch(big, big.cap_bytes, n_small) is None
 
 
 def test_code_hash_ignores_comments_and_whitespace(tmp_path, monkeypatch):
@@ -104,13 +118,18 @@ def test_kernel_sources_exist():
 
 
 def test_replicas_override():
-    a = types.SimpleNamespace(config="llama1b", replicas=16)
+    a = types.SimpleNamespace(config="llama1b", replicas=16, microbatches=None)
     c = bench.config_of(a)
     assert c.R == 16 and c.psi == CONFIGS["llama1b"].psi
     assert bench.algorithmic_bytes_per_param(c)["fused"] == 2 * 16 + 26
     assert bench.config_of(types.SimpleNamespace(config="gpt2", replicas=None)) is CONFIGS["gpt2"]
     with pytest.raises(SystemExit):
         bench.config_of(types.SimpleNamespace(config="gpt2", replicas=65))
+    c = bench.config_of(types.SimpleNamespace(config="gpt2", replicas=4, microbatches=4))
+    assert (c.R, c.K) == (4, 4)
+    assert bench.algorithmic_bytes_per_param(c) == {"fused": 50, "step": 154}
+    with pytest.raises(SystemExit):
+        bench.config_of(types.SimpleNamespace(config="gpt2", replicas=None, microbatches=0))
 
 
 def test_reference_line_states_what_it_timed():

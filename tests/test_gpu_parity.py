@@ -310,6 +310,25 @@ def test_multi_segment_bucket_norms_and_counter_reset():
     assert (nfb == 0).all()
 
 
+def test_short_and_long_bucket_norms_in_one_finalize():
+    """Buckets of at most 256 tiles (1,048,576 elements) are finalized by one
+    warp each, longer ones by one CTA per segment, in the same launch; a
+    bucket of exactly 256 tiles, one of 257, a two-segment bucket and small
+    packed buckets side by side, launched whole and split at every bucket
+    boundary: parity with the oracle, and the same norm bits in every split."""
+    numels = [9_000_000, 1_052_672, 1_048_576, 5000, 70_000, 300_000, 1_048_568, 12_345, 777,
+              2_000_000, 4096, 1]
+    whole = run_case(StepCase(numels=numels, cap_bytes=2 << 20, R=2, seed=43))
+    assert_parity(whole)
+    tiles = -(-np.asarray(whole.plan.bucket_padded) // 4096)
+    assert 256 in tiles and 257 in tiles and (tiles > 2048).any() and (tiles < 256).sum() >= 3
+    for b in range(1, whole.plan.n_buckets):
+        part = run_case(StepCase(numels=numels, cap_bytes=2 << 20, R=2, seed=43, b_split=b))
+        assert_parity(part)
+        assert np.array_equal(part.gpu["sq"].view(np.uint32), whole.gpu["sq"].view(np.uint32)), b
+        np.testing.assert_array_equal(part.gpu["nf"], whole.gpu["nf"])
+
+
 def test_launch_count_and_kernels():
     cfg = CONFIGS["tiny"]
     before = dpg.dpg_launch_count()

@@ -1,0 +1,77 @@
+"""One rank's update of the ZeRO-2 split on the GPU ("Parallelisms" -- ZeRO-2).
+
+For every rank r of R = 2, 4, 8 (and a generic R = 3): the slices the
+exchange would deliver are copied locally from all R replica buffers
+(sharded.loopback_receive), then the library's fused update runs on the shard
+plan (dpg_plan_shards) with those R slice buffers as its replicas.  Its
+master/m/v shard and bf16 parameter shard must equal, bit for bit, shard r of
+the single-device dpg_step over all R replicas and of the CPU oracle's step;
+the per-bucket norms of the R shards must add up to the bucket's norm.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import zero_optimizer_step_gb300 as dpg
+from parity_util import np_bf16, np_f32
+from workloads import KIND_GRAD, KIND_MASTER, flat_grads_bf16, master_f32, random_param_list, segments, stream_seed
+from zero_optimizer_step_gb300.sharded import ShardedStep, loopback_receive
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    from zero_optimizer_step_gb300 import build
+    build.build()
+
+
+@pytest.mark.parametrize("R", [2, 3, 4, 8])
+def test_shard_update_equals_single_device_step(R):
+    numels = random_param_list(np.random.Generator(np.random.Philox(70 + R)), 40, 300_000)
+    plan = dpg.dpg_plan_buckets(numels, 1 << 19, R)
+    N, nb = plan.total_padded, plan.n_buckets
+    assert nb >= 5
+    segs = segments(plan.param_offset, numels)
+    grads = [flat_grads_bf16(segs, N, 1e-3, stream_seed(70, KIND_GRAD, s), device="cuda")
+             for s in range(R)]
+    master0 = master_f32(N, stream_seed(70, KIND_MASTER), device="cuda")
+    tok = [2900 + 31 * s for s in range(R)]
+    hp = dpg.HParams(step=2)
+
+    # the single-device step over every replica
+    w, m, v = master0.clone(), torch.zeros(N, device="cuda"), torch.zeros(N, device="cuda")
+    p = torch.empty(N, dtype=torch.bfloat16, device="cuda")
+    sq = torch.empty(nb, device="cuda")
+    dpg.dpg_step(plan, grads, tok, hp, w, m, v, [p], bucket_sqnorm=sq)
+    torch.cuda.synchronize()
+    # and the oracle's
+    ow, om, ov = np_f32(master0).copy(), np.zeros(N, np.float32), np.zeros(N, np.float32)
+    oviews, _, _ = oracle.step(plan.bucket_offset, plan.bucket_padded, [np_bf16(g) for g in grads],
+                               np.asarray(tok, np.int64), ow, om, ov, t=2)
+
+    shard_sq = []
+    for r in range(R):
+        st = ShardedStep(plan, r, R, "cuda")
+        S = st.shard.total_padded
+        ms = st.state_from_global(master0)
+        mm, vv = torch.zeros(S, device="cuda"), torch.zeros(S, device="cuda")
+        ssq = torch.full((nb,), float("nan"), device="cuda")
+        loopback_receive(st, grads)
+        st.update(tok, hp, ms, mm, vv, bucket_sqnorm=ssq)
+        torch.cuda.synchronize()
+        for b in range(nb):
+            lo, hi = st.global_slice(b, r)
+            a, z = st.shard_slice(b)
+            for name, mine, ref, oref in (("master", ms, w, ow), ("m", mm, m, om), ("v", vv, v, ov)):
+                got = np_f32(mine[a:z]).view(np.uint32)
+                assert np.array_equal(got, np_f32(ref[lo:hi]).view(np.uint32)), (name, r, b)
+                assert np.array_equal(got, oref[lo:hi].view(np.uint32)), (name, r, b)
+            gp = np_bf16(st.param_shard[a:z])
+            assert np.array_equal(gp, np_bf16(p[lo:hi])), ("param", r, b)
+            assert np.array_equal(gp, oviews[0][lo:hi]), ("param", r, b)
+        shard_sq.append(np_f32(ssq).astype(np.float64))
+    total = np.sum(shard_sq, axis=0)
+    ref = np_f32(sq).astype(np.float64)
+    assert np.all(np.abs(total - ref) <= 1e-5 * ref)

@@ -42,6 +42,7 @@ EXPORTED = (
     "dpg_allreduce_grads", "dpg_adam_from_reduced", "dpg_gather_params_bf16",
     "dpg_accumulate_pair", "dpg_step_fold2", "dpg_set_fused_max_ctas",
     "dpg_set_programmatic_launch", "dpg_reduce_scatter_adam_when_ready", "dpg_step_deferred",
+    "dpg_plan_shards",
 )
 DPG_MAX_STATE_ARRAYS = 8
 DPG_NOALLOC_SCRATCH_BYTES = 8 << 20
@@ -130,6 +131,7 @@ def lib() -> ctypes.CDLL:
         L.dpg_export_state.argtypes = [P, P, P, i32, P]
         L.dpg_import_state.argtypes = [P, P, P, i32, P]
         L.dpg_time_next_fused_launch.argtypes = [P, P]
+        L.dpg_plan_shards.argtypes = [P, ctypes.POINTER(P)]
         L.dpg_time_next_fused_launch.restype = c_int
         for name in ("dpg_plan_buckets", "dpg_plan_info", "dpg_plan_bucket", "dpg_plan_param",
                      "dpg_plan_export", "dpg_plan_upload", "dpg_pack", "dpg_unpack",
@@ -139,7 +141,8 @@ def lib() -> ctypes.CDLL:
                      "dpg_set_staged_fault", "dpg_allreduce_grads", "dpg_adam_from_reduced",
                      "dpg_gather_params_bf16", "dpg_accumulate_pair", "dpg_step_fold2",
                      "dpg_set_fused_max_ctas", "dpg_set_programmatic_launch",
-                     "dpg_reduce_scatter_adam_when_ready", "dpg_step_deferred"):
+                     "dpg_reduce_scatter_adam_when_ready", "dpg_step_deferred",
+                     "dpg_plan_shards"):
             getattr(L, name).restype = c_int
         _lib = L
     return _lib
@@ -283,6 +286,14 @@ def dpg_plan_buckets(numels: Sequence[int], cap_bytes: int, R: int) -> Plan:
     _check(lib().dpg_plan_buckets(n.ctypes.data if n.size else None, n.size, int(cap_bytes),
                                   int(R), ctypes.byref(out)))
     return Plan(out.value, n)
+
+
+def dpg_plan_shards(plan: Plan) -> Plan:
+    """Shard plan of the ZeRO-2 split across plan.R ranks: one bucket per
+    bucket of `plan`, holding that bucket's shard (see include/dpg.h)."""
+    out = ctypes.c_void_p()
+    _check(lib().dpg_plan_shards(plan.handle, ctypes.byref(out)))
+    return Plan(out.value, plan.shard_numel[::-1])
 
 
 def dpg_plan_upload(plan: Plan):

@@ -525,9 +525,15 @@ __global__ void __launch_bounds__(NT) k_norm_chunk(const __grid_constant__ RsAda
 // butterfly tree (within each warp, then over the 32 warp sums) gives the
 // segment's sum.  The CTA that completes a bucket's last segment (a per-bucket
 // arrival counter, which it resets to zero for the next launch) adds the
-// bucket's segment sums in segment order.  Every grouping is fixed by the
-// plan, so the result is the same on every run and for any bucket range.
+// bucket's segment sums in segment order.  A short bucket (at most
+// kShortTiles tiles: one segment of <= 1024 chunks) is summed by one warp
+// along the same tree, so it gets the same bits.
+// One launch does both: the long buckets' segment CTAs first, then CTAs of
+// 32 warps for the short buckets.  Every grouping is fixed by the plan, so
+// the result is the same on every run and for any bucket range.
 constexpr int kChunkFinalizeThreads = 1024;
+static_assert(kShortTiles * kChunksPerTile <= kChunkFinalizeThreads && kShortTiles <= kSegTiles,
+              "a short bucket is one segment with at most one chunk per finalize thread");
 
 struct FinalizeArgs {
     const double* chunk_sq;     // per-chunk partials of the launch (chunk 0 = tile t0)
@@ -538,13 +544,73 @@ struct FinalizeArgs {
     double* seg_sq;             // per-segment sums
     long long* seg_nf;
     int32_t* done;              // per-bucket arrival counters
+    const int32_t* long_list;   // segment ids of the long buckets
+    const int32_t* short_list;  // short bucket ids
     int64_t t0;                 // first tile of the launch
     int32_t cpt;                // chunks per tile
-    int32_t s0;                 // first segment of the launch
+    int32_t l0, l1;             // the launch's slice of long_list
+    int32_t q0, q1;             // the launch's slice of short_list
     float* sqnorm;              // outputs, indexed by bucket (nullable)
     int64_t* nonfinite;
     double* sqnorm64;
 };
+
+// One warp per short bucket (n <= 1024 chunks, a single segment): the same
+// tree as k_chunk_finalize.  There thread j of the segment's CTA holds
+// 0 + chunk j (chunk j < n; 0 otherwise; adding zeros to a non-negative sum
+// of squares changes nothing), each warp sums its 32 threads by butterfly,
+// and warp 0 sums the 32 warp results by butterfly; here the warp forms the
+// 32 warp results one after the other, lane w keeping the w-th, then sums
+// them by the same butterfly.
+__device__ __forceinline__ void finalize_short_bucket(const FinalizeArgs& f, int32_t q) {
+    constexpr int U = 8;
+    const int lane = threadIdx.x & 31;
+    if (q >= f.q1) return;
+    const int b = __ldg(f.short_list + q);
+    const int64_t cb = (__ldg(f.tile_begin + b) - f.t0) * f.cpt;
+    const int n = int((__ldg(f.tile_begin + b + 1) - f.t0) * f.cpt - cb);
+    const int rows = (n + 31) >> 5;       // warp results with any chunk (<= 32)
+    double keep = 0.0;
+    long long keep_n = 0;
+    for (int w0 = 0; w0 < rows; w0 += U) {
+        double x[U];
+        int y[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int k = (w0 + u) * 32 + lane;
+            x[u] = k < n ? f.chunk_sq[cb + k] : 0.0;
+            y[u] = k < n ? f.chunk_nf[cb + k] : 0;
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            double acc = 0.0;
+            long long cnt = 0;
+            acc += x[u];
+            cnt += y[u];
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+                acc += __shfl_xor_sync(0xFFFFFFFFu, acc, o);
+                cnt += __shfl_xor_sync(0xFFFFFFFFu, cnt, o);
+            }
+            if (lane == w0 + u) {
+                keep = acc;
+                keep_n = cnt;
+            }
+        }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        keep += __shfl_xor_sync(0xFFFFFFFFu, keep, o);
+        keep_n += __shfl_xor_sync(0xFFFFFFFFu, keep_n, o);
+    }
+    if (lane != 0) return;
+    // the CTA path's last step adds the bucket's one segment sum to 0.0
+    double tot = 0.0;
+    tot += keep;
+    if (f.sqnorm) f.sqnorm[b] = float(tot);
+    if (f.nonfinite) f.nonfinite[b] = keep_n;
+    if (f.sqnorm64) f.sqnorm64[b] = tot;
+}
 
 __global__ void __launch_bounds__(kChunkFinalizeThreads)
 k_chunk_finalize(const __grid_constant__ FinalizeArgs f) {
@@ -553,7 +619,15 @@ k_chunk_finalize(const __grid_constant__ FinalizeArgs f) {
     __shared__ double w_sq[NW];
     __shared__ long long w_nf[NW];
     pdl_enter();
-    const int32_t s = f.s0 + int32_t(blockIdx.x);
+    // CTAs [0, l1 - l0): one long-bucket segment each; the CTAs after them:
+    // one short bucket per warp
+    const int32_t n_long = f.l1 - f.l0;
+    if (int32_t(blockIdx.x) >= n_long) {
+        finalize_short_bucket(f, f.q0 + (int32_t(blockIdx.x) - n_long) * NW +
+                                     int32_t(threadIdx.x >> 5));
+        return;
+    }
+    const int32_t s = __ldg(f.long_list + f.l0 + int32_t(blockIdx.x));
     const int b = __ldg(f.seg_bucket + s);
     const int64_t span = kSegTiles * f.cpt;
     const int64_t cb = (__ldg(f.tile_begin + b) - f.t0) * f.cpt;
@@ -781,12 +855,20 @@ static int launch_chunked(RsKernel fn, RsAdamArgs a, const Plan& p, bool want_no
         f.done = p.d_bucket_done;
         f.t0 = a.t0;
         f.cpt = cpt;
-        f.s0 = p.seg_first[size_t(a.b0)];
         f.sqnorm = sqnorm;
         f.nonfinite = nonfinite;
         f.sqnorm64 = sqnorm64;
-        const int32_t n_seg = p.seg_first[size_t(a.b1)] - f.s0;
-        if (n_seg > 0) st = launch_k(k_chunk_finalize, unsigned(n_seg), kChunkFinalizeThreads, s, who, f);
+        // the range's long-bucket segments (one CTA each), then its short
+        // buckets (one warp each)
+        f.long_list = p.d_long_seg;
+        f.l0 = p.long_first[size_t(a.b0)];
+        f.l1 = p.long_first[size_t(a.b1)];
+        f.short_list = p.d_short_bucket;
+        f.q0 = p.short_first[size_t(a.b0)];
+        f.q1 = p.short_first[size_t(a.b1)];
+        constexpr int32_t warps = kChunkFinalizeThreads / 32;
+        const int64_t grid = int64_t(f.l1 - f.l0) + (f.q1 - f.q0 + warps - 1) / warps;
+        if (grid > 0) st = launch_k(k_chunk_finalize, unsigned(grid), kChunkFinalizeThreads, s, who, f);
     }
     return st;
 }

@@ -45,6 +45,9 @@ constexpr int kPackPtrs = 1024;
 // round of 8 loads for each of its 1024 threads); the last CTA of a bucket
 // adds its segments' sums.
 constexpr int64_t kSegTiles = 2048;
+// A bucket of at most kShortTiles tiles (<= 1024 chunk partials) is summed by
+// one warp instead of a CTA: many small buckets then cost a few warps each.
+constexpr int64_t kShortTiles = 256;
 
 struct PackItem {
     int32_t param;     // registration index of the parameter
@@ -97,6 +100,13 @@ struct Plan {
     double* d_seg_sq = nullptr;       // n_seg
     long long* d_seg_nf = nullptr;    // n_seg
     int32_t* d_bucket_done = nullptr; // n_buckets
+    // short buckets (<= kShortTiles tiles) are finalized by one warp each,
+    // the segments of the other buckets by one CTA each; both lists ascend,
+    // and the host prefixes give each bucket range's slice of them
+    std::vector<int32_t> short_first; // n_buckets + 1: short buckets before b
+    std::vector<int32_t> long_first;  // n_buckets + 1: long-bucket segments before b
+    int32_t* d_short_bucket = nullptr;// short bucket ids
+    int32_t* d_long_seg = nullptr;    // segment ids of the long buckets
     // global-norm clipping: per-bucket fp64 squared norms and the coefficient
     void* d_clip = nullptr;
     double* d_bucket_sq64 = nullptr;  // n_buckets + 1

@@ -171,6 +171,34 @@ int dpg_plan_buckets(const int64_t* numels, int32_t n_params, int64_t cap_bytes,
     return DPG_OK;
 }
 
+int dpg_plan_shards(const dpg_plan_t* plan, dpg_plan_t** out) {
+    dpg::clear_error();
+    if (!out) return fail(DPG_ERR_INVALID_ARG, "dpg_plan_shards: out is NULL");
+    *out = nullptr;
+    if (!plan) return fail(DPG_ERR_INVALID_ARG, "dpg_plan_shards: plan is NULL");
+    const dpg::Plan& g = plan->p;
+    // one "parameter" per bucket of the global plan, registered in reverse
+    // bucket order so that the planner (which walks registration order
+    // backwards) places shard 0 first; a 2-byte cap keeps each alone
+    std::vector<int64_t> numels;
+    try {
+        numels.assign(size_t(g.n_buckets), 0);
+    } catch (const std::bad_alloc&) {
+        return fail(DPG_ERR_OOM, "dpg_plan_shards: out of host memory");
+    }
+    for (int32_t b = 0; b < g.n_buckets; ++b)
+        numels[size_t(g.n_buckets - 1 - b)] = (g.bucket_offset[b + 1] - g.bucket_offset[b]) / g.R;
+    dpg_plan_t* h = nullptr;
+    const int st = dpg_plan_buckets(numels.data(), g.n_buckets, 2, g.R, &h);
+    if (st != DPG_OK) return st;
+    if (h->p.n_buckets != g.n_buckets) {
+        dpg_plan_destroy(h);
+        return fail(DPG_ERR_INVALID_ARG, "dpg_plan_shards: a bucket of the plan holds no element");
+    }
+    *out = h;
+    return DPG_OK;
+}
+
 void dpg_plan_destroy(dpg_plan_t* plan) {
     if (!plan) return;
     dpg::release_device(plan->p);

@@ -137,13 +137,22 @@ int upload(Plan& p) {
     const size_t csq_bytes = round256(n_chunks1 * sizeof(double));
     void* chunk = nullptr;
     if (e == cudaSuccess) e = cudaMalloc(&chunk, tb_bytes + csq_bytes + n_chunks1 * sizeof(int32_t));
-    // finalize segments: ceil(tiles / kSegTiles) per bucket, at least one
+    // finalize segments: ceil(tiles / kSegTiles) per bucket, at least one;
+    // short buckets (one segment of <= kShortTiles tiles) go to the warp list
     std::vector<int32_t> seg_first(nb1, 0), seg_bucket;
+    std::vector<int32_t> short_first(nb1, 0), long_first(nb1, 0), short_bucket, long_seg;
     for (int32_t b = 0; b < p.n_buckets; ++b) {
         const int64_t nt = p.tile_begin[b + 1] - p.tile_begin[b];
         const int64_t ns = nt > 0 ? (nt + kSegTiles - 1) / kSegTiles : 1;
-        for (int64_t k = 0; k < ns; ++k) seg_bucket.push_back(b);
+        const bool is_short = nt <= kShortTiles;
+        if (is_short) short_bucket.push_back(b);
+        for (int64_t k = 0; k < ns; ++k) {
+            if (!is_short) long_seg.push_back(int32_t(seg_bucket.size()));
+            seg_bucket.push_back(b);
+        }
         seg_first[size_t(b) + 1] = int32_t(seg_bucket.size());
+        short_first[size_t(b) + 1] = int32_t(short_bucket.size());
+        long_first[size_t(b) + 1] = int32_t(long_seg.size());
     }
     const size_t n_seg1 = seg_bucket.empty() ? 1 : seg_bucket.size();
     const size_t sf_bytes = round256(nb1 * sizeof(int32_t));
@@ -151,9 +160,14 @@ int upload(Plan& p) {
     const size_t ss_bytes = round256(n_seg1 * sizeof(double));
     const size_t sn_bytes = round256(n_seg1 * sizeof(long long));
     const size_t done_bytes = round256(nb1 * sizeof(int32_t));
+    const size_t shb_bytes = round256(nb1 * sizeof(int32_t));     // short bucket ids
+    const size_t lsg_bytes = round256(n_seg1 * sizeof(int32_t));  // long-bucket segment ids
     void* seg = nullptr;
-    if (e == cudaSuccess) e = cudaMalloc(&seg, sf_bytes + sb_bytes + ss_bytes + sn_bytes + done_bytes);
+    if (e == cudaSuccess)
+        e = cudaMalloc(&seg, sf_bytes + sb_bytes + ss_bytes + sn_bytes + done_bytes + shb_bytes +
+                                 lsg_bytes);
     unsigned char* sbase = static_cast<unsigned char*>(seg);
+    unsigned char* shb = sbase + sf_bytes + sb_bytes + ss_bytes + sn_bytes + done_bytes;
     if (e == cudaSuccess)
         e = cudaMemcpy(sbase, seg_first.data(), nb1 * sizeof(int32_t), cudaMemcpyHostToDevice);
     if (e == cudaSuccess && !seg_bucket.empty())
@@ -161,6 +175,12 @@ int upload(Plan& p) {
                        cudaMemcpyHostToDevice);
     if (e == cudaSuccess)
         e = cudaMemset(sbase + sf_bytes + sb_bytes + ss_bytes + sn_bytes, 0, done_bytes);
+    if (e == cudaSuccess && !short_bucket.empty())
+        e = cudaMemcpy(shb, short_bucket.data(), short_bucket.size() * sizeof(int32_t),
+                       cudaMemcpyHostToDevice);
+    if (e == cudaSuccess && !long_seg.empty())
+        e = cudaMemcpy(shb + shb_bytes, long_seg.data(), long_seg.size() * sizeof(int32_t),
+                       cudaMemcpyHostToDevice);
     std::vector<int64_t> tile_span(2 * n_tiles1, 0);
     for (int32_t b = 0; b < p.n_buckets; ++b)
         for (int64_t t = p.tile_begin[b]; t < p.tile_begin[b + 1]; ++t) {
@@ -205,6 +225,10 @@ int upload(Plan& p) {
     p.d_seg_sq = reinterpret_cast<double*>(sbase + sf_bytes + sb_bytes);
     p.d_seg_nf = reinterpret_cast<long long*>(sbase + sf_bytes + sb_bytes + ss_bytes);
     p.d_bucket_done = reinterpret_cast<int32_t*>(sbase + sf_bytes + sb_bytes + ss_bytes + sn_bytes);
+    p.short_first = std::move(short_first);
+    p.long_first = std::move(long_first);
+    p.d_short_bucket = reinterpret_cast<int32_t*>(shb);
+    p.d_long_seg = reinterpret_cast<int32_t*>(shb + shb_bytes);
     p.cap_visits = cap_visits;
     p.cap_ctas = int32_t(cap_ctas);
     p.device = dev;
