@@ -101,6 +101,10 @@ def parse():
                     help="--overlap: give the backward stream the higher priority")
     ap.add_argument("--backward-ms", type=float, default=30.0,
                     help="duration of the simulated backward (--overlap)")
+    ap.add_argument("--launch-floor", action="store_true",
+                    help="one fused launch over one bucket of n elements, n = 1M..128M (R = 8), "
+                         "timed from CUDA graphs with L2 flushed: the fixed cost per launch "
+                         "(T = T0 + bytes / bandwidth)")
     ap.add_argument("--hockney", action="store_true",
                     help="bucket-cap sweep: per-bucket launches vs one fused launch, alpha-beta fit")
     a = ap.parse_args()
@@ -1159,6 +1163,72 @@ def run_hockney(a):
     print(json.dumps(out), flush=True)
 
 
+def run_launch_floor(a):
+    """Single fused launches (no norm) over one bucket of n elements, R = 8,
+    for n from 1M to 128M elements: least squares T = T0 + bytes / B over the
+    sizes from 4M up gives the fixed cost T0 of a launch (start-up of the
+    first CTAs, the drain of the last) and its streaming bandwidth B."""
+    import torch
+    from zero_optimizer_step_gb300 import build as _build
+    _build.build()
+    import zero_optimizer_step_gb300 as dpg
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    R = 8
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    sizes = [1 << 20, 2 << 20, CONFIGS["sweep"].psi, 8 << 20, 16 << 20, 32 << 20, 64 << 20,
+             128 << 20]
+    rows = []
+    for n in sizes:
+        plan = dpg.dpg_plan_buckets([n], 2 * n + 1024, R)
+        dpg.dpg_plan_upload(plan)
+        N = plan.total_padded
+        g = [flat_grads_bf16([(0, n)], N, 1e-3, stream_seed(7, KIND_GRAD, r), device=dev)
+             for r in range(R)]
+        w = master_f32(N, stream_seed(7, KIND_MASTER), device=dev)
+        m, v = torch.zeros(N, device=dev), torch.zeros(N, device=dev)
+        p = torch.empty(N, dtype=torch.bfloat16, device=dev)
+        tok = [3500] * R
+        hp = dpg.HParams(step=1)
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            for _ in range(2):
+                dpg.dpg_reduce_scatter_adam(plan, g, tok, hp, w, m, v, [p])
+        torch.cuda.current_stream().wait_stream(s)
+        gr = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gr):
+            dpg.dpg_reduce_scatter_adam(plan, g, tok, hp, w, m, v, [p])
+        ts = []
+        for _ in range(max(5, a.steps)):
+            flush.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            gr.replay()
+            e1.record()
+            torch.cuda.synchronize()
+            ts.append(e0.elapsed_time(e1))
+        ms = statistics.median(ts)
+        rows.append({"elements": n, "bytes": (2 * R + 26) * n, "ms": ms,
+                     "gbs": (2 * R + 26) * n / (ms * 1e-3) / 1e9})
+        del gr, g, w, m, v, p
+        plan.destroy()
+        torch.cuda.empty_cache()
+    big = [q for q in rows if q["elements"] >= 4 << 20]
+    A = np.stack([np.ones(len(big)), [q["bytes"] for q in big]], axis=1)
+    (t0, inv_b), *_ = np.linalg.lstsq(A, np.array([q["ms"] * 1e-3 for q in big]), rcond=None)
+    peak, peak_kind = load_peak()
+    for q in rows:
+        q["frac"] = q["gbs"] / peak
+    print(json.dumps({"metric": "fixed cost of one fused reduce-scatter+Adam launch",
+                      "R": R, "rows": rows,
+                      "fit": {"t0_us": t0 * 1e6, "bandwidth_gbs": 1.0 / inv_b / 1e9,
+                              "model": "T = T0 + bytes / B, least squares over n >= 4M"},
+                      "peak_gbs": peak, "peak_kind": peak_kind,
+                      "timing": "median CUDA graph replay, L2 flushed (256 MB write) before each"}),
+          flush=True)
+
+
 def hockney_compact(dpg, reps=5):
     """The alpha-beta record of the default line: the 1B list at its three caps
     (1 / 25 / 100 MiB), one launch per bucket against one launch in all."""
@@ -1511,6 +1581,9 @@ def main():
         return
     if a.hockney:
         run_hockney(a)
+        return
+    if a.launch_floor:
+        run_launch_floor(a)
         return
     if a.impl == "reference":
         run_reference(a)
