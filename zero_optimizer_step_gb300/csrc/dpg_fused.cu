@@ -550,6 +550,7 @@ struct FinalizeArgs {
     int32_t cpt;                // chunks per tile
     int32_t l0, l1;             // the launch's slice of long_list
     int32_t q0, q1;             // the launch's slice of short_list
+    int32_t short_per_cta;      // short buckets (warps) per CTA, <= 32
     float* sqnorm;              // outputs, indexed by bucket (nullable)
     int64_t* nonfinite;
     double* sqnorm64;
@@ -583,6 +584,7 @@ __device__ __forceinline__ void finalize_short_bucket(const FinalizeArgs& f, int
         }
 #pragma unroll
         for (int u = 0; u < U; ++u) {
+            if (w0 + u >= rows) break;        // the rest are sums of zeros: 0 (uniform)
             double acc = 0.0;
             long long cnt = 0;
             acc += x[u];
@@ -598,10 +600,14 @@ __device__ __forceinline__ void finalize_short_bucket(const FinalizeArgs& f, int
             }
         }
     }
+    // with one warp result (n <= 32) the tree over the 32 results adds only
+    // zeros to it, which changes no bit of a sum of squares
+    if (rows > 1) {
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-        keep += __shfl_xor_sync(0xFFFFFFFFu, keep, o);
-        keep_n += __shfl_xor_sync(0xFFFFFFFFu, keep_n, o);
+        for (int o = 16; o > 0; o >>= 1) {
+            keep += __shfl_xor_sync(0xFFFFFFFFu, keep, o);
+            keep_n += __shfl_xor_sync(0xFFFFFFFFu, keep_n, o);
+        }
     }
     if (lane != 0) return;
     // the CTA path's last step adds the bucket's one segment sum to 0.0
@@ -623,8 +629,9 @@ k_chunk_finalize(const __grid_constant__ FinalizeArgs f) {
     // one short bucket per warp
     const int32_t n_long = f.l1 - f.l0;
     if (int32_t(blockIdx.x) >= n_long) {
-        finalize_short_bucket(f, f.q0 + (int32_t(blockIdx.x) - n_long) * NW +
-                                     int32_t(threadIdx.x >> 5));
+        const int32_t warp = int32_t(threadIdx.x >> 5);
+        if (warp < f.short_per_cta)
+            finalize_short_bucket(f, f.q0 + (int32_t(blockIdx.x) - n_long) * f.short_per_cta + warp);
         return;
     }
     const int32_t s = __ldg(f.long_list + f.l0 + int32_t(blockIdx.x));
@@ -866,8 +873,16 @@ static int launch_chunked(RsKernel fn, RsAdamArgs a, const Plan& p, bool want_no
         f.short_list = p.d_short_bucket;
         f.q0 = p.short_first[size_t(a.b0)];
         f.q1 = p.short_first[size_t(a.b1)];
-        constexpr int32_t warps = kChunkFinalizeThreads / 32;
-        const int64_t grid = int64_t(f.l1 - f.l0) + (f.q1 - f.q0 + warps - 1) / warps;
+        // the short buckets are spread over the SMs: up to 32 warps per CTA,
+        // fewer when there are fewer short buckets than 32 per SM
+        int sms = 1;
+        st = sm_count(p.device, &sms);
+        if (st != DPG_OK) return st;
+        const int32_t n_short = f.q1 - f.q0;
+        int32_t per = (n_short + sms - 1) / sms;
+        per = per < 1 ? 1 : (per > kChunkFinalizeThreads / 32 ? kChunkFinalizeThreads / 32 : per);
+        f.short_per_cta = per;
+        const int64_t grid = int64_t(f.l1 - f.l0) + (n_short + per - 1) / per;
         if (grid > 0) st = launch_k(k_chunk_finalize, unsigned(grid), kChunkFinalizeThreads, s, who, f);
     }
     return st;
