@@ -797,27 +797,35 @@ def run_sharded(a):
 
     import zero_optimizer_step_gb300 as dpg
     from zero_optimizer_step_gb300.sharded import ShardedStep
-    cfg = dataclasses.replace(CONFIGS[a.config], R=world, K=1)
+    cfg = dataclasses.replace(CONFIGS[a.config], R=world)
+    if getattr(a, "microbatches", None) is not None:
+        cfg = dataclasses.replace(cfg, K=a.microbatches)
+    K = cfg.K
     cap = cap_of(cfg, a)
     plan = dpg.dpg_plan_buckets(cfg.numels, cap, world)
     N = plan.total_padded
     segs = segments(plan.param_offset, cfg.numels)
     grad = flat_grads_bf16(segs, N, cfg.grad_std, stream_seed(cfg.seed, KIND_GRAD, rank), device=dev)
-    st = ShardedStep(plan, rank, world, dev)
+    # K > 1: every microbatch is added into an fp32 buffer on the rank, whose
+    # fp32 slices are exchanged
+    acc = torch.empty(N, device=dev) if K > 1 else None
+    st = ShardedStep(plan, rank, world, dev, grad_dtype=torch.float32 if K > 1 else None)
     dpg.dpg_plan_upload(st.shard)
     S = st.shard.total_padded
     master = st.state_from_global(master_f32(N, stream_seed(cfg.seed, KIND_MASTER), device=dev))
     m, v = torch.zeros(S, device=dev), torch.zeros(S, device=dev)
     param = torch.empty(N, dtype=torch.bfloat16, device=dev)
     sq = torch.empty(plan.n_buckets, device=dev)
-    local_tokens = token_counts(cfg)[rank:rank + 1]
+    local_tokens = token_counts(cfg)[rank * K:(rank + 1) * K]
     stream = torch.cuda.current_stream()
     state = {"t": 0}
 
     def step(ev=None):
         state["t"] += 1
         tokens = st.all_tokens(local_tokens)
-        st.exchange(grad)
+        for k in range(K if K > 1 else 0):
+            dpg.dpg_accumulate(plan, grad, acc, first=(k == 0), stream=stream)
+        st.exchange(acc if K > 1 else grad)
         if ev is not None:
             dpg.dpg_time_next_fused_launch(*ev)
         st.update(tokens, dpg.HParams(step=state["t"]), master, m, v, bucket_sqnorm=sq,
@@ -827,7 +835,7 @@ def run_sharded(a):
     ms, k_all = timed_cycles(step, a.steps, a.warmup, world, dev, stream)
     k_all = [max_over_ranks(x, world, dev) for x in k_all]
     peak, peak_kind = load_peak()
-    bpp = 2 * world + 26
+    bpp = (4 if K > 1 else 2) * world + 26
     line = {"metric": "params/s of the fused bucket reduce-scatter + Adam + all-gather step "
                       "(achieved HBM GB/s vs GB300 peak in roofline)",
             "value": cfg.psi / (ms * 1e-3), "unit": "params/s", "n_gpus": world,
@@ -835,8 +843,11 @@ def run_sharded(a):
             "scaling": "strong", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
             "config": {**workload_desc(cfg, cap, plan.n_buckets, N),
                        "sharded": "ZeRO-2 split: rank r owns shard r of every bucket; NCCL "
-                                  "point-to-point exchange of bf16 gradient slices, the fused "
-                                  "update of the rank's shard, NCCL all-gather of bf16 shards",
+                                  "point-to-point exchange of " +
+                                  ("fp32 slices of the rank's K-microbatch accumulator"
+                                   if K > 1 else "bf16 gradient slices") +
+                                  ", the fused update of the rank's shard, NCCL all-gather of "
+                                  "bf16 shards",
                        "shard_elements_per_rank": S},
             "roofline": fused_roofline(f"k_rs_adam_chunk<R={world}> on the rank's shard", bpp,
                                        S, k_all, peak, peak_kind, None)}

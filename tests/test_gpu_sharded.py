@@ -75,3 +75,46 @@ def test_shard_update_equals_single_device_step(R):
     total = np.sum(shard_sq, axis=0)
     ref = np_f32(sq).astype(np.float64)
     assert np.all(np.abs(total - ref) <= 1e-5 * ref)
+
+
+@pytest.mark.parametrize("R,K", [(2, 3), (4, 4)])
+def test_shard_update_of_accumulated_microbatches(R, K):
+    # each rank adds its K microbatches into an fp32 buffer (dpg_accumulate),
+    # the exchange carries fp32 slices: the single-device accumulation path's
+    # bits (K - 1 fp32 passes, the last microbatch fused into the step)
+    numels = random_param_list(np.random.Generator(np.random.Philox(90 + R)), 30, 200_000)
+    plan = dpg.dpg_plan_buckets(numels, 1 << 19, R)
+    N, nb = plan.total_padded, plan.n_buckets
+    segs = segments(plan.param_offset, numels)
+    micro = [[flat_grads_bf16(segs, N, 1e-3, stream_seed(91, KIND_GRAD, s, k), device="cuda")
+              for k in range(K)] for s in range(R)]
+    master0 = master_f32(N, stream_seed(91, KIND_MASTER), device="cuda")
+    tok = [2000 + 17 * i for i in range(R * K)]
+    hp = dpg.HParams(step=5)
+
+    acc_k1 = [torch.empty(N, device="cuda") for _ in range(R)]      # K - 1 microbatches
+    acc_all = [torch.empty(N, device="cuda") for _ in range(R)]     # all K
+    for s in range(R):
+        for k in range(K):
+            if k < K - 1:
+                dpg.dpg_accumulate(plan, micro[s][k], acc_k1[s], first=(k == 0))
+            dpg.dpg_accumulate(plan, micro[s][k], acc_all[s], first=(k == 0))
+    w, m, v = master0.clone(), torch.zeros(N, device="cuda"), torch.zeros(N, device="cuda")
+    p = torch.empty(N, dtype=torch.bfloat16, device="cuda")
+    dpg.dpg_step(plan, acc_k1, tok, hp, w, m, v, [p], last_micro=[micro[s][K - 1] for s in range(R)])
+    torch.cuda.synchronize()
+
+    for r in range(R):
+        st = ShardedStep(plan, r, R, "cuda", grad_dtype=torch.float32)
+        S = st.shard.total_padded
+        ms = st.state_from_global(master0)
+        mm, vv = torch.zeros(S, device="cuda"), torch.zeros(S, device="cuda")
+        loopback_receive(st, acc_all)
+        st.update(tok, hp, ms, mm, vv)
+        torch.cuda.synchronize()
+        for b in range(nb):
+            lo, hi = st.global_slice(b, r)
+            a, z = st.shard_slice(b)
+            for name, mine, ref in (("master", ms, w), ("m", mm, m), ("v", vv, v)):
+                assert torch.equal(mine[a:z].view(torch.int32), ref[lo:hi].view(torch.int32)), (name, r, b)
+            assert torch.equal(st.param_shard[a:z].view(torch.int16), p[lo:hi].view(torch.int16))

@@ -16,7 +16,9 @@ checks it against the single-device step on the GPU).  Checked on every rank:
   R replicas at the shard's positions, bit for bit;
 * the all-gathered bf16 parameters equal the concatenated owned shards and
   the single-process oracle's parameters, bit for bit;
-* exchanging and updating in two bucket ranges gives the same bits.
+* exchanging and updating in two bucket ranges gives the same bits;
+* with K = 3 microbatches accumulated on each rank and fp32 slices exchanged,
+  the same holds against the oracle's accumulation path.
 """
 import os
 import socket
@@ -40,6 +42,12 @@ def _u16(t):
     return t.view(torch.int16).numpy().view(np.uint16)
 
 
+def _host(t):
+    """numpy view of a CPU tensor: uint16 bit patterns for bf16, else float32."""
+    import torch
+    return _u16(t) if t.dtype == torch.bfloat16 else t.numpy()
+
+
 def _oracle_update(shard_plan, recv, tokens, hp, master, m, v, views, *, bucket_sqnorm=None,
                    bucket_nonfinite=None, b0=0, b1=None, stream=None):
     """The shard update on the CPU: the oracle's step over the shard plan's
@@ -50,7 +58,7 @@ def _oracle_update(shard_plan, recv, tokens, hp, master, m, v, views, *, bucket_
     b1 = shard_plan.n_buckets if b1 is None else b1
     bo = shard_plan.bucket_offset[b0:b1]
     bp = shard_plan.bucket_padded[b0:b1]
-    out, _, sq = oracle.step(bo, bp, [_u16(x) for x in recv], tokens, master.numpy(), m.numpy(),
+    out, _, sq = oracle.step(bo, bp, [_host(x) for x in recv], tokens, master.numpy(), m.numpy(),
                              v.numpy(), lr=hp.lr, beta1=hp.beta1, beta2=hp.beta2, eps=hp.eps,
                              wd=hp.weight_decay, t=hp.step)
     p = _u16(views[0])
@@ -66,7 +74,7 @@ def _case(world):
     return numels, 1 << 16
 
 
-def _worker(rank, world, port, split):
+def _worker(rank, world, port, split, K):
     sys.path.insert(0, ROOT)
     import torch
     import torch.distributed as dist
@@ -83,18 +91,32 @@ def _worker(rank, world, port, split):
     N, nb = plan.total_padded, plan.n_buckets
     assert nb >= 4
     segs = segments(plan.param_offset, numels)
-    grads = [flat_grads_bf16(segs, N, 1e-3, stream_seed(61, KIND_GRAD, s)) for s in range(world)]
+    micro = [[flat_grads_bf16(segs, N, 1e-3, stream_seed(61, KIND_GRAD, s, k)) for k in range(K)]
+             for s in range(world)]
     master0 = master_f32(N, stream_seed(61, KIND_MASTER))
-    tokens_all = np.array([3001 + 97 * s for s in range(world)], np.int64)
+    tokens_all = np.array([3001 + 97 * s + 13 * k for s in range(world) for k in range(K)],
+                          np.int64)
     hp = dpg.HParams(step=3)
+    if K == 1:
+        grads = [mr[0] for mr in micro]
+    else:
+        # each rank adds all K microbatches into its fp32 buffer, then the
+        # exchange carries fp32 slices
+        grads = []
+        for s in range(world):
+            acc = np.empty(N, np.float32)
+            for k in range(K):
+                oracle.accumulate(_u16(micro[s][k]), acc, first=(k == 0))
+            grads.append(torch.from_numpy(acc))
 
-    st = ShardedStep(plan, rank, world, "cpu", update_fn=_oracle_update)
+    st = ShardedStep(plan, rank, world, "cpu", update_fn=_oracle_update,
+                     grad_dtype=torch.bfloat16 if K == 1 else torch.float32)
     S = st.shard.total_padded
     master = st.state_from_global(master0)
     m, v = torch.zeros(S), torch.zeros(S)
     param = torch.full((N,), float("nan"), dtype=torch.bfloat16)
 
-    tokens = st.all_tokens([tokens_all[rank]])
+    tokens = st.all_tokens(tokens_all[rank * K:(rank + 1) * K])
     np.testing.assert_array_equal(tokens, tokens_all)
     cuts = [(0, nb)] if not split else [(0, nb // 2), (nb // 2, nb)]
     for b0, b1 in cuts:
@@ -104,20 +126,31 @@ def _worker(rank, world, port, split):
 
     # the exchange delivered exactly rank s's slice of this rank's shard
     for s in range(world):
-        got = _u16(st.recv[s])
+        got = _host(st.recv[s]).view(np.uint16 if K == 1 else np.uint32)
+        sent = _host(grads[s]).view(got.dtype)
         filled = np.zeros(S, bool)
         for b in range(nb):
             lo, hi = st.global_slice(b, rank)
             a, z = st.shard_slice(b)
             assert z - a == plan.shard_numel[b]
-            np.testing.assert_array_equal(got[a:z], _u16(grads[s])[lo:hi])
+            np.testing.assert_array_equal(got[a:z], sent[lo:hi])
             filled[a:z] = True
         assert not got[~filled].any(), "padding of a receive buffer is not zero"
 
-    # the single-process oracle over all R replicas
+    # the single-process oracle over all R replicas: for K > 1 the
+    # accumulation path (K - 1 microbatches in fp32, the last one fused)
     w, mm, vv = master0.numpy().copy(), np.zeros(N, np.float32), np.zeros(N, np.float32)
-    views, _, _ = oracle.step(plan.bucket_offset, plan.bucket_padded, [_u16(g) for g in grads],
-                              tokens_all, w, mm, vv, t=3)
+    if K == 1:
+        ref_grads, last = [_u16(g) for g in grads], None
+    else:
+        ref_grads, last = [], [_u16(micro[s][K - 1]) for s in range(world)]
+        for s in range(world):
+            acc = np.empty(N, np.float32)
+            for k in range(K - 1):
+                oracle.accumulate(_u16(micro[s][k]), acc, first=(k == 0))
+            ref_grads.append(acc)
+    views, _, _ = oracle.step(plan.bucket_offset, plan.bucket_padded, ref_grads, tokens_all, w, mm,
+                              vv, last=last, t=3)
     for b in range(nb):
         lo, hi = st.global_slice(b, rank)
         a, z = st.shard_slice(b)
@@ -142,7 +175,18 @@ def test_sharded_exchange_matches_single_process_oracle(world, split):
     oracle.build()
     from zero_optimizer_step_gb300 import build
     build.build()
-    mp.spawn(_worker, args=(world, _free_port(), split), nprocs=world, join=True)
+    mp.spawn(_worker, args=(world, _free_port(), split, 1), nprocs=world, join=True)
+
+
+@pytest.mark.parametrize("world", [2, 4])
+def test_sharded_exchange_of_accumulated_microbatches(world):
+    # K = 3 microbatches accumulated in fp32 on each rank, fp32 slices
+    # exchanged: the single-process accumulation path's bits
+    import oracle
+    oracle.build()
+    from zero_optimizer_step_gb300 import build
+    build.build()
+    mp.spawn(_worker, args=(world, _free_port(), True, 3), nprocs=world, join=True)
 
 
 def test_sharded_step_rejects_a_plan_for_another_world_size():
@@ -154,3 +198,17 @@ def test_sharded_step_rejects_a_plan_for_another_world_size():
         ShardedStep(plan, 0, 2, "cpu")
     with pytest.raises(ValueError):
         ShardedStep(plan, 4, 4, "cpu")
+
+
+def test_sharded_step_checks_the_exchange_dtype():
+    sys.path.insert(0, ROOT)
+    import torch
+
+    import zero_optimizer_step_gb300 as dpg
+    from zero_optimizer_step_gb300.sharded import ShardedStep
+    plan = dpg.dpg_plan_buckets([1000, 2000], 1 << 12, 2)
+    with pytest.raises(ValueError):
+        ShardedStep(plan, 0, 2, "cpu", grad_dtype=torch.float16)
+    st = ShardedStep(plan, 0, 2, "cpu", grad_dtype=torch.float32)
+    with pytest.raises(ValueError):
+        st.exchange(torch.zeros(plan.total_padded, dtype=torch.bfloat16))

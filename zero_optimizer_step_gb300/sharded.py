@@ -25,6 +25,14 @@ G, the global valid-token count, needs every rank's counts: they are
 all-gathered first.  Steps 1-3 run per bucket range, so a caller can start a
 bucket's exchange as soon as the backward has produced it.
 
+With K microbatches per step ("Distributed Training and Parallelism" -- Data
+parallelism and the global gradient: accumulate locally, reduce once), each
+rank first adds all K microbatches into its fp32 buffer (dpg_accumulate, the
+first with first=True) and the exchange carries fp32 slices
+(grad_dtype=torch.float32).  The owner's rank-ordered sum of those slices is
+the single-device accumulation path's: there too each replica's accumulator
+and its last microbatch are added in binary32 before the rank-ordered sum.
+
 Every collective here is a torch.distributed call on the caller's process
 group (NCCL for CUDA tensors, gloo for CPU tensors); no kernel of the library
 ever reads another GPU's memory.  The local update is the library's CUDA
@@ -44,16 +52,20 @@ class ShardedStep:
     """Buffers and collectives of one rank's part of the ZeRO-2 split.
 
     plan: the global bucket plan (R = world size).  The rank's own buffers:
-      recv[s]      bf16, shard-plan layout: slices of this rank's shard
-                   received from rank s (padding zero);
+      recv[s]      bf16 (fp32 with grad_dtype=torch.float32), shard-plan
+                   layout: slices of this rank's shard received from rank s
+                   (padding zero);
       param_shard  bf16, shard-plan layout: this rank's updated parameters.
     The fp32 master/m/v shards (shard-plan layout, shard.total_padded
     elements each) belong to the caller.
     """
 
     def __init__(self, plan: Plan, rank: int, world: int, device, group=None,
-                 update_fn: Optional[Callable] = None):
+                 update_fn: Optional[Callable] = None, grad_dtype=None):
         import torch
+        grad_dtype = torch.bfloat16 if grad_dtype is None else grad_dtype
+        if grad_dtype not in (torch.bfloat16, torch.float32):
+            raise ValueError(f"gradients are exchanged as bf16 or fp32, not {grad_dtype}")
         if plan.R != world:
             raise ValueError(f"the plan's R ({plan.R}) must equal the world size ({world})")
         if not 0 <= rank < world:
@@ -65,7 +77,7 @@ class ShardedStep:
         self.n = [int(x) for x in plan.shard_numel]
         self.soff = [int(x) for x in self.shard.bucket_offset]
         S = self.shard.total_padded
-        self.recv = [torch.zeros(S, dtype=torch.bfloat16, device=device) for _ in range(world)]
+        self.recv = [torch.zeros(S, dtype=grad_dtype, device=device) for _ in range(world)]
         self.param_shard = torch.zeros(S, dtype=torch.bfloat16, device=device)
         self.update_fn = update_fn or dpg_reduce_scatter_adam
 
@@ -108,6 +120,9 @@ class ShardedStep:
         """Step 1 for buckets [b0, b1): slice q of this rank's bucket gradient
         to rank q; slice `rank` of every rank's into recv[src]."""
         import torch.distributed as dist
+        if grad_flat.dtype != self.recv[0].dtype:
+            raise ValueError(f"gradient buffer is {grad_flat.dtype}, the exchange carries "
+                             f"{self.recv[0].dtype}")
         b1 = self.plan.n_buckets if b1 is None else b1
         ops = []
         for b in range(b0, b1):
