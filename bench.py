@@ -842,6 +842,9 @@ def run_sharded(a):
             "steps": a.steps, "warmup": a.warmup, "ms_per_step": ms, "higher_is_better": True,
             "scaling": "strong", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
             "config": {**workload_desc(cfg, cap, plan.n_buckets, N),
+                       **({"accumulation": "every microbatch added into the rank's fp32 "
+                                           "buffer, then its fp32 slices exchanged"}
+                          if K > 1 else {}),
                        "sharded": "ZeRO-2 split: rank r owns shard r of every bucket; NCCL "
                                   "point-to-point exchange of " +
                                   ("fp32 slices of the rank's K-microbatch accumulator"
