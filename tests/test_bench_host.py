@@ -152,3 +152,36 @@ def test_reference_line_states_what_it_timed():
     assert 32768 / (line["sample_ms_per_step"] * 1e-3) == pytest.approx(line["value"], rel=1e-9)
     assert line["cpu_baseline"]["value"] == line["value"]
     assert line["e2e"]["h2d_bytes_per_step"] == 0
+
+
+def test_fused_roofline_arithmetic():
+    # achieved = algorithmic bytes per launch / mean launch time; frac = achieved / peak
+    k = [7.0, 7.1, 7.2, 7.3, 7.4]
+    r = bench.fused_roofline("k", 42, 1_000_000_000, k, 6761.6, "measured", None)
+    mean_ms = sum(k) / len(k)
+    assert r["algorithmic_bytes_per_launch"] == 42_000_000_000
+    assert r["achieved"] == pytest.approx(42e9 / (mean_ms * 1e-3) / 1e9)
+    assert r["frac"] == pytest.approx(r["achieved"] / 6761.6)
+    assert r["kernel_ms_p10_p50_p90"] == [7.0, 7.2, 7.4]
+    assert r["bound"] == "hbm" and r["unit"] == "GB/s"
+
+
+def test_secondary_workload_bytes():
+    # the 4.5B line: fused step 6R+26, cycle (10K-8)R+26, deferred 2KR+26
+    c = CONFIGS["llama8b16l"]
+    assert (c.R, c.K, c.cap_bytes) == (4, 4, 100 << 20)
+    assert bench.algorithmic_bytes_per_param(c) == {"fused": 50, "step": 154}
+    assert bench.algorithmic_bytes_per_param(c, deferred=True)["step"] == 58
+    assert bench.traffic_key(c) == "k_rs_adam_chunk R=4 K=4 acc_fp32_last_bf16"
+    assert bench.traffic_key(c, deferred=True) == "k_rs_adam_chunk R=4 K=4 deferred"
+    assert bench.traffic_key(CONFIGS["llama1b"]) == "k_rs_adam_chunk R=8 K=1 bf16"
+
+
+def test_hockney_fit_recovers_alpha_and_beta():
+    # K launches moving M bytes: T = K*alpha + M/B; exact data gives exact parameters
+    alpha, bw = 4.5e-6, 7.1e12
+    pts = [{"n_buckets": k, "bytes": m, "per_bucket_ms": (k * alpha + m / bw) * 1e3}
+           for k, m in ((147, 5.06e10), (83, 5.06e10), (24, 5.06e10), (2595, 2.0e8))]
+    fit = bench.hockney_fit(pts)
+    assert fit["alpha_us"] == pytest.approx(4.5, rel=1e-9)
+    assert fit["inv_beta_gbs"] == pytest.approx(7100.0, rel=1e-9)
