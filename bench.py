@@ -79,6 +79,9 @@ def parse():
                     help="ZeRO-2 split across the torchrun ranks (R = number of GPUs): each "
                          "rank exchanges gradient slices (NCCL point-to-point), updates its "
                          "shard with the library's fused pass and all-gathers the bf16 shards")
+    ap.add_argument("--sharded-groups", type=int, default=1,
+                    help="--sharded: pipeline the step over this many bucket ranges (the "
+                         "exchange of one range in flight while the previous one is updated)")
     ap.add_argument("--no-secondary", action="store_true",
                     help="default line only: skip the Hockney record and the 4.5B workload")
     ap.add_argument("--cpu-sample-elems", type=int, default=CPU_SAMPLE_ELEMS,
@@ -820,16 +823,22 @@ def run_sharded(a):
     stream = torch.cuda.current_stream()
     state = {"t": 0}
 
+    groups = max(1, a.sharded_groups)
+
     def step(ev=None):
         state["t"] += 1
-        tokens = st.all_tokens(local_tokens)
+        hp = dpg.HParams(step=state["t"])
         for k in range(K if K > 1 else 0):
             dpg.dpg_accumulate(plan, grad, acc, first=(k == 0), stream=stream)
-        st.exchange(acc if K > 1 else grad)
+        src = acc if K > 1 else grad
+        if groups > 1:
+            st.step(src, local_tokens, hp, master, m, v, param, bucket_sqnorm=sq, groups=groups)
+            return
+        tokens = st.all_tokens(local_tokens)
+        st.exchange(src)
         if ev is not None:
             dpg.dpg_time_next_fused_launch(*ev)
-        st.update(tokens, dpg.HParams(step=state["t"]), master, m, v, bucket_sqnorm=sq,
-                  stream=stream)
+        st.update(tokens, hp, master, m, v, bucket_sqnorm=sq, stream=stream)
         st.allgather(param)
 
     ms, k_all = timed_cycles(step, a.steps, a.warmup, world, dev, stream)
@@ -852,8 +861,11 @@ def run_sharded(a):
                                   ", the fused update of the rank's shard, NCCL all-gather of "
                                   "bf16 shards",
                        "shard_elements_per_rank": S},
-            "roofline": fused_roofline(f"k_rs_adam_chunk<R={world}> on the rank's shard", bpp,
-                                       S, k_all, peak, peak_kind, None)}
+            "roofline": (fused_roofline(f"k_rs_adam_chunk<R={world}> on the rank's shard", bpp,
+                                        S, k_all, peak, peak_kind, None) if groups == 1 else
+                         None)}
+    if groups > 1:
+        line["config"]["pipelined_groups"] = len(st.bucket_groups(groups))
     if rank == 0:
         print(json.dumps(line), flush=True)
     dist.barrier()

@@ -16,7 +16,8 @@ checks it against the single-device step on the GPU).  Checked on every rank:
   R replicas at the shard's positions, bit for bit;
 * the all-gathered bf16 parameters equal the concatenated owned shards and
   the single-process oracle's parameters, bit for bit;
-* exchanging and updating in two bucket ranges gives the same bits;
+* exchanging and updating in two bucket ranges, or pipelined over three
+  (ShardedStep.step with groups=3), gives the same bits;
 * with K = 3 microbatches accumulated on each rank and fp32 slices exchanged,
   the same holds against the oracle's accumulation path.
 """
@@ -116,13 +117,20 @@ def _worker(rank, world, port, split, K):
     m, v = torch.zeros(S), torch.zeros(S)
     param = torch.full((N,), float("nan"), dtype=torch.bfloat16)
 
-    tokens = st.all_tokens(tokens_all[rank * K:(rank + 1) * K])
+    local = tokens_all[rank * K:(rank + 1) * K]
+    if split == "pipelined":
+        # three bucket ranges, each range's exchange in flight while the
+        # previous one is updated
+        assert len(st.bucket_groups(3)) == 3
+        tokens = st.step(grads[rank], local, hp, master, m, v, param, groups=3)
+    else:
+        tokens = st.all_tokens(local)
+        cuts = [(0, nb)] if not split else [(0, nb // 2), (nb // 2, nb)]
+        for b0, b1 in cuts:
+            st.exchange(grads[rank], b0, b1)
+            st.update(tokens, hp, master, m, v, b0=b0, b1=b1)
+            st.allgather(param, b0, b1)
     np.testing.assert_array_equal(tokens, tokens_all)
-    cuts = [(0, nb)] if not split else [(0, nb // 2), (nb // 2, nb)]
-    for b0, b1 in cuts:
-        st.exchange(grads[rank], b0, b1)
-        st.update(tokens, hp, master, m, v, b0=b0, b1=b1)
-        st.allgather(param, b0, b1)
 
     # the exchange delivered exactly rank s's slice of this rank's shard
     for s in range(world):
@@ -169,7 +177,7 @@ def _worker(rank, world, port, split, K):
 
 
 @pytest.mark.parametrize("world", [2, 4])
-@pytest.mark.parametrize("split", [False, True])
+@pytest.mark.parametrize("split", [False, True, "pipelined"])
 def test_sharded_exchange_matches_single_process_oracle(world, split):
     import oracle
     oracle.build()
@@ -212,3 +220,19 @@ def test_sharded_step_checks_the_exchange_dtype():
     st = ShardedStep(plan, 0, 2, "cpu", grad_dtype=torch.float32)
     with pytest.raises(ValueError):
         st.exchange(torch.zeros(plan.total_padded, dtype=torch.bfloat16))
+
+
+def test_bucket_groups_cover_the_plan_in_order():
+    sys.path.insert(0, ROOT)
+    import zero_optimizer_step_gb300 as dpg
+    from workloads import CONFIGS
+    from zero_optimizer_step_gb300.sharded import ShardedStep
+    c = CONFIGS["llama1b"]
+    st = ShardedStep(dpg.dpg_plan_buckets(c.numels, c.cap_bytes, 2), 0, 2, "cpu")
+    for n in (1, 2, 4, 7, 83, 500):
+        g = st.bucket_groups(n)
+        assert g[0][0] == 0 and g[-1][1] == st.plan.n_buckets
+        assert all(a < b for a, b in g) and all(g[i][1] == g[i + 1][0] for i in range(len(g) - 1))
+        assert len(g) <= min(n, st.plan.n_buckets)
+    sizes = [int(st.plan.bucket_padded[a:b].sum()) for a, b in st.bucket_groups(4)]
+    assert max(sizes) < 2 * min(sizes)

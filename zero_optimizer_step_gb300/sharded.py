@@ -116,9 +116,23 @@ class ShardedStep:
         dist.all_gather_into_tensor(out, mine, group=self.group)
         return out.cpu().numpy()
 
-    def exchange(self, grad_flat, b0: int = 0, b1: Optional[int] = None):
+    def bucket_groups(self, n_groups: int):
+        """[b0, b1) ranges of about equal padded size, in bucket order."""
+        n_groups = max(1, min(int(n_groups), self.plan.n_buckets))
+        ends = np.cumsum(self.plan.bucket_padded)
+        total = int(ends[-1]) if len(ends) else 0
+        cuts = [0]
+        for g in range(1, n_groups):
+            b = int(np.searchsorted(ends, total * g / n_groups)) + 1
+            if cuts[-1] < b < self.plan.n_buckets:
+                cuts.append(b)
+        cuts.append(self.plan.n_buckets)
+        return list(zip(cuts[:-1], cuts[1:]))
+
+    def exchange(self, grad_flat, b0: int = 0, b1: Optional[int] = None, wait: bool = True):
         """Step 1 for buckets [b0, b1): slice q of this rank's bucket gradient
-        to rank q; slice `rank` of every rank's into recv[src]."""
+        to rank q; slice `rank` of every rank's into recv[src].  wait=False
+        returns the pending works instead of waiting for them."""
         import torch.distributed as dist
         if grad_flat.dtype != self.recv[0].dtype:
             raise ValueError(f"gradient buffer is {grad_flat.dtype}, the exchange carries "
@@ -134,9 +148,12 @@ class ShardedStep:
                     continue
                 ops.append(dist.P2POp(dist.isend, grad_flat[lo:hi], q, group=self.group))
                 ops.append(dist.P2POp(dist.irecv, self.recv[q][a:z], q, group=self.group))
-        if ops:
-            for w in dist.batch_isend_irecv(ops):
-                w.wait()
+        works = dist.batch_isend_irecv(ops) if ops else []
+        if not wait:
+            return works
+        for w in works:
+            w.wait()
+        return []
 
     def update(self, tokens, hp: HParams, master, exp_avg, exp_avg_sq, *, bucket_sqnorm=None,
                bucket_nonfinite=None, b0: int = 0, b1: Optional[int] = None, stream=None):
@@ -147,25 +164,51 @@ class ShardedStep:
                        [self.param_shard], bucket_sqnorm=bucket_sqnorm,
                        bucket_nonfinite=bucket_nonfinite, b0=b0, b1=b1, stream=stream)
 
-    def allgather(self, param_flat, b0: int = 0, b1: Optional[int] = None):
+    def allgather(self, param_flat, b0: int = 0, b1: Optional[int] = None, wait: bool = True):
         """Step 3 for buckets [b0, b1): every rank's bf16 shard of bucket b
-        into param_flat's bucket slice (shard q at slice q)."""
+        into param_flat's bucket slice (shard q at slice q).  wait=False
+        returns the pending works instead of waiting for them."""
         import torch.distributed as dist
         b1 = self.plan.n_buckets if b1 is None else b1
+        works = []
         for b in range(b0, b1):
             a, z = self.shard_slice(b)
             lo, hi = self.off[b], self.off[b] + self.world * self.n[b]
-            dist.all_gather_into_tensor(param_flat[lo:hi], self.param_shard[a:z], group=self.group)
+            w = dist.all_gather_into_tensor(param_flat[lo:hi], self.param_shard[a:z],
+                                            group=self.group, async_op=not wait)
+            if w is not None:
+                works.append(w)
+        return works
 
     def step(self, grad_flat, local_counts, hp: HParams, master, exp_avg, exp_avg_sq,
-             param_flat, *, bucket_sqnorm=None, bucket_nonfinite=None, stream=None):
+             param_flat, *, bucket_sqnorm=None, bucket_nonfinite=None, stream=None,
+             groups: int = 1):
         """The whole split step over every bucket: tokens, exchange, update,
-        all-gather."""
+        all-gather.  With groups > 1 the buckets are cut into that many ranges
+        and pipelined ("Distributed Training and Parallelism" -- Hide
+        communication): the exchange of range g + 1 is in flight while range
+        g is updated, and range g's all-gather while range g + 1 is; the
+        results are the same bits."""
         tokens = self.all_tokens(local_counts)
-        self.exchange(grad_flat)
-        self.update(tokens, hp, master, exp_avg, exp_avg_sq, bucket_sqnorm=bucket_sqnorm,
-                    bucket_nonfinite=bucket_nonfinite, stream=stream)
-        self.allgather(param_flat)
+        kw = dict(bucket_sqnorm=bucket_sqnorm, bucket_nonfinite=bucket_nonfinite, stream=stream)
+        if groups <= 1:
+            self.exchange(grad_flat)
+            self.update(tokens, hp, master, exp_avg, exp_avg_sq, **kw)
+            self.allgather(param_flat)
+            return tokens
+        cuts = self.bucket_groups(groups)
+        pending = self.exchange(grad_flat, *cuts[0], wait=False)
+        gathers = []
+        for g, (b0, b1) in enumerate(cuts):
+            nxt = (self.exchange(grad_flat, *cuts[g + 1], wait=False)
+                   if g + 1 < len(cuts) else [])
+            for w in pending:
+                w.wait()
+            self.update(tokens, hp, master, exp_avg, exp_avg_sq, b0=b0, b1=b1, **kw)
+            gathers += self.allgather(param_flat, b0, b1, wait=False)
+            pending = nxt
+        for w in gathers:
+            w.wait()
         return tokens
 
 
