@@ -5,7 +5,8 @@
  * step through dpg_reduce_scatter_adam_when_ready gated on per-bucket events
  * recorded on another stream, and one dpg_allgather_params, and compares
  * every output bit for bit with the oracle (a test-only C library) run on the
- * same inputs.
+ * same inputs.  It also checks the layout of the plan's shard plan (the split
+ * across R GPUs).
  * Exit status 0 on a match; prints the first mismatch otherwise.
  * Inputs: a fixed xorshift stream of normals (Box-Muller), plain and
  * reproducible; nothing here computes the method's arithmetic.
@@ -100,6 +101,34 @@ int main(void) {
             return 5;
         }
     }
+
+    /* the shard plan of the split across R GPUs: one bucket per bucket of
+     * the plan, holding that bucket's shard, padded to a multiple of 8R */
+    dpg_plan_t* shards = NULL;
+    CHECK_DPG(dpg_plan_shards(plan, &shards));
+    int32_t s_buckets = 0, s_r = 0;
+    int64_t s_total = 0, s_expect = 0;
+    CHECK_DPG(dpg_plan_info(shards, NULL, &s_buckets, &s_total, &s_r));
+    if (s_buckets != n_buckets || s_r != R) {
+        fprintf(stderr, "shard plan shape differs\n");
+        return 6;
+    }
+    for (int32_t b = 0; b < n_buckets; ++b) {
+        int64_t off = 0, pad = 0, soff = 0, spad = 0;
+        CHECK_DPG(dpg_plan_bucket(plan, b, &off, &pad, NULL));
+        CHECK_DPG(dpg_plan_bucket(shards, b, &soff, &spad, NULL));
+        const int64_t want = (pad / R + 8 * R - 1) / (8 * R) * (8 * R);
+        if (soff != s_expect || spad != want) {
+            fprintf(stderr, "shard bucket %d differs\n", b);
+            return 6;
+        }
+        s_expect += want;
+    }
+    if (s_total != s_expect) {
+        fprintf(stderr, "shard plan size differs\n");
+        return 6;
+    }
+    dpg_plan_destroy(shards);
 
     const size_t n = (size_t)total;
     uint16_t* hg[R];
