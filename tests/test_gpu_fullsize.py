@@ -110,3 +110,50 @@ def test_fullsize_sampled(name):
         check_norms(gsq[b:b + 1], np.array([ref]))
         pos += e - a
     assert nf.sum().item() == 0
+
+
+def test_fullsize_deferred_llama8b16l():
+    """The deferred schedule the benchmark also times on the 4.5B list: every
+    replica's K = 4 bf16 microbatches held at once (16 buffers of 4.5B
+    elements) and summed inside one dpg_step_deferred pass; sampled outputs
+    against the oracle's one-microbatch-at-a-time accumulation path."""
+    torch.cuda.empty_cache()         # the other full-size cases' cached blocks
+    cfg = CONFIGS["llama8b16l"]
+    plan = dpg.dpg_plan_buckets(cfg.numels, cfg.cap_bytes, cfg.R)
+    N, R, K = plan.total_padded, cfg.R, cfg.K
+    segs = segments(plan.param_offset, cfg.numels)
+    rng = np.random.Generator(np.random.Philox(cfg.seed + 7))
+    b = int(rng.integers(0, plan.n_buckets))
+    ranges = [(int(plan.bucket_offset[b]), int(plan.bucket_offset[b] + plan.bucket_padded[b]))]
+    idx = torch.from_numpy(np.sort(rng.integers(0, N, N_RANDOM)).astype(np.int64)).cuda()
+    sel = dict(ranges=ranges, idx=idx)
+    dev = "cuda"
+    tokens = token_counts(cfg)
+    w = master_f32(N, stream_seed(cfg.seed, KIND_MASTER), device=dev)
+    m, v = torch.zeros(N, device=dev), torch.zeros(N, device=dev)
+    param = torch.empty(N, dtype=torch.bfloat16, device=dev)
+    sq = torch.empty(plan.n_buckets, device=dev)
+    h_w0 = _gather(w, sel).numpy()
+    gd = [[flat_grads_bf16(segs, N, cfg.grad_std, stream_seed(cfg.seed, KIND_GRAD, r, k), device=dev)
+           for k in range(K)] for r in range(R)]
+    h_micro = [[np_bf16(_gather(gd[r][k], sel)) for k in range(K)] for r in range(R)]
+    dpg.dpg_step_deferred(plan, gd, tokens, dpg.HParams(step=1), w, m, v, [param], bucket_sqnorm=sq)
+    torch.cuda.synchronize()
+    got = dict(w=_gather(w, sel).numpy(), m=_gather(m, sel).numpy(), v=_gather(v, sel).numpy(),
+               p=np_bf16(_gather(param, sel)))
+    del gd
+    torch.cuda.empty_cache()
+
+    hw = h_w0.copy()
+    hm, hv = np.zeros_like(hw), np.zeros_like(hw)
+    accs = [np.empty(hw.size, np.float32) for _ in range(R)]
+    for k in range(K - 1):
+        for r in range(R):
+            oracle.accumulate(h_micro[r][k], accs[r], first=(k == 0))
+    gr = oracle.reduce(accs, oracle.grad_scale(tokens), last=[h_micro[r][K - 1] for r in range(R)])
+    oracle.adam(gr, hw, hm, hv, t=1)
+    for name, ref in (("w", hw), ("m", hm), ("v", hv)):
+        assert ulp_f32(got[name], ref) == 0, name
+    assert ulp_bf16(got["p"], oracle.f32_to_bf16(hw)) == 0
+    e = ranges[0][1] - ranges[0][0]
+    check_norms(sq.cpu().numpy()[b:b + 1], np.array([float(np.sum(gr[:e].astype(np.float64) ** 2))]))
