@@ -118,3 +118,44 @@ def test_shard_update_of_accumulated_microbatches(R, K):
             for name, mine, ref in (("master", ms, w), ("m", mm, m), ("v", vv, v)):
                 assert torch.equal(mine[a:z].view(torch.int32), ref[lo:hi].view(torch.int32)), (name, r, b)
             assert torch.equal(st.param_shard[a:z].view(torch.int16), p[lo:hi].view(torch.int16))
+
+
+@pytest.mark.parametrize("groups", [1, 3])
+def test_whole_split_step_over_nccl_single_rank(groups):
+    # the real collectives (token all-gather, exchange, all-gather of the
+    # parameter shards) over a one-rank NCCL group on this GPU, plain and
+    # pipelined: the single-device step's bits
+    import socket
+
+    import torch.distributed as dist
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        port = s.getsockname()[1]
+    dist.init_process_group("nccl", init_method=f"tcp://127.0.0.1:{port}", rank=0, world_size=1,
+                            device_id=torch.device("cuda", torch.cuda.current_device()))
+    try:
+        numels = random_param_list(np.random.Generator(np.random.Philox(95)), 30, 300_000)
+        plan = dpg.dpg_plan_buckets(numels, 1 << 19, 1)
+        N = plan.total_padded
+        segs = segments(plan.param_offset, numels)
+        g = flat_grads_bf16(segs, N, 1e-3, stream_seed(95, KIND_GRAD, 0), device="cuda")
+        master0 = master_f32(N, stream_seed(95, KIND_MASTER), device="cuda")
+        hp = dpg.HParams(step=1)
+        w, m, v = master0.clone(), torch.zeros(N, device="cuda"), torch.zeros(N, device="cuda")
+        p = torch.empty(N, dtype=torch.bfloat16, device="cuda")
+        dpg.dpg_step(plan, [g], [3333], hp, w, m, v, [p])
+        st = ShardedStep(plan, 0, 1, "cuda")
+        S = st.shard.total_padded
+        ms = st.state_from_global(master0)
+        mm, vv = torch.zeros(S, device="cuda"), torch.zeros(S, device="cuda")
+        param = torch.full((N,), float("nan"), dtype=torch.bfloat16, device="cuda")
+        tokens = st.step(g, [3333], hp, ms, mm, vv, param, groups=groups)
+        torch.cuda.synchronize()
+        assert list(tokens) == [3333]
+        assert torch.equal(param.view(torch.int16), p.view(torch.int16))
+        for b in range(plan.n_buckets):
+            lo, hi = st.global_slice(b, 0)
+            a, z = st.shard_slice(b)
+            assert torch.equal(ms[a:z].view(torch.int32), w[lo:hi].view(torch.int32))
+    finally:
+        dist.destroy_process_group()
