@@ -185,3 +185,16 @@ def test_hockney_fit_recovers_alpha_and_beta():
     fit = bench.hockney_fit(pts)
     assert fit["alpha_us"] == pytest.approx(4.5, rel=1e-9)
     assert fit["inv_beta_gbs"] == pytest.approx(7100.0, rel=1e-9)
+
+
+def test_resident_bytes_decide_the_l2_flush():
+    # only the 10,000-tensor list is small enough to be flushed between steps
+    c = CONFIGS["llama1b"]
+    assert bench.resident_bytes(c, c.psi) == (2 * 8 + 12 + 2) * c.psi
+    c4 = CONFIGS["llama8b16l"]
+    assert bench.resident_bytes(c4, c4.psi) == (2 * 4 + 4 * 4 + 14) * c4.psi
+    assert bench.resident_bytes(c4, c4.psi, deferred=True) == (2 * 4 * 4 + 14) * c4.psi
+    assert bench.resident_bytes(c4, c4.psi, fold2=True) == (2 * 4 * 2 + 4 * 4 + 14) * c4.psi
+    small = [n for n, c in CONFIGS.items() if n != "tiny"
+             and bench.resident_bytes(c, c.psi) < bench.L2_FLUSH_BELOW]
+    assert small == ["sweep"]
