@@ -527,6 +527,37 @@ def fused_roofline(kernel, bpp, psi, k_all, peak, peak_kind, traffic):
                                       for q in (0.1, 0.5, 0.9)]}
 
 
+def optional_leg(fn, world: int):
+    """Run one of the default line's extra legs; on one GPU, a device out of
+    memory records the leg as skipped instead of losing the whole line."""
+    import torch
+    try:
+        return fn()
+    except torch.cuda.OutOfMemoryError as e:
+        if world > 1:
+            raise
+        torch.cuda.empty_cache()
+        return {"skipped": "out of device memory: " + str(e).splitlines()[0][:200]}
+
+
+def all_ranks_agree(ok: bool, world: int, device) -> bool:
+    """True only if `ok` holds on every rank (the same answer on all)."""
+    if world <= 1:
+        return bool(ok)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([1 if ok else 0], dtype=torch.int32, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MIN)
+    return bool(t.item())
+
+
+def device_room(needed_bytes: int, world: int, device) -> bool:
+    """Whether every rank's GPU has needed_bytes free, with 2 GB to spare."""
+    import torch
+    free, _ = torch.cuda.mem_get_info(device)
+    return all_ranks_agree(free >= needed_bytes + (2 << 30), world, device)
+
+
 def run_secondary(a, dpg, dev, world):
     """The 4.5B accumulation workload (Llama-3-8B shapes cut to 16 layers,
     R = 4, K = 4 microbatches, 100 MiB buckets) measured in the default line:
@@ -539,8 +570,11 @@ def run_secondary(a, dpg, dev, world):
     cfg = CONFIGS["llama8b16l"]
     R, K = cfg.R, cfg.K
     plan = dpg.dpg_plan_buckets(cfg.numels, cfg.cap_bytes, R)
-    dpg.dpg_plan_upload(plan)
     N = plan.total_padded
+    torch.cuda.empty_cache()
+    if not device_room(resident_bytes(cfg, N), world, dev):
+        return {"skipped": f"needs {resident_bytes(cfg, N) / 1e9:.0f} GB free on the device"}
+    dpg.dpg_plan_upload(plan)
     segs = segments(plan.param_offset, cfg.numels)
     tokens = token_counts(cfg)
     stream = torch.cuda.current_stream()
@@ -588,6 +622,14 @@ def run_secondary(a, dpg, dev, world):
     # deferred: every replica's K microbatches held in bf16, summed in the step
     del acc
     torch.cuda.empty_cache()
+    if not device_room((K - 1) * R * N * 2, world, dev):
+        out["deferred"] = {"skipped": f"needs {(K - 1) * R * N * 2 / 1e9:.0f} GB more free on "
+                                      f"the device"}
+        out["clocks"] = clocks.stop()
+        del gd, w, m, v, param, sq, nf
+        plan.destroy()
+        torch.cuda.empty_cache()
+        return out
     for r in range(R):
         gd[r] += [grad(r, k) for k in range(1, K)]
 
@@ -760,8 +802,8 @@ def run_dpg(a):
             and a.variant == "direct" and not a.no_secondary):
         del g, gd, acc, g2, w, m, v, param, sq, nf
         torch.cuda.empty_cache()
-        extra["hockney"] = hockney_compact(dpg)
-        extra["secondary"] = run_secondary(a, dpg, dev, world)
+        extra["hockney"] = optional_leg(lambda: hockney_compact(dpg), world)
+        extra["secondary"] = optional_leg(lambda: run_secondary(a, dpg, dev, world), world)
 
     bpp = algorithmic_bytes_per_param(cfg, fold2, deferred)
     peak, peak_kind = load_peak()

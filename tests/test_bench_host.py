@@ -198,3 +198,16 @@ def test_resident_bytes_decide_the_l2_flush():
     small = [n for n, c in CONFIGS.items() if n != "tiny"
              and bench.resident_bytes(c, c.psi) < bench.L2_FLUSH_BELOW]
     assert small == ["sweep"]
+
+
+def test_optional_leg_records_out_of_memory():
+    import torch
+
+    def boom():
+        raise torch.cuda.OutOfMemoryError("CUDA out of memory. Tried to allocate 9 GiB")
+    out = bench.optional_leg(boom, 1)
+    assert out["skipped"].startswith("out of device memory: CUDA out of memory")
+    assert bench.optional_leg(lambda: {"ok": 1}, 1) == {"ok": 1}
+    with pytest.raises(torch.cuda.OutOfMemoryError):
+        bench.optional_leg(boom, 2)        # several ranks: fail together, not apart
+    assert bench.all_ranks_agree(True, 1, "cpu") and not bench.all_ranks_agree(False, 1, "cpu")
