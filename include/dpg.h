@@ -504,6 +504,27 @@ int64_t dpg_launch_count(void);
  * the request is then cleared.  NULL, NULL clears a pending request.  Lets a
  * caller time the fused kernel alone inside a whole step. */
 int dpg_time_next_fused_launch(void* start_event, void* stop_event);
+/* Index checks.  A library built with `python -m zero_optimizer_step_gb300.build
+ * --debug` (libdpg_debug.so, compiled with DPG_DEBUG) checks, in the kernels
+ * that derive indices from the plan's device tables -- the chunked fused and
+ * norm passes, the chunk finalize, pack/unpack -- every element and table
+ * index before using it.  A failed check skips its access and records the
+ * first failure in a word of the plan; it never faults or traps.
+ * dpg_debug_checks: *built = 1 for such a library, 0 otherwise;
+ * *first_failure = the first failure recorded for `plan` since the last call
+ * ((code << 32) | CTA index; codes 1 fused or norm pass, 2 finalize of a
+ * long bucket, 3 finalize of a short bucket, 4 pack/unpack; 0 = none), which
+ * it then clears.  Synchronizes the device in a checking build.  No
+ * counterpart on the pages. */
+int dpg_debug_checks(const dpg_plan_t* plan, int32_t* built, int64_t* first_failure);
+/* Test hook of a checking build: index checks of later launches from the
+ * calling thread bound element indices by `limit` instead of the plan's
+ * total (limit < 0 restores it), so that a test can make a check fail
+ * without any out-of-range access.  Honoured only by a checking build and
+ * only when DPG_TEST_HOOKS is "1" in the environment; otherwise
+ * DPG_ERR_INVALID_ARG. */
+int dpg_debug_set_limit(int64_t limit);
+
 /* Test-only fault injection for the staged step: its next launch by the
  * calling thread never fetches unit `skip_unit` (-1: none), so the CTA
  * that owns it must run out its wait, and every wait is bounded by

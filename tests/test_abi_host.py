@@ -349,3 +349,14 @@ def test_shard_plan_validation():
     assert z.n_buckets == 1 and z.total_padded == 0
     zs = dpg.dpg_plan_shards(z)
     assert zs.n_buckets == 1 and zs.total_padded == 0
+
+
+def test_release_library_has_no_index_checks(monkeypatch):
+    plan = dpg.dpg_plan_buckets([1000], 4096, 2)
+    assert dpg.dpg_debug_checks(plan) == (False, 0)
+    monkeypatch.setenv("DPG_TEST_HOOKS", "1")
+    with pytest.raises(dpg.DpgError) as e:
+        dpg.dpg_debug_set_limit(8)
+    assert e.value.status == dpg.DPG_ERR_INVALID_ARG and "--debug" in str(e.value)
+    L = dpg.lib()
+    assert L.dpg_debug_checks(None, None, None) == dpg.DPG_ERR_INVALID_ARG

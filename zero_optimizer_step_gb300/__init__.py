@@ -17,7 +17,9 @@ from typing import Optional, Sequence, Union
 import numpy as np
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_PKG, "libdpg.so")
+# DPG_LIBRARY=debug loads the index-checking build (libdpg_debug.so) instead
+LIB_PATH = os.path.join(_PKG, "libdpg_debug.so" if os.environ.get("DPG_LIBRARY") == "debug"
+                        else "libdpg.so")
 
 DPG_OK = 0
 DPG_ERR_INVALID_ARG = -1
@@ -42,7 +44,7 @@ EXPORTED = (
     "dpg_allreduce_grads", "dpg_adam_from_reduced", "dpg_gather_params_bf16",
     "dpg_accumulate_pair", "dpg_step_fold2", "dpg_set_fused_max_ctas",
     "dpg_set_programmatic_launch", "dpg_reduce_scatter_adam_when_ready", "dpg_step_deferred",
-    "dpg_plan_shards",
+    "dpg_plan_shards", "dpg_debug_checks", "dpg_debug_set_limit",
 )
 DPG_MAX_STATE_ARRAYS = 8
 DPG_NOALLOC_SCRATCH_BYTES = 8 << 20
@@ -88,7 +90,8 @@ def lib() -> ctypes.CDLL:
     if _lib is None:
         if not os.path.exists(LIB_PATH):
             raise DpgLibraryMissing(
-                f"{LIB_PATH} is missing: build it with `python -m zero_optimizer_step_gb300.build`")
+                f"{LIB_PATH} is missing: build it with `python -m zero_optimizer_step_gb300.build`"
+                + (" --debug" if LIB_PATH.endswith("_debug.so") else ""))
         L = ctypes.CDLL(LIB_PATH)
         P, i32, i64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64
         c_int = ctypes.c_int
@@ -132,6 +135,8 @@ def lib() -> ctypes.CDLL:
         L.dpg_import_state.argtypes = [P, P, P, i32, P]
         L.dpg_time_next_fused_launch.argtypes = [P, P]
         L.dpg_plan_shards.argtypes = [P, ctypes.POINTER(P)]
+        L.dpg_debug_checks.argtypes = [P, P, P]
+        L.dpg_debug_set_limit.argtypes = [i64]
         L.dpg_time_next_fused_launch.restype = c_int
         for name in ("dpg_plan_buckets", "dpg_plan_info", "dpg_plan_bucket", "dpg_plan_param",
                      "dpg_plan_export", "dpg_plan_upload", "dpg_pack", "dpg_unpack",
@@ -142,7 +147,7 @@ def lib() -> ctypes.CDLL:
                      "dpg_gather_params_bf16", "dpg_accumulate_pair", "dpg_step_fold2",
                      "dpg_set_fused_max_ctas", "dpg_set_programmatic_launch",
                      "dpg_reduce_scatter_adam_when_ready", "dpg_step_deferred",
-                     "dpg_plan_shards"):
+                     "dpg_plan_shards", "dpg_debug_checks", "dpg_debug_set_limit"):
             getattr(L, name).restype = c_int
         _lib = L
     return _lib
@@ -699,6 +704,18 @@ def dpg_set_programmatic_launch(on: bool = True):
     (default on): same stream order and results, shorter gaps between
     back-to-back kernels."""
     _check(lib().dpg_set_programmatic_launch(1 if on else 0))
+
+
+def dpg_debug_checks(plan: Plan):
+    """(built, first_failure): whether the loaded library checks indices, and
+    the first failed check recorded for `plan` since the last call (0: none)."""
+    built, first = ctypes.c_int32(), ctypes.c_int64()
+    _check(lib().dpg_debug_checks(plan.handle, ctypes.byref(built), ctypes.byref(first)))
+    return bool(built.value), int(first.value)
+
+
+def dpg_debug_set_limit(limit: int = -1):
+    _check(lib().dpg_debug_set_limit(int(limit)))
 
 
 def dpg_launch_count() -> int:

@@ -1,10 +1,13 @@
 """Build libdpg.so (the sm_103a CUDA library behind include/dpg.h) in-tree.
 
-    python -m zero_optimizer_step_gb300.build [--force] [--verbose]
+    python -m zero_optimizer_step_gb300.build [--force] [--verbose] [--debug]
 
 Each translation unit is compiled in parallel with nvcc for sm_103a only, then
 linked with the static CUDA runtime into zero_optimizer_step_gb300/libdpg.so.
-Objects go to zero_optimizer_step_gb300/_build/ (git-ignored).
+Objects go to zero_optimizer_step_gb300/_build/ (git-ignored).  --debug
+builds libdpg_debug.so instead, with the kernels' index checks compiled in
+(-DDPG_DEBUG; objects in _build_debug/); DPG_LIBRARY=debug makes the Python
+binding load it.
 """
 from __future__ import annotations
 
@@ -22,6 +25,9 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libdpg.so")
+# the index-checking build (-DDPG_DEBUG): its own objects and library
+BUILD_DEBUG = os.path.join(PKG, "_build_debug")
+LIB_DEBUG = os.path.join(PKG, "libdpg_debug.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
@@ -44,16 +50,16 @@ def _inputs():
             + [os.path.join(INCLUDE, "dpg.h"), os.path.abspath(__file__)])
 
 
-def up_to_date() -> bool:
-    if not os.path.exists(LIB):
+def up_to_date(lib: str = LIB) -> bool:
+    if not os.path.exists(lib):
         return False
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(lib)
     return all(os.path.getmtime(f) <= t for f in _inputs())
 
 
-def _compile(src: str, verbose: bool) -> str:
-    obj = os.path.join(BUILD, os.path.basename(src) + ".o")
-    cmd = [nvcc(), *ARCH, *NVCC_FLAGS, "-c", src, "-o", obj]
+def _compile(src: str, verbose: bool, debug: bool = False) -> str:
+    obj = os.path.join(BUILD_DEBUG if debug else BUILD, os.path.basename(src) + ".o")
+    cmd = [nvcc(), *ARCH, *NVCC_FLAGS, *(["-DDPG_DEBUG"] if debug else []), "-c", src, "-o", obj]
     if verbose and src.endswith(".cu"):
         cmd += ["-Xptxas", "-v"]
     r = subprocess.run(cmd, capture_output=True, text=True)
@@ -64,24 +70,28 @@ def _compile(src: str, verbose: bool) -> str:
     return obj
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
-    if not force and up_to_date():
-        return LIB
-    os.makedirs(BUILD, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, debug: bool = False) -> str:
+    """Build libdpg.so, or with debug=True the index-checking libdpg_debug.so."""
+    lib = LIB_DEBUG if debug else LIB
+    if not force and up_to_date(lib):
+        return lib
+    os.makedirs(BUILD_DEBUG if debug else BUILD, exist_ok=True)
     with cf.ThreadPoolExecutor(max_workers=len(sources())) as ex:
-        objs = list(ex.map(lambda s: _compile(s, verbose), sources()))
-    tmp = LIB + f".tmp{os.getpid()}"
+        objs = list(ex.map(lambda s: _compile(s, verbose, debug), sources()))
+    tmp = lib + f".tmp{os.getpid()}"
     r = subprocess.run([nvcc(), *ARCH, "-shared", "-cudart", "static", "-o", tmp, *objs],
                        capture_output=True, text=True)
     if r.returncode != 0:
-        raise RuntimeError(f"link of libdpg.so failed:\n{r.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+        raise RuntimeError(f"link of {os.path.basename(lib)} failed:\n{r.stderr}")
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":
     ap = argparse.ArgumentParser()
     ap.add_argument("--force", action="store_true")
     ap.add_argument("--verbose", action="store_true")
+    ap.add_argument("--debug", action="store_true",
+                    help="the index-checking build (libdpg_debug.so, -DDPG_DEBUG)")
     a = ap.parse_args()
-    print(build(force=a.force, verbose=a.verbose))
+    print(build(force=a.force, verbose=a.verbose, debug=a.debug))

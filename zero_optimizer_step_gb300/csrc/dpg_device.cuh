@@ -139,6 +139,10 @@ struct RsAdamArgs {
     const longlong2* tile_span;
     double* chunk_sq;
     int32_t* chunk_nf;
+#ifdef DPG_DEBUG
+    unsigned long long* dbg;  // the plan's debug word (NULL: checks record nothing)
+    int64_t dbg_limit;        // elements an index must stay below (the plan's total)
+#endif
 };
 
 // Bucket holding tile t, searching forward from bucket b (tile_begin[b] <= t
@@ -311,6 +315,21 @@ __device__ __forceinline__ void pdl_enter() {
     asm volatile("griddepcontrol.wait;" ::: "memory");
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
+
+#ifdef DPG_DEBUG
+// Index checks of a checking build (-DDPG_DEBUG): a table-driven kernel checks
+// the element and table indices it derives from the plan's device tables
+// before using them.  A failed check records (code << 32 | CTA index) as the
+// first failure in the plan's debug word and the access is skipped; nothing
+// traps, and control flow (barriers) is unchanged.  Codes: 1 chunked fused or
+// norm pass, 2 chunk finalize (long buckets), 3 chunk finalize (short
+// buckets), 4 pack / unpack.
+__device__ __forceinline__ bool debug_ok(unsigned long long* word, bool ok, unsigned code) {
+    if (!ok && word != nullptr)
+        atomicCAS(word, 0ull, (static_cast<unsigned long long>(code) << 32) | blockIdx.x);
+    return ok;
+}
+#endif
 
 // Chunked launches: one 128-thread CTA per 1024-element chunk (a quarter of a
 // bucket-aligned tile), one 8-element vector per thread.

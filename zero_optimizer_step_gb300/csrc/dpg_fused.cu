@@ -403,7 +403,13 @@ __global__ void __launch_bounds__(kChunkThreads) k_rs_adam_chunk(const __grid_co
     const int64_t i = span.x + (c % kChunksPerTile) * kChunk + int64_t(threadIdx.x) * kVec;
     float sq = 0.0f;
     int nf = 0;
-    if (i < span.y) {
+#ifdef DPG_DEBUG
+    const bool in_range = debug_ok(a.dbg, span.x >= 0 && span.x <= span.y && span.y <= a.dbg_limit &&
+                                              (i >= span.y || i + kVec <= span.y), 1);
+#else
+    constexpr bool in_range = true;
+#endif
+    if (i < span.y && in_range) {
         float coef = 1.0f;
         if constexpr (PHASE == kUpdate) coef = __ldg(a.clip_coef);
         float s[8];
@@ -478,7 +484,13 @@ __global__ void __launch_bounds__(NT) k_norm_chunk(const __grid_constant__ RsAda
     const bool norm = a.chunk_sq != nullptr;
     NormAcc acc;
     int nf = 0;
-    if (i < span.y) {
+#ifdef DPG_DEBUG
+    const bool in_range = debug_ok(a.dbg, span.x >= 0 && span.x <= span.y && span.y <= a.dbg_limit &&
+                                              (i >= span.y || i + kVec <= span.y), 1);
+#else
+    constexpr bool in_range = true;
+#endif
+    if (i < span.y && in_range) {
         float s[8];
         reduce_vector<RT, MODE>(a, i, s);
         norm_vector(a, i, s, acc, nf, norm);
@@ -551,6 +563,11 @@ struct FinalizeArgs {
     int32_t l0, l1;             // the launch's slice of long_list
     int32_t q0, q1;             // the launch's slice of short_list
     int32_t short_per_cta;      // short buckets (warps) per CTA, <= 32
+#ifdef DPG_DEBUG
+    unsigned long long* dbg;    // the plan's debug word
+    int64_t dbg_chunks;         // chunk partials of the launch
+    int32_t dbg_buckets, dbg_segs;
+#endif
     float* sqnorm;              // outputs, indexed by bucket (nullable)
     int64_t* nonfinite;
     double* sqnorm64;
@@ -568,8 +585,16 @@ __device__ __forceinline__ void finalize_short_bucket(const FinalizeArgs& f, int
     const int lane = threadIdx.x & 31;
     if (q >= f.q1) return;
     const int b = __ldg(f.short_list + q);
+#ifdef DPG_DEBUG
+    if (!debug_ok(f.dbg, b >= 0 && b < f.dbg_buckets, 3)) return;   // warp-uniform
+#endif
     const int64_t cb = (__ldg(f.tile_begin + b) - f.t0) * f.cpt;
-    const int n = int((__ldg(f.tile_begin + b + 1) - f.t0) * f.cpt - cb);
+    int n = int((__ldg(f.tile_begin + b + 1) - f.t0) * f.cpt - cb);
+#ifdef DPG_DEBUG
+    // a failed check: no partial is loaded and the bucket's outputs are not written
+    const bool bad = !debug_ok(f.dbg, cb >= 0 && n >= 0 && n <= 1024 && cb + n <= f.dbg_chunks, 3);
+    if (bad) n = 0;
+#endif
     const int rows = (n + 31) >> 5;       // warp results with any chunk (<= 32)
     double keep = 0.0;
     long long keep_n = 0;
@@ -610,6 +635,9 @@ __device__ __forceinline__ void finalize_short_bucket(const FinalizeArgs& f, int
         }
     }
     if (lane != 0) return;
+#ifdef DPG_DEBUG
+    if (bad) return;
+#endif
     // the CTA path's last step adds the bucket's one segment sum to 0.0
     double tot = 0.0;
     tot += keep;
@@ -634,13 +662,28 @@ k_chunk_finalize(const __grid_constant__ FinalizeArgs f) {
             finalize_short_bucket(f, f.q0 + (int32_t(blockIdx.x) - n_long) * f.short_per_cta + warp);
         return;
     }
-    const int32_t s = __ldg(f.long_list + f.l0 + int32_t(blockIdx.x));
-    const int b = __ldg(f.seg_bucket + s);
+    int32_t s = __ldg(f.long_list + f.l0 + int32_t(blockIdx.x));
+#ifdef DPG_DEBUG
+    // a failed check: the table reads stay at index 0, the CTA loads no
+    // partial and writes nothing (it still meets the CTA barrier)
+    bool bad = !debug_ok(f.dbg, s >= 0 && s < f.dbg_segs, 2);
+    if (bad) s = 0;
+#endif
+    int b = __ldg(f.seg_bucket + s);
+#ifdef DPG_DEBUG
+    if (!bad && !debug_ok(f.dbg, b >= 0 && b < f.dbg_buckets, 2)) bad = true;
+    if (bad) b = 0;
+#endif
     const int64_t span = kSegTiles * f.cpt;
     const int64_t cb = (__ldg(f.tile_begin + b) - f.t0) * f.cpt;
     const int64_t ce = (__ldg(f.tile_begin + b + 1) - f.t0) * f.cpt;
     const int64_t c0 = cb + int64_t(s - __ldg(f.seg_first + b)) * span;
+#ifdef DPG_DEBUG
+    if (!bad && !debug_ok(f.dbg, cb >= 0 && c0 >= cb && ce <= f.dbg_chunks, 2)) bad = true;
+    const int64_t c1 = bad ? c0 : (c0 + span < ce ? c0 + span : ce);
+#else
     const int64_t c1 = c0 + span < ce ? c0 + span : ce;
+#endif
     double acc = 0.0;
     long long cnt = 0;
     for (int64_t c = c0 + threadIdx.x; c < c1; c += int64_t(T) * U) {
@@ -678,6 +721,9 @@ k_chunk_finalize(const __grid_constant__ FinalizeArgs f) {
         cnt += __shfl_xor_sync(0xFFFFFFFFu, cnt, o);
     }
     if (lane != 0) return;
+#ifdef DPG_DEBUG
+    if (bad) return;
+#endif
     f.seg_sq[s] = acc;
     f.seg_nf[s] = cnt;
     __threadfence();                      // the sums before the arrival
@@ -838,6 +884,10 @@ static int launch_chunked(RsKernel fn, RsAdamArgs a, const Plan& p, bool want_no
     a.tile_span = reinterpret_cast<const longlong2*>(p.d_tile_span);
     a.chunk_sq = want_norm ? p.d_chunk_sq : nullptr;
     a.chunk_nf = want_norm ? p.d_chunk_nf : nullptr;
+#ifdef DPG_DEBUG
+    a.dbg = p.d_debug;
+    a.dbg_limit = t_debug_limit >= 0 ? t_debug_limit : p.total_padded;
+#endif
     const int64_t n_chunks = (a.t1 - a.t0) * cpt;
     if (n_chunks > 0x7FFFFFFF) return fail(DPG_ERR_INVALID_ARG, "%s: %lld chunks in one launch", who,
                                            (long long)n_chunks);
@@ -865,6 +915,12 @@ static int launch_chunked(RsKernel fn, RsAdamArgs a, const Plan& p, bool want_no
         f.sqnorm = sqnorm;
         f.nonfinite = nonfinite;
         f.sqnorm64 = sqnorm64;
+#ifdef DPG_DEBUG
+        f.dbg = p.d_debug;
+        f.dbg_chunks = n_chunks;
+        f.dbg_buckets = p.n_buckets;
+        f.dbg_segs = p.n_seg;
+#endif
         // the range's long-bucket segments (one CTA each), then its short
         // buckets (one warp each)
         f.long_list = p.d_long_seg;

@@ -33,6 +33,10 @@ extern thread_local int32_t t_fused_max_ctas;
 // 1: the streaming and chunked kernels are launched with programmatic stream
 // serialization (the default); 0: plain stream-ordered launches.
 extern thread_local int32_t t_programmatic;
+// Checking builds: the element bound the index checks of the next launches
+// from this thread use (< 0: the plan's total; a smaller bound is a test of
+// the checks themselves).
+extern thread_local int64_t t_debug_limit;
 
 int sm_count(int dev, int* out);
 // one CTA per unit of work (the streaming kernels)

@@ -112,6 +112,7 @@ struct Plan {
     double* d_bucket_sq64 = nullptr;  // n_buckets + 1
     float* d_clip_coef = nullptr;     // 1
     int32_t* d_status = nullptr;      // status word of the staged pass (0 = OK)
+    unsigned long long* d_debug = nullptr;  // first failed index check (checking builds)
 };
 
 // thread-local error message

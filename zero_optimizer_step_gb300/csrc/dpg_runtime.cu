@@ -6,6 +6,8 @@
 #include <atomic>
 #include <cmath>
 #include <cstdint>
+#include <cstdlib>
+#include <cstring>
 #include <map>
 #include <mutex>
 #include <utility>
@@ -21,6 +23,7 @@ thread_local int64_t t_staged_skip = -1;
 thread_local int64_t t_staged_timeout_ns = 0;
 thread_local int32_t t_fused_max_ctas = 0;
 thread_local int32_t t_programmatic = 1;
+thread_local int64_t t_debug_limit = -1;
 
 // ---------------------------------------------------------------------------
 // host helpers
@@ -193,6 +196,9 @@ int upload(Plan& p) {
     if (e == cudaSuccess) e = cudaMemcpy(tb, p.tile_begin.data(), nb1 * sizeof(int64_t), cudaMemcpyHostToDevice);
     if (e == cudaSuccess && !p.items.empty())
         e = cudaMemcpy(it, p.items.data(), p.items.size() * sizeof(PackItem), cudaMemcpyHostToDevice);
+#ifdef DPG_DEBUG
+    if (e == cudaSuccess) e = cudaMemset(static_cast<unsigned char*>(clip) + clip_sq_bytes + 192, 0, 8);
+#endif
     if (e != cudaSuccess) {
         cudaFree(bo); cudaFree(tb); cudaFree(it); cudaFree(vis); cudaFree(clip); cudaFree(chunk);
         cudaFree(seg);
@@ -213,6 +219,8 @@ int upload(Plan& p) {
     p.d_bucket_sq64 = static_cast<double*>(clip);
     p.d_clip_coef = reinterpret_cast<float*>(static_cast<unsigned char*>(clip) + clip_sq_bytes);
     p.d_status = reinterpret_cast<int32_t*>(static_cast<unsigned char*>(clip) + clip_sq_bytes + 128);
+    p.d_debug = reinterpret_cast<unsigned long long*>(static_cast<unsigned char*>(clip) +
+                                                      clip_sq_bytes + 192);
     p.d_chunk = chunk;
     p.d_tile_span = static_cast<int64_t*>(chunk);
     p.d_chunk_sq = reinterpret_cast<double*>(static_cast<unsigned char*>(chunk) + tb_bytes);
@@ -301,6 +309,43 @@ int dpg_set_fused_max_ctas(int32_t max_ctas) {
     if (max_ctas < 0) return fail(DPG_ERR_INVALID_ARG, "dpg_set_fused_max_ctas: %d < 0", max_ctas);
     dpg::t_fused_max_ctas = max_ctas;
     return DPG_OK;
+}
+
+int dpg_debug_checks(const dpg_plan_t* plan, int32_t* built, int64_t* first_failure) {
+    dpg::clear_error();
+#ifdef DPG_DEBUG
+    if (built) *built = 1;
+#else
+    if (built) *built = 0;
+#endif
+    if (first_failure) *first_failure = 0;
+    if (!plan) return fail(DPG_ERR_INVALID_ARG, "dpg_debug_checks: plan is NULL");
+#ifdef DPG_DEBUG
+    const dpg::Plan& p = plan->p;
+    if (p.device < 0 || !first_failure) return DPG_OK;   // nothing ran on a device yet
+    DPG_CUDA_TRY(cudaDeviceSynchronize());
+    unsigned long long word = 0;
+    DPG_CUDA_TRY(cudaMemcpy(&word, p.d_debug, sizeof word, cudaMemcpyDeviceToHost));
+    DPG_CUDA_TRY(cudaMemset(p.d_debug, 0, sizeof word));
+    *first_failure = static_cast<int64_t>(word);
+#endif
+    return DPG_OK;
+}
+
+int dpg_debug_set_limit(int64_t limit) {
+    dpg::clear_error();
+#ifdef DPG_DEBUG
+    const char* on = std::getenv("DPG_TEST_HOOKS");
+    if (!on || std::strcmp(on, "1") != 0)
+        return fail(DPG_ERR_INVALID_ARG, "dpg_debug_set_limit: test hooks are disabled "
+                                         "(set DPG_TEST_HOOKS=1 in the environment)");
+    dpg::t_debug_limit = limit;
+    return DPG_OK;
+#else
+    (void)limit;
+    return fail(DPG_ERR_INVALID_ARG, "dpg_debug_set_limit: this library was built without "
+                                     "index checks (build it with --debug)");
+#endif
 }
 
 int dpg_set_programmatic_launch(int32_t on) {

@@ -108,6 +108,10 @@ struct PackArgs {
     int64_t item0;
     int64_t n_items;
     uint16_t* flat;
+#ifdef DPG_DEBUG
+    unsigned long long* dbg;  // the plan's debug word
+    int64_t dbg_limit;        // elements of the flat buffer
+#endif
 };
 
 // Copy n bf16 elements.  When both ends are 16-byte aligned, each thread
@@ -144,6 +148,14 @@ __device__ __forceinline__ void copy_elems(uint16_t* __restrict__ dst,
 __global__ void __launch_bounds__(256) k_pack(const __grid_constant__ PackArgs a) {
     for (int64_t j = blockIdx.x; j < a.n_items; j += gridDim.x) {
         const PackItem it = a.items[a.item0 + j];
+#ifdef DPG_DEBUG
+        if (!debug_ok(a.dbg, it.param - a.p_base >= 0 && it.param - a.p_base < kPackPtrs &&
+                                 it.flat_off >= 0 && it.count >= 0 && it.tail >= 0 &&
+                                 it.src_off >= 0 &&
+                                 it.flat_off + it.count + (a.unpack ? 0 : it.tail) <= a.dbg_limit,
+                      4))
+            continue;                           // uniform over the CTA: no barrier below
+#endif
         uint16_t* param = static_cast<uint16_t*>(const_cast<void*>(a.ptrs[it.param - a.p_base]));
         uint16_t* flat = a.flat + it.flat_off;
         if (!a.unpack) {
@@ -344,6 +356,10 @@ static int pack_common(const dpg_plan_t* plan, const void* const* ptrs, void* fl
         a.item0 = int64_t(i0);
         a.flat = static_cast<uint16_t*>(flat);
         a.n_items = int64_t(i1 - i0);
+#ifdef DPG_DEBUG
+        a.dbg = p.d_debug;
+        a.dbg_limit = dpg::t_debug_limit >= 0 ? dpg::t_debug_limit : p.total_padded;
+#endif
         int grid = 0;
         st = dpg::grid_cover(a.n_items, &grid, who);
         if (st != DPG_OK) return st;
