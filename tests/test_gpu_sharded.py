@@ -27,7 +27,7 @@ def built():
     build.build()
 
 
-@pytest.mark.parametrize("R", [2, 3, 4, 8])
+@pytest.mark.parametrize("R", [2, 3, 4, 8, 16])
 def test_shard_update_equals_single_device_step(R):
     numels = random_param_list(np.random.Generator(np.random.Philox(70 + R)), 40, 300_000)
     plan = dpg.dpg_plan_buckets(numels, 1 << 19, R)
@@ -120,8 +120,8 @@ def test_shard_update_of_accumulated_microbatches(R, K):
             assert torch.equal(st.param_shard[a:z].view(torch.int16), p[lo:hi].view(torch.int16))
 
 
-@pytest.mark.parametrize("groups", [1, 3])
-def test_whole_split_step_over_nccl_single_rank(groups):
+@pytest.mark.parametrize("groups,K", [(1, 1), (3, 1), (3, 2)])
+def test_whole_split_step_over_nccl_single_rank(groups, K):
     # the real collectives (token all-gather, exchange, all-gather of the
     # parameter shards) over a one-rank NCCL group on this GPU, plain and
     # pipelined: the single-device step's bits
@@ -138,20 +138,31 @@ def test_whole_split_step_over_nccl_single_rank(groups):
         plan = dpg.dpg_plan_buckets(numels, 1 << 19, 1)
         N = plan.total_padded
         segs = segments(plan.param_offset, numels)
-        g = flat_grads_bf16(segs, N, 1e-3, stream_seed(95, KIND_GRAD, 0), device="cuda")
+        micro = [flat_grads_bf16(segs, N, 1e-3, stream_seed(95, KIND_GRAD, 0, k), device="cuda")
+                 for k in range(K)]
         master0 = master_f32(N, stream_seed(95, KIND_MASTER), device="cuda")
         hp = dpg.HParams(step=1)
+        counts = [3333 + k for k in range(K)]
         w, m, v = master0.clone(), torch.zeros(N, device="cuda"), torch.zeros(N, device="cuda")
         p = torch.empty(N, dtype=torch.bfloat16, device="cuda")
-        dpg.dpg_step(plan, [g], [3333], hp, w, m, v, [p])
-        st = ShardedStep(plan, 0, 1, "cuda")
+        if K == 1:
+            dpg.dpg_step(plan, micro, counts, hp, w, m, v, [p])
+            src = micro[0]
+        else:
+            acc, src = torch.empty(N, device="cuda"), torch.empty(N, device="cuda")
+            for k in range(K):
+                if k < K - 1:
+                    dpg.dpg_accumulate(plan, micro[k], acc, first=(k == 0))
+                dpg.dpg_accumulate(plan, micro[k], src, first=(k == 0))
+            dpg.dpg_step(plan, [acc], counts, hp, w, m, v, [p], last_micro=[micro[K - 1]])
+        st = ShardedStep(plan, 0, 1, "cuda", grad_dtype=torch.bfloat16 if K == 1 else torch.float32)
         S = st.shard.total_padded
         ms = st.state_from_global(master0)
         mm, vv = torch.zeros(S, device="cuda"), torch.zeros(S, device="cuda")
         param = torch.full((N,), float("nan"), dtype=torch.bfloat16, device="cuda")
-        tokens = st.step(g, [3333], hp, ms, mm, vv, param, groups=groups)
+        tokens = st.step(src, counts, hp, ms, mm, vv, param, groups=groups)
         torch.cuda.synchronize()
-        assert list(tokens) == [3333]
+        assert list(tokens) == counts
         assert torch.equal(param.view(torch.int16), p.view(torch.int16))
         for b in range(plan.n_buckets):
             lo, hi = st.global_slice(b, 0)
