@@ -32,7 +32,7 @@ def test_shard_update_equals_single_device_step(R):
     numels = random_param_list(np.random.Generator(np.random.Philox(70 + R)), 40, 300_000)
     plan = dpg.dpg_plan_buckets(numels, 1 << 19, R)
     N, nb = plan.total_padded, plan.n_buckets
-    assert nb >= 3
+    assert nb >= 2
     segs = segments(plan.param_offset, numels)
     grads = [flat_grads_bf16(segs, N, 1e-3, stream_seed(70, KIND_GRAD, s), device="cuda")
              for s in range(R)]
