@@ -803,6 +803,10 @@ def run_dpg(a):
         del g, gd, acc, g2, w, m, v, param, sq, nf
         torch.cuda.empty_cache()
         extra["hockney"] = optional_leg(lambda: hockney_compact(dpg), world)
+        # the 10,000-tensor latency list at four caps: 2595 / 149 / 10 / 1 buckets
+        extra["hockney_sweep"] = optional_leg(
+            lambda: hockney_compact(dpg, name="sweep",
+                                    caps=(4 << 10, 64 << 10, 1 << 20, 16 << 20)), world)
         extra["secondary"] = optional_leg(lambda: run_secondary(a, dpg, dev, world), world)
 
     bpp = algorithmic_bytes_per_param(cfg, fold2, deferred)
@@ -1323,13 +1327,15 @@ def run_launch_floor(a):
           flush=True)
 
 
-def hockney_compact(dpg, reps=5):
-    """The alpha-beta record of the default line: the 1B list at its three caps
-    (1 / 25 / 100 MiB), one launch per bucket against one launch in all."""
-    cfg = CONFIGS["llama1b"]
-    points = hockney_points(dpg, cfg, cfg.cap_sweep, reps, modes=("per_bucket", "fused"))
+def hockney_compact(dpg, reps=5, name="llama1b", caps=None):
+    """The alpha-beta record of the default line: a list at a few caps (the 1B
+    list at its three, 1 / 25 / 100 MiB), one launch per bucket against one
+    launch in all."""
+    cfg = CONFIGS[name]
+    caps = cfg.cap_sweep if caps is None else caps
+    points = hockney_points(dpg, cfg, caps, reps, modes=("per_bucket", "fused"))
     return {"workload": f"{cfg.name}: psi={cfg.psi}, R={cfg.R}, caps "
-                        + "/".join(f"{c / (1 << 20):g}" for c in cfg.cap_sweep) + " MiB",
+                        + "/".join(f"{c / (1 << 20):g}" for c in caps) + " MiB",
             "model": "T_per_bucket = K*alpha + beta*M (least squares; K launches, M bytes)",
             "fit": hockney_fit(points, "per_bucket"),
             "points": [{"cap_mib": q["cap_bytes"] / (1 << 20), "n_buckets": q["n_buckets"],

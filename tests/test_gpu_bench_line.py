@@ -60,6 +60,9 @@ def test_default_line_keys_and_arithmetic():
 
     h = line["hockney"]
     assert len(h["points"]) == 3 and h["fit"]["alpha_us"] > 0 and h["fit"]["inv_beta_gbs"] > 0
+    hs = line["hockney_sweep"]
+    assert [q["n_buckets"] for q in hs["points"]] == [2595, 149, 10, 1]
+    assert hs["fit"]["alpha_us"] > 0
 
     s = line["secondary"]
     if "skipped" in s:
