@@ -83,7 +83,8 @@ def parse():
                     help="--sharded: pipeline the step over this many bucket ranges (the "
                          "exchange of one range in flight while the previous one is updated)")
     ap.add_argument("--no-secondary", action="store_true",
-                    help="default line only: skip the Hockney record and the 4.5B workload")
+                    help="default line only: skip its extra legs (the Hockney records, the "
+                         "4.5B workload, the GPT-2 list)")
     ap.add_argument("--cpu-sample-elems", type=int, default=CPU_SAMPLE_ELEMS,
                     help="elements of each oracle sample (CPU baseline and reference arm)")
     ap.add_argument("--kernels", action="store_true",
@@ -558,6 +559,49 @@ def device_room(needed_bytes: int, world: int, device) -> bool:
     return all_ranks_agree(free >= needed_bytes + (2 << 30), world, device)
 
 
+def run_gpt2_leg(a, dpg, dev, world):
+    """The GPT-2-small-shaped list (R = 8, 25 MiB buckets) in the default line:
+    the whole step (fused pass + norm finalize) and its fused launch."""
+    import torch
+    cfg = CONFIGS["gpt2"]
+    plan = dpg.dpg_plan_buckets(cfg.numels, cfg.cap_bytes, cfg.R)
+    N = plan.total_padded
+    if not device_room(resident_bytes(cfg, N), world, dev):
+        return {"skipped": f"needs {resident_bytes(cfg, N) / 1e9:.0f} GB free on the device"}
+    dpg.dpg_plan_upload(plan)
+    segs = segments(plan.param_offset, cfg.numels)
+    g = [flat_grads_bf16(segs, N, cfg.grad_std, stream_seed(cfg.seed, KIND_GRAD, r), device=dev)
+         for r in range(cfg.R)]
+    w = master_f32(N, stream_seed(cfg.seed, KIND_MASTER), device=dev)
+    m, v = torch.zeros(N, device=dev), torch.zeros(N, device=dev)
+    param = torch.empty(N, dtype=torch.bfloat16, device=dev)
+    sq = torch.empty(plan.n_buckets, device=dev)
+    tokens = token_counts(cfg)
+    stream = torch.cuda.current_stream()
+    state = {"t": 0}
+
+    def step(ev):
+        state["t"] += 1
+        if ev is not None:
+            dpg.dpg_time_next_fused_launch(*ev)
+        dpg.dpg_step(plan, g, tokens, dpg.HParams(step=state["t"]), w, m, v, [param],
+                     bucket_sqnorm=sq, stream=stream)
+
+    ms, k_all = timed_cycles(step, max(3, a.steps), 3, world, dev, stream)
+    peak, peak_kind = load_peak()
+    bpp = algorithmic_bytes_per_param(cfg)
+    out = {"config": workload_desc(cfg, cfg.cap_bytes, plan.n_buckets, N),
+           "steps": max(3, a.steps), "warmup": 3, "ms_per_step": ms,
+           "value": job_throughput(cfg.psi, world, ms), "unit": "params/s",
+           "hbm_gbs_step": bpp["step"] * cfg.psi / (ms * 1e-3) / 1e9,
+           "roofline": fused_roofline(fused_kernel_name(a, cfg.R, 1), bpp["fused"], cfg.psi, k_all,
+                                      peak, peak_kind, traffic_per_launch(cfg, cfg.cap_bytes, N))}
+    del g, w, m, v, param, sq
+    plan.destroy()
+    torch.cuda.empty_cache()
+    return out
+
+
 def run_secondary(a, dpg, dev, world):
     """The 4.5B accumulation workload (Llama-3-8B shapes cut to 16 layers,
     R = 4, K = 4 microbatches, 100 MiB buckets) measured in the default line:
@@ -808,6 +852,7 @@ def run_dpg(a):
             lambda: hockney_compact(dpg, name="sweep",
                                     caps=(4 << 10, 64 << 10, 1 << 20, 16 << 20)), world)
         extra["secondary"] = optional_leg(lambda: run_secondary(a, dpg, dev, world), world)
+        extra["gpt2"] = optional_leg(lambda: run_gpt2_leg(a, dpg, dev, world), world)
 
     bpp = algorithmic_bytes_per_param(cfg, fold2, deferred)
     peak, peak_kind = load_peak()

@@ -6,7 +6,8 @@ is there and its figures can be recomputed from its own fields.
   frac = achieved / peak, the kernel's share of the step;
 * the 4.5B leg: cycle_frac from (10K - 8)R + 26 = 154 B/param, the fused
   launch from 6R + 26 = 50, the deferred cycle from 2KR + 26 = 58;
-* the Hockney record, clocks, the end-to-end leg with its copied bytes, the
+* the GPT-2 list's step and fused launch (42 B/param);
+* the Hockney records, clocks, the end-to-end leg with its copied bytes, the
   CPU baseline, and the launch count (two per step: fused pass + finalize).
 """
 import json
@@ -63,6 +64,12 @@ def test_default_line_keys_and_arithmetic():
     hs = line["hockney_sweep"]
     assert [q["n_buckets"] for q in hs["points"]] == [2595, 149, 10, 1]
     assert hs["fit"]["alpha_us"] > 0
+
+    g2 = line["gpt2"]
+    assert g2["config"]["workload"].startswith("gpt2") and g2["config"]["R"] == 8
+    assert g2["roofline"]["algorithmic_bytes_per_launch"] == 42 * g2["config"]["psi"]
+    assert g2["value"] == pytest.approx(g2["config"]["psi"] / (g2["ms_per_step"] * 1e-3), rel=1e-9)
+    assert 0.8 < g2["roofline"]["frac"] < 1.3
 
     s = line["secondary"]
     if "skipped" in s:
